@@ -1,0 +1,424 @@
+"""Benchmark of the batch-invariant MoE hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of M synthetic
+tokens: bf16->fp32 cast, fp32 router GEMM, sigmoid top-k, token permute,
+gate/up grouped GEMM with SwiGLU x probability, down grouped GEMM, slot-order
+combine.  Default workload: Qwen3-30B-A3B-shaped MoE layer (H=2048, E=128,
+top-8, I=768, router K=2048 N=128), M=4096 tokens per GPU per step, bf16
+weights/activations ~ N(0, 0.02), fp32 router.  The expert weights (1.2 GB)
+are larger than L2, so every step streams them from HBM (no explicit flush).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload qwen|dsv4] [--tokens M] [--no-extras]
+
+Prints one JSON line (rank 0).  N > 1: launched by torchrun, one rank per
+GPU, every rank runs its own M tokens (weak scaling, no collective on the
+data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "qwen": dict(name="qwen3-30b-a3b-moe-layer", H=2048, E=128, I=768, top_k=8),
+    "dsv4": dict(name="dsv4-router-moe-layer", H=4096, E=256, I=2048, top_k=8),
+}
+
+
+# ------------------------------------------------------------ distributed --
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: tokens processed by all ranks / slowest rank's time."""
+    return tokens_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def snapshot(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                 timeout=10).stdout.strip()
+            if out:
+                self.lines.append(out)
+        except (OSError, subprocess.TimeoutExpired):
+            pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if not self.lines:
+            self.snapshot()
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our GPU arm --
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), \
+            d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import invariant_moe_gb300 as bm
+    from tests import synthetic as syn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    wl = WORKLOADS[args.workload]
+    H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
+    M = args.tokens
+    P = M * k
+
+    w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
+    x = syn.moe_tokens(M, H, seed=21 + rank, device=str(dev))
+    # step buffers (allocated once, reused)
+    x32 = torch.empty(M, H, dtype=torch.float32, device=dev)
+    scores = torch.empty(M, E, dtype=torch.float32, device=dev)
+    ids = torch.empty(M, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(M, k, dtype=torch.float32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(P, dtype=torch.int32, device=dev)
+    act = torch.empty(P, I, dtype=torch.bfloat16, device=dev)
+    contrib = torch.empty(P, H, dtype=torch.float32, device=dev)
+    out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    lib = bm.load_library()
+    ws_perm = torch.empty(max(int(lib.bi_moe_permute_workspace_bytes(M, E)), 256), dtype=torch.uint8, device=dev)
+    ws_gu = torch.empty(max(int(lib.bi_moe_gate_up_workspace_bytes(M, H, k)), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = {n: [] for n in ("gate_up", "down")}
+
+    def step(record=False):
+        bm.bi_cast_bf16_to_f32(x, out=x32)
+        bm.bi_router_gemm(x32, w.w_router, None, out=scores)
+        bm.bi_topk(scores, k, ids=ids, wts=wts)
+        bm.bi_moe_permute(ids, E, offsets=offsets, perm=perm, workspace=ws_perm)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        bm.bi_moe_gate_up(x, offsets, perm, wts, w.w13, k, act=act, workspace=ws_gu)
+        if record:
+            e1.record(stream)
+        bm.bi_moe_down(act, offsets, perm, w.w2, M, k, contrib=contrib)
+        if record:
+            e2.record(stream)
+            ev["gate_up"].append((e0, e1))
+            ev["down"].append((e1, e2))
+        bm.bi_moe_combine(contrib, M, k, out=out)
+
+    launches_per_step = 1 + 1 + 1 + 3 + 2 + 1 + 1  # cast router topk permute(3) gather+gateup down combine
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if bm.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    sec = t0.elapsed_time(t1) / 1e3
+    sec_max = max_over_ranks(sec, world, dev)
+    gu_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["gate_up"])
+    dn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["down"])
+
+    # ---- end to end through the public API from pinned host buffers
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        o, _, _, _ = bm.moe_layer(x_dev, w.w_router, w.w13, w.w2, k)
+        out_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_sec = max_over_ranks(a0.elapsed_time(a1) / 1e3, world, dev)
+    if bm.device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras["router_us_vs_M"] = router_sweep(dev)
+
+    if rank != 0:
+        return None
+    hbm, tc_burst, tc_sust, peak_src = measured_peaks()
+    gu_flops = 2.0 * P * 2 * I * H
+    dn_flops = 2.0 * P * H * I
+    gu_tf = gu_flops / (gu_ms / 1e3) / 1e12
+    line = {
+        "metric": "BI MoE-layer tokens/s (whole hot path: router GEMM + top-k + fused experts)",
+        "value": aggregate(M, args.steps, world, sec_max),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 experts / fp32 router", "data": "synthetic (seeded N(0,0.02) weights and tokens)",
+        "config": {"workload": wl["name"], "tokens_per_gpu": M, "H": H, "E": E, "top_k": k, "I": I,
+                   "router": f"fp32 [{M},{H}] x [{E},{H}]^T", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights %.2f GB streamed per step)"
+                         % ((E * 3 * I * H * 2) / 1e9)},
+        "roofline": {"kernel": "gate_up stage (row gather + tcgen05 grouped GEMM + SwiGLU*p)",
+                     "bound": "tensor", "achieved": gu_tf, "peak": tc_sust, "unit": "TFLOP/s",
+                     "frac": gu_tf / tc_sust, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained",
+                     "ms_per_launch": gu_ms,
+                     "down_ms_per_launch": dn_ms,
+                     "down_tflops": dn_flops / (dn_ms / 1e3) / 1e12},
+        "e2e": {"value": aggregate(M, e2e_steps, world, e2e_sec), "unit": "tokens/s",
+                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
+                "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    line.update(extras)
+    return line
+
+
+def router_sweep(dev):
+    """Device us per router call (DSv4 router: K=4096, N=256, fp32) vs M:
+    warm = back-to-back calls; cold = L2 flushed (256 MB write) before each."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    from tests import synthetic as syn
+    inp = syn.router_inputs()
+    x, w, b = inp.x.to(dev), inp.w.to(dev), inp.b.to(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    res = {}
+    for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096):
+        xm = x[:M].contiguous()
+        y = torch.empty(M, 256, dtype=torch.float32, device=dev)
+        for _ in range(5):
+            bm.bi_router_gemm(xm, w, b, out=y)
+        n = 50
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            bm.bi_router_gemm(xm, w, b, out=y)
+        e1.record()
+        torch.cuda.synchronize()
+        warm = e0.elapsed_time(e1) / n * 1e3
+        cold = []
+        for _ in range(10):
+            flush.fill_(1.0)
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record()
+            bm.bi_router_gemm(xm, w, b, out=y)
+            c1.record()
+            torch.cuda.synchronize()
+            cold.append(c0.elapsed_time(c1) * 1e3)
+        res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(statistics.median(cold), 2)}
+    return res
+
+
+# ------------------------------------------------------ oracle (CPU) arm --
+def oracle_tokens(args, n_tokens, seed=21):
+    """Run the fp64 oracle on n_tokens of the workload; returns seconds."""
+    import oracle
+    from tests import synthetic as syn
+    wl = WORKLOADS[args.workload]
+    H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
+    if not hasattr(oracle_tokens, "_cache"):
+        oracle_tokens._cache = {}
+    key = args.workload
+    if key not in oracle_tokens._cache:
+        w = syn.moe_weights(H, E, I, seed=11)
+        oracle_tokens._cache[key] = (w.w_router.numpy(), syn.bf16_bits(w.w13), syn.bf16_bits(w.w2))
+    wr, w13, w2 = oracle_tokens._cache[key]
+    x = syn.moe_tokens(n_tokens, H, seed=seed)
+    xb = syn.bf16_bits(x)
+    t = time.perf_counter()
+    r = oracle.router(x.float().numpy(), wr)
+    ids, wts = oracle.topk(r.astype("float32"), k)
+    oracle.moe(xb, ids, wts.astype("float32"), w13, w2, E, I)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(args, budget_s=12.0):
+    n, total, tok = 2, 0.0, 0
+    while total < budget_s:
+        total += oracle_tokens(args, n, seed=100 + tok)
+        tok += n
+    return {"value": tok / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{tok} tokens of the {WORKLOADS[args.workload]['name']} workload "
+                      f"(fp64 router + top-k + experts, single thread, {total:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    per_step = 1  # tokens per step: a bounded sample of the workload
+    for _ in range(args.warmup):
+        oracle_tokens(args, per_step)
+    t = 0.0
+    for s in range(args.steps):
+        t += oracle_tokens(args, per_step, seed=1000 + s)
+    value = per_step * args.steps / t
+    return {
+        "impl": "reference",
+        "metric": "BI MoE-layer tokens/s (whole hot path: router GEMM + top-k + fused experts)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl["name"], "tokens_per_gpu": args.tokens, "H": wl["H"], "E": wl["E"],
+                   "top_k": wl["top_k"], "I": wl["I"], "parallelism": "oracle on 1 host core"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} token(s) per step, fp64 single thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=tuple(WORKLOADS), default="qwen")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+        if line is not None and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

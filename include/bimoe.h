@@ -1,0 +1,245 @@
+/*
+ * bimoe.h -- C ABI of the batch-invariant MoE hot path for GB300 (sm_103a).
+ *
+ * One library, libbimoe.so, holding hand-written CUDA kernels.  Every entry
+ * point takes plain device pointers owned by the caller plus sizes and a CUDA
+ * stream, launches asynchronously on that stream, never synchronises the
+ * host and never allocates device memory.  Calls are safe to capture in a
+ * CUDA graph (argument checks are host-side; nothing reads device memory on
+ * the host).
+ *
+ * Batch invariance contract: for fixed weights and fixed (N,K) resp.
+ * (H,E,top_k,I), every output row of every entry point is bit-identical
+ * whatever M is and whatever other rows share the call.  Nothing in the
+ * library keys any arithmetic on M; M only sizes grids and schedules.
+ *
+ * Layouts are row-major and contiguous.  "bf16" arguments are bfloat16
+ * values stored as 16-bit patterns.  Device pointers must be 16-byte
+ * aligned where stated (TMA operands).
+ *
+ * Errors: entry points return bi_status.  BI_ERR_INVALID_ARG for a null
+ * required pointer, a negative size, a misaligned pointer or top_k outside
+ * its range; BI_ERR_UNSUPPORTED for a shape that has no kernel (the library
+ * never falls back to another recipe); BI_ERR_WORKSPACE for a workspace that
+ * is too small; BI_ERR_CUDA when a launch fails.  M == 0 returns BI_OK and
+ * launches nothing.  A kernel that detects bad data (an expert id outside
+ * [0,E), repeated experts in one row) or whose bounded wait times out
+ * records a code in a device-side error word; bi_device_error() reads it.
+ * bi_last_error_message() returns a human-readable detail of the last
+ * failing call on this host thread.
+ */
+#ifndef BIMOE_H_
+#define BIMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BI_API __attribute__((visibility("default")))
+#else
+#define BI_API
+#endif
+
+/* A cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st *bi_stream_t;
+/* bfloat16 storage. */
+typedef uint16_t bi_bf16;
+
+typedef enum {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,
+  BI_ERR_UNSUPPORTED = 2,
+  BI_ERR_WORKSPACE = 3,
+  BI_ERR_CUDA = 4,
+  BI_ERR_DEVICE = 5 /* bad data or a bounded wait timed out on the device */
+} bi_status;
+
+/* Device error codes recorded by kernels (bi_device_error). */
+#define BI_DEVERR_NONE 0
+#define BI_DEVERR_BAD_EXPERT_ID 1   /* id outside [0,E) */
+#define BI_DEVERR_REPEATED_EXPERT 2 /* one row routed twice to one expert */
+#define BI_DEVERR_WAIT_TIMEOUT 3    /* an mbarrier wait exceeded its limit */
+
+BI_API const char *bi_status_str(bi_status s);
+BI_API const char *bi_last_error_message(void);
+BI_API const char *bi_version(void);
+
+/*
+ * bi_device_error -- read and clear the device error word of the current
+ * device.  Synchronises the device.  *code receives a BI_DEVERR_* value.
+ * Returns BI_ERR_CUDA if the read fails.
+ */
+BI_API bi_status bi_device_error(int32_t *code);
+
+/*
+ * bi_cast_bf16_to_f32 -- y[i] = float(x[i]) for i < n, exact.
+ * The router reads fp32 activations: MoE-layer activations arrive in bf16
+ * and widen exactly, so scores never round through bf16 (GateLinear router
+ * page, section "What").  x: n bf16, y: n fp32 (device).
+ */
+BI_API bi_status bi_cast_bf16_to_f32(const bi_bf16 *x, float *y, int64_t n,
+                                     bi_stream_t stream);
+
+/*
+ * bi_router_gemm -- fp32 router GEMM  y = x W^T (+ bias).
+ * Source: "[BI][DSv4] Batch-invariant GateLinear router with fp32
+ * persistent matmul", sections "What" and "A correction to why the key
+ * excludes M": fp32 scores, bias preserved, one reduction recipe that does
+ * not depend on M.
+ *   x    [M,K] fp32 row-major (device), ld = K
+ *   w    [N,K] fp32 row-major (device), the nn.Linear weight used as W^T
+ *   bias [N] fp32 (device) or NULL
+ *   y    [M,N] fp32 row-major (device), written
+ * Reduction recipe (fixed by K alone, never by M): K is cut into K/128
+ * contiguous slices; slice s is an fp32 fused-multiply-add chain over
+ * k = 128s .. 128s+127 in increasing k starting from +0.0; the slice results
+ * are added in slice order starting from +0.0; the bias is added last.  All
+ * schedules (chosen from M) evaluate exactly this sequence per element.
+ * Requirements: K % 128 == 0, 1 <= N <= 4096, x/w 16-byte aligned.
+ * Otherwise BI_ERR_UNSUPPORTED / BI_ERR_INVALID_ARG.
+ */
+BI_API bi_status bi_router_gemm(const float *x, const float *w, const float *bias,
+                                float *y, int64_t M, int64_t K, int64_t N,
+                                bi_stream_t stream);
+
+/*
+ * bi_router_gemm_schedule -- test hook: bi_router_gemm with the schedule
+ * forced (0 = automatic by M, 1 = per-row warp kernel, 2 = slice-parallel
+ * tile kernel, 3 = register-tiled kernel).  Every schedule computes the same
+ * recipe; tests use this to show that the bits do not depend on it.
+ */
+BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,
+                                         const float *bias, float *y, int64_t M,
+                                         int64_t K, int64_t N, int32_t schedule,
+                                         bi_stream_t stream);
+
+/*
+ * bi_router_gemm_splitk_negctl -- NEGATIVE CONTROL, test use only.  Same
+ * signature as bi_router_gemm but its K split depends on M (one chain over
+ * all of K for M > 16, sixteen 256-long slices for M <= 16), the kind of
+ * batch-dependent reduction the GateLinear page diagnoses in the default
+ * route.  Row bits change across that boundary; the tests assert that they
+ * do, to prove the invariance tests can fail.
+ */
+BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w,
+                                              const float *bias, float *y,
+                                              int64_t M, int64_t K, int64_t N,
+                                              bi_stream_t stream);
+
+/*
+ * bi_topk -- sigmoid scoring and deterministic top-k expert selection.
+ * Source: "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling under
+ * batch invariance", commit log, deterministic per-row top-k commit: score
+ * descending, exact ties broken by ascending index, -0.0 equal to +0.0,
+ * ranking on a monotone int32 key of the fp32 score, no shared-memory
+ * atomics.
+ *   scores [M,E] fp32 (device): router outputs
+ *   ids    [M,top_k] int32 (device), written: ids[m,t] = rank-t expert
+ *   wts    [M,top_k] fp32 (device), written: sigmoid(scores[m, ids[m,t]])
+ *   probs  [M,E] fp32 (device) or NULL: sigmoid of every score
+ * Selection is on the fp32 score (sigmoid is monotone, so this is the
+ * selection by probability without ties manufactured by rounding the
+ * sigmoid).  One warp per row.  Requirements: 1 <= E <= 512,
+ * 1 <= top_k <= min(E, 16).
+ */
+BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts,
+                         float *probs, int64_t M, int64_t E, int32_t top_k,
+                         bi_stream_t stream);
+
+/*
+ * bi_moe_workspace_bytes -- bytes of device workspace bi_moe_forward needs
+ * for these sizes (a multiple of 256).  Returns 0 for invalid sizes.
+ */
+BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E,
+                                     int32_t top_k, int64_t I);
+
+/*
+ * bi_moe_forward -- batch-invariant fused-MoE expert path.
+ * Source: "Batch-invariance generation with vLLM fused-MoE backend at
+ * improved performance", section "What's included" and the strict-review
+ * summary: permute tokens by expert; gate/up grouped GEMM with fp32
+ * accumulation, a fixed K step and no split-K; SwiGLU with the routing
+ * probability applied at the activation (fp32 math, one bf16 round, gate
+ * half = rows [0,I) of each expert's W13, up half = rows [I,2I)); down
+ * grouped GEMM (fp32 accumulation, fixed K step, no split-K); top-k sum with
+ * unit weights in slot order t = 0..top_k-1 in fp32, one bf16 round.
+ *   x    [M,H] bf16 (device, 16-byte aligned)
+ *   ids  [M,top_k] int32 (device): distinct experts per row in [0,E)
+ *   wts  [M,top_k] fp32 (device): routing probabilities
+ *   w13  [E,2I,H] bf16 (device, 16-byte aligned)
+ *   w2   [E,H,I] bf16 (device, 16-byte aligned)
+ *   out  [M,H] bf16 (device), written
+ *   workspace: >= bi_moe_workspace_bytes(...) bytes of device memory,
+ *   256-byte aligned, owned by the caller, contents need not be initialised.
+ * Requirements: H % 128 == 0, I % 128 == 0, 1 <= E <= 1024,
+ * 1 <= top_k <= 16, M * top_k < 2^31.
+ */
+BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids,
+                                const float *wts, const bi_bf16 *w13,
+                                const bi_bf16 *w2, bi_bf16 *out, int64_t M,
+                                int64_t H, int64_t E, int32_t top_k, int64_t I,
+                                void *workspace, size_t workspace_bytes,
+                                bi_stream_t stream);
+
+/* ---- the stages of bi_moe_forward, callable one by one (same contracts) --
+ *
+ * bi_moe_permute -- group the M*top_k (token, slot) pairs by expert, stable
+ * (by expert, then token, then slot).  offsets [E+1] int32 written:
+ * offsets[e] = first position of expert e, offsets[E] = M*top_k.
+ * perm [M*top_k] int32 written: perm[p] = token*top_k + slot at position p.
+ * workspace: >= bi_moe_permute_workspace_bytes(M, E) bytes.
+ * Integer-only and deterministic (counts and bit masks, no ordering by
+ * atomics).
+ */
+BI_API size_t bi_moe_permute_workspace_bytes(int64_t M, int64_t E);
+BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets,
+                                int32_t *perm, int64_t M, int64_t E,
+                                int32_t top_k, void *workspace,
+                                size_t workspace_bytes, bi_stream_t stream);
+
+/*
+ * bi_moe_gate_up -- act[p, j] = bf16(silu(g) * u * wts[perm[p]]) for every
+ * permuted position p < M*top_k, with g/u the gate/up projections of token
+ * perm[p]/top_k by the expert owning position p (tcgen05 bf16 MMA, fp32
+ * accumulation in tensor memory, K step 64, no split-K).
+ *   x [M,H] bf16; offsets/perm from bi_moe_permute; wts [M,top_k] fp32;
+ *   w13 [E,2I,H] bf16; act [M*top_k, I] bf16 (device, written).
+ *   workspace: >= bi_moe_gate_up_workspace_bytes(M, H, top_k) bytes (holds
+ *   the gathered token rows).
+ */
+BI_API size_t bi_moe_gate_up_workspace_bytes(int64_t M, int64_t H, int32_t top_k);
+BI_API bi_status bi_moe_gate_up(const bi_bf16 *x, const int32_t *offsets,
+                                const int32_t *perm, const float *wts,
+                                const bi_bf16 *w13, bi_bf16 *act, int64_t M,
+                                int64_t H, int64_t E, int32_t top_k, int64_t I,
+                                void *workspace, size_t workspace_bytes,
+                                bi_stream_t stream);
+
+/*
+ * bi_moe_down -- contrib[perm[p], h] = sum_j act[p,j] * W2[e,h,j] for every
+ * permuted position p (tcgen05 bf16 MMA, fp32 accumulation, K step 64, no
+ * split-K).  act [M*top_k, I] bf16 (16-byte aligned); w2 [E,H,I] bf16;
+ * contrib [M*top_k, H] fp32 (row = token*top_k + slot), written.
+ */
+BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets,
+                             const int32_t *perm, const bi_bf16 *w2,
+                             float *contrib, int64_t M, int64_t H, int64_t E,
+                             int32_t top_k, int64_t I, bi_stream_t stream);
+
+/*
+ * bi_moe_combine -- out[m,h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) +
+ * c[m,top_k-1,h]) in fp32, slot order, unit weights.
+ * contrib [M,top_k,H] fp32; out [M,H] bf16 (device, written).
+ */
+BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
+                                int64_t H, int32_t top_k, bi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIMOE_H_ */

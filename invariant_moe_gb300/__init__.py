@@ -1,0 +1,272 @@
+"""Python binding of libbimoe.so, the batch-invariant MoE hot path for GB300.
+
+Argument marshalling only: every function checks tensor dtypes / devices /
+contiguity, passes raw device pointers and the current CUDA stream to the C
+ABI declared in ``include/bimoe.h``, and raises on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU fallback.  If
+the library is missing the first call raises ``RuntimeError`` -- build it with
+``python -m invariant_moe_gb300._build`` (or ``__graft_entry__.build()``).
+
+Names follow the C entry points: ``bi_router_gemm``, ``bi_topk``,
+``bi_moe_forward`` and the per-stage calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbimoe.so")
+
+BI_OK = 0
+STATUS = {0: "BI_OK", 1: "BI_ERR_INVALID_ARG", 2: "BI_ERR_UNSUPPORTED", 3: "BI_ERR_WORKSPACE",
+          4: "BI_ERR_CUDA", 5: "BI_ERR_DEVICE"}
+DEVERR = {0: "none", 1: "expert id out of range", 2: "repeated expert in a row",
+          3: "bounded wait timed out"}
+
+# every symbol include/bimoe.h declares (checked by the CPU test-suite)
+EXPORTS = [
+    "bi_status_str", "bi_last_error_message", "bi_version", "bi_device_error",
+    "bi_cast_bf16_to_f32", "bi_router_gemm", "bi_router_gemm_schedule",
+    "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
+    "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gate_up_workspace_bytes",
+    "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine",
+]
+
+
+class BimoeError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """dlopen libbimoe.so and declare its signatures (no GPU needed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing; build it with "
+                "`python -m invariant_moe_gb300._build`")
+        lib = ctypes.CDLL(path)
+        P, I64, I32, SZ, ST = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                               ctypes.c_size_t, ctypes.c_int)
+        sig = {
+            "bi_status_str": ([ctypes.c_int], ctypes.c_char_p),
+            "bi_last_error_message": ([], ctypes.c_char_p),
+            "bi_version": ([], ctypes.c_char_p),
+            "bi_device_error": ([P], ST),
+            "bi_cast_bf16_to_f32": ([P, P, I64, P], ST),
+            "bi_router_gemm": ([P, P, P, P, I64, I64, I64, P], ST),
+            "bi_router_gemm_schedule": ([P, P, P, P, I64, I64, I64, I32, P], ST),
+            "bi_router_gemm_splitk_negctl": ([P, P, P, P, I64, I64, I64, P], ST),
+            "bi_topk": ([P, P, P, P, I64, I64, I32, P], ST),
+            "bi_moe_workspace_bytes": ([I64, I64, I64, I32, I64], SZ),
+            "bi_moe_forward": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
+            "bi_moe_permute_workspace_bytes": ([I64, I64], SZ),
+            "bi_moe_permute": ([P, P, P, I64, I64, I32, P, SZ, P], ST),
+            "bi_moe_gate_up_workspace_bytes": ([I64, I64, I32], SZ),
+            "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
+            "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
+            "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _call(name, *args):
+    lib = load_library()
+    st = getattr(lib, name)(*args)
+    if st != BI_OK:
+        raise BimoeError(name, st, lib.bi_last_error_message().decode())
+
+
+def _ptr(t, dtype, name, device=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def device_error() -> int:
+    """Read and clear the device error word (synchronises the device)."""
+    lib = load_library()
+    v = ctypes.c_int32(0)
+    st = lib.bi_device_error(ctypes.byref(v))
+    if st != BI_OK:
+        raise BimoeError("bi_device_error", st, lib.bi_last_error_message().decode())
+    return v.value
+
+
+# ----------------------------------------------------------------- router --
+def bi_cast_bf16_to_f32(x, out=None, stream=None):
+    out = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _call("bi_cast_bf16_to_f32", _ptr(x, torch.bfloat16, "x"), _ptr(out, torch.float32, "out", x.device),
+          x.numel(), _stream(stream))
+    return out
+
+
+def bi_router_gemm(x, w, bias=None, out=None, schedule=0, stream=None):
+    """y[M,N] = x[M,K] @ w[N,K]^T (+ bias), fp32, batch-invariant recipe."""
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w must be [N, K]")
+    out = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
+    if out.shape != (M, N):
+        raise ValueError("out must be [M, N]")
+    args = (_ptr(x, torch.float32, "x"), _ptr(w, torch.float32, "w", x.device),
+            _ptr(bias, torch.float32, "bias", x.device), _ptr(out, torch.float32, "out", x.device),
+            M, K, N)
+    if schedule:
+        _call("bi_router_gemm_schedule", *args, schedule, _stream(stream))
+    else:
+        _call("bi_router_gemm", *args, _stream(stream))
+    return out
+
+
+def bi_router_gemm_splitk_negctl(x, w, bias=None, out=None, stream=None):
+    """Negative control (tests only): K split depends on M."""
+    M, K = x.shape
+    N = w.shape[0]
+    out = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _call("bi_router_gemm_splitk_negctl", _ptr(x, torch.float32, "x"),
+          _ptr(w, torch.float32, "w", x.device), _ptr(bias, torch.float32, "bias", x.device),
+          _ptr(out, torch.float32, "out", x.device), M, K, N, _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------ top-k --
+def bi_topk(scores, top_k, ids=None, wts=None, probs=None, want_probs=False, stream=None):
+    """(ids int32 [M,k], wts fp32 [M,k], probs fp32 [M,E] or None)."""
+    M, E = scores.shape
+    dev = scores.device
+    ids = ids if ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    wts = wts if wts is not None else torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    if want_probs and probs is None:
+        probs = torch.empty(M, E, dtype=torch.float32, device=dev)
+    _call("bi_topk", _ptr(scores, torch.float32, "scores"), _ptr(ids, torch.int32, "ids", dev),
+          _ptr(wts, torch.float32, "wts", dev), _ptr(probs, torch.float32, "probs", dev),
+          M, E, top_k, _stream(stream))
+    return ids, wts, probs
+
+
+# -------------------------------------------------------------------- MoE --
+def bi_moe_workspace_bytes(M, H, E, top_k, I) -> int:
+    return int(load_library().bi_moe_workspace_bytes(M, H, E, top_k, I))
+
+
+def moe_workspace(M, H, E, top_k, I, device):
+    n = bi_moe_workspace_bytes(M, H, E, top_k, I)
+    if n == 0 and M > 0:
+        raise ValueError("unsupported MoE sizes")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def bi_moe_forward(x, ids, wts, w13, w2, out=None, workspace=None, stream=None):
+    """out[M,H] bf16 = batch-invariant SwiGLU MoE of x [M,H] bf16."""
+    M, H = x.shape
+    E, twoI, H2 = w13.shape
+    I = twoI // 2
+    top_k = ids.shape[1]
+    if H2 != H or tuple(w2.shape) != (E, H, I):
+        raise ValueError("w13 must be [E, 2I, H] and w2 [E, H, I]")
+    dev = x.device
+    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = moe_workspace(M, H, E, top_k, I, dev)
+    _call("bi_moe_forward", _ptr(x, torch.bfloat16, "x"), _ptr(ids, torch.int32, "ids", dev),
+          _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+          _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
+          M, H, E, top_k, I, _ptr(workspace, torch.uint8, "workspace", dev),
+          workspace.numel(), _stream(stream))
+    return out
+
+
+def bi_moe_permute(ids, E, offsets=None, perm=None, workspace=None, stream=None):
+    M, top_k = ids.shape
+    dev = ids.device
+    lib = load_library()
+    offsets = offsets if offsets is not None else torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = perm if perm is not None else torch.empty(max(M * top_k, 1), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.bi_moe_permute_workspace_bytes(M, E)), 256),
+                                dtype=torch.uint8, device=dev)
+    _call("bi_moe_permute", _ptr(ids, torch.int32, "ids"), _ptr(offsets, torch.int32, "offsets", dev),
+          _ptr(perm, torch.int32, "perm", dev), M, E, top_k,
+          _ptr(workspace, torch.uint8, "workspace", dev), workspace.numel(), _stream(stream))
+    return offsets, perm
+
+
+def bi_moe_gate_up(x, offsets, perm, wts, w13, top_k, act=None, workspace=None, stream=None):
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dev = x.device
+    lib = load_library()
+    act = act if act is not None else torch.empty(M * top_k, I, dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.bi_moe_gate_up_workspace_bytes(M, H, top_k)), 256),
+                                dtype=torch.uint8, device=dev)
+    _call("bi_moe_gate_up", _ptr(x, torch.bfloat16, "x"), _ptr(offsets, torch.int32, "offsets", dev),
+          _ptr(perm, torch.int32, "perm", dev), _ptr(wts, torch.float32, "wts", dev),
+          _ptr(w13, torch.bfloat16, "w13", dev), _ptr(act, torch.bfloat16, "act", dev),
+          M, H, E, top_k, I, _ptr(workspace, torch.uint8, "workspace", dev), workspace.numel(),
+          _stream(stream))
+    return act
+
+
+def bi_moe_down(act, offsets, perm, w2, M, top_k, contrib=None, stream=None):
+    E, H, I = w2.shape
+    dev = act.device
+    contrib = contrib if contrib is not None else torch.empty(M * top_k, H, dtype=torch.float32, device=dev)
+    _call("bi_moe_down", _ptr(act, torch.bfloat16, "act"), _ptr(offsets, torch.int32, "offsets", dev),
+          _ptr(perm, torch.int32, "perm", dev), _ptr(w2, torch.bfloat16, "w2", dev),
+          _ptr(contrib, torch.float32, "contrib", dev), M, H, E, top_k, I, _stream(stream))
+    return contrib
+
+
+def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
+    H = contrib.shape[-1]
+    dev = contrib.device
+    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_combine", _ptr(contrib, torch.float32, "contrib"), _ptr(out, torch.bfloat16, "out", dev),
+          M, H, top_k, _stream(stream))
+    return out
+
+
+def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
+    """Whole hot path of one MoE layer: cast -> router -> top-k -> experts.
+    Returns (out, scores, ids, wts)."""
+    x32 = bi_cast_bf16_to_f32(x_bf16, stream=stream)
+    scores = bi_router_gemm(x32, w_router, bias, stream=stream)
+    ids, wts, _ = bi_topk(scores, top_k, stream=stream)
+    out = bi_moe_forward(x_bf16, ids, wts, w13, w2, stream=stream)
+    return out, scores, ids, wts

@@ -1,0 +1,380 @@
+// api.cu -- the extern "C" entry points of libbimoe.so: argument checks,
+// workspace layout, TMA descriptor encoding, and the device error word.
+// All arithmetic happens in the kernels of router.cu, topk.cu, moe_route.cu
+// and moe_gemm.cu.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "bimoe_internal.cuh"
+
+namespace bimoe {
+
+bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
+                        int64_t, int, cudaStream_t);
+bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
+                               int64_t, int64_t, cudaStream_t);
+bi_status launch_cast_bf16_f32(const void *, float *, int64_t, cudaStream_t);
+bi_status launch_topk(const float *, int32_t *, float *, float *, int64_t, int64_t, int32_t,
+                      cudaStream_t);
+size_t permute_scratch_bytes(int64_t M, int64_t E);
+bi_status launch_permute(const int32_t *, int32_t *, int32_t *, int64_t, int64_t, int32_t, void *,
+                         cudaStream_t);
+bi_status launch_gather(const void *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
+                        int32_t, void *, cudaStream_t);
+bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, cudaStream_t);
+bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const float *,
+                         const void *, void *, int64_t, int64_t, int64_t, int32_t, int64_t,
+                         cudaStream_t);
+bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
+                      int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
+
+// ------------------------------------------------------------ error state --
+static thread_local char g_msg[512] = "";
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+}
+
+// One word per device: kernels record the first BI_DEVERR_* they hit.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_mu;
+static int *g_err_ptr[kMaxDevices] = {};
+static int g_sms[kMaxDevices] = {};
+
+static int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return 0;
+  return d;
+}
+
+int *device_error_word() {
+  const int d = current_device();
+  if (d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_ptr[d] = static_cast<int *>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int num_sms() {
+  const int d = current_device();
+  if (d >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 148;
+    g_sms[d] = v;
+  }
+  return g_sms[d];
+}
+
+// ------------------------------------------------------------ TMA encode --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return false;
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for [%llu x %llu]", (int)r,
+              (unsigned long long)rows, (unsigned long long)cols);
+    return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------- MoE workspace --
+static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+struct MoeWorkspace {
+  size_t offsets, perm, scratch, xperm, act, contrib, total;
+};
+
+static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
+  MoeWorkspace w{};
+  const size_t P = static_cast<size_t>(M) * top_k;
+  size_t off = 0;
+  w.offsets = off; off += align256((E + 1) * sizeof(int32_t));
+  w.perm = off;    off += align256(P * sizeof(int32_t));
+  w.scratch = off; off += align256(permute_scratch_bytes(M, E));
+  w.xperm = off;   off += align256(P * H * 2);
+  w.act = off;     off += align256(P * I * 2);
+  w.contrib = off; off += align256(P * H * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static bi_status check_moe_dims(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
+  if (M < 0 || H <= 0 || E <= 0 || I <= 0) {
+    set_error("negative or zero size (M=%lld H=%lld E=%lld I=%lld)", (long long)M, (long long)H,
+              (long long)E, (long long)I);
+    return BI_ERR_INVALID_ARG;
+  }
+  if (top_k < 1 || top_k > 16 || top_k > E) {
+    set_error("top_k=%d outside [1, min(16, E)]", top_k);
+    return BI_ERR_INVALID_ARG;
+  }
+  if (E > 1024 || H % 128 != 0 || I % 128 != 0) {
+    set_error("unsupported MoE shape (needs H%%128==0, I%%128==0, E<=1024): H=%lld I=%lld E=%lld",
+              (long long)H, (long long)I, (long long)E);
+    return BI_ERR_UNSUPPORTED;
+  }
+  if (M * top_k >= (int64_t(1) << 31) || M * top_k * H >= (int64_t(1) << 40) ||
+      E * 2 * I >= (int64_t(1) << 31) || E * H >= (int64_t(1) << 31)) {
+    set_error("MoE sizes exceed the 32-bit index range");
+    return BI_ERR_UNSUPPORTED;
+  }
+  return BI_OK;
+}
+
+}  // namespace bimoe
+
+using namespace bimoe;
+
+#define BI_REQUIRE(cond, code, ...) \
+  do {                              \
+    if (!(cond)) {                  \
+      set_error(__VA_ARGS__);       \
+      return code;                  \
+    }                               \
+  } while (0)
+
+extern "C" {
+
+BI_API const char *bi_status_str(bi_status s) {
+  switch (s) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG";
+    case BI_ERR_UNSUPPORTED: return "BI_ERR_UNSUPPORTED";
+    case BI_ERR_WORKSPACE: return "BI_ERR_WORKSPACE";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA";
+    case BI_ERR_DEVICE: return "BI_ERR_DEVICE";
+  }
+  return "BI_ERR_UNKNOWN";
+}
+
+BI_API const char *bi_last_error_message(void) { return g_msg; }
+
+BI_API const char *bi_version(void) { return "bimoe 0.1 sm_103a"; }
+
+BI_API bi_status bi_device_error(int32_t *code) {
+  BI_REQUIRE(code, BI_ERR_INVALID_ARG, "code is NULL");
+  int v = 0, zero = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) {
+    set_error("reading the device error word: %s", cudaGetErrorString(e));
+    return BI_ERR_CUDA;
+  }
+  *code = v;
+  return BI_OK;
+}
+
+BI_API bi_status bi_cast_bf16_to_f32(const bi_bf16 *x, float *y, int64_t n, bi_stream_t stream) {
+  BI_REQUIRE(n >= 0, BI_ERR_INVALID_ARG, "n < 0");
+  if (n == 0) return BI_OK;
+  BI_REQUIRE(x && y, BI_ERR_INVALID_ARG, "null pointer");
+  return launch_cast_bf16_f32(x, y, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static bi_status router_checks(const float *x, const float *w, float *y, int64_t M, int64_t K,
+                               int64_t N) {
+  BI_REQUIRE(M >= 0 && K > 0 && N > 0, BI_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld N=%lld",
+             (long long)M, (long long)K, (long long)N);
+  BI_REQUIRE(M == 0 || (x && w && y), BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(K % 128 == 0 && K <= 32768 && N <= 4096, BI_ERR_UNSUPPORTED,
+             "router recipe needs K %% 128 == 0, K <= 32768, N <= 4096 (K=%lld N=%lld)",
+             (long long)K, (long long)N);
+  BI_REQUIRE(M * K < (int64_t(1) << 40) && M * N < (int64_t(1) << 31), BI_ERR_UNSUPPORTED,
+             "router sizes exceed the index range");
+  BI_REQUIRE(M == 0 || (aligned(x, 16) && aligned(w, 16)), BI_ERR_INVALID_ARG,
+             "x and w must be 16-byte aligned");
+  return BI_OK;
+}
+
+BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w, const float *bias,
+                                         float *y, int64_t M, int64_t K, int64_t N,
+                                         int32_t schedule, bi_stream_t stream) {
+  bi_status st = router_checks(x, w, y, M, K, N);
+  if (st != BI_OK) return st;
+  BI_REQUIRE(schedule >= 0 && schedule <= 3, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  if (M == 0) return BI_OK;
+  return launch_router(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_router_gemm(const float *x, const float *w, const float *bias, float *y,
+                                int64_t M, int64_t K, int64_t N, bi_stream_t stream) {
+  return bi_router_gemm_schedule(x, w, bias, y, M, K, N, 0, stream);
+}
+
+BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w, const float *bias,
+                                              float *y, int64_t M, int64_t K, int64_t N,
+                                              bi_stream_t stream) {
+  bi_status st = router_checks(x, w, y, M, K, N);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  return launch_router_negctl(x, w, bias, y, M, K, N, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts, float *probs, int64_t M,
+                         int64_t E, int32_t top_k, bi_stream_t stream) {
+  BI_REQUIRE(M >= 0, BI_ERR_INVALID_ARG, "M < 0");
+  BI_REQUIRE(E >= 1 && E <= 512, BI_ERR_UNSUPPORTED, "E=%lld outside [1, 512]", (long long)E);
+  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= E, BI_ERR_INVALID_ARG,
+             "top_k=%d outside [1, min(16, E)]", top_k);
+  BI_REQUIRE(M * E < (int64_t(1) << 31), BI_ERR_UNSUPPORTED, "M*E exceeds the index range");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(scores && ids && wts, BI_ERR_INVALID_ARG, "null pointer");
+  return launch_topk(scores, ids, wts, probs, M, E, top_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
+  if (check_moe_dims(M, H, E, top_k, I) != BI_OK) return 0;
+  return moe_layout(M, H, E, top_k, I).total;
+}
+
+BI_API size_t bi_moe_permute_workspace_bytes(int64_t M, int64_t E) {
+  if (M < 0 || E <= 0) return 0;
+  return align256(permute_scratch_bytes(M, E));
+}
+
+BI_API size_t bi_moe_gate_up_workspace_bytes(int64_t M, int64_t H, int32_t top_k) {
+  if (M < 0 || H <= 0 || top_k <= 0) return 0;
+  return align256(static_cast<size_t>(M) * top_k * H * 2);
+}
+
+BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, int64_t M,
+                                int64_t E, int32_t top_k, void *workspace, size_t workspace_bytes,
+                                bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && E >= 1 && E <= 1024, BI_ERR_INVALID_ARG, "bad sizes M=%lld E=%lld",
+             (long long)M, (long long)E);
+  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= E, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  BI_REQUIRE(M * top_k < (int64_t(1) << 31), BI_ERR_UNSUPPORTED, "M*top_k exceeds int32");
+  BI_REQUIRE(offsets, BI_ERR_INVALID_ARG, "offsets is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s) != cudaSuccess) {
+      set_error("cudaMemsetAsync failed");
+      return BI_ERR_CUDA;
+    }
+    return BI_OK;
+  }
+  BI_REQUIRE(ids && perm && workspace, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(workspace_bytes >= bi_moe_permute_workspace_bytes(M, E), BI_ERR_WORKSPACE,
+             "workspace %zu < %zu bytes", workspace_bytes, bi_moe_permute_workspace_bytes(M, E));
+  return launch_permute(ids, offsets, perm, M, E, top_k, workspace, s);
+}
+
+BI_API bi_status bi_moe_gate_up(const bi_bf16 *x, const int32_t *offsets, const int32_t *perm,
+                                const float *wts, const bi_bf16 *w13, bi_bf16 *act, int64_t M,
+                                int64_t H, int64_t E, int32_t top_k, int64_t I, void *workspace,
+                                size_t workspace_bytes, bi_stream_t stream) {
+  bi_status st = check_moe_dims(M, H, E, top_k, I);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(x && offsets && perm && wts && w13 && act && workspace, BI_ERR_INVALID_ARG,
+             "null pointer");
+  BI_REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(workspace, 256), BI_ERR_INVALID_ARG,
+             "x/w13 must be 16-byte and workspace 256-byte aligned");
+  BI_REQUIRE(workspace_bytes >= bi_moe_gate_up_workspace_bytes(M, H, top_k), BI_ERR_WORKSPACE,
+             "workspace too small");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t P = M * top_k;
+  st = launch_gather(x, perm, offsets, P, H, E, top_k, workspace, s);
+  if (st != BI_OK) return st;
+  return launch_gate_up(workspace, offsets, perm, wts, w13, act, P, H, E, top_k, I, s);
+}
+
+BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets, const int32_t *perm,
+                             const bi_bf16 *w2, float *contrib, int64_t M, int64_t H, int64_t E,
+                             int32_t top_k, int64_t I, bi_stream_t stream) {
+  bi_status st = check_moe_dims(M, H, E, top_k, I);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(act && offsets && perm && w2 && contrib, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(act, 16) && aligned(w2, 16), BI_ERR_INVALID_ARG,
+             "act/w2 must be 16-byte aligned");
+  return launch_down(act, offsets, perm, w2, contrib, M * top_k, H, E, top_k, I,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M, int64_t H,
+                                int32_t top_k, bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && H > 0 && H % 4 == 0, BI_ERR_INVALID_ARG, "bad sizes (H %% 4 == 0 needed)");
+  BI_REQUIRE(top_k >= 1 && top_k <= 16, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(contrib && out, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(contrib, 16) && aligned(out, 8), BI_ERR_INVALID_ARG,
+             "contrib must be 16-byte and out 8-byte aligned");
+  return launch_combine(contrib, out, M, H, top_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const float *wts,
+                                const bi_bf16 *w13, const bi_bf16 *w2, bi_bf16 *out, int64_t M,
+                                int64_t H, int64_t E, int32_t top_k, int64_t I, void *workspace,
+                                size_t workspace_bytes, bi_stream_t stream) {
+  bi_status st = check_moe_dims(M, H, E, top_k, I);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(x && ids && wts && w13 && w2 && out && workspace, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(w2, 16) && aligned(out, 8) &&
+                 aligned(workspace, 256),
+             BI_ERR_INVALID_ARG, "misaligned pointer (x/w13/w2 16 B, out 8 B, workspace 256 B)");
+  const MoeWorkspace L = moe_layout(M, H, E, top_k, I);
+  BI_REQUIRE(workspace_bytes >= L.total, BI_ERR_WORKSPACE, "workspace %zu < %zu bytes",
+             workspace_bytes, L.total);
+  char *ws = static_cast<char *>(workspace);
+  int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+  int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
+  void *xperm = ws + L.xperm;
+  void *act = ws + L.act;
+  float *contrib = reinterpret_cast<float *>(ws + L.contrib);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t P = M * top_k;
+  if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s)) != BI_OK) return st;
+  if ((st = launch_gather(x, perm, offsets, P, H, E, top_k, xperm, s)) != BI_OK) return st;
+  if ((st = launch_gate_up(xperm, offsets, perm, wts, w13, act, P, H, E, top_k, I, s)) != BI_OK)
+    return st;
+  if ((st = launch_down(act, offsets, perm, w2, contrib, P, H, E, top_k, I, s)) != BI_OK) return st;
+  return launch_combine(contrib, out, M, H, top_k, s);
+}
+
+}  // extern "C"

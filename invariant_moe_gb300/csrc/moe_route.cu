@@ -1,0 +1,221 @@
+// moe_route.cu -- token permutation by expert, row gather, and the top-k
+// combine of the batch-invariant fused-MoE path.
+//
+// Source: "Batch-invariance generation with vLLM fused-MoE backend at
+// improved performance", section "What's included" and the strict-review
+// summary (tokens grouped per expert for the grouped GEMMs; the top-k
+// contributions reduced with unit weights in a fixed `for t in range(topk)`
+// order).
+//
+// Permutation = stable grouping of the (token, slot) pairs by expert, in
+// three launches with integer arithmetic only:
+//   count   per 256-token block, per-expert pair counts (shared-memory
+//           counters: a count does not depend on the order of increments)
+//   scan    per expert, exclusive scan over blocks; exclusive scan over
+//           experts -> offsets
+//   scatter per block, one bit per (expert, token) in shared memory; the rank
+//           of a pair inside its expert and block is the popcount of the lower
+//           tokens' bits, so positions never depend on thread timing.
+// A pair is skipped (and BI_DEVERR_* recorded) when its expert id is outside
+// [0,E) or repeats an earlier slot of the same row; the other pairs keep
+// their positions.
+#include "bimoe_internal.cuh"
+
+namespace bimoe {
+
+constexpr int kTokBlock = 256;
+
+__device__ __forceinline__ bool pair_ok(const int32_t *row_ids, int t, int E, int *err) {
+  const int e = row_ids[t];
+  if (e < 0 || e >= E) {
+    report_error(err, BI_DEVERR_BAD_EXPERT_ID);
+    return false;
+  }
+  for (int u = 0; u < t; ++u)
+    if (row_ids[u] == e) {
+      report_error(err, BI_DEVERR_REPEATED_EXPERT);
+      return false;
+    }
+  return true;
+}
+
+__global__ void __launch_bounds__(kTokBlock) moe_count_kernel(const int32_t *__restrict__ ids,
+                                                              int M, int E, int top_k,
+                                                              int32_t *__restrict__ blkcnt,
+                                                              int *err) {
+  extern __shared__ int s_cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int m = blockIdx.x * kTokBlock + threadIdx.x;
+  if (m < M) {
+    const int32_t *r = ids + static_cast<size_t>(m) * top_k;
+    for (int t = 0; t < top_k; ++t)
+      if (pair_ok(r, t, E, err)) atomicAdd(&s_cnt[r[t]], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blkcnt[static_cast<size_t>(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// One CTA of 1024 threads.  blkoff[b,e] = offsets[e] + pairs of expert e in
+// blocks < b; offsets[E] = number of valid pairs.
+__global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restrict__ blkcnt,
+                                                        int nblk, int E,
+                                                        int32_t *__restrict__ blkoff,
+                                                        int32_t *__restrict__ offsets) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blkcnt[static_cast<size_t>(b) * E + e];
+      blkoff[static_cast<size_t>(b) * E + e] = run;
+      run += c;
+    }
+  }
+  // exclusive scan of run over e (warp shuffles, then warp totals)
+  const int lane = e & 31, w = e >> 5;
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = s_warp[lane];
+    int inc2 = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc2, off);
+      if (lane >= off) inc2 += u;
+    }
+    s_warp[lane] = inc2 - v;  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = s_warp[w] + incl - run;
+  if (e < E) {
+    offsets[e] = excl;
+    for (int b = 0; b < nblk; ++b) blkoff[static_cast<size_t>(b) * E + e] += excl;
+  }
+  if (e == E - 1) offsets[E] = excl + run;
+}
+
+__global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *__restrict__ ids,
+                                                                int M, int E, int top_k,
+                                                                const int32_t *__restrict__ blkoff,
+                                                                int32_t *__restrict__ perm) {
+  constexpr int W = kTokBlock / 32;
+  extern __shared__ uint32_t s_bits[];  // [E][W]
+  for (int i = threadIdx.x; i < E * W; i += blockDim.x) s_bits[i] = 0u;
+  __syncthreads();
+  const int lm = threadIdx.x;
+  const int m = blockIdx.x * kTokBlock + lm;
+  const int32_t *r = ids + static_cast<size_t>(m) * top_k;
+  if (m < M)
+    for (int t = 0; t < top_k; ++t)
+      if (pair_ok(r, t, E, nullptr)) atomicOr(&s_bits[r[t] * W + (lm >> 5)], 1u << (lm & 31));
+  __syncthreads();
+  if (m < M) {
+    for (int t = 0; t < top_k; ++t) {
+      if (!pair_ok(r, t, E, nullptr)) continue;
+      const int e = r[t];
+      int rank = 0;
+      for (int w = 0; w < (lm >> 5); ++w) rank += __popc(s_bits[e * W + w]);
+      rank += __popc(s_bits[e * W + (lm >> 5)] & ((1u << (lm & 31)) - 1u));
+      const int pos = blkoff[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+      perm[pos] = m * top_k + t;
+    }
+  }
+}
+
+// x_perm[p, :] = x[perm[p] / top_k, :] for p < offsets[E]; one warp per row,
+// 16-byte copies.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict__ x,
+                                                         const int32_t *__restrict__ perm,
+                                                         const int32_t *__restrict__ offsets,
+                                                         int E, int top_k, int row_vec,
+                                                         uint4 *__restrict__ xp) {
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= offsets[E]) return;
+  const int m = perm[p] / top_k;
+  const uint4 *src = x + static_cast<size_t>(m) * row_vec;
+  uint4 *dst = xp + static_cast<size_t>(p) * row_vec;
+  for (int c = lane; c < row_vec; c += 32) dst[c] = src[c];
+}
+
+// out[m, h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) + c[m,k-1,h]), fp32 adds in
+// slot order; four consecutive h per thread.
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
+                                                          __nv_bfloat16 *__restrict__ out, int M,
+                                                          int H4, int top_k) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(M) * H4) return;
+  const int64_t m = idx / H4;
+  const int h4 = static_cast<int>(idx % H4);
+  const float4 *c = contrib + m * top_k * H4 + h4;
+  float4 s = c[0];
+  for (int t = 1; t < top_k; ++t) {
+    const float4 v = c[static_cast<int64_t>(t) * H4];
+    s.x = __fadd_rn(s.x, v.x);
+    s.y = __fadd_rn(s.y, v.y);
+    s.z = __fadd_rn(s.z, v.z);
+    s.w = __fadd_rn(s.w, v.w);
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(s.z, s.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t *>(&lo);
+  pk.y = *reinterpret_cast<uint32_t *>(&hi);
+  *reinterpret_cast<uint2 *>(out + idx * 4) = pk;
+}
+
+// ------------------------------------------------------------------- host --
+size_t permute_scratch_bytes(int64_t M, int64_t E) {
+  const int64_t nblk = (M + kTokBlock - 1) / kTokBlock;
+  const size_t one = static_cast<size_t>(nblk * E) * sizeof(int32_t);
+  return 2 * ((one + 255) / 256 * 256);
+}
+
+bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, int64_t M,
+                         int64_t E, int32_t top_k, void *scratch, cudaStream_t stream) {
+  const int nblk = static_cast<int>((M + kTokBlock - 1) / kTokBlock);
+  const size_t one = (static_cast<size_t>(nblk) * E * sizeof(int32_t) + 255) / 256 * 256;
+  int32_t *blkcnt = static_cast<int32_t *>(scratch);
+  int32_t *blkoff = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + one);
+  int *err = device_error_word();
+  moe_count_kernel<<<nblk, kTokBlock, E * sizeof(int), stream>>>(ids, (int)M, (int)E, top_k,
+                                                                 blkcnt, err);
+  BI_CHECK_LAUNCH();
+  moe_scan_kernel<<<1, 1024, 0, stream>>>(blkcnt, nblk, (int)E, blkoff, offsets);
+  BI_CHECK_LAUNCH();
+  moe_scatter_kernel<<<nblk, kTokBlock, E * (kTokBlock / 32) * sizeof(uint32_t), stream>>>(
+      ids, (int)M, (int)E, top_k, blkoff, perm);
+  BI_CHECK_LAUNCH();
+  return BI_OK;
+}
+
+bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offsets, int64_t P,
+                        int64_t H, int64_t E, int32_t top_k, void *xp, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((P + 7) / 8);
+  moe_gather_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(x), perm, offsets,
+                                                (int)E, top_k, (int)(H / 8),
+                                                static_cast<uint4 *>(xp));
+  BI_CHECK_LAUNCH();
+  return BI_OK;
+}
+
+bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, int32_t top_k,
+                         cudaStream_t stream) {
+  const int64_t total = M * (H / 4);
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+  moe_combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(contrib),
+                                                 static_cast<__nv_bfloat16 *>(out), (int)M,
+                                                 (int)(H / 4), top_k);
+  BI_CHECK_LAUNCH();
+  return BI_OK;
+}
+
+}  // namespace bimoe

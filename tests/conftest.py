@@ -18,3 +18,28 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    """cuda:0 with the CUDA library built and loaded (gpu tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("gpu test run without a CUDA device")
+    from invariant_moe_gb300 import _build
+    _build.build()
+    import invariant_moe_gb300 as bm
+    bm.load_library()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error(request):
+    """Every gpu test must leave the device error word clear."""
+    yield
+    if request.node.get_closest_marker("gpu") is not None and "cuda" in request.fixturenames:
+        import invariant_moe_gb300 as bm
+        code = bm.device_error()
+        expected = getattr(request.node, "expected_device_error", 0)
+        assert code == expected, f"device error word = {code}"

@@ -1,0 +1,85 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/bimoe.h declares, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_moe_gb300 import _build
+    _build.build()
+    import invariant_moe_gb300 as bm
+    return bm.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "bimoe.h")).read()
+    return sorted(set(re.findall(r"BI_API\s+[\w\s\*]+?\b(bi_\w+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    import invariant_moe_gb300 as bm
+    assert declared_symbols() == sorted(bm.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.bi_status_str(0) == b"BI_OK"
+    assert lib.bi_status_str(3) == b"BI_ERR_WORKSPACE"
+    assert lib.bi_version().startswith(b"bimoe")
+
+
+def test_workspace_sizes(lib):
+    qwen = lib.bi_moe_workspace_bytes(4096, 2048, 128, 8, 768)
+    assert qwen % 256 == 0
+    P = 4096 * 8
+    # gathered rows + activations + fp32 contributions dominate
+    assert qwen >= P * (2048 * 2 + 768 * 2 + 2048 * 4)
+    assert lib.bi_moe_workspace_bytes(4096, 2000, 128, 8, 768) == 0   # H % 128 != 0
+    assert lib.bi_moe_workspace_bytes(16, 2048, 8, 9, 768) == 0       # top_k > E
+    assert lib.bi_moe_workspace_bytes(0, 2048, 128, 8, 768) > 0
+
+
+def test_host_side_rejections(lib):
+    """Argument checks run on the host and never touch the GPU."""
+    nul = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(0x10000)        # never dereferenced: rejected first
+    odd = ctypes.c_void_p(0x10004)         # not 16-byte aligned
+    # K not a multiple of 128
+    assert lib.bi_router_gemm(fake, fake, nul, fake, 4, 100, 256, nul) == 2
+    # misaligned x
+    assert lib.bi_router_gemm(odd, fake, nul, fake, 4, 128, 256, nul) == 1
+    # null x with M > 0
+    assert lib.bi_router_gemm(nul, fake, nul, fake, 4, 128, 256, nul) == 1
+    assert b"null" in lib.bi_last_error_message()
+    # M == 0 is a no-op
+    assert lib.bi_router_gemm(nul, nul, nul, nul, 0, 128, 256, nul) == 0
+    # top_k > E, E too large
+    assert lib.bi_topk(fake, fake, fake, nul, 4, 8, 9, nul) == 1
+    assert lib.bi_topk(fake, fake, fake, nul, 4, 600, 8, nul) == 2
+    # MoE: workspace too small, unsupported H
+    assert lib.bi_moe_forward(fake, fake, fake, fake, fake, fake, 4, 2048, 128, 8, 768,
+                              fake, 1024, nul) == 3
+    assert lib.bi_moe_forward(fake, fake, fake, fake, fake, fake, 4, 2000, 128, 8, 768,
+                              fake, 1 << 30, nul) == 2
+    assert lib.bi_moe_forward(nul, nul, nul, nul, nul, nul, 0, 2048, 128, 8, 768,
+                              nul, 0, nul) == 0
+    assert lib.bi_moe_combine(fake, fake, 4, 2046, 8, nul) == 1
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import invariant_moe_gb300 as bm
+    with pytest.raises(ValueError):
+        bm.bi_router_gemm(torch.zeros(2, 128), torch.zeros(4, 128))

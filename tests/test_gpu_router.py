@@ -1,0 +1,156 @@
+"""Router GEMM on the GPU: parity with the fp64 oracle, bitwise row
+invariance across batch sizes and schedules, and the negative control.
+
+Tolerance: the GateLinear page's bar, |y - r| <= 2e-3 + 1e-4 |r| per element
+(section "Tests" of "[BI][DSv4] Batch-invariant GateLinear router with fp32
+persistent matmul")."""
+import numpy as np
+import pytest
+import torch
+
+from tests import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-4
+
+
+@pytest.fixture(scope="module")
+def inputs():
+    return syn.router_inputs()  # x[4096,4096], W[256,4096], b[256]
+
+
+@pytest.fixture(scope="module")
+def dev_inputs(inputs, cuda):
+    return inputs.x.to(cuda), inputs.w.to(cuda), inputs.b.to(cuda)
+
+
+def run(x, w, b, M, schedule=0):
+    import invariant_moe_gb300 as bm
+    y = bm.bi_router_gemm(x[:M].contiguous(), w, b, schedule=schedule)
+    torch.cuda.synchronize()
+    return y
+
+
+def check_parity(y, r):
+    err = np.abs(y - r)
+    ok = err <= ATOL + RTOL * np.abs(r)
+    assert ok.all(), f"{(~ok).sum()} elements outside tolerance, max err {err.max():.3e}"
+    return err.max()
+
+
+def test_parity_config1(oracle_mod, inputs, dev_inputs):
+    x, w, b = dev_inputs
+    for M in (1, 8, 15, 16, 17, 32, 33, 64):
+        y = run(x, w, b, M).cpu().numpy()
+        r = oracle_mod.router(inputs.x[:M].numpy(), inputs.w.numpy(), inputs.b.numpy())
+        e = check_parity(y, r)
+        assert e < 1e-4  # fp32 recipe: far inside the bar
+
+
+def test_row_bits_invariant_over_M(dev_inputs):
+    x, w, b = dev_inputs
+    full = run(x, w, b, 4096)
+    for M in syn.batch_sizes(4096) + [2, 3, 4, 5, 6, 7, 100, 383, 384, 385, 1000]:
+        y = run(x, w, b, M)
+        assert torch.equal(y, full[:M]), f"M={M}: rows differ from the M=4096 run"
+
+
+@pytest.mark.parametrize("M", [1, 5, 9, 64, 130, 700])
+def test_forced_schedules_agree(dev_inputs, M):
+    x, w, b = dev_inputs
+    ys = [run(x, w, b, M, schedule=s) for s in (1, 2, 3)]
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+
+
+def test_same_row_at_any_position(dev_inputs):
+    """A row's bits do not depend on its position or its neighbours."""
+    x, w, b = dev_inputs
+    g = syn.gen(77)
+    target = x[123:124]
+    ref = run(target, w, b, 1)
+    for B in (7, 64, 513, 2048):
+        xb = x[torch.randperm(4096, generator=g)[:B].to(x.device)].clone()
+        pos = int(torch.randint(0, B, (1,), generator=g))
+        xb[pos] = target[0]
+        y = run(xb, w, b, B)
+        assert torch.equal(y[pos], ref[0]), f"B={B} pos={pos}"
+
+
+def test_negative_control_flips_bits(dev_inputs):
+    """The M-dependent split must change row bits across its switch (M=16 vs
+    17); otherwise the invariance tests above could not fail."""
+    import invariant_moe_gb300 as bm
+    x, w, b = dev_inputs
+    y16 = bm.bi_router_gemm_splitk_negctl(x[:16].contiguous(), w, b)
+    y17 = bm.bi_router_gemm_splitk_negctl(x[:17].contiguous(), w, b)
+    torch.cuda.synchronize()
+    flips = (y16 != y17[:16]).sum().item()
+    assert flips > 0
+    # while the batch-invariant path keeps them
+    assert torch.equal(run(x, w, b, 16), run(x, w, b, 17)[:16])
+
+
+def test_exact_integer_case(oracle_mod, cuda):
+    """x in multiples of 1/8, W and b in multiples of 1/64: every partial sum
+    is exact in fp32, so GPU == oracle == integer sum, bit for bit."""
+    g = syn.gen(3)
+    M, K, N = 37, 4096, 256
+    xi = torch.randint(-16, 17, (M, K), generator=g)
+    wi = torch.randint(-64, 65, (N, K), generator=g)
+    bi = torch.randint(-64, 65, (N,), generator=g)
+    x, w, b = xi.float() / 8, wi.float() / 64, bi.float() / 64
+    for s in (1, 2, 3):
+        y = run(x.to(cuda), w.to(cuda), b.to(cuda), M, schedule=s).cpu().numpy()
+        r = oracle_mod.router(x.numpy(), w.numpy(), b.numpy())
+        assert np.array_equal(y.astype(np.float64), r)
+
+
+def test_one_hot_rows(cuda):
+    K, N = 4096, 256
+    w = syn.normal((N, K), 1 / 64, 9).to(cuda)
+    b = syn.normal((N,), 0.01, 10).to(cuda)
+    x = torch.zeros(3, K, device=cuda)
+    x[0, 0] = 1
+    x[1, 1000] = 1
+    x[2, K - 1] = 1
+    y = run(x, w, b, 3)
+    for i, j in enumerate((0, 1000, K - 1)):
+        assert torch.equal(y[i], w[:, j] + b)
+
+
+def test_no_bias_and_other_shapes(oracle_mod, cuda):
+    """Qwen-shaped router (K=2048, N=128), a ragged N, and no bias."""
+    for (M, K, N) in ((50, 2048, 128), (9, 1024, 200), (600, 2048, 100)):
+        x = syn.normal((M, K), 1.0, 21)
+        w = syn.normal((N, K), K ** -0.5, 22)
+        y = run(x.to(cuda), w.to(cuda), None, M).cpu().numpy()
+        r = oracle_mod.router(x.numpy(), w.numpy(), None)
+        check_parity(y, r)
+        ys = [run(x.to(cuda), w.to(cuda), None, M, schedule=s) for s in (1, 2, 3)]
+        assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
+def test_full_size_sampled_parity(oracle_mod, inputs, dev_inputs):
+    """M=4096 (the largest batch) on sampled rows the oracle can afford."""
+    x, w, b = dev_inputs
+    y = run(x, w, b, 4096).cpu().numpy()
+    rows = torch.randperm(4096, generator=syn.gen(5))[:48].numpy()
+    r = oracle_mod.router(inputs.x[rows].numpy(), inputs.w.numpy(), inputs.b.numpy())
+    check_parity(y[rows], r)
+
+
+def test_empty_batch(cuda):
+    import invariant_moe_gb300 as bm
+    x = torch.empty(0, 4096, device=cuda)
+    w = torch.zeros(256, 4096, device=cuda)
+    assert bm.bi_router_gemm(x, w).shape == (0, 256)
+
+
+def test_bf16_cast_exact(cuda):
+    import invariant_moe_gb300 as bm
+    x = syn.normal((333, 2048), 1.0, 4, torch.bfloat16).to(cuda)
+    y = bm.bi_cast_bf16_to_f32(x)
+    assert torch.equal(y, x.float())
+    xo = x.flatten()[3:3 + 1001]  # misaligned, ragged
+    assert torch.equal(bm.bi_cast_bf16_to_f32(xo), xo.float())
