@@ -73,8 +73,8 @@ def router_tie_inputs(M=4096, K=4096, N=256, n_groups=16, copies=3, frac=0.3, se
     w = base.w.clone()
     b = base.b.clone()
     for i in range(n_groups):
-        w[dst[i]] = w[src[i]]
-        b[dst[i]] = b[src[i]]
+        w[dst[i]] = w[src[i]].clone()
+        b[dst[i]] = b[src[i]].clone()
     rows = torch.rand(M, generator=g) < frac
     x = base.x.clone()
     x[rows] = torch.clamp(torch.round(x[rows] * 8.0) / 8.0, -4.0, 4.0)
