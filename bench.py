@@ -202,7 +202,7 @@ def run_ours(args, rank, world, local):
             ev["down"].append((e1, e2))
         bm.bi_moe_combine(contrib, M, k, out=out)
 
-    launches_per_step = 1 + 1 + 1 + 3 + 2 + 1 + 1  # cast router topk permute(3) gather+gateup down combine
+    launches_per_step = 1 + 1 + 1 + 3 + 2 + 1 + 1  # cast router topk permute(3) gather+gate/up down combine
 
     for _ in range(args.warmup):
         step()
@@ -293,9 +293,12 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def router_sweep(dev):
-    """Device us per router call (DSv4 router: K=4096, N=256, fp32) vs M:
-    warm = back-to-back calls; cold = L2 flushed (256 MB write) before each."""
+def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
+    """Device us per router call (DSv4 router: K=4096, N=256, fp32, bias) vs M,
+    from CUDA-graph replays so host launch cost is excluded.
+    warm: a graph of 20 back-to-back calls (W stays in L2);
+    cold: a graph of 20 x (256 MB L2-flushing write, call) minus a graph of
+    the 20 flushes alone."""
     import torch
 
     import invariant_moe_gb300 as bm
@@ -303,32 +306,55 @@ def router_sweep(dev):
     inp = syn.router_inputs()
     x, w, b = inp.x.to(dev), inp.w.to(dev), inp.b.to(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    n = 20
+
+    def graph_time(fn, reps=5):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    def flushes():
+        for _ in range(n):
+            flush.fill_(1.0)
+
+    t_flush = graph_time(flushes)
     res = {}
-    for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096):
+    for M in Ms:
         xm = x[:M].contiguous()
         y = torch.empty(M, 256, dtype=torch.float32, device=dev)
-        for _ in range(5):
-            bm.bi_router_gemm(xm, w, b, out=y)
-        n = 50
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(n):
-            bm.bi_router_gemm(xm, w, b, out=y)
-        e1.record()
-        torch.cuda.synchronize()
-        warm = e0.elapsed_time(e1) / n * 1e3
-        cold = []
-        for _ in range(10):
-            flush.fill_(1.0)
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record()
-            bm.bi_router_gemm(xm, w, b, out=y)
-            c1.record()
-            torch.cuda.synchronize()
-            cold.append(c0.elapsed_time(c1) * 1e3)
-        res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(statistics.median(cold), 2)}
+
+        def calls():
+            for _ in range(n):
+                bm.bi_router_gemm(xm, w, b, out=y, stream=stream)
+
+        def cold_calls():
+            for _ in range(n):
+                flush.fill_(1.0)
+                bm.bi_router_gemm(xm, w, b, out=y, stream=stream)
+
+        warm = graph_time(calls) / n
+        cold = (graph_time(cold_calls) - t_flush) / n
+        flops = 2.0 * M * 4096 * 256
+        bytes_ = 4.0 * (256 * 4096 + 256 + M * (4096 + 256))
+        res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(cold, 2),
+                       "cold_hbm_frac": round(bytes_ / (cold * 1e-6) / 1e9 / measured_peaks()[0], 3),
+                       "warm_tflops": round(flops / (warm * 1e-6) / 1e12, 2)}
     return res
 
 
@@ -402,10 +428,17 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router-sweep", action="store_true",
+                    help="only print the router device-time sweep (DSv4 router shape)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_env()
+    if args.router_sweep:
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps({"router_us_vs_M": router_sweep(torch.device("cuda", local))}), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

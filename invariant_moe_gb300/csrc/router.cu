@@ -15,52 +15,83 @@
 // contraction or reassociation freedom.  Schedules differ only in which
 // thread evaluates which p_s and in tile sizes; they are chosen from M for
 // speed:
-//   rows    (M <= 8)      one warp per weight row, lanes own slices: streams
-//                         W once at HBM rate for decode batches
-//   sliced  (8 < M < 384) 8x32 output tile per CTA, one warp per slice, the
+//   rows    (M <= 16)     one warp per weight row and up to 4 token rows,
+//                         lanes own slices: streams W for decode batches
+//   sliced  (16 < M < 384) 8x16 output tile per CTA, one warp per slice, the
 //                         partials combined in slice order through smem
-//   tiled   (M >= 384)    64x64 register-tiled FFMA kernel, 8x8 outputs per
-//                         thread, slices summed into a running register sum
+//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps spanning N,
+//                         TMR x 4 outputs per thread, cp.async pipeline,
+//                         slices summed into a running register sum
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
 
 constexpr int kSlice = 128;
 
+// Shared-memory staging used by every schedule: a slice (128 fp32 = 512 B)
+// of a row is copied with 32 coalesced 16-byte cp.async pieces into a padded
+// row (132 floats), so that lanes walking different slices / rows along k
+// read distinct banks.
+constexpr int kSlicePad = kSlice + 4;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // -------------------------------------------------------------------- rows --
-// Lane l of a warp serves weight row n = n0 + l / LPR and slices
-// s = l % LPR, l % LPR + LPR, ...; MR token rows share each W load.
+// One warp per weight row n and MR token rows; lane l owns slice l of each
+// group of 32 slices.  The W row slices and the MR x row slices of a group
+// are staged (coalesced) in shared memory, then every lane runs its MR chains
+// from there; the S partials meet in shared memory and lane i < MR adds them
+// in slice order.
 template <int MR>
 __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict__ x,
                                                          const float *__restrict__ w,
                                                          const float *__restrict__ bias,
                                                          float *__restrict__ y, int M, int K,
-                                                         int N, int LPR) {
-  extern __shared__ float part[];  // [rows_per_warp][MR][S]
+                                                         int N) {
+  extern __shared__ __align__(16) float sm[];
+  float *ws = sm;                              // [32][kSlicePad]
+  float *xs = sm + 32 * kSlicePad;             // [MR][32][kSlicePad]
+  float *part = xs + MR * 32 * kSlicePad;      // [MR][S]
   const int lane = threadIdx.x;
   const int S = K / kSlice;
-  const int rpw = 32 / LPR;
-  const int r = lane / LPR;
-  const int n = blockIdx.x * rpw + r;
+  const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
-  if (n < N) {
-    const float4 *w4 = reinterpret_cast<const float4 *>(w + static_cast<size_t>(n) * K);
-    const float4 *x4[MR];
+  const float *wrow = w + static_cast<size_t>(n) * K;
+  const float *xrow[MR];
 #pragma unroll
-    for (int i = 0; i < MR; ++i) {
-      const int m = min(m0 + i, M - 1);
-      x4[i] = reinterpret_cast<const float4 *>(x + static_cast<size_t>(m) * K);
+  for (int i = 0; i < MR; ++i) xrow[i] = x + static_cast<size_t>(min(m0 + i, M - 1)) * K;
+
+  for (int g0 = 0; g0 < S; g0 += 32) {
+    const int ns = min(32, S - g0);
+    __syncwarp();
+    for (int sl = 0; sl < ns; ++sl) {
+      const int k0 = (g0 + sl) * kSlice + lane * 4;
+      cp_async16(smem_u32(ws + sl * kSlicePad + lane * 4), wrow + k0);
+#pragma unroll
+      for (int i = 0; i < MR; ++i)
+        cp_async16(smem_u32(xs + (i * 32 + sl) * kSlicePad + lane * 4), xrow[i] + k0);
     }
-    for (int s = lane % LPR; s < S; s += LPR) {
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    if (lane < ns) {
       float p[MR];
 #pragma unroll
       for (int i = 0; i < MR; ++i) p[i] = 0.0f;
+      const float *wl = ws + lane * kSlicePad;
 #pragma unroll 8
-      for (int j = 0; j < kSlice / 4; ++j) {
-        const float4 wv = __ldg(w4 + s * (kSlice / 4) + j);
+      for (int k = 0; k < kSlice; k += 4) {
+        const float4 wv = *reinterpret_cast<const float4 *>(wl + k);
 #pragma unroll
         for (int i = 0; i < MR; ++i) {
-          const float4 xv = __ldg(x4[i] + s * (kSlice / 4) + j);
+          const float4 xv = *reinterpret_cast<const float4 *>(xs + (i * 32 + lane) * kSlicePad + k);
           p[i] = __fmaf_rn(xv.x, wv.x, p[i]);
           p[i] = __fmaf_rn(xv.y, wv.y, p[i]);
           p[i] = __fmaf_rn(xv.z, wv.z, p[i]);
@@ -68,61 +99,79 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
         }
       }
 #pragma unroll
-      for (int i = 0; i < MR; ++i) part[(r * MR + i) * S + s] = p[i];
+      for (int i = 0; i < MR; ++i) part[i * S + g0 + lane] = p[i];
     }
   }
   __syncwarp();
-  for (int c = lane; c < rpw * MR; c += 32) {
-    const int rr = c / MR, i = c % MR;
-    const int nn = blockIdx.x * rpw + rr;
-    const int m = m0 + i;
-    if (nn < N && m < M) {
-      float acc = 0.0f;
-      for (int s = 0; s < S; ++s) acc = __fadd_rn(acc, part[c * S + s]);
-      if (bias) acc = __fadd_rn(acc, bias[nn]);
-      y[static_cast<size_t>(m) * N + nn] = acc;
-    }
+  if (lane < MR && m0 + lane < M) {
+    float acc = 0.0f;
+    for (int sl = 0; sl < S; ++sl) acc = __fadd_rn(acc, part[lane * S + sl]);
+    if (bias) acc = __fadd_rn(acc, bias[n]);
+    y[static_cast<size_t>(m0 + lane) * N + n] = acc;
   }
 }
 
 // ------------------------------------------------------------------ sliced --
-// CTA = G warps, output tile 8 (m) x 32 (n): lane l owns column n0 + l and
-// the 8 rows.  In round r warp g evaluates slice s = r*G + g for the whole
-// tile; partials meet in shared memory and thread (i, l) adds them to its
-// running sum in slice order.
-template <int G>
-__global__ void __launch_bounds__(32 * G) router_sliced_kernel(const float *__restrict__ x,
-                                                               const float *__restrict__ w,
-                                                               const float *__restrict__ bias,
-                                                               float *__restrict__ y, int M,
-                                                               int K, int N) {
-  __shared__ float part[G][8][32];
-  const int lane = threadIdx.x & 31;
-  const int g = threadIdx.x >> 5;
+// CTA = 8 warps, output tile 8 (m) x 16 (n).  K is processed in rounds of 8
+// slices; in a round warp g evaluates slice 8r+g for the whole tile (lane l:
+// column l % 16, rows 4 (l / 16) .. +3).  Each round's 8 x rows and 16 W rows
+// (8 slices each) are staged by cp.async into a double-buffered shared tile
+// while the previous round computes.  Partials meet in shared memory and
+// thread (i, j) adds them to its running sum in slice order.
+constexpr int kSlMT = 8, kSlNT = 16, kSlG = 8;
+constexpr int kSlRow = kSlG * kSlicePad + 4;  // floats per staged row (stride = 4 mod 32)
+constexpr int kSlStage = (kSlMT + kSlNT) * kSlRow;
+
+__global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restrict__ x,
+                                                            const float *__restrict__ w,
+                                                            const float *__restrict__ bias,
+                                                            float *__restrict__ y, int M, int K,
+                                                            int N) {
+  extern __shared__ __align__(16) float sm[];
+  float *stage_buf = sm;                         // [2][MT + NT][kSlRow]
+  float *part = sm + 2 * kSlStage;               // [G][MT][NT]
+  const int tid = threadIdx.x;
+  const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
-  const int n0 = blockIdx.x * 32;
-  const int m0 = blockIdx.y * 8;
-  const int nl = min(n0 + lane, N - 1);
-  const float4 *w4 = reinterpret_cast<const float4 *>(w + static_cast<size_t>(nl) * K);
-  const float4 *x4[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    x4[i] = reinterpret_cast<const float4 *>(x + static_cast<size_t>(min(m0 + i, M - 1)) * K);
-  // combine role: thread t owns output (m0 + t/32, n0 + t%32) for t < 256
-  const int ci = threadIdx.x >> 5, cl = threadIdx.x & 31;
+  const int rounds = (S + kSlG - 1) / kSlG;
+  const int m0 = blockIdx.y * kSlMT, n0 = blockIdx.x * kSlNT;
+
+  auto load_round = [&](int rd, int buf) {
+    float *dst = stage_buf + buf * kSlStage;
+    // (MT + NT) rows x G slices x 32 pieces of 16 B
+    for (int q = tid; q < (kSlMT + kSlNT) * kSlG * 32; q += 256) {
+      const int piece = q & 31, sl = (q >> 5) % kSlG, row = (q >> 5) / kSlG;
+      const int s = rd * kSlG + sl;
+      if (s >= S) continue;
+      const float *src = row < kSlMT ? x + static_cast<size_t>(min(m0 + row, M - 1)) * K
+                                     : w + static_cast<size_t>(min(n0 + row - kSlMT, N - 1)) * K;
+      cp_async16(smem_u32(dst + row * kSlRow + sl * kSlicePad + piece * 4),
+                 src + s * kSlice + piece * 4);
+    }
+  };
+
+  const int cn = lane & 15, cm = (lane >> 4) * 4;  // compute role
+  const int oi = tid >> 4, oj = tid & 15;          // combine role (tid < 128)
   float acc = 0.0f;
-  for (int base = 0; base < S; base += G) {
-    const int s = base + g;
+  load_round(0, 0);
+  cp_async_commit();
+  for (int rd = 0; rd < rounds; ++rd) {
+    if (rd + 1 < rounds) load_round(rd + 1, (rd + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const float *buf = stage_buf + (rd & 1) * kSlStage;
+    const int s = rd * kSlG + g;
     if (s < S) {
-      float p[8];
+      float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const float *wl = buf + (kSlMT + cn) * kSlRow + g * kSlicePad;
+      const float *xl = buf + cm * kSlRow + g * kSlicePad;
+#pragma unroll 8
+      for (int k = 0; k < kSlice; k += 4) {
+        const float4 wv = *reinterpret_cast<const float4 *>(wl + k);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = 0.0f;
-#pragma unroll 4
-      for (int j = 0; j < kSlice / 4; ++j) {
-        const float4 wv = __ldg(w4 + s * (kSlice / 4) + j);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 xv = __ldg(x4[i] + s * (kSlice / 4) + j);
+        for (int i = 0; i < 4; ++i) {
+          const float4 xv = *reinterpret_cast<const float4 *>(xl + i * kSlRow + k);
           p[i] = __fmaf_rn(xv.x, wv.x, p[i]);
           p[i] = __fmaf_rn(xv.y, wv.y, p[i]);
           p[i] = __fmaf_rn(xv.z, wv.z, p[i]);
@@ -130,17 +179,17 @@ __global__ void __launch_bounds__(32 * G) router_sliced_kernel(const float *__re
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) part[g][i][lane] = p[i];
+      for (int i = 0; i < 4; ++i) part[(g * kSlMT + cm + i) * kSlNT + cn] = p[i];
     }
     __syncthreads();
-    if (threadIdx.x < 256) {
-      const int ng = min(G, S - base);
-      for (int gg = 0; gg < ng; ++gg) acc = __fadd_rn(acc, part[gg][ci][cl]);
+    if (tid < kSlMT * kSlNT) {
+      const int ng = min(kSlG, S - rd * kSlG);
+      for (int gg = 0; gg < ng; ++gg) acc = __fadd_rn(acc, part[(gg * kSlMT + oi) * kSlNT + oj]);
     }
-    __syncthreads();
   }
-  if (threadIdx.x < 256) {
-    const int m = m0 + ci, n = n0 + cl;
+  cp_async_wait<0>();
+  if (tid < kSlMT * kSlNT) {
+    const int m = m0 + oi, n = n0 + oj;
     if (m < M && n < N) {
       if (bias) acc = __fadd_rn(acc, bias[n]);
       y[static_cast<size_t>(m) * N + n] = acc;
@@ -149,120 +198,183 @@ __global__ void __launch_bounds__(32 * G) router_sliced_kernel(const float *__re
 }
 
 // ------------------------------------------------------------------- tiled --
-// 64x64 output tile, 64 threads in an 8x8 grid, 8x8 outputs per thread (rows
-// tr*4+{0..3} and 32+tr*4+{0..3}, same for columns).  K advances in chunks of
-// 16 through double-buffered, transposed shared-memory tiles; at every
-// 128-element slice boundary the chain value is added to the running sum and
-// restarted from +0.0f.
-constexpr int kTBM = 64, kTBN = 64, kTBK = 16, kTPad = 4;
+// Register-tiled FFMA kernel for large M.  A CTA is 8 warps arranged as RB
+// row blocks x CB column blocks (CB = 32-column blocks covering N, at most
+// 8); thread (r, c) of a warp owns rows base + 4i + r (i < TMR) and columns
+// base + 8j + c (j < 4).  K advances in chunks of 32 through a 3-stage
+// cp.async ring of [rows][32 + 4] fp32 tiles (k contiguous, padded so the
+// 16-byte loads along k are bank-conflict free); each chunk is consumed four
+// k at a time, each output's chain in increasing k.  Every 128 k (4 chunks)
+// the chain value is added to the running sum and restarted from +0.0f.
+// TMR is chosen on the host so the grid fills the SMs in one wave.
+constexpr int kTBK = 32;              // k per chunk
+constexpr int kTLd = kTBK + 4;        // padded smem row length (floats)
+constexpr int kTStages = 3;
 
-__global__ void __launch_bounds__(64) router_tiled_kernel(const float *__restrict__ x,
-                                                          const float *__restrict__ w,
-                                                          const float *__restrict__ bias,
-                                                          float *__restrict__ y, int M, int K,
-                                                          int N) {
-  __shared__ __align__(16) float xs[2][kTBK][kTBM + kTPad];
-  __shared__ __align__(16) float ws[2][kTBK][kTBN + kTPad];
+template <int TMR, int CB>
+__global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restrict__ x,
+                                                           const float *__restrict__ w,
+                                                           const float *__restrict__ bias,
+                                                           float *__restrict__ y, int M, int K,
+                                                           int N) {
+  constexpr int RB = 8 / CB;                 // row blocks per CTA
+  constexpr int BM = RB * 4 * TMR;           // rows per CTA
+  constexpr int BN = CB * 32;                // columns per CTA
+  constexpr int XS = BM * kTLd, WS = BN * kTLd;  // floats per stage
+  extern __shared__ __align__(16) float smem_f[];
+  float *xs = smem_f;                        // [kTStages][BM][kTLd]
+  float *ws = smem_f + kTStages * XS;        // [kTStages][BN][kTLd]
+
   const int tid = threadIdx.x;
-  const int tr = tid >> 3, tc = tid & 7;
-  const int m0 = blockIdx.y * kTBM, n0 = blockIdx.x * kTBN;
-  const float4 *xg = reinterpret_cast<const float4 *>(
-      x + static_cast<size_t>(min(m0 + tid, M - 1)) * K);
-  const float4 *wg = reinterpret_cast<const float4 *>(
-      w + static_cast<size_t>(min(n0 + tid, N - 1)) * K);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int rb = warp / CB, cb = warp % CB;
+  const int r = lane >> 3, c = lane & 7;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
 
-  float p[8][8], acc[8][8];
+  // global -> shared copy of one chunk (16-byte pieces; rows past M / N read
+  // a clamped valid row and are never stored)
+  auto load_chunk = [&](int chunk, int stage) {
+    const int k0 = chunk * kTBK;
+    for (int q = tid; q < (BM + BN) * (kTBK / 4); q += 256) {
+      const int row = q / (kTBK / 4), piece = q % (kTBK / 4);
+      if (row < BM) {
+        const int gm = min(m0 + row, M - 1);
+        cp_async16(smem_u32(xs + stage * XS + row * kTLd + piece * 4),
+                   x + static_cast<size_t>(gm) * K + k0 + piece * 4);
+      } else {
+        const int wr = row - BM;
+        const int gn = min(n0 + wr, N - 1);
+        cp_async16(smem_u32(ws + stage * WS + wr * kTLd + piece * 4),
+                   w + static_cast<size_t>(gn) * K + k0 + piece * 4);
+      }
+    }
+  };
+
+  float p[TMR][4], acc[TMR][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < TMR; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       p[i][j] = 0.0f;
       acc[i][j] = 0.0f;
     }
 
-  float4 xr[4], wr[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    xr[q] = __ldg(xg + q);
-    wr[q] = __ldg(wg + q);
-  }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    xs[0][4 * q + 0][tid] = xr[q].x;
-    xs[0][4 * q + 1][tid] = xr[q].y;
-    xs[0][4 * q + 2][tid] = xr[q].z;
-    xs[0][4 * q + 3][tid] = xr[q].w;
-    ws[0][4 * q + 0][tid] = wr[q].x;
-    ws[0][4 * q + 1][tid] = wr[q].y;
-    ws[0][4 * q + 2][tid] = wr[q].z;
-    ws[0][4 * q + 3][tid] = wr[q].w;
-  }
-  __syncthreads();
-
   const int nchunks = K / kTBK;
-  constexpr int kChunksPerSlice = kSlice / kTBK;
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    const bool more = (c + 1) < nchunks;
-    if (more) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xr[q] = __ldg(xg + (c + 1) * (kTBK / 4) + q);
-        wr[q] = __ldg(wg + (c + 1) * (kTBK / 4) + q);
-      }
+  for (int s = 0; s < kTStages - 1; ++s) {
+    if (s < nchunks) load_chunk(s, s);
+    cp_async_commit();
+  }
+  const int xrow0 = rb * 4 * TMR + r;  // + 4i
+  const int wrow0 = cb * 32 + c;       // + 8j
+  for (int ch = 0; ch < nchunks; ++ch) {
+    cp_async_wait<kTStages - 2>();
+    __syncthreads();
+    if (ch + kTStages - 1 < nchunks) load_chunk(ch + kTStages - 1, (ch + kTStages - 1) % kTStages);
+    cp_async_commit();
+    const float *xb = xs + (ch % kTStages) * XS;
+    const float *wb = ws + (ch % kTStages) * WS;
+#pragma unroll
+    for (int kk = 0; kk < kTBK; kk += 4) {
+      float4 xv[TMR], wv[4];
+#pragma unroll
+      for (int i = 0; i < TMR; ++i)
+        xv[i] = *reinterpret_cast<const float4 *>(xb + (xrow0 + 4 * i) * kTLd + kk);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        wv[j] = *reinterpret_cast<const float4 *>(wb + (wrow0 + 8 * j) * kTLd + kk);
+#pragma unroll
+      for (int i = 0; i < TMR; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          p[i][j] = __fmaf_rn(xv[i].x, wv[j].x, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].y, wv[j].y, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].z, wv[j].z, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].w, wv[j].w, p[i][j]);
+        }
     }
+    if ((ch + 1) % (kSlice / kTBK) == 0) {
 #pragma unroll
-    for (int k = 0; k < kTBK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&xs[buf][k][tr * 4]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&xs[buf][k][32 + tr * 4]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&ws[buf][k][tc * 4]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&ws[buf][k][32 + tc * 4]);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      for (int i = 0; i < TMR; ++i)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) p[i][j] = __fmaf_rn(a[i], b[j], p[i][j]);
-    }
-    if ((c + 1) % kChunksPerSlice == 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           acc[i][j] = __fadd_rn(acc[i][j], p[i][j]);
           p[i][j] = 0.0f;
         }
     }
-    if (more) {
-      const int nb = buf ^ 1;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[nb][4 * q + 0][tid] = xr[q].x;
-        xs[nb][4 * q + 1][tid] = xr[q].y;
-        xs[nb][4 * q + 2][tid] = xr[q].z;
-        xs[nb][4 * q + 3][tid] = xr[q].w;
-        ws[nb][4 * q + 0][tid] = wr[q].x;
-        ws[nb][4 * q + 1][tid] = wr[q].y;
-        ws[nb][4 * q + 2][tid] = wr[q].z;
-        ws[nb][4 * q + 3][tid] = wr[q].w;
-      }
-    }
-    __syncthreads();
   }
+  cp_async_wait<0>();
 
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0 + (i < 4 ? tr * 4 + i : 32 + tr * 4 + (i - 4));
+  for (int i = 0; i < TMR; ++i) {
+    const int m = m0 + xrow0 + 4 * i;
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int n = n0 + (j < 4 ? tc * 4 + j : 32 + tc * 4 + (j - 4));
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + wrow0 + 8 * j;
       if (n >= N) continue;
       float v = acc[i][j];
       if (bias) v = __fadd_rn(v, bias[n]);
       y[static_cast<size_t>(m) * N + n] = v;
     }
   }
+}
+
+template <int TMR, int CB>
+static bi_status launch_tiled_t(const float *x, const float *w, const float *b, float *y, int64_t M,
+                                int64_t K, int64_t N, cudaStream_t stream) {
+  constexpr int RB = 8 / CB, BM = RB * 4 * TMR, BN = CB * 32;
+  const size_t smem = static_cast<size_t>(kTStages) * (BM + BN) * kTLd * sizeof(float);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(router_tiled_kernel<TMR, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      set_error("router tiled: cannot reserve %zu bytes of shared memory", smem);
+      return BI_ERR_CUDA;
+    }
+    attr_done[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>((M + BM - 1) / BM), static_cast<unsigned>((N + BN - 1) / BN));
+  router_tiled_kernel<TMR, CB><<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
+  return BI_OK;
+}
+
+// Rows per thread for the tiled schedule: the smallest per-SM load
+// ceil(CTAs / SMs) * TMR (one CTA per SM per wave), ties to larger TMR.
+static int pick_tmr(int64_t M, int rows_per_tmr, int sms) {
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int t = 1; t <= 8; ++t) {
+    const int64_t ctas = (M + rows_per_tmr * t - 1) / (rows_per_tmr * t);
+    const int64_t cost = ((ctas + sms - 1) / sms) * t;
+    if (cost <= best_cost) {
+      best_cost = cost;
+      best = t;
+    }
+  }
+  return best;
+}
+
+static bi_status launch_tiled(const float *x, const float *w, const float *b, float *y, int64_t M,
+                              int64_t K, int64_t N, cudaStream_t stream) {
+  const int cb = N > 128 ? 8 : (N > 64 ? 4 : (N > 32 ? 2 : 1));
+  const int rows_per_tmr = (8 / cb) * 4;
+  const int tmr = pick_tmr(M, rows_per_tmr, num_sms());
+#define BI_TILED(T)                                                                      case T:                                                                                  switch (cb) {                                                                            case 8: return launch_tiled_t<T, 8>(x, w, b, y, M, K, N, stream);                      case 4: return launch_tiled_t<T, 4>(x, w, b, y, M, K, N, stream);                      case 2: return launch_tiled_t<T, 2>(x, w, b, y, M, K, N, stream);                      default: return launch_tiled_t<T, 1>(x, w, b, y, M, K, N, stream);                   }
+  switch (tmr) {
+    BI_TILED(1)
+    BI_TILED(2)
+    BI_TILED(3)
+    BI_TILED(4)
+    BI_TILED(5)
+    BI_TILED(6)
+    BI_TILED(7)
+    BI_TILED(8)
+  }
+#undef BI_TILED
+  return BI_ERR_UNSUPPORTED;
 }
 
 // ------------------------------------------------------- negative control --
@@ -310,42 +422,50 @@ __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float 
 bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
                         int64_t K, int64_t N, int schedule, cudaStream_t stream) {
   const int S = static_cast<int>(K / kSlice);
-  if (schedule == 0) schedule = (M <= 8) ? 1 : (M < 384 ? 2 : 3);
+  if (schedule == 0) schedule = (M <= 16) ? 1 : (M < 384 ? 2 : 3);
   if (schedule == 1) {
-    int LPR = 1;
-    while (LPR * 2 <= S && LPR * 2 <= 32) LPR *= 2;
-    const int rpw = 32 / LPR;
-    const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
-    dim3 grid(static_cast<unsigned>((N + rpw - 1) / rpw), static_cast<unsigned>((M + mr - 1) / mr));
-    const size_t smem = static_cast<size_t>(rpw) * mr * S * sizeof(float);
-    if (grid.y > 65535u || smem > 48 * 1024) {
-      set_error("router rows schedule: M=%lld or K=%lld too large for it", (long long)M,
-                (long long)K);
+    const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
+    dim3 grid(static_cast<unsigned>(N), static_cast<unsigned>((M + mr - 1) / mr));
+    const size_t smem = (static_cast<size_t>(1 + mr) * 32 * kSlicePad + static_cast<size_t>(mr) * S) * sizeof(float);
+    if (grid.y > 65535u) {
+      set_error("router rows schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    switch (mr) {
-      case 1: router_rows_kernel<1><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, LPR); break;
-      case 2: router_rows_kernel<2><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, LPR); break;
-      case 4: router_rows_kernel<4><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, LPR); break;
-      default: router_rows_kernel<8><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, LPR); break;
-    }
+#define BI_ROWS(R)                                                                                     \
+  {                                                                                                    \
+    static bool attr[64] = {};                                                                         \
+    int dv = 0;                                                                                        \
+    cudaGetDevice(&dv);                                                                                \
+    if (dv < 64 && !attr[dv]) {                                                                        \
+      cudaFuncSetAttribute(router_rows_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
+      attr[dv] = true;                                                                                 \
+    }                                                                                                  \
+    router_rows_kernel<R><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);            \
+  }
+    if (mr == 1) BI_ROWS(1) else if (mr == 2) BI_ROWS(2) else BI_ROWS(4)
+#undef BI_ROWS
   } else if (schedule == 2) {
-    dim3 grid(static_cast<unsigned>((N + 31) / 32), static_cast<unsigned>((M + 7) / 8));
+    dim3 grid(static_cast<unsigned>((N + kSlNT - 1) / kSlNT), static_cast<unsigned>((M + kSlMT - 1) / kSlMT));
+    const size_t smem = (2 * static_cast<size_t>(kSlStage) + kSlG * kSlMT * kSlNT) * sizeof(float);
     if (grid.y > 65535u) {
       set_error("router sliced schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    if (S % 16 == 0)
-      router_sliced_kernel<16><<<grid, 512, 0, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
-    else
-      router_sliced_kernel<8><<<grid, 256, 0, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
+    static bool attr[64] = {};
+    int dv = 0;
+    cudaGetDevice(&dv);
+    if (dv < 64 && !attr[dv]) {
+      cudaFuncSetAttribute(router_sliced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      attr[dv] = true;
+    }
+    router_sliced_kernel<<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
   } else if (schedule == 3) {
-    dim3 grid(static_cast<unsigned>((N + kTBN - 1) / kTBN), static_cast<unsigned>((M + kTBM - 1) / kTBM));
-    if (grid.y > 65535u) {
+    if ((M + 3) / 4 > 65535LL * 8 * 4) {
       set_error("router tiled schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    router_tiled_kernel<<<grid, 64, 0, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
+    const bi_status st = launch_tiled(x, w, b, y, M, K, N, stream);
+    if (st != BI_OK) return st;
   } else {
     set_error("unknown router schedule %d", schedule);
     return BI_ERR_INVALID_ARG;
