@@ -4,9 +4,10 @@
  * One library, libbimoe.so, holding hand-written CUDA kernels.  Every entry
  * point takes plain device pointers owned by the caller plus sizes and a CUDA
  * stream, launches asynchronously on that stream, never synchronises the
- * host and never allocates device memory.  Calls are safe to capture in a
- * CUDA graph (argument checks are host-side; nothing reads device memory on
- * the host).
+ * host and never allocates device memory.  bi_router_gemm, bi_topk,
+ * bi_moe_forward and the stage entry points are safe to capture in a CUDA
+ * graph (argument checks are host-side; nothing reads device memory on the
+ * host).
  *
  * Batch invariance contract: for fixed weights and fixed (N,K) resp.
  * (H,E,top_k,I), every output row of every entry point is bit-identical
@@ -237,6 +238,42 @@ BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets,
  */
 BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
                                 int64_t H, int32_t top_k, bi_stream_t stream);
+
+/*
+ * bi_moe_forward_noalloc -- bi_moe_forward without a caller-provided
+ * workspace, for callers that cannot allocate device memory where they run
+ * the layer (code inside an allocator or memory-pool callback, runtimes that
+ * own all device memory and forbid allocations behind their back).  This
+ * entry point has no counterpart in the papers; it exists only for such
+ * callers.
+ *
+ * Arguments, layouts, requirements and results are those of bi_moe_forward
+ * (same kernels, same bits).  The scratch space is a fixed array of
+ * BI_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device code: every
+ * GPU that loads the library holds it until the process exits.  Sizes whose
+ * bi_moe_workspace_bytes() exceeds it are rejected with BI_ERR_WORKSPACE and
+ * a message naming both sizes (64 MiB covers e.g. 606 tokens of H=2048,
+ * E=128, top-8, I=768, or 292 tokens of H=4096, E=256, top-8, I=2048).
+ * The call never allocates or frees device memory.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture begins.
+ *
+ * All calls on a device share the one array and it keeps the previous
+ * call's contents; nothing in it needs to start at zero, because every call
+ * writes each scratch byte it reads before reading it.  Calls whose
+ * executions overlap on the GPU (different streams, or host threads issuing
+ * concurrently without ordering) race on the array and give undefined
+ * results: order them on one stream.
+ */
+#define BI_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+BI_API bi_status bi_moe_forward_noalloc(const bi_bf16 *x, const int32_t *ids,
+                                        const float *wts, const bi_bf16 *w13,
+                                        const bi_bf16 *w2, bi_bf16 *out,
+                                        int64_t M, int64_t H, int64_t E,
+                                        int32_t top_k, int64_t I,
+                                        bi_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ EXPORTS = [
     "bi_cast_bf16_to_f32", "bi_router_gemm", "bi_router_gemm_schedule",
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gate_up_workspace_bytes",
-    "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine",
+    "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
 ]
 
 
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
+            "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -207,6 +208,22 @@ def bi_moe_forward(x, ids, wts, w13, w2, out=None, workspace=None, stream=None):
           _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
           M, H, E, top_k, I, _ptr(workspace, torch.uint8, "workspace", dev),
           workspace.numel(), _stream(stream))
+    return out
+
+
+def bi_moe_forward_noalloc(x, ids, wts, w13, w2, out=None, stream=None):
+    """bi_moe_forward with the library's built-in scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory; the
+    output tensor, if not given, is still allocated here by torch)."""
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dev = x.device
+    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_forward_noalloc", _ptr(x, torch.bfloat16, "x"), _ptr(ids, torch.int32, "ids", dev),
+          _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+          _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
+          M, H, E, ids.shape[1], I, _stream(stream))
     return out
 
 
