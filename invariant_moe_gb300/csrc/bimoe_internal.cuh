@@ -30,6 +30,9 @@ int num_sms();
 // [box_rows, 64]-element box and 128-byte swizzle.  Returns false on failure.
 bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
+// Same for a row-major fp32 tensor with a [box_rows, 32]-element box.
+bool make_tma_2d_f32(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows);
 void set_error(const char *fmt, ...);
 
 #define BI_CHECK_LAUNCH()                                                  \

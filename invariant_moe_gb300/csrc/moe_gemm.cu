@@ -8,47 +8,55 @@
 // gate|up half split, single final bf16 round).
 //
 // Design (sm_103a):
-//   * swap-AB: the weight rows are the MMA "M" side (128 rows of one expert),
-//     the tokens routed to that expert are the "N" side (128 per tile), K runs
-//     over the hidden (gate/up) or intermediate (down) dimension.
-//   * one instruction shape for every M: tcgen05.mma.cta_group::1.kind::f16,
-//     M=128, N=128, K=16, bf16 operands, fp32 accumulator in tensor memory.
-//     K advances in steps of 64 (one 128-byte swizzle atom: four MMAs) in
-//     increasing k, always accumulating into the same tensor-memory tile,
-//     with no split-K: each output element sees the same instruction sequence
-//     whatever the batch is.
-//   * TMA (cp.async.bulk.tensor, 128-byte swizzle) stages weight and token
-//     tiles through a 4-6 deep shared-memory ring guarded by mbarriers.
+//   * swap-AB: weight rows are the MMA "M" side (128 rows), the tokens routed
+//     to one expert are the "N" side (up to 256 per tile), K runs over the
+//     hidden (gate/up) or intermediate (down) dimension.
+//   * one tcgen05.mma.cta_group::1.kind::f16 per K=16 step: M=128, N = the
+//     tile's token count rounded up to 16, bf16 operands, fp32 accumulator in
+//     tensor memory.  K advances in steps of 64 (one 128-byte swizzle atom,
+//     four MMAs) in increasing k into the same accumulator, no split-K: each
+//     output element sees the same K order whatever the batch is (the N of
+//     the instruction only decides how many token columns are computed; the
+//     tests check that a token's bits do not depend on it).
+//   * gate/up: a tile is 128 gate rows j0.. and the 128 matching up rows
+//     I+j0.. against up to 128 tokens: two MMAs per K step share the token
+//     tile, into two accumulators (gate, up); the epilogue computes
+//     act = bf16(silu(g) * u * p).  (Interleaving 64 gate + 64 up rows into
+//     one MMA with 256 tokens was measured slower: twice the weight blocks
+//     re-read each token tile, and the kernel is bound by memory traffic.)
+//   * down: 128 rows of W2 (h) against up to 256 tokens per tile; the
+//     epilogue writes fp32 contributions to row token*top_k + slot.
+//   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a 4-deep ring of
+//     48 KB stages; accumulators are double buffered (2 x 256 tensor-memory
+//     columns) so the epilogue of one tile overlaps the MMAs of the next.
 //   * warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues the
-//     MMAs from one thread, warps 2-5 drain the accumulator (tcgen05.ld) and
-//     run the epilogue.  Accumulators are double-buffered in tensor memory so
-//     the epilogue of one tile overlaps the MMAs of the next.
-//   * persistent grid (at most one CTA per SM); tiles are ordered expert,
-//     weight block, token block so the token blocks sharing a weight block run
-//     back to back and read it from L2.
-//   * gate/up: two accumulators per tile (gate rows j, up rows I+j); the
-//     epilogue computes act = bf16(silu(g) * u * p) in fp32.
-//   * down: one accumulator; the epilogue writes fp32 contributions to row
-//     token*top_k + slot.
+//     MMAs from one thread, warps 2-5 drain the accumulator (tcgen05.ld).
+//   * persistent grid (one CTA per SM); tiles are ordered expert, weight
+//     block, token block, so the token blocks of a weight block run back to
+//     back and share it through L2.
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
 
-constexpr int kBM = 128;                 // weight rows per tile (MMA M)
-constexpr int kBN = 128;                 // tokens per tile (MMA N)
-constexpr int kBK = 64;                  // K step per stage (one swizzle atom)
-constexpr int kUK = 16;                  // K of one MMA
-constexpr int kTileBytes = kBM * kBK * 2;  // one 128 x 64 bf16 operand tile
+constexpr int kBM = 128;                    // MMA M: weight rows per tile
+constexpr int kBK = 64;                     // K per stage (one swizzle atom of bf16)
+constexpr int kUK = 16;                     // K of one MMA
+constexpr int kTileBytes = kBM * kBK * 2;   // 16 KB: one 128-row operand tile
+constexpr int kStages = 4;
+constexpr int kAccCols = 256;               // tensor-memory columns per accumulator buffer
+constexpr int kNumAcc = 2;                  // double-buffered
+constexpr int kTmemCols = kNumAcc * kAccCols;
 constexpr int kGemmThreads = 192;
+constexpr int kAuxBytes = 8192;             // barriers, tile prefix
 
+// gate/up: A = gate + up tiles (32 KB), 128 tokens (16 KB), two 128-column
+// accumulators per buffer.  down: A = one tile (16 KB), 256 tokens (32 KB),
+// one 256-column accumulator per buffer.  Both stages are 48 KB.
 template <bool GATE_UP>
 struct GemmCfg {
-  static constexpr int kNumA = GATE_UP ? 2 : 1;
-  static constexpr int kStages = GATE_UP ? 4 : 6;
-  static constexpr int kStageBytes = (kNumA + 1) * kTileBytes;
-  static constexpr int kAccCols = GATE_UP ? 2 * kBN : kBN;  // per accumulator buffer
-  static constexpr int kTmemCols = 2 * kAccCols;             // double buffered
-  static constexpr int kAuxBytes = 8192;
+  static constexpr int kBN = GATE_UP ? 128 : 256;   // tokens per tile (largest MMA N)
+  static constexpr int kABytes = (GATE_UP ? 2 : 1) * kTileBytes;
+  static constexpr int kStageBytes = kABytes + kBN * kBK * 2;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes;
 };
 
@@ -59,7 +67,8 @@ struct GemmParams {
   void *out;               // gate/up: act bf16 [P, I]; down: contrib fp32 [M*top_k, H]
   int E;
   int K;                   // reduction length (H for gate/up, I for down)
-  int n_wb;                // 128-row weight blocks per expert (I/128 or H/128)
+  int n_wb;                // weight blocks per expert (I/128 for gate/up, H/128 for down)
+  int wb_rows;             // output features per weight block (128)
   int out_ld;              // output row length (I or H)
   int a_rows_per_expert;   // rows of the weight tensor per expert (2I or H)
   int up_offset;           // row offset of the up half (I), gate/up only
@@ -70,6 +79,7 @@ struct TileInfo {
   int e, wb, tok0, ntok;
 };
 
+template <int kBN>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix,
                                                 const GemmParams &p) {
   int lo = 0, hi = p.E - 1;
@@ -91,21 +101,30 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix
   return t;
 }
 
+// act = silu(g) * u * p: a fixed fp32 sequence, one bf16 rounding.
+__device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
+  const float sg = __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
+  return __float2bfloat16_rn(__fmul_rn(__fmul_rn(sg, u), p));
+}
+
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
   using C = GemmCfg<GATE_UP>;
+  constexpr int kBN = C::kBN;
+  constexpr int kStageBytes = C::kStageBytes;
+  constexpr int kABytes = C::kABytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *tiles = smem;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
   uint64_t *full = bars;
-  uint64_t *empty = bars + C::kStages;
-  uint64_t *tfull = bars + 2 * C::kStages;
-  uint64_t *tempty = tfull + 2;
-  uint64_t *drain = tempty + 2;
+  uint64_t *empty = bars + kStages;
+  uint64_t *tfull = bars + 2 * kStages;
+  uint64_t *tempty = tfull + kNumAcc;
+  uint64_t *drain = tempty + kNumAcc;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *tile_prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [E+1]
@@ -115,11 +134,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = prm.K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kNumAcc; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), 128);
     }
@@ -132,7 +151,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   if (warp == 2) {
@@ -171,23 +190,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, tile_prefix, prm);
-        const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * kBM;
+        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+        const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, prm.err)) {
             ok = false;
             break;
           }
-          uint8_t *st = tiles + stage * C::kStageBytes;
+          uint8_t *st = tiles + stage * kStageBytes;
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          mbar_arrive_expect_tx(fb, kStageBytes);
           tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
           if (GATE_UP) tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
-          tma_load_2d(smem_u32(st + C::kNumA * kTileBytes), &tmB, fb, kb * kBK, ti.tok0);
+          tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, ti.tok0);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == C::kStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -196,7 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (*abort_flag) {
         // let every copy this thread started land before the CTA can exit
-        for (int s = 0; s < C::kStages; ++s)
+        for (int s = 0; s < kStages; ++s)
           if ((issued_mask >> s) & 1u)
             mbar_wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, nullptr, prm.err);
       }
@@ -204,16 +223,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued_any = false;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+        // the MMA N covers the tile's real tokens (a multiple of 16), so a
+        // ragged last tile of an expert does not pay for padding columns
+        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+        const uint32_t idesc = idesc_bf16_f32(kBM, (ti.ntok + 15) & ~15);
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, prm.err)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, prm.err)) {
@@ -221,8 +243,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(tiles + stage * C::kStageBytes);
-          const uint32_t b0 = a0 + C::kNumA * kTileBytes;
+          const uint32_t a0 = smem_u32(tiles + stage * kStageBytes);
+          const uint32_t b0 = a0 + kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k) {
             const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
@@ -233,14 +255,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           issued_any = true;
           umma_commit(smem_u32(&empty[stage]));
-          if (++stage == C::kStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
         umma_commit(smem_u32(&tfull[acc]));
-        if (++acc == 2) {
+        if (++acc == kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -254,46 +276,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
-    const int q = warp & 3;        // tensor-memory lane quarter of this warp
-    const int row = q * 32 + lane;  // weight row inside the tile
+    // Warp w reads tensor-memory lanes 32*(w%4).. (weight rows of the tile);
+    // the per-token data of a tile (pair ids, probabilities) is loaded one
+    // tile ahead, lane l holding token 32i + l, so the dependent global loads
+    // overlap the wait for the accumulator.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int nx_pair[kBN / 32];
+    float nx_p[kBN / 32];
+    auto prefetch = [&](int tile) {
+      const TileInfo t = decode_tile<kBN>(tile, tile_prefix, prm);
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        const int c = 32 * i + lane;
+        nx_pair[i] = c < t.ntok ? __ldg(prm.perm + t.tok0 + c) : 0;
+        nx_p[i] = 0.0f;
+      }
+      if (GATE_UP) {
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i) {
+          const int c = 32 * i + lane;
+          nx_p[i] = c < t.ntok ? __ldg(prm.wts + nx_pair[i]) : 0.0f;
+        }
+      }
+    };
+    if (static_cast<int>(blockIdx.x) < total_tiles) prefetch(blockIdx.x);
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, tile_prefix, prm);
+      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+      int my_pair[kBN / 32];
+      float my_p[kBN / 32];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        my_pair[i] = nx_pair[i];
+        my_p[i] = nx_p[i];
+      }
+      if (tile + static_cast<int>(gridDim.x) < total_tiles) prefetch(tile + gridDim.x);
       if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, prm.err)) break;
       tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
-      const int col = ti.wb * kBM + row;
-      for (int c0 = 0; c0 < ti.ntok; c0 += 32) {
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * kAccCols);
+      const int col = ti.wb * prm.wb_rows + row;
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        const int c0 = 32 * i;
+        if (c0 >= ti.ntok) break;  // warp-uniform
         uint32_t d[32];
         tmem_ld32(tbase + c0, d);
-        // per-token data: lane c holds token c0 + c, broadcast by shuffles
-        const bool tv = c0 + lane < ti.ntok;
-        const int my_pair = tv ? __ldg(prm.perm + ti.tok0 + c0 + lane) : 0;
         if (GATE_UP) {
           uint32_t u[32];
           tmem_ld32(tbase + kBN + c0, u);
-          const float my_p = tv ? __ldg(prm.wts + my_pair) : 0.0f;
           tmem_ld_wait();
           __nv_bfloat16 *act = static_cast<__nv_bfloat16 *>(prm.out);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float pc = __shfl_sync(0xffffffffu, my_p, c);
-            if (c0 + c < ti.ntok) {
-              const float g = __uint_as_float(d[c]);
-              const float uu = __uint_as_float(u[c]);
-              const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
-              const float a = __fmul_rn(__fmul_rn(__fmul_rn(g, sg), uu), pc);
-              act[static_cast<size_t>(ti.tok0 + c0 + c) * prm.out_ld + col] = __float2bfloat16_rn(a);
-            }
+            const float pc = __shfl_sync(0xffffffffu, my_p[i], c);
+            if (c0 + c < ti.ntok)
+              act[static_cast<size_t>(ti.tok0 + c0 + c) * prm.out_ld + col] =
+                  swiglu_p(__uint_as_float(d[c]), __uint_as_float(u[c]), pc);
           }
         } else {
           tmem_ld_wait();
           float *contrib = static_cast<float *>(prm.out);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int pair = __shfl_sync(0xffffffffu, my_pair, c);
+            const int pair = __shfl_sync(0xffffffffu, my_pair[i], c);
             if (c0 + c < ti.ntok)
               contrib[static_cast<size_t>(pair) * prm.out_ld + col] = __uint_as_float(d[c]);
           }
@@ -301,7 +349,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
-      if (++acc == 2) {
+      if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -312,7 +360,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -320,23 +368,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <bool GATE_UP>
 static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                              int64_t P, cudaStream_t stream) {
-  using C = GemmCfg<GATE_UP>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GemmCfg<GATE_UP>::kSmemBytes);
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
       return BI_ERR_CUDA;
     }
     attr_done[dev] = true;
   }
-  // upper bound on the number of tiles (token blocks per expert <= P/128 + 1)
-  const int64_t ub = static_cast<int64_t>(p.n_wb) * (std::min<int64_t>(p.E, P) + P / kBN + 1);
+  // upper bound on the number of tiles (token blocks per expert <= P/kBN + 1)
+  const int64_t ub = static_cast<int64_t>(p.n_wb) *
+                     (std::min<int64_t>(p.E, P) + P / GemmCfg<GATE_UP>::kBN + 1);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), ub)));
-  moe_gemm_kernel<GATE_UP><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(tmA, tmB, p);
+  moe_gemm_kernel<GATE_UP><<<grid, kGemmThreads, GemmCfg<GATE_UP>::kSmemBytes, stream>>>(tmA, tmB, p);
   BI_CHECK_LAUNCH();
   return BI_OK;
 }
@@ -347,10 +396,11 @@ bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32
   (void)top_k;
   CUtensorMap tmA, tmB;
   if (!make_tma_2d_bf16(&tmA, w13, static_cast<uint64_t>(E * 2 * I), static_cast<uint64_t>(H), kBM) ||
-      !make_tma_2d_bf16(&tmB, x_perm, static_cast<uint64_t>(P), static_cast<uint64_t>(H), kBN))
+      !make_tma_2d_bf16(&tmB, x_perm, static_cast<uint64_t>(P), static_cast<uint64_t>(H),
+                        GemmCfg<true>::kBN))
     return BI_ERR_CUDA;
-  GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / kBM), (int)I, (int)(2 * I), (int)I,
-               device_error_word()};
+  GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / kBM), kBM, (int)I,
+               (int)(2 * I), (int)I, device_error_word()};
   return launch_gemm<true>(tmA, tmB, p, P, stream);
 }
 
@@ -360,10 +410,11 @@ bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *pe
   (void)top_k;
   CUtensorMap tmA, tmB;
   if (!make_tma_2d_bf16(&tmA, w2, static_cast<uint64_t>(E * H), static_cast<uint64_t>(I), kBM) ||
-      !make_tma_2d_bf16(&tmB, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I), kBN))
+      !make_tma_2d_bf16(&tmB, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I),
+                        GemmCfg<false>::kBN))
     return BI_ERR_CUDA;
-  GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / kBM), (int)H, (int)H, 0,
-               device_error_word()};
+  GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / kBM), kBM, (int)H, (int)H,
+               0, device_error_word()};
   return launch_gemm<false>(tmA, tmB, p, P, stream);
 }
 

@@ -19,20 +19,19 @@
 //                         lanes own slices: streams W for decode batches
 //   sliced  (16 < M < 384) 8x16 output tile per CTA, one warp per slice, the
 //                         partials combined in slice order through smem
-//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps spanning N,
-//                         TMR x 4 outputs per thread, cp.async pipeline,
-//                         slices summed into a running register sum
+//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over up to 128
+//                         columns, TMR x 4 outputs per thread, cp.async
+//                         3-stage ring, slices summed into a running sum
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
 
 constexpr int kSlice = 128;
 
-// Shared-memory staging used by every schedule: a slice (128 fp32 = 512 B)
-// of a row is copied with 32 coalesced 16-byte cp.async pieces into a padded
-// row (132 floats), so that lanes walking different slices / rows along k
-// read distinct banks.
+// Padded shared row for one slice (128 fp32 + 4): lanes walking different
+// slices along k then read distinct banks.
 constexpr int kSlicePad = kSlice + 4;
+
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -43,44 +42,63 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes
+// on an mbarrier.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // -------------------------------------------------------------------- rows --
 // One warp per weight row n and MR token rows; lane l owns slice l of each
-// group of 32 slices.  The W row slices and the MR x row slices of a group
-// are staged (coalesced) in shared memory, then every lane runs its MR chains
-// from there; the S partials meet in shared memory and lane i < MR adds them
-// in slice order.
+// group of 32 slices.  Each lane bulk-copies its slice of the W row and of
+// the MR x rows (512 B each) into padded shared rows, then runs its MR
+// chains from there; the partials meet in shared memory and lane i < MR adds
+// them in slice order.
 template <int MR>
 __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict__ x,
                                                          const float *__restrict__ w,
                                                          const float *__restrict__ bias,
                                                          float *__restrict__ y, int M, int K,
-                                                         int N) {
+                                                         int N, int *err) {
   extern __shared__ __align__(16) float sm[];
   float *ws = sm;                              // [32][kSlicePad]
   float *xs = sm + 32 * kSlicePad;             // [MR][32][kSlicePad]
   float *part = xs + MR * 32 * kSlicePad;      // [MR][S]
+  __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   const int S = K / kSlice;
   const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
   const float *wrow = w + static_cast<size_t>(n) * K;
-  const float *xrow[MR];
-#pragma unroll
-  for (int i = 0; i < MR; ++i) xrow[i] = x + static_cast<size_t>(min(m0 + i, M - 1)) * K;
-
+  const uint32_t b = smem_u32(&bar);
+  if (lane == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  uint32_t phase = 0;
   for (int g0 = 0; g0 < S; g0 += 32) {
     const int ns = min(32, S - g0);
+    if (lane == 0) mbar_arrive_expect_tx(b, static_cast<uint32_t>(ns) * kSlice * 4 * (1 + MR));
     __syncwarp();
-    for (int sl = 0; sl < ns; ++sl) {
-      const int k0 = (g0 + sl) * kSlice + lane * 4;
-      cp_async16(smem_u32(ws + sl * kSlicePad + lane * 4), wrow + k0);
+    if (lane < ns) {
+      const int k0 = (g0 + lane) * kSlice;
+      bulk_g2s(smem_u32(ws + lane * kSlicePad), wrow + k0, kSlice * 4, b);
 #pragma unroll
       for (int i = 0; i < MR; ++i)
-        cp_async16(smem_u32(xs + (i * 32 + sl) * kSlicePad + lane * 4), xrow[i] + k0);
+        bulk_g2s(smem_u32(xs + (i * 32 + lane) * kSlicePad),
+                 x + static_cast<size_t>(min(m0 + i, M - 1)) * K + k0, kSlice * 4, b);
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncwarp();
+    const bool got = mbar_wait(b, phase, nullptr, err);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (!got) mbar_wait(b, phase, nullptr, err);  // let the copies land before exit
+      return;
+    }
+    phase ^= 1u;
     if (lane < ns) {
       float p[MR];
 #pragma unroll
@@ -101,11 +119,13 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
 #pragma unroll
       for (int i = 0; i < MR; ++i) part[i * S + g0 + lane] = p[i];
     }
+    __syncwarp();
   }
-  __syncwarp();
   if (lane < MR && m0 + lane < M) {
     float acc = 0.0f;
-    for (int sl = 0; sl < S; ++sl) acc = __fadd_rn(acc, part[lane * S + sl]);
+    const float *pr = part + lane * S;
+#pragma unroll 8
+    for (int sl = 0; sl < S; ++sl) acc = __fadd_rn(acc, pr[sl]);
     if (bias) acc = __fadd_rn(acc, bias[n]);
     y[static_cast<size_t>(m0 + lane) * N + n] = acc;
   }
@@ -113,73 +133,94 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
 
 // ------------------------------------------------------------------ sliced --
 // CTA = 8 warps, output tile 8 (m) x 16 (n).  K is processed in rounds of 8
-// slices; in a round warp g evaluates slice 8r+g for the whole tile (lane l:
-// column l % 16, rows 4 (l / 16) .. +3).  Each round's 8 x rows and 16 W rows
-// (8 slices each) are staged by cp.async into a double-buffered shared tile
-// while the previous round computes.  Partials meet in shared memory and
-// thread (i, j) adds them to its running sum in slice order.
+// slices; in a round warp g evaluates slice 8r+g for the whole tile, lane l
+// owning rows {l/8, l/8+4} x columns {l%8, l%8+8}.  A round's 8 x rows and
+// 16 W rows (8 slices = 4 KB contiguous each) are bulk-copied into a
+// double-buffered shared tile (row stride 1028 floats: conflict-free for
+// lanes reading different rows at the same k) while the previous round
+// computes.  Partials meet in shared memory and thread (i, j) adds them to
+// its running sum in slice order.
 constexpr int kSlMT = 8, kSlNT = 16, kSlG = 8;
-constexpr int kSlRow = kSlG * kSlicePad + 4;  // floats per staged row (stride = 4 mod 32)
+constexpr int kSlRow = kSlG * kSlice + 4;  // floats per staged row
 constexpr int kSlStage = (kSlMT + kSlNT) * kSlRow;
 
 __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restrict__ x,
                                                             const float *__restrict__ w,
                                                             const float *__restrict__ bias,
                                                             float *__restrict__ y, int M, int K,
-                                                            int N) {
+                                                            int N, int *err) {
   extern __shared__ __align__(16) float sm[];
   float *stage_buf = sm;                         // [2][MT + NT][kSlRow]
   float *part = sm + 2 * kSlStage;               // [G][MT][NT]
+  __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
   const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
   const int rounds = (S + kSlG - 1) / kSlG;
   const int m0 = blockIdx.y * kSlMT, n0 = blockIdx.x * kSlNT;
 
-  auto load_round = [&](int rd, int buf) {
-    float *dst = stage_buf + buf * kSlStage;
-    // (MT + NT) rows x G slices x 32 pieces of 16 B
-    for (int q = tid; q < (kSlMT + kSlNT) * kSlG * 32; q += 256) {
-      const int piece = q & 31, sl = (q >> 5) % kSlG, row = (q >> 5) / kSlG;
-      const int s = rd * kSlG + sl;
-      if (s >= S) continue;
-      const float *src = row < kSlMT ? x + static_cast<size_t>(min(m0 + row, M - 1)) * K
-                                     : w + static_cast<size_t>(min(n0 + row - kSlMT, N - 1)) * K;
-      cp_async16(smem_u32(dst + row * kSlRow + sl * kSlicePad + piece * 4),
-                 src + s * kSlice + piece * 4);
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // lanes of warp 0 issue the copies of a round: row q (< 24) by lane q
+  auto load_round = [&](int rd) {
+    if (g != 0) return;
+    const int buf = rd & 1;
+    const uint32_t b = smem_u32(&bars[buf]);
+    const int ns = min(kSlG, S - rd * kSlG);
+    const uint32_t bytes = static_cast<uint32_t>(ns) * kSlice * 4;
+    if (lane == 0) mbar_arrive_expect_tx(b, bytes * (kSlMT + kSlNT));
+    __syncwarp();
+    if (lane < kSlMT + kSlNT) {
+      const float *src = lane < kSlMT ? x + static_cast<size_t>(min(m0 + lane, M - 1)) * K
+                                      : w + static_cast<size_t>(min(n0 + lane - kSlMT, N - 1)) * K;
+      bulk_g2s(smem_u32(stage_buf + buf * kSlStage + lane * kSlRow), src + rd * kSlG * kSlice, bytes, b);
     }
   };
 
-  const int cn = lane & 15, cm = (lane >> 4) * 4;  // compute role
-  const int oi = tid >> 4, oj = tid & 15;          // combine role (tid < 128)
+  const int cr = lane >> 3, cc = lane & 7;  // compute role: rows cr, cr+4; cols cc, cc+8
+  const int oi = tid >> 4, oj = tid & 15;   // combine role (tid < 128)
   float acc = 0.0f;
-  load_round(0, 0);
-  cp_async_commit();
+  bool ok = true;
+  load_round(0);
+  uint32_t phases = 0;  // bit b: parity of the next wait on bars[b]
   for (int rd = 0; rd < rounds; ++rd) {
-    if (rd + 1 < rounds) load_round(rd + 1, (rd + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const float *buf = stage_buf + (rd & 1) * kSlStage;
-    const int s = rd * kSlG + g;
-    if (s < S) {
-      float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const float *wl = buf + (kSlMT + cn) * kSlRow + g * kSlicePad;
-      const float *xl = buf + cm * kSlRow + g * kSlicePad;
+    if (rd + 1 < rounds) load_round(rd + 1);
+    const int buf = rd & 1;
+    if (!mbar_wait(smem_u32(&bars[buf]), (phases >> buf) & 1u, nullptr, err)) ok = false;
+    phases ^= 1u << buf;
+    if (__syncthreads_or(!ok)) break;
+    const float *sb = stage_buf + buf * kSlStage;
+    const int sl = rd * kSlG + g;
+    if (sl < S) {
+      float p00 = 0.0f, p01 = 0.0f, p10 = 0.0f, p11 = 0.0f;
+      const float *x0 = sb + cr * kSlRow + g * kSlice;
+      const float *x1 = x0 + 4 * kSlRow;
+      const float *w0 = sb + (kSlMT + cc) * kSlRow + g * kSlice;
+      const float *w1 = w0 + 8 * kSlRow;
 #pragma unroll 8
       for (int k = 0; k < kSlice; k += 4) {
-        const float4 wv = *reinterpret_cast<const float4 *>(wl + k);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 xv = *reinterpret_cast<const float4 *>(xl + i * kSlRow + k);
-          p[i] = __fmaf_rn(xv.x, wv.x, p[i]);
-          p[i] = __fmaf_rn(xv.y, wv.y, p[i]);
-          p[i] = __fmaf_rn(xv.z, wv.z, p[i]);
-          p[i] = __fmaf_rn(xv.w, wv.w, p[i]);
-        }
+        const float4 a0 = *reinterpret_cast<const float4 *>(x0 + k);
+        const float4 a1 = *reinterpret_cast<const float4 *>(x1 + k);
+        const float4 b0 = *reinterpret_cast<const float4 *>(w0 + k);
+        const float4 b1 = *reinterpret_cast<const float4 *>(w1 + k);
+        p00 = __fmaf_rn(a0.x, b0.x, p00); p01 = __fmaf_rn(a0.x, b1.x, p01);
+        p10 = __fmaf_rn(a1.x, b0.x, p10); p11 = __fmaf_rn(a1.x, b1.x, p11);
+        p00 = __fmaf_rn(a0.y, b0.y, p00); p01 = __fmaf_rn(a0.y, b1.y, p01);
+        p10 = __fmaf_rn(a1.y, b0.y, p10); p11 = __fmaf_rn(a1.y, b1.y, p11);
+        p00 = __fmaf_rn(a0.z, b0.z, p00); p01 = __fmaf_rn(a0.z, b1.z, p01);
+        p10 = __fmaf_rn(a1.z, b0.z, p10); p11 = __fmaf_rn(a1.z, b1.z, p11);
+        p00 = __fmaf_rn(a0.w, b0.w, p00); p01 = __fmaf_rn(a0.w, b1.w, p01);
+        p10 = __fmaf_rn(a1.w, b0.w, p10); p11 = __fmaf_rn(a1.w, b1.w, p11);
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) part[(g * kSlMT + cm + i) * kSlNT + cn] = p[i];
+      float *pg = part + g * kSlMT * kSlNT;
+      pg[cr * kSlNT + cc] = p00;
+      pg[cr * kSlNT + cc + 8] = p01;
+      pg[(cr + 4) * kSlNT + cc] = p10;
+      pg[(cr + 4) * kSlNT + cc + 8] = p11;
     }
     __syncthreads();
     if (tid < kSlMT * kSlNT) {
@@ -187,7 +228,13 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
       for (int gg = 0; gg < ng; ++gg) acc = __fadd_rn(acc, part[(gg * kSlMT + oi) * kSlNT + oj]);
     }
   }
-  cp_async_wait<0>();
+  if (!ok) {
+    // let any copy still in flight land before the CTA exits
+    if (tid == 0)
+      for (int bb = 0; bb < 2; ++bb) mbar_wait(smem_u32(&bars[bb]), (phases >> bb) & 1u, nullptr, err);
+    __syncthreads();
+    return;
+  }
   if (tid < kSlMT * kSlNT) {
     const int m = m0 + oi, n = n0 + oj;
     if (m < M && n < N) {
@@ -199,20 +246,21 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
 
 // ------------------------------------------------------------------- tiled --
 // Register-tiled FFMA kernel for large M.  A CTA is 8 warps arranged as RB
-// row blocks x CB column blocks (CB = 32-column blocks covering N, at most
-// 8); thread (r, c) of a warp owns rows base + 4i + r (i < TMR) and columns
-// base + 8j + c (j < 4).  K advances in chunks of 32 through a 3-stage
-// cp.async ring of [rows][32 + 4] fp32 tiles (k contiguous, padded so the
-// 16-byte loads along k are bank-conflict free); each chunk is consumed four
-// k at a time, each output's chain in increasing k.  Every 128 k (4 chunks)
-// the chain value is added to the running sum and restarted from +0.0f.
-// TMR is chosen on the host so the grid fills the SMs in one wave.
+// row blocks x CB column blocks (CB = 32-column blocks, at most 4: a CTA
+// covers up to 128 columns); thread (r, c) of a warp owns rows base + 4i + r
+// (i < TMR) and columns base + 8j + c (j < 4).  K advances in chunks of 32
+// through a 3-stage cp.async ring of [rows][32 + 4] fp32 tiles (k
+// contiguous, padded so the 16-byte loads along k are bank-conflict free);
+// each chunk is consumed four k at a time, each output's chain in increasing
+// k.  Every 128 k (4 chunks) the chain value is added to the running sum and
+// restarted from +0.0f.  At most 128 registers per thread so that two CTAs
+// (16 warps) share an SM: with 8 warps the FFMA issue rate was ~50%.
 constexpr int kTBK = 32;              // k per chunk
 constexpr int kTLd = kTBK + 4;        // padded smem row length (floats)
 constexpr int kTStages = 3;
 
 template <int TMR, int CB>
-__global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restrict__ x,
+__global__ void __launch_bounds__(256, 2) router_tiled_kernel(const float *__restrict__ x,
                                                            const float *__restrict__ w,
                                                            const float *__restrict__ bias,
                                                            float *__restrict__ y, int M, int K,
@@ -341,37 +389,27 @@ static bi_status launch_tiled_t(const float *x, const float *w, const float *b, 
   return BI_OK;
 }
 
-// Rows per thread for the tiled schedule: the smallest per-SM load
-// ceil(CTAs / SMs) * TMR (one CTA per SM per wave), ties to larger TMR.
-static int pick_tmr(int64_t M, int rows_per_tmr, int sms) {
-  int best = 1;
-  int64_t best_cost = INT64_MAX;
-  for (int t = 1; t <= 8; ++t) {
-    const int64_t ctas = (M + rows_per_tmr * t - 1) / (rows_per_tmr * t);
-    const int64_t cost = ((ctas + sms - 1) / sms) * t;
-    if (cost <= best_cost) {
-      best_cost = cost;
-      best = t;
-    }
+// Rows per thread for the tiled schedule: the largest TMR (<= 4) whose grid
+// still gives every SM two CTAs (16 warps), else TMR = 1.
+static int pick_tmr(int64_t M, int rows_per_tmr, int64_t col_blocks, int sms) {
+  for (int t = 4; t > 1; --t) {
+    const int64_t ctas = (M + rows_per_tmr * t - 1) / (rows_per_tmr * t) * col_blocks;
+    if (ctas >= 2 * static_cast<int64_t>(sms) * 4 / 5) return t;
   }
-  return best;
+  return 1;
 }
 
 static bi_status launch_tiled(const float *x, const float *w, const float *b, float *y, int64_t M,
                               int64_t K, int64_t N, cudaStream_t stream) {
-  const int cb = N > 128 ? 8 : (N > 64 ? 4 : (N > 32 ? 2 : 1));
+  const int cb = N > 64 ? 4 : (N > 32 ? 2 : 1);
   const int rows_per_tmr = (8 / cb) * 4;
-  const int tmr = pick_tmr(M, rows_per_tmr, num_sms());
+  const int tmr = pick_tmr(M, rows_per_tmr, (N + cb * 32 - 1) / (cb * 32), num_sms());
 #define BI_TILED(T)                                                                      case T:                                                                                  switch (cb) {                                                                            case 8: return launch_tiled_t<T, 8>(x, w, b, y, M, K, N, stream);                      case 4: return launch_tiled_t<T, 4>(x, w, b, y, M, K, N, stream);                      case 2: return launch_tiled_t<T, 2>(x, w, b, y, M, K, N, stream);                      default: return launch_tiled_t<T, 1>(x, w, b, y, M, K, N, stream);                   }
   switch (tmr) {
     BI_TILED(1)
     BI_TILED(2)
     BI_TILED(3)
     BI_TILED(4)
-    BI_TILED(5)
-    BI_TILED(6)
-    BI_TILED(7)
-    BI_TILED(8)
   }
 #undef BI_TILED
   return BI_ERR_UNSUPPORTED;
@@ -440,7 +478,7 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
       cudaFuncSetAttribute(router_rows_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
       attr[dv] = true;                                                                                 \
     }                                                                                                  \
-    router_rows_kernel<R><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);            \
+    router_rows_kernel<R><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, device_error_word());            \
   }
     if (mr == 1) BI_ROWS(1) else if (mr == 2) BI_ROWS(2) else BI_ROWS(4)
 #undef BI_ROWS
@@ -458,7 +496,7 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
       cudaFuncSetAttribute(router_sliced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       attr[dv] = true;
     }
-    router_sliced_kernel<<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
+    router_sliced_kernel<<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, device_error_word());
   } else if (schedule == 3) {
     if ((M + 3) / 4 > 65535LL * 8 * 4) {
       set_error("router tiled schedule: M=%lld too large for it", (long long)M);
