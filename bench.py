@@ -293,6 +293,29 @@ def run_ours(args, rank, world, local):
     return line
 
 
+def fp32_fma_peak(dev):
+    """Measured FP32 (non-tensor) FMA throughput of this GPU in TFLOP/s: the
+    library's probe kernel (16 independent FMA chains per thread, 8 CTAs of
+    256 threads per SM, no memory traffic), timed with CUDA events."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    props = torch.cuda.get_device_properties(dev)
+    blocks, iters = props.multi_processor_count * 8, 20000
+    bm.bi_fp32_fma_probe(blocks, 200)
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bm.bi_fp32_fma_probe(blocks, iters)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return blocks * 256 * 16 * 2 * iters / min(ts) / 1e12
+
+
 def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
     """Device us per router call (DSv4 router: K=4096, N=256, fp32, bias) vs M,
     from CUDA-graph replays so host launch cost is excluded.
@@ -334,7 +357,8 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
             flush.fill_(1.0)
 
     t_flush = graph_time(flushes)
-    res = {}
+    fp32_peak = fp32_fma_peak(dev)
+    res = {"fp32_fma_peak_tflops_measured": round(fp32_peak, 2)}
     for M in Ms:
         xm = x[:M].contiguous()
         y = torch.empty(M, 256, dtype=torch.float32, device=dev)
@@ -354,7 +378,8 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
         bytes_ = 4.0 * (256 * 4096 + 256 + M * (4096 + 256))
         res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(cold, 2),
                        "cold_hbm_frac": round(bytes_ / (cold * 1e-6) / 1e9 / measured_peaks()[0], 3),
-                       "warm_tflops": round(flops / (warm * 1e-6) / 1e12, 2)}
+                       "warm_tflops": round(flops / (warm * 1e-6) / 1e12, 2),
+                       "warm_fp32_frac": round(flops / (warm * 1e-6) / 1e12 / fp32_peak, 3)}
     return res
 
 

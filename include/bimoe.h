@@ -132,6 +132,17 @@ BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w,
                                               bi_stream_t stream);
 
 /*
+ * bi_fp32_fma_probe -- MEASUREMENT ONLY, not part of the MoE path: blocks x
+ * 256 threads, each running 16 independent fp32 FMA chains for `iters`
+ * steps (2 * 16 * iters flop per thread, no memory traffic in the loop).
+ * The benchmark times it to measure the FP32 (non-tensor) peak that the
+ * router's FFMA roofline is reported against.  out: blocks * 256 floats
+ * (device), written.
+ */
+BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
+                                   bi_stream_t stream);
+
+/*
  * bi_topk -- sigmoid scoring and deterministic top-k expert selection.
  * Source: "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling under
  * batch invariance", commit log, deterministic per-row top-k commit: score

@@ -34,6 +34,7 @@ EXPORTS = [
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gate_up_workspace_bytes",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
+    "bi_fp32_fma_probe",
 ]
 
 
@@ -79,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
+            "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -276,6 +278,13 @@ def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
     out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     _call("bi_moe_combine", _ptr(contrib, torch.float32, "contrib"), _ptr(out, torch.bfloat16, "out", dev),
           M, H, top_k, _stream(stream))
+    return out
+
+
+def bi_fp32_fma_probe(blocks, iters, stream=None):
+    """Run the FP32 FMA throughput probe; returns its output tensor."""
+    out = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    _call("bi_fp32_fma_probe", _ptr(out, torch.float32, "out"), blocks, iters, _stream(stream))
     return out
 
 

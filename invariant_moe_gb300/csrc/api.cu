@@ -28,6 +28,7 @@ bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const f
                          cudaStream_t);
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
+bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
 
 // ------------------------------------------------------------ error state --
 static thread_local char g_msg[512] = "";
@@ -286,6 +287,12 @@ BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts, float *p
   if (M == 0) return BI_OK;
   BI_REQUIRE(scores && ids && wts, BI_ERR_INVALID_ARG, "null pointer");
   return launch_topk(scores, ids, wts, probs, M, E, top_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, bi_stream_t stream) {
+  BI_REQUIRE(out && blocks > 0 && blocks < (int64_t(1) << 31) && iters > 0, BI_ERR_INVALID_ARG,
+             "bad probe arguments");
+  return launch_fp32_fma_probe(out, blocks, iters, reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {

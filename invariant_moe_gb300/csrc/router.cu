@@ -19,8 +19,8 @@
 //                         lanes own slices: streams W for decode batches
 //   sliced  (16 < M < 384) 8x16 output tile per CTA, one warp per slice, the
 //                         partials combined in slice order through smem
-//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over up to 128
-//                         columns, TMR x 4 outputs per thread, cp.async
+//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over 128 or
+//                         256 columns, TMR x 4 outputs per thread, cp.async
 //                         3-stage ring, slices summed into a running sum
 #include "bimoe_internal.cuh"
 
@@ -246,21 +246,21 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
 
 // ------------------------------------------------------------------- tiled --
 // Register-tiled FFMA kernel for large M.  A CTA is 8 warps arranged as RB
-// row blocks x CB column blocks (CB = 32-column blocks, at most 4: a CTA
-// covers up to 128 columns); thread (r, c) of a warp owns rows base + 4i + r
+// row blocks x CB column blocks (32 columns each, CB <= 8); thread (r, c)
+// of a warp owns rows base + 4i + r
 // (i < TMR) and columns base + 8j + c (j < 4).  K advances in chunks of 32
 // through a 3-stage cp.async ring of [rows][32 + 4] fp32 tiles (k
 // contiguous, padded so the 16-byte loads along k are bank-conflict free);
 // each chunk is consumed four k at a time, each output's chain in increasing
 // k.  Every 128 k (4 chunks) the chain value is added to the running sum and
-// restarted from +0.0f.  At most 128 registers per thread so that two CTAs
-// (16 warps) share an SM: with 8 warps the FFMA issue rate was ~50%.
+// restarted from +0.0f.  TMR <= 4 keeps a thread under 128 registers so two
+// CTAs can share an SM; TMR 7 and 8 take one CTA per SM.
 constexpr int kTBK = 32;              // k per chunk
 constexpr int kTLd = kTBK + 4;        // padded smem row length (floats)
 constexpr int kTStages = 3;
 
 template <int TMR, int CB>
-__global__ void __launch_bounds__(256, 2) router_tiled_kernel(const float *__restrict__ x,
+__global__ void __launch_bounds__(256, (TMR > 4 ? 1 : 2)) router_tiled_kernel(const float *__restrict__ x,
                                                            const float *__restrict__ w,
                                                            const float *__restrict__ bias,
                                                            float *__restrict__ y, int M, int K,
@@ -389,30 +389,39 @@ static bi_status launch_tiled_t(const float *x, const float *w, const float *b, 
   return BI_OK;
 }
 
-// Rows per thread for the tiled schedule: the largest TMR (<= 4) whose grid
-// still gives every SM two CTAs (16 warps), else TMR = 1.
-static int pick_tmr(int64_t M, int rows_per_tmr, int64_t col_blocks, int sms) {
-  for (int t = 4; t > 1; --t) {
-    const int64_t ctas = (M + rows_per_tmr * t - 1) / (rows_per_tmr * t) * col_blocks;
-    if (ctas >= 2 * static_cast<int64_t>(sms) * 4 / 5) return t;
-  }
-  return 1;
-}
-
+// Tile shape for the tiled schedule: the (column blocks, rows per thread)
+// pair with the smallest per-SM load ceil(CTAs / SMs) * TMR, taking the first
+// of a preference list on ties (measured on GB300: a full-width 7-row tile
+// for the widest batches, 128-column tiles with fewer rows otherwise).
 static bi_status launch_tiled(const float *x, const float *w, const float *b, float *y, int64_t M,
                               int64_t K, int64_t N, cudaStream_t stream) {
-  const int cb = N > 64 ? 4 : (N > 32 ? 2 : 1);
-  const int rows_per_tmr = (8 / cb) * 4;
-  const int tmr = pick_tmr(M, rows_per_tmr, (N + cb * 32 - 1) / (cb * 32), num_sms());
-#define BI_TILED(T)                                                                      case T:                                                                                  switch (cb) {                                                                            case 8: return launch_tiled_t<T, 8>(x, w, b, y, M, K, N, stream);                      case 4: return launch_tiled_t<T, 4>(x, w, b, y, M, K, N, stream);                      case 2: return launch_tiled_t<T, 2>(x, w, b, y, M, K, N, stream);                      default: return launch_tiled_t<T, 1>(x, w, b, y, M, K, N, stream);                   }
-  switch (tmr) {
-    BI_TILED(1)
-    BI_TILED(2)
-    BI_TILED(3)
-    BI_TILED(4)
+  struct Shape { int cb, tmr; };
+  static const Shape wide[] = {{8, 7}, {8, 8}, {4, 4}, {4, 3}, {4, 2}, {4, 1}};
+  static const Shape narrow[] = {{4, 4}, {4, 3}, {4, 2}, {4, 1}};
+  const bool is_wide = N > 128;
+  const Shape *list = is_wide ? wide : narrow;
+  const int nlist = is_wide ? 6 : 4;
+  const int sms = num_sms();
+  Shape pick = list[0];
+  int64_t best = INT64_MAX;
+  for (int i = 0; i < nlist; ++i) {
+    const Shape sh = list[i];
+    const int bm = (8 / sh.cb) * 4 * sh.tmr, bn = sh.cb * 32;
+    const int64_t ctas = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+    const int64_t cost = ((ctas + sms - 1) / sms) * sh.tmr;
+    if (cost < best) {
+      best = cost;
+      pick = sh;
+    }
   }
-#undef BI_TILED
-  return BI_ERR_UNSUPPORTED;
+  switch (pick.cb * 16 + pick.tmr) {
+    case 8 * 16 + 7: return launch_tiled_t<7, 8>(x, w, b, y, M, K, N, stream);
+    case 8 * 16 + 8: return launch_tiled_t<8, 8>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 4: return launch_tiled_t<4, 4>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 3: return launch_tiled_t<3, 4>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 2: return launch_tiled_t<2, 4>(x, w, b, y, M, K, N, stream);
+    default: return launch_tiled_t<1, 4>(x, w, b, y, M, K, N, stream);
+  }
 }
 
 // ------------------------------------------------------- negative control --
