@@ -15,9 +15,9 @@
 // contraction or reassociation freedom.  Schedules differ only in which
 // thread evaluates which p_s and in tile sizes; they are chosen from M for
 // speed:
-//   rows    (M <= 16)     one warp per weight row and up to 4 token rows,
+//   rows    (M <= 4)      one warp per weight row and up to 4 token rows,
 //                         lanes own slices: streams W for decode batches
-//   sliced  (16 < M < 384) 8x16 output tile per CTA, one warp per slice, the
+//   sliced  (4 < M < 384) 8x16 output tile per CTA, one warp per slice, the
 //                         partials combined in slice order through smem
 //   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over 128 or
 //                         256 columns, TMR x 4 outputs per thread, cp.async
@@ -469,7 +469,7 @@ __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float 
 bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
                         int64_t K, int64_t N, int schedule, cudaStream_t stream) {
   const int S = static_cast<int>(K / kSlice);
-  if (schedule == 0) schedule = (M <= 16) ? 1 : (M < 384 ? 2 : 3);
+  if (schedule == 0) schedule = (M <= 4) ? 1 : (M < 384 ? 2 : 3);
   if (schedule == 1) {
     const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
     dim3 grid(static_cast<unsigned>(N), static_cast<unsigned>((M + mr - 1) / mr));

@@ -169,3 +169,15 @@ def batch_sizes(max_m=4096):
         s.update({p - 1, p, p + 1})
         p *= 2
     return sorted(v for v in s if v <= max_m)
+
+
+def unambiguous_rows(r64, k, margin=1e-4):
+    """Rows of fp64 scores whose top-k selection cannot be changed by a
+    perturbation smaller than `margin`: among the k+1 largest scores every
+    adjacent gap is either exactly 0 (an exact tie, decided by index on both
+    sides) or at least `margin`.  Used to compare selections made from
+    scores computed in different precisions."""
+    r = np.asarray(r64, np.float64)
+    s = -np.sort(-r, axis=1)[:, : k + 1]
+    gaps = s[:, :-1] - s[:, 1:]
+    return np.where(np.all((gaps == 0) | (gaps >= margin), axis=1))[0]

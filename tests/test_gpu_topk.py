@@ -40,16 +40,24 @@ def test_quantised_tie_plateaus(oracle_mod, cuda, E, k):
 
 def test_router_tie_construction(oracle_mod, cuda):
     """Duplicated W rows give exact ties in every row (the GEMM computes every
-    column with the same arithmetic); the selection must break them by index."""
+    column with the same arithmetic); both sides must break them by index.
+    The oracle selects on its own fp64 scores (from the host inputs) rounded
+    to fp32; rows with a near-tie closer than 1e-4 are left out of the id
+    comparison (exact ties stay in)."""
     import invariant_moe_gb300 as bm
     inp, _ = syn.router_tie_inputs(M=4096)
     y = bm.bi_router_gemm(inp.x.to(cuda), inp.w.to(cuda), inp.b.to(cuda))
+    ids, _, _ = bm.bi_topk(y, 8)
     torch.cuda.synchronize()
-    yc = y.cpu()
-    ids = check(oracle_mod, yc, 8, cuda)
-    # duplicated experts really tie: some row selects a member of a plateau
-    # while an equal-scored higher-index copy is left out
-    assert (yc.numpy()[:, None, :] == yc.numpy()[:, :, None]).sum() > 4096 * 256
+    ids = ids.cpu().numpy()
+    rows = torch.randperm(4096, generator=syn.gen(6))[:512].numpy()
+    r = oracle_mod.router(inp.x[rows].numpy(), inp.w.numpy(), inp.b.numpy())
+    ok = syn.unambiguous_rows(r, 8)
+    assert len(ok) >= 0.9 * len(rows)
+    ids_o, _ = oracle_mod.topk(r.astype(np.float32), 8)
+    assert np.array_equal(ids[rows][ok], ids_o[ok])
+    # the plateaus are real: duplicated experts score exactly alike
+    assert (r[:, None, :] == r[:, :, None]).sum() > len(rows) * 256
     # invariance of the selection over batch sizes
     for M in syn.batch_sizes(4096):
         y_m = bm.bi_router_gemm(inp.x[:M].contiguous().to(cuda), inp.w.to(cuda), inp.b.to(cuda))
