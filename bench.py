@@ -150,6 +150,21 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def captured_traffic(kernel):
+    """DRAM bytes per launch of an expert GEMM from the committed ncu capture,
+    or None when the kernel source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "moe_gemm_qwen4096_traffic.json")
+    src = os.path.join(ROOT, "invariant_moe_gb300", "csrc", "moe_gemm.cu")
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    d = json.load(open(path))
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("kernel_source_sha256"):
+        return None
+    k = d.get(kernel, {})
+    return k.get("dram_read_bytes", 0) + k.get("dram_write_bytes", 0) or None
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -178,7 +193,7 @@ def run_ours(args, rank, world, local):
     out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     lib = bm.load_library()
     ws_perm = torch.empty(max(int(lib.bi_moe_permute_workspace_bytes(M, E)), 256), dtype=torch.uint8, device=dev)
-    ws_gu = torch.empty(max(int(lib.bi_moe_gate_up_workspace_bytes(M, H, k)), 256), dtype=torch.uint8, device=dev)
+    x_perm = torch.empty(P, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = {n: [] for n in ("gate_up", "down")}
 
@@ -187,12 +202,13 @@ def run_ours(args, rank, world, local):
         bm.bi_router_gemm(x32, w.w_router, None, out=scores)
         bm.bi_topk(scores, k, ids=ids, wts=wts)
         bm.bi_moe_permute(ids, E, offsets=offsets, perm=perm, workspace=ws_perm)
+        bm.bi_moe_gather(x, offsets, perm, k, x_perm=x_perm)
         if record:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e2 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        bm.bi_moe_gate_up(x, offsets, perm, wts, w.w13, k, act=act, workspace=ws_gu)
+        bm.bi_moe_gate_up(x_perm, offsets, perm, wts, w.w13, k, act=act)
         if record:
             e1.record(stream)
         bm.bi_moe_down(act, offsets, perm, w.w2, M, k, contrib=contrib)
@@ -276,9 +292,13 @@ def run_ours(args, rank, world, local):
                    "router": f"fp32 [{M},{H}] x [{E},{H}]^T", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights %.2f GB streamed per step)"
                          % ((E * 3 * I * H * 2) / 1e9)},
-        "roofline": {"kernel": "gate_up stage (row gather + tcgen05 grouped GEMM + SwiGLU*p)",
+        "roofline": {"kernel": "moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)",
                      "bound": "tensor", "achieved": gu_tf, "peak": tc_sust, "unit": "TFLOP/s",
-                     "frac": gu_tf / tc_sust, "traffic": None,
+                     "frac": gu_tf / tc_sust,
+                     "traffic": (captured_traffic("gate_up") if args.workload == "qwen" and M == 4096
+                                 else None),
+                     "traffic_unit": "bytes per launch (ncu dram read+write)",
+                     "algorithmic_flops_per_launch": gu_flops,
                      "peak_source": f"{peak_src} bf16 sustained",
                      "ms_per_launch": gu_ms,
                      "down_ms_per_launch": dn_ms,

@@ -214,21 +214,30 @@ BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets,
                                 size_t workspace_bytes, bi_stream_t stream);
 
 /*
- * bi_moe_gate_up -- act[p, j] = bf16(silu(g) * u * wts[perm[p]]) for every
- * permuted position p < M*top_k, with g/u the gate/up projections of token
- * perm[p]/top_k by the expert owning position p (tcgen05 bf16 MMA, fp32
- * accumulation in tensor memory, K step 64, no split-K).
- *   x [M,H] bf16; offsets/perm from bi_moe_permute; wts [M,top_k] fp32;
- *   w13 [E,2I,H] bf16; act [M*top_k, I] bf16 (device, written).
- *   workspace: >= bi_moe_gate_up_workspace_bytes(M, H, top_k) bytes (holds
- *   the gathered token rows).
+ * bi_moe_gather -- x_perm[p, :] = x[perm[p] / top_k, :] for every permuted
+ * position p < offsets[E]: the token rows in expert order, contiguous so the
+ * gate/up GEMM can stream them with TMA.  x [M,H] bf16; x_perm [M*top_k, H]
+ * bf16 (device, written; 16-byte aligned).  Rows at positions >= offsets[E]
+ * are left untouched.
  */
-BI_API size_t bi_moe_gate_up_workspace_bytes(int64_t M, int64_t H, int32_t top_k);
-BI_API bi_status bi_moe_gate_up(const bi_bf16 *x, const int32_t *offsets,
+BI_API bi_status bi_moe_gather(const bi_bf16 *x, const int32_t *offsets,
+                               const int32_t *perm, bi_bf16 *x_perm, int64_t M,
+                               int64_t H, int64_t E, int32_t top_k,
+                               bi_stream_t stream);
+
+/*
+ * bi_moe_gate_up -- act[p, j] = bf16(silu(g) * u * wts[perm[p]]) for every
+ * permuted position p < M*top_k, with g/u the gate/up projections of row p
+ * of x_perm by the expert owning position p (tcgen05 bf16 MMA, fp32
+ * accumulation in tensor memory, K step 64, no split-K).
+ *   x_perm [M*top_k, H] bf16 from bi_moe_gather (16-byte aligned);
+ *   offsets/perm from bi_moe_permute; wts [M,top_k] fp32;
+ *   w13 [E,2I,H] bf16 (16-byte aligned); act [M*top_k, I] bf16 (written).
+ */
+BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets,
                                 const int32_t *perm, const float *wts,
                                 const bi_bf16 *w13, bi_bf16 *act, int64_t M,
                                 int64_t H, int64_t E, int32_t top_k, int64_t I,
-                                void *workspace, size_t workspace_bytes,
                                 bi_stream_t stream);
 
 /*

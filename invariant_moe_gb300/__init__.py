@@ -32,7 +32,7 @@ EXPORTS = [
     "bi_status_str", "bi_last_error_message", "bi_version", "bi_device_error",
     "bi_cast_bf16_to_f32", "bi_router_gemm", "bi_router_gemm_schedule",
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
-    "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gate_up_workspace_bytes",
+    "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe",
 ]
@@ -75,8 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_forward": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
             "bi_moe_permute_workspace_bytes": ([I64, I64], SZ),
             "bi_moe_permute": ([P, P, P, I64, I64, I32, P, SZ, P], ST),
-            "bi_moe_gate_up_workspace_bytes": ([I64, I64, I32], SZ),
-            "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
+            "bi_moe_gather": ([P, P, P, P, I64, I64, I64, I32, P], ST),
+            "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
@@ -244,21 +244,30 @@ def bi_moe_permute(ids, E, offsets=None, perm=None, workspace=None, stream=None)
     return offsets, perm
 
 
-def bi_moe_gate_up(x, offsets, perm, wts, w13, top_k, act=None, workspace=None, stream=None):
+def bi_moe_gather(x, offsets, perm, top_k, x_perm=None, stream=None):
+    """x_perm [M*top_k, H] bf16: token rows in expert order."""
     M, H = x.shape
+    E = offsets.numel() - 1
+    dev = x.device
+    x_perm = x_perm if x_perm is not None else torch.empty(M * top_k, H, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_gather", _ptr(x, torch.bfloat16, "x"), _ptr(offsets, torch.int32, "offsets", dev),
+          _ptr(perm, torch.int32, "perm", dev), _ptr(x_perm, torch.bfloat16, "x_perm", dev),
+          M, H, E, top_k, _stream(stream))
+    return x_perm
+
+
+def bi_moe_gate_up(x_perm, offsets, perm, wts, w13, top_k, act=None, stream=None):
+    """act [M*top_k, I] bf16 from gathered rows x_perm [M*top_k, H]."""
+    P, H = x_perm.shape
+    M = P // top_k
     E, twoI, _ = w13.shape
     I = twoI // 2
-    dev = x.device
-    lib = load_library()
-    act = act if act is not None else torch.empty(M * top_k, I, dtype=torch.bfloat16, device=dev)
-    if workspace is None:
-        workspace = torch.empty(max(int(lib.bi_moe_gate_up_workspace_bytes(M, H, top_k)), 256),
-                                dtype=torch.uint8, device=dev)
-    _call("bi_moe_gate_up", _ptr(x, torch.bfloat16, "x"), _ptr(offsets, torch.int32, "offsets", dev),
-          _ptr(perm, torch.int32, "perm", dev), _ptr(wts, torch.float32, "wts", dev),
-          _ptr(w13, torch.bfloat16, "w13", dev), _ptr(act, torch.bfloat16, "act", dev),
-          M, H, E, top_k, I, _ptr(workspace, torch.uint8, "workspace", dev), workspace.numel(),
-          _stream(stream))
+    dev = x_perm.device
+    act = act if act is not None else torch.empty(P, I, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_gate_up", _ptr(x_perm, torch.bfloat16, "x_perm"),
+          _ptr(offsets, torch.int32, "offsets", dev), _ptr(perm, torch.int32, "perm", dev),
+          _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+          _ptr(act, torch.bfloat16, "act", dev), M, H, E, top_k, I, _stream(stream))
     return act
 
 

@@ -305,11 +305,6 @@ BI_API size_t bi_moe_permute_workspace_bytes(int64_t M, int64_t E) {
   return align256(permute_scratch_bytes(M, E));
 }
 
-BI_API size_t bi_moe_gate_up_workspace_bytes(int64_t M, int64_t H, int32_t top_k) {
-  if (M < 0 || H <= 0 || top_k <= 0) return 0;
-  return align256(static_cast<size_t>(M) * top_k * H * 2);
-}
-
 BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, int64_t M,
                                 int64_t E, int32_t top_k, void *workspace, size_t workspace_bytes,
                                 bi_stream_t stream) {
@@ -332,24 +327,32 @@ BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets, int32_t *p
   return launch_permute(ids, offsets, perm, M, E, top_k, workspace, s);
 }
 
-BI_API bi_status bi_moe_gate_up(const bi_bf16 *x, const int32_t *offsets, const int32_t *perm,
+BI_API bi_status bi_moe_gather(const bi_bf16 *x, const int32_t *offsets, const int32_t *perm,
+                               bi_bf16 *x_perm, int64_t M, int64_t H, int64_t E, int32_t top_k,
+                               bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && H > 0 && H % 8 == 0 && E >= 1, BI_ERR_INVALID_ARG, "bad sizes (H %% 8 == 0)");
+  BI_REQUIRE(top_k >= 1 && top_k <= 16, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  BI_REQUIRE(M * top_k < (int64_t(1) << 31), BI_ERR_UNSUPPORTED, "M*top_k exceeds int32");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(x && offsets && perm && x_perm, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(x, 16) && aligned(x_perm, 16), BI_ERR_INVALID_ARG,
+             "x and x_perm must be 16-byte aligned");
+  return launch_gather(x, perm, offsets, M * top_k, H, E, top_k, x_perm,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets, const int32_t *perm,
                                 const float *wts, const bi_bf16 *w13, bi_bf16 *act, int64_t M,
-                                int64_t H, int64_t E, int32_t top_k, int64_t I, void *workspace,
-                                size_t workspace_bytes, bi_stream_t stream) {
+                                int64_t H, int64_t E, int32_t top_k, int64_t I,
+                                bi_stream_t stream) {
   bi_status st = check_moe_dims(M, H, E, top_k, I);
   if (st != BI_OK) return st;
   if (M == 0) return BI_OK;
-  BI_REQUIRE(x && offsets && perm && wts && w13 && act && workspace, BI_ERR_INVALID_ARG,
-             "null pointer");
-  BI_REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(workspace, 256), BI_ERR_INVALID_ARG,
-             "x/w13 must be 16-byte and workspace 256-byte aligned");
-  BI_REQUIRE(workspace_bytes >= bi_moe_gate_up_workspace_bytes(M, H, top_k), BI_ERR_WORKSPACE,
-             "workspace too small");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t P = M * top_k;
-  st = launch_gather(x, perm, offsets, P, H, E, top_k, workspace, s);
-  if (st != BI_OK) return st;
-  return launch_gate_up(workspace, offsets, perm, wts, w13, act, P, H, E, top_k, I, s);
+  BI_REQUIRE(x_perm && offsets && perm && wts && w13 && act, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(x_perm, 16) && aligned(w13, 16), BI_ERR_INVALID_ARG,
+             "x_perm/w13 must be 16-byte aligned");
+  return launch_gate_up(x_perm, offsets, perm, wts, w13, act, M * top_k, H, E, top_k, I,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets, const int32_t *perm,

@@ -79,14 +79,27 @@ def stage_inputs(M, H, E, I, k, seed, unit=False):
     return w, x, ids, wts
 
 
+def test_gather_stage_exact(oracle_mod, cuda):
+    """Gathered rows are the token rows in expert order, bit for bit."""
+    import invariant_moe_gb300 as bm
+    M, H, E, k = 333, 384, 16, 4
+    x = syn.moe_tokens(M, H, seed=91, unit=True)
+    ids, _ = syn.random_routing(M, E, k, seed=92)
+    off, perm = oracle_mod.permute(ids.numpy(), E)
+    xp = bm.bi_moe_gather(x.to(cuda), torch.from_numpy(off).to(cuda), torch.from_numpy(perm).to(cuda), k)
+    torch.cuda.synchronize()
+    assert torch.equal(xp.cpu(), x[torch.from_numpy(perm).long() // k])
+
+
 @pytest.mark.parametrize("M,H,E,I,k,unit", [(64, 2048, 128, 768, 8, False), (37, 256, 8, 256, 2, True),
                                             (1, 2048, 128, 768, 8, True), (300, 512, 4, 128, 1, True)])
 def test_gate_up_stage(oracle_mod, cuda, M, H, E, I, k, unit):
     import invariant_moe_gb300 as bm
     w, x, ids, wts = stage_inputs(M, H, E, I, k, seed=M + H, unit=unit)
     off, perm = oracle_mod.permute(ids.numpy(), E)
-    act = bm.bi_moe_gate_up(x.to(cuda), torch.from_numpy(off).to(cuda), torch.from_numpy(perm).to(cuda),
-                            wts.to(cuda), w.w13.to(cuda), k)
+    offd, permd = torch.from_numpy(off).to(cuda), torch.from_numpy(perm).to(cuda)
+    xp = bm.bi_moe_gather(x.to(cuda), offd, permd, k)
+    act = bm.bi_moe_gate_up(xp, offd, permd, wts.to(cuda), w.w13.to(cuda), k)
     torch.cuda.synchronize()
     got = act.float().cpu().numpy()
     ref = oracle_mod.gate_up(bits(x), off, perm, wts.numpy(), bits(w.w13), E, k, I)
