@@ -260,6 +260,24 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
                                 int64_t H, int32_t top_k, bi_stream_t stream);
 
 /*
+ * bi_moe_gemm_variant -- selects how the expert GEMMs (bi_moe_gate_up,
+ * bi_moe_down and the two GEMMs inside bi_moe_forward) are scheduled, for
+ * the whole process, from the next call on:
+ *   0  automatic (the default): CTA pairs whenever the GEMM's output
+ *      features (I for gate/up, H for down) are a multiple of 256, else one
+ *      CTA per tile;
+ *   1  one CTA per tile (128 weight rows), tcgen05 cta_group::1;
+ *   2  CTA pairs (256 weight rows over two SMs of a cluster), cta_group::2;
+ *      a call whose output features are not a multiple of 256 then fails
+ *      with BI_ERR_UNSUPPORTED.
+ * Both variants evaluate the same per-element K order, so the bits do not
+ * depend on the choice (tests compare them).  *previous (may be NULL)
+ * receives the old setting.  Other values: BI_ERR_INVALID_ARG.  Not
+ * synchronised with calls in flight on other host threads.
+ */
+BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous);
+
+/*
  * bi_moe_forward_noalloc -- bi_moe_forward without a caller-provided
  * workspace, for callers that cannot allocate device memory where they run
  * the layer (code inside an allocator or memory-pool callback, runtimes that

@@ -34,7 +34,7 @@ EXPORTS = [
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
-    "bi_fp32_fma_probe",
+    "bi_fp32_fma_probe", "bi_moe_gemm_variant",
 ]
 
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
+            "bi_moe_gemm_variant": ([I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
         }
@@ -288,6 +289,14 @@ def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
     _call("bi_moe_combine", _ptr(contrib, torch.float32, "contrib"), _ptr(out, torch.bfloat16, "out", dev),
           M, H, top_k, _stream(stream))
     return out
+
+
+def bi_moe_gemm_variant(variant):
+    """Select the expert-GEMM schedule for the process (0 automatic, 1 one CTA
+    per tile, 2 CTA pairs); returns the previous setting."""
+    prev = ctypes.c_int32(0)
+    _call("bi_moe_gemm_variant", int(variant), ctypes.byref(prev))
+    return prev.value
 
 
 def bi_fp32_fma_probe(blocks, iters, stream=None):

@@ -26,6 +26,7 @@ bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, cudaS
 bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const float *,
                          const void *, void *, int64_t, int64_t, int64_t, int32_t, int64_t,
                          cudaStream_t);
+int set_gemm_variant(int v);
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
@@ -410,3 +411,10 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
 }
 
 }  // extern "C"
+
+BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous) {
+  BI_REQUIRE(variant >= 0 && variant <= 2, BI_ERR_INVALID_ARG, "variant %d not in {0, 1, 2}", variant);
+  const int old = bimoe::set_gemm_variant(variant);
+  if (previous) *previous = old;
+  return BI_OK;
+}

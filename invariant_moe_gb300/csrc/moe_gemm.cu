@@ -26,14 +26,26 @@
 //     re-read each token tile, and the kernel is bound by memory traffic.)
 //   * down: 128 rows of W2 (h) against up to 256 tokens per tile; the
 //     epilogue writes fp32 contributions to row token*top_k + slot.
-//   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a 4-deep ring of
-//     48 KB stages; accumulators are double buffered (2 x 256 tensor-memory
-//     columns) so the epilogue of one tile overlaps the MMAs of the next.
+//   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a ring of stages;
+//     accumulators are double buffered (2 x 256 tensor-memory columns) so the
+//     epilogue of one tile overlaps the MMAs of the next.
+//   * CTA pairs (cta_group::2, the default when the output features are a
+//     multiple of 256): two SMs of a cluster share one tile of 256 weight
+//     rows.  Each SM stages its own 128 weight rows and HALF of the token
+//     rows; one thread of the even CTA issues M=256 MMAs that read the token
+//     rows from both SMs, so each SM receives 32 KB (down) or 40 KB
+//     (gate/up) per K step instead of 48 KB for the same MMA work per SM.
+//     The kernels are bound by how many bytes each SM can keep in flight,
+//     so this is the lever.  Every output element still sees the same K
+//     order (64-wide steps of four K=16 MMAs, increasing k).
 //   * warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues the
 //     MMAs from one thread, warps 2-5 drain the accumulator (tcgen05.ld).
-//   * persistent grid (one CTA per SM); tiles are ordered expert, weight
-//     block, token block, so the token blocks of a weight block run back to
-//     back and share it through L2.
+//   * persistent grid (one CTA, or CTA pair, per SM or SM pair); tiles are
+//     ordered expert, weight block, token block, so the token blocks of a
+//     weight block run back to back and share it through L2.
+#include <atomic>
+#include <mutex>
+
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
@@ -42,22 +54,27 @@ constexpr int kBM = 128;                    // MMA M: weight rows per tile
 constexpr int kBK = 64;                     // K per stage (one swizzle atom of bf16)
 constexpr int kUK = 16;                     // K of one MMA
 constexpr int kTileBytes = kBM * kBK * 2;   // 16 KB: one 128-row operand tile
-constexpr int kStages = 4;
 constexpr int kAccCols = 256;               // tensor-memory columns per accumulator buffer
 constexpr int kNumAcc = 2;                  // double-buffered
 constexpr int kTmemCols = kNumAcc * kAccCols;
 constexpr int kGemmThreads = 192;
 constexpr int kAuxBytes = 8192;             // barriers, tile prefix
 
-// gate/up: A = gate + up tiles (32 KB), 128 tokens (16 KB), two 128-column
-// accumulators per buffer.  down: A = one tile (16 KB), 256 tokens (32 KB),
-// one 256-column accumulator per buffer.  Both stages are 48 KB.
-template <bool GATE_UP>
+// gate/up: A = gate + up tiles (32 KB), up to 128 tokens, two 128-column
+// accumulators per buffer.  down: A = one tile (16 KB), up to 256 tokens, one
+// 256-column accumulator per buffer.  One CTA per tile stages all the tile's
+// token rows (48 KB stages, 4 deep); a CTA pair stages half of them per SM
+// (40 KB x 5 for gate/up, 32 KB x 6 for down).
+template <bool GATE_UP, bool PAIR>
 struct GemmCfg {
   static constexpr int kBN = GATE_UP ? 128 : 256;   // tokens per tile (largest MMA N)
+  static constexpr int kBNc = PAIR ? kBN / 2 : kBN; // token rows staged per CTA
   static constexpr int kABytes = (GATE_UP ? 2 : 1) * kTileBytes;
-  static constexpr int kStageBytes = kABytes + kBN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBNc * kBK * 2;
+  static constexpr int kStages = PAIR ? (GATE_UP ? 5 : 6) : 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
 };
 
 struct GemmParams {
@@ -67,8 +84,8 @@ struct GemmParams {
   void *out;               // gate/up: act bf16 [P, I]; down: contrib fp32 [M*top_k, H]
   int E;
   int K;                   // reduction length (H for gate/up, I for down)
-  int n_wb;                // weight blocks per expert (I/128 for gate/up, H/128 for down)
-  int wb_rows;             // output features per weight block (128)
+  int n_wb;                // weight blocks per expert (output features / wb_rows)
+  int wb_rows;             // output features per weight block (128, or 256 for a CTA pair)
   int out_ld;              // output row length (I or H)
   int a_rows_per_expert;   // rows of the weight tensor per expert (2I or H)
   int up_offset;           // row offset of the up half (I), gate/up only
@@ -107,12 +124,13 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
   return __float2bfloat16_rn(__fmul_rn(__fmul_rn(sg, u), p));
 }
 
-template <bool GATE_UP>
+template <bool GATE_UP, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
-  using C = GemmCfg<GATE_UP>;
+  using C = GemmCfg<GATE_UP, PAIR>;
   constexpr int kBN = C::kBN;
+  constexpr int kStages = C::kStages;
   constexpr int kStageBytes = C::kStageBytes;
   constexpr int kABytes = C::kABytes;
   extern __shared__ uint8_t smem_raw[];
@@ -132,6 +150,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nkb = prm.K / kBK;
+  // A CTA pair walks the tile list as one unit: both CTAs see the same tiles.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+  auto wait = [&](uint32_t bar, uint32_t parity, volatile int *ab) {
+    return PAIR ? mbar_wait_cl(bar, parity, ab, prm.err) : mbar_wait(bar, parity, ab, prm.err);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -140,7 +166,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < kNumAcc; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 128);
+      // pair: one arrival per epilogue warp of both CTAs, on the even CTA's barrier
+      mbar_init(smem_u32(&tempty[a]), PAIR ? 8 : 128);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -151,8 +178,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      if (lane == 0) *tmem_slot = 0u;
+      __syncwarp();
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == 2) {
     // tile_prefix[e] = tiles of experts < e; each lane scans a contiguous chunk
@@ -179,99 +213,175 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers are initialised before anything is sent to them
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = tile_prefix[prm.E];
 
+  // The producer and MMA warps run their loops on all 32 lanes (warp-uniform
+  // control flow and operand math); lane 0 performs the waits and the result
+  // is broadcast, and one elected lane issues each TMA / tcgen05 instruction.
+  auto wait_u = [&](uint32_t bar, uint32_t parity, volatile int *ab) {
+    bool okw = true;
+    if (lane == 0) okw = wait(bar, parity, ab);
+    return __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
+  };
+  auto aborted_u = [&]() { return __shfl_sync(0xffffffffu, *abort_flag, 0) != 0; };
+
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_parity = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
-        const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, prm.err)) {
-            ok = false;
-            break;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
+      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+      const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
+                        static_cast<int>(rank) * kBM;
+      // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
+      const int b_row = ti.tok0 + (rank ? ((ti.ntok + 15) & ~15) / 2 : 0);
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_u(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t *st = tiles + stage * kStageBytes;
+        if (PAIR) {
+          // both CTAs' copies complete on the even CTA's barrier, which the
+          // even CTA arms with the bytes of both
+          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+          if (elect_one()) {
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * kStageBytes);
+            tma_load_2d_pair(smem_u32(st), &tmA, fb, kb * kBK, a_row);
+            if (GATE_UP)
+              tma_load_2d_pair(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
+            tma_load_2d_pair(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
           }
-          uint8_t *st = tiles + stage * kStageBytes;
+        } else {
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
-          if (GATE_UP) tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
-          tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, ti.tok0);
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
+            if (GATE_UP) tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
+            tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
           }
         }
-        if (!ok) break;
+        __syncwarp();
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (*abort_flag) {
-        // let every copy this thread started land before the CTA can exit
+      if (!ok) break;
+    }
+    if (lane == 0 && *abort_flag) {
+      // let every copy this warp started land before the CTA can exit
+      if (!PAIR || leader) {
         for (int s = 0; s < kStages; ++s)
-          if ((issued_mask >> s) & 1u)
-            mbar_wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, nullptr, prm.err);
+          if ((issued_mask >> s) & 1u) wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, nullptr);
+      }
+      if (PAIR) {
+        // the odd CTA's copies complete on the even CTA's barriers: give
+        // them time to land (copies take microseconds; this path only runs
+        // after a wait has already given up)
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    if (leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+      for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
         // the MMA N covers the tile's real tokens (a multiple of 16), so a
         // ragged last tile of an expert does not pay for padding columns
         const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
-        const uint32_t idesc = idesc_bf16_f32(kBM, (ti.ntok + 15) & ~15);
-        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, prm.err)) break;
+        const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, (ti.ntok + 15) & ~15);
+        if (!wait_u(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         bool ok = true;
+        // `ready` is lane 0's non-blocking test of the next stage's barrier,
+        // taken while the current stage's MMAs are being accepted, so a
+        // stage that has already landed costs no blocking wait
+        bool ready = lane == 0 && mbar_test<PAIR>(smem_u32(&full[stage]), phase);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, prm.err)) {
+          if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0) &&
+              !wait_u(smem_u32(&full[stage]), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(tiles + stage * kStageBytes);
           const uint32_t b0 = a0 + kABytes;
+          const int nstage = stage + 1 == kStages ? 0 : stage + 1;
+          const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k) {
+            if (k == kBK / kUK / 2)
+              ready = lane == 0 && kb + 1 < nkb && mbar_test<PAIR>(smem_u32(&full[nstage]), nphase);
             const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
             const uint64_t bdesc = sdesc_sw128(b0 + k * kUK * 2);
-            umma_f16(d0, sdesc_sw128(a0 + k * kUK * 2), bdesc, idesc, acc_in);
-            if (GATE_UP)
-              umma_f16(d0 + kBN, sdesc_sw128(a0 + kTileBytes + k * kUK * 2), bdesc, idesc, acc_in);
+            const uint64_t adesc = sdesc_sw128(a0 + k * kUK * 2);
+            const uint64_t udesc = sdesc_sw128(a0 + kTileBytes + k * kUK * 2);
+            if (elect_one()) {
+              if (PAIR) {
+                umma_f16_pair(d0, adesc, bdesc, idesc, acc_in);
+                if (GATE_UP) umma_f16_pair(d0 + kBN, udesc, bdesc, idesc, acc_in);
+              } else {
+                umma_f16(d0, adesc, bdesc, idesc, acc_in);
+                if (GATE_UP) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
+              }
+            }
+            __syncwarp();
           }
           issued_any = true;
-          umma_commit(smem_u32(&empty[stage]));
+          // frees the stage (in both CTAs of a pair) once these MMAs are done;
+          // elect.sync picks the same lane as for the MMAs
+          if (elect_one()) {
+            if (PAIR) umma_commit_pair(smem_u32(&empty[stage]), 0x3);
+            else umma_commit(smem_u32(&empty[stage]));
+          }
+          __syncwarp();
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&tfull[acc]));
+        if (elect_one()) {
+          if (PAIR) umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+          else umma_commit(smem_u32(&tfull[acc]));
+        }
+        __syncwarp();
         if (++acc == kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      if (*abort_flag && issued_any) {
-        // wait for the MMAs in flight before tensor memory is released
-        umma_commit(smem_u32(drain));
-        mbar_wait(smem_u32(drain), 0, nullptr, prm.err);
+      if (PAIR || (aborted_u() && issued_any)) {
+        // pair: always, telling both CTAs that every MMA into their tensor
+        // memory (and every read of their shared memory) has completed;
+        // single CTA: after an abort, before tensor memory is released
+        if (elect_one()) {
+          if (PAIR) umma_commit_pair(smem_u32(drain), 0x3);
+          else umma_commit(smem_u32(drain));
+        }
+        __syncwarp();
+        if (lane == 0) wait(smem_u32(drain), 0, nullptr);
       }
+    } else if (lane == 0) {
+      // odd CTA of a pair: the even CTA's final commit arrives here
+      wait(smem_u32(drain), 0, nullptr);
     }
     __syncwarp();
   } else {
@@ -302,8 +412,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     };
-    if (static_cast<int>(blockIdx.x) < total_tiles) prefetch(blockIdx.x);
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    if (unit0 < total_tiles) prefetch(unit0);
+    for (int tile = unit0; tile < total_tiles; tile += nunits) {
       const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
       int my_pair[kBN / 32];
       float my_p[kBN / 32];
@@ -312,12 +422,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         my_pair[i] = nx_pair[i];
         my_p[i] = nx_p[i];
       }
-      if (tile + static_cast<int>(gridDim.x) < total_tiles) prefetch(tile + gridDim.x);
-      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, prm.err)) break;
+      if (tile + nunits < total_tiles) prefetch(tile + nunits);
+      if (!wait(smem_u32(&tfull[acc]), acc_phase, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
-      const int col = ti.wb * prm.wb_rows + row;
+      const int col = ti.wb * prm.wb_rows + static_cast<int>(rank) * kBM + row;
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         const int c0 = 32 * i;
@@ -348,7 +458,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[acc]));
+      if (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      } else {
+        mbar_arrive(smem_u32(&tempty[acc]));
+      }
       if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
@@ -358,64 +473,133 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves (or frees tensor memory) while the other
+  // may still signal its barriers
+  if (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------- host --
-template <bool GATE_UP>
+// 0 = automatic (CTA pairs whenever the output features are a multiple of
+// 256), 1 = one CTA per tile, 2 = CTA pairs.
+static std::atomic<int> g_gemm_variant{0};
+
+int set_gemm_variant(int v) { return g_gemm_variant.exchange(v); }
+
+template <bool GATE_UP, bool PAIR>
 static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                              int64_t P, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+  using C = GemmCfg<GATE_UP, PAIR>;
+  static std::mutex mu;
+  static int max_units[64] = {};  // CTAs (or CTA pairs) resident at once, per device
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmCfg<GATE_UP>::kSmemBytes);
-    if (e != cudaSuccess) {
-      set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      return BI_ERR_CUDA;
+  if (dev < 0 || dev >= 64) {
+    set_error("device ordinal %d out of range", dev);
+    return BI_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (max_units[dev] == 0) {
+      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return BI_ERR_CUDA;
+      }
+      int units = num_sms();
+      if (PAIR) {
+        cfg.gridDim = dim3(2 * (num_sms() / 2));
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR>, &cfg);
+        if (e != cudaSuccess || clusters <= 0) {
+          set_error("cudaOccupancyMaxActiveClusters: %s (%d clusters)", cudaGetErrorString(e), clusters);
+          return BI_ERR_CUDA;
+        }
+        units = clusters;
+      }
+      max_units[dev] = units;
     }
-    attr_done[dev] = true;
   }
   // upper bound on the number of tiles (token blocks per expert <= P/kBN + 1)
-  const int64_t ub = static_cast<int64_t>(p.n_wb) *
-                     (std::min<int64_t>(p.E, P) + P / GemmCfg<GATE_UP>::kBN + 1);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), ub)));
-  moe_gemm_kernel<GATE_UP><<<grid, kGemmThreads, GemmCfg<GATE_UP>::kSmemBytes, stream>>>(tmA, tmB, p);
+  const int64_t ub = static_cast<int64_t>(p.n_wb) * (std::min<int64_t>(p.E, P) + P / C::kBN + 1);
+  const int units = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_units[dev], ub)));
+  cfg.gridDim = dim3(PAIR ? 2 * units : units);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR>, tmA, tmB, p);
+  if (e != cudaSuccess) {
+    set_error("moe_gemm launch: %s", cudaGetErrorString(e));
+    return BI_ERR_CUDA;
+  }
   BI_CHECK_LAUNCH();
   return BI_OK;
+}
+
+// Which variant runs for `features` output features per expert, or -1 (error
+// set) when a forced pair variant does not fit.
+static int pick_variant(int64_t features) {
+  const int v = g_gemm_variant.load();
+  const bool fits = features % (2 * kBM) == 0;
+  if (v == 2 && !fits) {
+    set_error("CTA-pair expert GEMMs need output features %% 256 == 0 (got %lld)",
+              static_cast<long long>(features));
+    return -1;
+  }
+  return (v == 1 || !fits) ? 1 : 2;
 }
 
 bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32_t *perm,
                          const float *wts, const void *w13, void *act, int64_t P, int64_t H,
                          int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
   (void)top_k;
+  const int v = pick_variant(I);
+  if (v < 0) return BI_ERR_UNSUPPORTED;
+  const bool pair = v == 2;
+  const int wb_rows = pair ? 2 * kBM : kBM;
   CUtensorMap tmA, tmB;
+  const uint32_t box_tokens = pair ? GemmCfg<true, true>::kBNc : GemmCfg<true, false>::kBNc;
   if (!make_tma_2d_bf16(&tmA, w13, static_cast<uint64_t>(E * 2 * I), static_cast<uint64_t>(H), kBM) ||
-      !make_tma_2d_bf16(&tmB, x_perm, static_cast<uint64_t>(P), static_cast<uint64_t>(H),
-                        GemmCfg<true>::kBN))
+      !make_tma_2d_bf16(&tmB, x_perm, static_cast<uint64_t>(P), static_cast<uint64_t>(H), box_tokens))
     return BI_ERR_CUDA;
-  GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / kBM), kBM, (int)I,
+  GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
                (int)(2 * I), (int)I, device_error_word()};
-  return launch_gemm<true>(tmA, tmB, p, P, stream);
+  return pair ? launch_gemm<true, true>(tmA, tmB, p, P, stream)
+              : launch_gemm<true, false>(tmA, tmB, p, P, stream);
 }
 
 bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *perm, const void *w2,
                       float *contrib, int64_t P, int64_t H, int64_t E, int32_t top_k, int64_t I,
                       cudaStream_t stream) {
   (void)top_k;
+  const int v = pick_variant(H);
+  if (v < 0) return BI_ERR_UNSUPPORTED;
+  const bool pair = v == 2;
+  const int wb_rows = pair ? 2 * kBM : kBM;
   CUtensorMap tmA, tmB;
+  const uint32_t box_tokens = pair ? GemmCfg<false, true>::kBNc : GemmCfg<false, false>::kBNc;
   if (!make_tma_2d_bf16(&tmA, w2, static_cast<uint64_t>(E * H), static_cast<uint64_t>(I), kBM) ||
-      !make_tma_2d_bf16(&tmB, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I),
-                        GemmCfg<false>::kBN))
+      !make_tma_2d_bf16(&tmB, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I), box_tokens))
     return BI_ERR_CUDA;
-  GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / kBM), kBM, (int)H, (int)H,
-               0, device_error_word()};
-  return launch_gemm<false>(tmA, tmB, p, P, stream);
+  GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / wb_rows), wb_rows, (int)H,
+               (int)H, 0, device_error_word()};
+  return pair ? launch_gemm<false, true>(tmA, tmB, p, P, stream)
+              : launch_gemm<false, false>(tmA, tmB, p, P, stream);
 }
 
 }  // namespace bimoe

@@ -51,6 +51,15 @@ def test_workspace_sizes(lib):
     assert lib.bi_moe_workspace_bytes(0, 2048, 128, 8, 768) > 0
 
 
+def test_gemm_variant_setting(lib):
+    """The expert-GEMM variant is a host-side setting: no GPU needed."""
+    prev = ctypes.c_int32(-1)
+    assert lib.bi_moe_gemm_variant(3, None) == 1
+    assert lib.bi_moe_gemm_variant(-1, None) == 1
+    assert lib.bi_moe_gemm_variant(1, ctypes.byref(prev)) == 0 and prev.value == 0
+    assert lib.bi_moe_gemm_variant(0, ctypes.byref(prev)) == 0 and prev.value == 1
+
+
 def test_host_side_rejections(lib):
     """Argument checks run on the host and never touch the GPU."""
     nul = ctypes.c_void_p(None)

@@ -135,6 +135,57 @@ def test_combine_stage(oracle_mod, cuda):
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * rms(ref))
 
 
+@pytest.fixture
+def gemm_variant():
+    """Set the expert-GEMM variant for one test; restores automatic after."""
+    import invariant_moe_gb300 as bm
+    yield bm.bi_moe_gemm_variant
+    bm.bi_moe_gemm_variant(0)
+
+
+@pytest.mark.parametrize("M,kind", [(1, "rand"), (17, "rand"), (300, "skew"), (4096, "rand")])
+def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
+    """One CTA per tile (M=128 MMAs) and CTA pairs (M=256 MMAs over two SMs)
+    evaluate the same K order, so act, the fp32 contributions and the layer
+    output agree bit for bit, ragged token blocks included."""
+    import invariant_moe_gb300 as bm
+    _, _, w13, w2 = qwen_w
+    H, E, I, k = QWEN["H"], QWEN["E"], QWEN["I"], QWEN["top_k"]
+    x = syn.moe_tokens(M, H, seed=M + 40).to(cuda)
+    f = syn.random_routing if kind == "rand" else syn.skewed_routing
+    ids, wts = f(M, E, k, seed=M + 41)
+    ids, wts = ids.to(cuda), wts.to(cuda)
+    off, perm = bm.bi_moe_permute(ids, E)
+    xp = bm.bi_moe_gather(x, off, perm, k)
+    res = {}
+    for v in (1, 2):
+        gemm_variant(v)
+        act = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
+        contrib = bm.bi_moe_down(act, off, perm, w2, M, k)
+        out = bm.bi_moe_forward(x, ids, wts, w13, w2)
+        torch.cuda.synchronize()
+        res[v] = (act, contrib, out)
+    assert bm.device_error() == 0
+    for a, b in zip(res[1], res[2]):
+        assert torch.equal(a, b)
+
+
+def test_gemm_pair_variant_rejects_unaligned_features(cuda, gemm_variant):
+    """Forcing CTA pairs on I = 128 (not a multiple of 256) is an error, not a
+    silent fallback; automatic selection runs it on one CTA per tile."""
+    import invariant_moe_gb300 as bm
+    M, H, E, I, k = 40, 256, 8, 128, 2
+    w, x, ids, wts = stage_inputs(M, H, E, I, k, seed=5, unit=True)
+    args = (x.to(cuda), ids.to(cuda), wts.to(cuda), w.w13.to(cuda), w.w2.to(cuda))
+    gemm_variant(2)
+    with pytest.raises(RuntimeError, match="BI_ERR_UNSUPPORTED"):
+        bm.bi_moe_forward(*args)
+    gemm_variant(0)
+    bm.bi_moe_forward(*args)
+    torch.cuda.synchronize()
+    assert bm.device_error() == 0
+
+
 # ------------------------------------------------------------ whole layer --
 @pytest.mark.parametrize("M,unit", [(64, False), (64, True), (1, True), (200, True)])
 def test_forward_parity_qwen(oracle_mod, cuda, qwen_w, M, unit):
