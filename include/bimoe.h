@@ -163,6 +163,36 @@ BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts,
                          bi_stream_t stream);
 
 /*
+ * bi_router_topk -- bi_router_gemm followed by bi_topk on its scores, as one
+ * call for the decode path.  The scores y are exactly bi_router_gemm's (same
+ * recipe, same bits) and ids / wts / probs exactly bi_topk's on y.  The
+ * selection grid is launched as a programmatic dependent of the router grid
+ * (programmatic stream serialization): its launch overlaps the router's run
+ * and it waits in hardware (griddepcontrol.wait) for the router's completion
+ * before reading y, which saves the launch gap between the two.  The pages
+ * keep the router ("[BI][DSv4] Batch-invariant GateLinear router with fp32
+ * persistent matmul", whose Perf table puts the decode-size router cost in
+ * microseconds per layer) and the selection as separate ops; they have no
+ * combined counterpart.
+ *   x, w, bias, y, M, K, N  as bi_router_gemm (N <= 512);
+ *   probs, ids, wts, top_k  as bi_topk on y (top_k <= min(16, N)).
+ * Errors as bi_router_gemm / bi_topk.  Stream-ordered, graph-capturable.
+ */
+BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bias,
+                                float *y, float *probs, int32_t *ids, float *wts,
+                                int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                bi_stream_t stream);
+/*
+ * bi_router_topk_schedule -- test hook: bi_router_topk with the router
+ * schedule forced as in bi_router_gemm_schedule.
+ */
+BI_API bi_status bi_router_topk_schedule(const float *x, const float *w,
+                                         const float *bias, float *y, float *probs,
+                                         int32_t *ids, float *wts, int64_t M, int64_t K,
+                                         int64_t N, int32_t top_k, int32_t schedule,
+                                         bi_stream_t stream);
+
+/*
  * bi_moe_workspace_bytes -- bytes of device workspace bi_moe_forward needs
  * for these sizes (a multiple of 256).  Returns 0 for invalid sizes.
  */

@@ -34,7 +34,7 @@ EXPORTS = [
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
-    "bi_fp32_fma_probe", "bi_moe_gemm_variant",
+    "bi_fp32_fma_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
 ]
 
 
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_gemm_variant": ([I32, P], ST),
+            "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
+            "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
         }
@@ -289,6 +291,24 @@ def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
     _call("bi_moe_combine", _ptr(contrib, torch.float32, "contrib"), _ptr(out, torch.bfloat16, "out", dev),
           M, H, top_k, _stream(stream))
     return out
+
+
+def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=0, stream=None):
+    """Router scores and top-k selection in one call (the selection grid is a
+    programmatic dependent of the router grid).  Returns
+    (scores [M,N] fp32, ids [M,top_k] int32, wts [M,top_k] fp32, probs or None)."""
+    M, K = x.shape
+    N = w.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=dev)
+    ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    wts = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    probs = torch.empty(M, N, dtype=torch.float32, device=dev) if want_probs else None
+    _call("bi_router_topk_schedule", _ptr(x, torch.float32, "x"), _ptr(w, torch.float32, "w", dev),
+          _ptr(bias, torch.float32, "bias", dev), _ptr(y, torch.float32, "out", dev),
+          _ptr(probs, torch.float32, "probs", dev), _ptr(ids, torch.int32, "ids", dev),
+          _ptr(wts, torch.float32, "wts", dev), M, K, N, top_k, schedule, _stream(stream))
+    return y, ids, wts, probs
 
 
 def bi_moe_gemm_variant(variant):

@@ -12,6 +12,8 @@ namespace bimoe {
 
 bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
                         int64_t, int, cudaStream_t);
+bi_status launch_topk_dependent(const float *, int32_t *, float *, float *, int64_t, int64_t,
+                                int32_t, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
                                int64_t, int64_t, cudaStream_t);
 bi_status launch_cast_bf16_f32(const void *, float *, int64_t, cudaStream_t);
@@ -288,6 +290,29 @@ BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts, float *p
   if (M == 0) return BI_OK;
   BI_REQUIRE(scores && ids && wts, BI_ERR_INVALID_ARG, "null pointer");
   return launch_topk(scores, ids, wts, probs, M, E, top_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_router_topk_schedule(const float *x, const float *w, const float *bias,
+                                         float *y, float *probs, int32_t *ids, float *wts,
+                                         int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                         int32_t schedule, bi_stream_t stream) {
+  bi_status st = router_checks(x, w, y, M, K, N);
+  if (st != BI_OK) return st;
+  BI_REQUIRE(schedule >= 0 && schedule <= 3, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  BI_REQUIRE(N <= 512, BI_ERR_UNSUPPORTED, "selection needs N <= 512 (N=%lld)", (long long)N);
+  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= N, BI_ERR_INVALID_ARG,
+             "top_k=%d outside [1, min(16, N)]", top_k);
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(ids && wts, BI_ERR_INVALID_ARG, "null pointer");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_router(x, w, bias, y, M, K, N, schedule, s)) != BI_OK) return st;
+  return launch_topk_dependent(y, ids, wts, probs, M, N, top_k, s);
+}
+
+BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bias, float *y,
+                                float *probs, int32_t *ids, float *wts, int64_t M, int64_t K,
+                                int64_t N, int32_t top_k, bi_stream_t stream) {
+  return bi_router_topk_schedule(x, w, bias, y, probs, ids, wts, M, K, N, top_k, 0, stream);
 }
 
 BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, bi_stream_t stream) {

@@ -49,6 +49,16 @@ __device__ __forceinline__ void report_error(int *err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch.  launch_dependents lets a grid launched
+// after this one with the programmatic-serialization attribute start its
+// prologue early; griddep_wait, in that dependent grid, returns once every
+// grid it depends on has completed and its memory is visible (a no-op
+// without such a dependency).  Neither spins in software.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

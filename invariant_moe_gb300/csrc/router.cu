@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
   float *part = xs + MR * 32 * kSlicePad;      // [MR][S]
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
+  griddep_launch_dependents();
   const int S = K / kSlice;
   const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
   float *part = sm + 2 * kSlStage;               // [G][MT][NT]
   __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
   const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
   const int rounds = (S + kSlG - 1) / kSlG;
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(256, (TMR > 4 ? 1 : 2)) router_tiled_kernel(co
   float *ws = smem_f + kTStages * XS;        // [kTStages][BN][kTLd]
 
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
   const int warp = tid >> 5, lane = tid & 31;
   const int rb = warp / CB, cb = warp % CB;
   const int r = lane >> 3, c = lane & 7;

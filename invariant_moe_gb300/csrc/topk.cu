@@ -1,120 +1,70 @@
-// topk.cu -- sigmoid scoring and deterministic top-k expert selection.
-//
-// Source: "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling under
-// batch invariance", commit log, the deterministic per-row top-k commit and
-// the sentinel/NaN audit commits that follow it: rank by score descending,
-// break exact ties by ascending index, canonicalise -0.0 to +0.0, compare a
-// monotone int32 key of the fp32 bits, rank on validity before key (no
-// reserved sentinel value), and never resolve ties through shared-memory
-// atomics.
-//
-// One warp per row, the row held in registers (lane l owns experts l, l+32,
-// ...).  top_k rounds; in each round every lane proposes its best untaken
-// expert and a butterfly of shuffles picks the warp winner by
-// (valid, key desc, index asc).  The result is a pure function of the row.
-#include "bimoe_internal.cuh"
+// topk.cu -- sigmoid scoring and deterministic top-k expert selection: one
+// warp per row running the selection of topk_warp.cuh.
+#include "topk_warp.cuh"
 
 namespace bimoe {
 
-__device__ __forceinline__ int32_t score_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  if (u & 0x80000000u) u ^= 0x7fffffffu;
-  return static_cast<int32_t>(u);
-}
-__device__ __forceinline__ float key_value(int32_t key) {
-  uint32_t u = static_cast<uint32_t>(key);
-  if (u & 0x80000000u) u ^= 0x7fffffffu;
-  return __uint_as_float(u);
-}
-// Logistic sigmoid in fp32: 1 / (1 + e^-v).
-__device__ __forceinline__ float sigmoid_f32(float v) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-v)));
-}
-
-template <int VPL>
+// DEPENDENT: launched as a programmatic dependent of the router grid that
+// writes `scores` (bi_router_topk); it waits for that grid before reading.
+template <int VPL, bool DEPENDENT>
 __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ scores,
                                                    int32_t *__restrict__ ids,
                                                    float *__restrict__ wts,
                                                    float *__restrict__ probs, int M, int E,
                                                    int top_k) {
+  if (DEPENDENT) griddep_wait();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= M) return;  // whole warp leaves together
-  const float *srow = scores + static_cast<size_t>(row) * E;
-  int32_t key[VPL];
-  uint32_t avail = 0;  // bit i: expert lane + 32 i exists and is not taken
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int j = lane + 32 * i;
-    if (j < E) {
-      const float v = srow[j];
-      key[i] = score_key(v);
-      avail |= 1u << i;
-      if (probs) probs[static_cast<size_t>(row) * E + j] = sigmoid_f32(v);
-    } else {
-      key[i] = 0;
-    }
+  topk_row_warp<VPL, DEPENDENT>(scores + static_cast<size_t>(row) * E, E, top_k,
+                            ids + static_cast<size_t>(row) * top_k,
+                            wts + static_cast<size_t>(row) * top_k,
+                            probs ? probs + static_cast<size_t>(row) * E : nullptr, lane);
+}
+
+template <bool DEPENDENT>
+static bi_status launch_topk_t(const float *scores, int32_t *ids, float *wts, float *probs,
+                               int64_t M, int64_t E, int32_t top_k, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((M + 3) / 4);
+  const int vpl = static_cast<int>((E + 31) / 32);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  if (DEPENDENT) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  int32_t my_id = 0;
-  float my_w = 0.0f;
-  for (int t = 0; t < top_k; ++t) {
-    // best candidate of this lane: ascending index, strictly greater key wins
-    int have = 0;
-    int32_t bk = 0;
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if ((avail >> i) & 1u) {
-        if (!have || key[i] > bk) {
-          have = 1;
-          bk = key[i];
-          bi = lane + 32 * i;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const int oh = __shfl_xor_sync(0xffffffffu, have, off);
-      const int32_t ok = __shfl_xor_sync(0xffffffffu, bk, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      const bool better = oh && (!have || ok > bk || (ok == bk && oi < bi));
-      if (better) {
-        have = oh;
-        bk = ok;
-        bi = oi;
-      }
-    }
-    // every lane now holds the winner (bk, bi)
-    if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-    if (lane == t) {
-      my_id = bi;
-      my_w = sigmoid_f32(key_value(bk));
-    }
+  const int Mi = static_cast<int>(M), Ei = static_cast<int>(E);
+  cudaError_t e;
+  switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : 16) {
+    case 1: e = cudaLaunchKernelEx(&cfg, topk_kernel<1, DEPENDENT>, scores, ids, wts, probs, Mi, Ei, top_k); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, topk_kernel<2, DEPENDENT>, scores, ids, wts, probs, Mi, Ei, top_k); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, topk_kernel<4, DEPENDENT>, scores, ids, wts, probs, Mi, Ei, top_k); break;
+    case 8: e = cudaLaunchKernelEx(&cfg, topk_kernel<8, DEPENDENT>, scores, ids, wts, probs, Mi, Ei, top_k); break;
+    default: e = cudaLaunchKernelEx(&cfg, topk_kernel<16, DEPENDENT>, scores, ids, wts, probs, Mi, Ei, top_k); break;
   }
-  if (lane < top_k) {
-    ids[static_cast<size_t>(row) * top_k + lane] = my_id;
-    wts[static_cast<size_t>(row) * top_k + lane] = my_w;
+  if (e != cudaSuccess) {
+    set_error("top-k launch: %s", cudaGetErrorString(e));
+    return BI_ERR_CUDA;
   }
+  BI_CHECK_LAUNCH();
+  return BI_OK;
 }
 
 bi_status launch_topk(const float *scores, int32_t *ids, float *wts, float *probs, int64_t M,
                       int64_t E, int32_t top_k, cudaStream_t stream) {
-  const unsigned blocks = static_cast<unsigned>((M + 3) / 4);
-  const int vpl = static_cast<int>((E + 31) / 32);
-#define BI_TOPK_CASE(V)                                                                       \
-  topk_kernel<V><<<blocks, 128, 0, stream>>>(scores, ids, wts, probs, (int)M, (int)E, top_k); \
-  break;
-  switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : 16) {
-    case 1: BI_TOPK_CASE(1)
-    case 2: BI_TOPK_CASE(2)
-    case 4: BI_TOPK_CASE(4)
-    case 8: BI_TOPK_CASE(8)
-    default: BI_TOPK_CASE(16)
-  }
-#undef BI_TOPK_CASE
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  return launch_topk_t<false>(scores, ids, wts, probs, M, E, top_k, stream);
+}
+
+// The selection of bi_router_topk: launched right behind the router grid
+// that writes `scores`, overlapping its launch with the router's run.
+bi_status launch_topk_dependent(const float *scores, int32_t *ids, float *wts, float *probs,
+                                int64_t M, int64_t E, int32_t top_k, cudaStream_t stream) {
+  return launch_topk_t<true>(scores, ids, wts, probs, M, E, top_k, stream);
 }
 
 }  // namespace bimoe

@@ -51,6 +51,19 @@ def test_workspace_sizes(lib):
     assert lib.bi_moe_workspace_bytes(0, 2048, 128, 8, 768) > 0
 
 
+def test_router_topk_host_checks(lib):
+    """The router + top-k call checks its arguments on the host."""
+    nul = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(0x10000)
+    args = lambda N, k, ids: (fake, fake, nul, fake, nul, ids, fake, 4096, 4096, N, k, nul)
+    assert lib.bi_router_topk(*args(600, 8, fake)) == 2          # N > 512
+    assert lib.bi_router_topk(*args(256, 17, fake)) == 1         # top_k > 16
+    assert lib.bi_router_topk(*args(256, 8, nul)) == 1           # no ids buffer
+    assert lib.bi_router_topk(fake, fake, nul, fake, nul, fake, fake, 4, 100, 256, 8, nul) == 2  # K % 128
+    # M == 0 is a no-op
+    assert lib.bi_router_topk(nul, nul, nul, nul, nul, nul, nul, 0, 4096, 256, 8, nul) == 0
+
+
 def test_gemm_variant_setting(lib):
     """The expert-GEMM variant is a host-side setting: no GPU needed."""
     prev = ctypes.c_int32(-1)
