@@ -165,6 +165,41 @@ def captured_traffic(kernel):
     return k.get("dram_read_bytes", 0) + k.get("dram_write_bytes", 0) or None
 
 
+def roofline_gate_up(args, M, H, E, I, k, gu_ms, dn_ms, hbm_gbs, tc_sust, peak_src):
+    """Roofline of the dominant kernel, the gate/up expert GEMM, against the
+    roof that binds it: its algorithmic bytes per launch (the touched experts'
+    W13, the gathered token rows read, the activations written) over the
+    measured copy bandwidth, or its flops over the sustained bf16 peak,
+    whichever floor is longer."""
+    P = M * k
+    touched = E * (1.0 - (1.0 - k / E) ** M)
+    gu_bytes = touched * 2 * I * H * 2 + P * H * 2 + P * I * 2
+    gu_flops = 2.0 * P * 2 * I * H
+    dn_flops = 2.0 * P * H * I
+    t = gu_ms / 1e3
+    gbs, tfs = gu_bytes / t / 1e9, gu_flops / t / 1e12
+    hbm_bound = gu_bytes / (hbm_gbs * 1e9) >= gu_flops / (tc_sust * 1e12)
+    r = {"kernel": "moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)"}
+    if hbm_bound:
+        r.update({"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+                  "peak_source": f"{peak_src} copy bandwidth"})
+    else:
+        r.update({"bound": "tensor", "achieved": tfs, "peak": tc_sust, "unit": "TFLOP/s", "frac": tfs / tc_sust,
+                  "peak_source": f"{peak_src} bf16 sustained"})
+    r.update({
+        "traffic": captured_traffic("gate_up") if args.workload == "qwen" and M == 4096 else None,
+        "traffic_unit": "bytes per launch (ncu dram read+write)",
+        "algorithmic_bytes_per_launch": gu_bytes,
+        "algorithmic_flops_per_launch": gu_flops,
+        "tensor_tflops": tfs, "tensor_frac_of_sustained": tfs / tc_sust,
+        "hbm_gbs": gbs, "hbm_frac": gbs / hbm_gbs,
+        "ms_per_launch": gu_ms,
+        "down_ms_per_launch": dn_ms,
+        "down_tflops": dn_flops / (dn_ms / 1e3) / 1e12,
+    })
+    return r
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -301,13 +336,11 @@ def run_ours(args, rank, world, local):
     extras = {}
     if rank == 0 and not args.no_extras:
         extras["router_us_vs_M"] = router_sweep(dev)
+        extras["moe_layer_us_vs_M"] = moe_sweep(dev, args.workload)
 
     if rank != 0:
         return None
     hbm, tc_burst, tc_sust, peak_src = measured_peaks()
-    gu_flops = 2.0 * P * 2 * I * H
-    dn_flops = 2.0 * P * H * I
-    gu_tf = gu_flops / (gu_ms / 1e3) / 1e12
     line = {
         "metric": "BI MoE-layer tokens/s (whole hot path: router GEMM + top-k + fused experts)",
         "value": aggregate(M, args.steps, world, sec_max),
@@ -320,17 +353,7 @@ def run_ours(args, rank, world, local):
                    "router": f"fp32 [{M},{H}] x [{E},{H}]^T", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights %.2f GB streamed per step)"
                          % ((E * 3 * I * H * 2) / 1e9)},
-        "roofline": {"kernel": "moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)",
-                     "bound": "tensor", "achieved": gu_tf, "peak": tc_sust, "unit": "TFLOP/s",
-                     "frac": gu_tf / tc_sust,
-                     "traffic": (captured_traffic("gate_up") if args.workload == "qwen" and M == 4096
-                                 else None),
-                     "traffic_unit": "bytes per launch (ncu dram read+write)",
-                     "algorithmic_flops_per_launch": gu_flops,
-                     "peak_source": f"{peak_src} bf16 sustained",
-                     "ms_per_launch": gu_ms,
-                     "down_ms_per_launch": dn_ms,
-                     "down_tflops": dn_flops / (dn_ms / 1e3) / 1e12},
+        "roofline": roofline_gate_up(args, M, H, E, I, k, gu_ms, dn_ms, hbm, tc_sust, peak_src),
         "e2e": {"value": aggregate(M, e2e_steps, world, e2e_sec), "unit": "tokens/s",
                 "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
                 "steps": e2e_steps},
@@ -469,6 +492,75 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
     return res
 
 
+def moe_sweep(dev, workload, Ms=(1, 16, 64, 256, 1024, 4096)):
+    """Whole-layer device time (moe_layer: cast, router, top-k, experts) vs
+    batch size M, through CUDA-graph replay of 10 calls: warm (weights stay
+    in L2 between calls where they fit) and cold (a 256 MB L2-flushing write
+    before each call, its time subtracted).  HBM fraction: touched-expert
+    weights E(1-(1-k/E)^M)*3*I*H*2 + router weights + x and out, over the cold
+    time, against the measured copy bandwidth."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    from tests import synthetic as syn
+    wl = WORKLOADS[workload]
+    H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
+    w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
+    x_all = syn.moe_tokens(max(Ms), H, seed=21, device=str(dev))
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    n = 10
+
+    def graph_time(fn, reps=5):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    def flushes():
+        for _ in range(n):
+            flush.fill_(1.0)
+
+    t_flush = graph_time(flushes)
+    res = {"workload": wl["name"]}
+    for M in Ms:
+        xm = x_all[:M].contiguous()
+
+        def calls():
+            for _ in range(n):
+                bm.moe_layer(xm, w.w_router, w.w13, w.w2, k, stream=stream)
+
+        def cold_calls():
+            for _ in range(n):
+                flush.fill_(1.0)
+                bm.moe_layer(xm, w.w_router, w.w13, w.w2, k, stream=stream)
+
+        warm = graph_time(calls) / n
+        cold = (graph_time(cold_calls) - t_flush) / n
+        touched = E * (1.0 - (1.0 - k / E) ** M)
+        bytes_ = touched * 3 * I * H * 2 + E * H * 4 + M * H * 2 * 2
+        res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(cold, 2),
+                       "cold_tokens_per_s": round(M / (cold * 1e-6), 1),
+                       "cold_hbm_frac": round(bytes_ / (cold * 1e-6) / 1e9 / measured_peaks()[0], 3)}
+    if bm.device_error() != 0:
+        raise RuntimeError("device error in the MoE sweep")
+    return res
+
+
 # ------------------------------------------------------ oracle (CPU) arm --
 def oracle_tokens(args, n_tokens, seed=21):
     """Run the fp64 oracle on n_tokens of the workload; returns seconds."""
@@ -541,6 +633,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router-sweep", action="store_true",
                     help="only print the router device-time sweep (DSv4 router shape)")
+    ap.add_argument("--moe-sweep", action="store_true",
+                    help="only print the whole-layer device-time sweep over M for --workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -549,6 +643,12 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(local)
         print(json.dumps({"router_us_vs_M": router_sweep(torch.device("cuda", local))}), flush=True)
+        return
+    if args.moe_sweep:
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps({"moe_layer_us_vs_M": moe_sweep(torch.device("cuda", local), args.workload)}),
+              flush=True)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

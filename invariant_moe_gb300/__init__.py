@@ -330,7 +330,11 @@ def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
     """Whole hot path of one MoE layer: cast -> router -> top-k -> experts.
     Returns (out, scores, ids, wts)."""
     x32 = bi_cast_bf16_to_f32(x_bf16, stream=stream)
-    scores = bi_router_gemm(x32, w_router, bias, stream=stream)
-    ids, wts, _ = bi_topk(scores, top_k, stream=stream)
+    if x_bf16.shape[0] < 1024:
+        # decode-size batches: the selection grid overlaps the router's launch
+        scores, ids, wts, _ = bi_router_topk(x32, w_router, top_k, bias=bias, stream=stream)
+    else:
+        scores = bi_router_gemm(x32, w_router, bias, stream=stream)
+        ids, wts, _ = bi_topk(scores, top_k, stream=stream)
     out = bi_moe_forward(x_bf16, ids, wts, w13, w2, stream=stream)
     return out, scores, ids, wts
