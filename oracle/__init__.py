@@ -53,6 +53,7 @@ def _load():
             lib.oracle_score_key.argtypes = [ctypes.c_float]
             lib.oracle_score_key.restype = I32
             lib.oracle_topk.argtypes = [P, I64, I64, I32, P, P]
+            lib.oracle_topk_window.argtypes = [P, I64, P, P, I64, I64, I32, P]
             lib.oracle_permute.argtypes = [P, I64, I64, I32, P, P]
             lib.oracle_permute.restype = ctypes.c_int
             lib.oracle_moe.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, P]
@@ -109,6 +110,26 @@ def topk(scores, top_k):
     lib.oracle_topk(ps, M, E, top_k, ids.ctypes.data_as(ctypes.c_void_p),
                     wts.ctypes.data_as(ctypes.c_void_p))
     return ids, wts
+
+
+def topk_window(scores, k, row_start=None, row_end=None, num_cols=None):
+    """Windowed per-row top-k (int32 [n_rows, k]): window-relative columns of
+    the k best in-window scores, ascending, -1 tail.  scores is fp32
+    [n_rows, width] (width = the row stride); num_cols <= width columns exist
+    (default width); row_start / row_end are int64 [n_rows] or None."""
+    lib = _load()
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    n_rows, width = s.shape
+    num_cols = width if num_cols is None else num_cols
+    assert 0 <= num_cols <= width and k > 0
+    rs = None if row_start is None else np.ascontiguousarray(row_start, dtype=np.int64)
+    re = None if row_end is None else np.ascontiguousarray(row_end, dtype=np.int64)
+    out = np.empty((n_rows, k), np.int32)
+    lib.oracle_topk_window(s.ctypes.data_as(ctypes.c_void_p), width,
+                           None if rs is None else rs.ctypes.data_as(ctypes.c_void_p),
+                           None if re is None else re.ctypes.data_as(ctypes.c_void_p),
+                           n_rows, num_cols, k, out.ctypes.data_as(ctypes.c_void_p))
+    return out
 
 
 def permute(ids, E):

@@ -26,7 +26,9 @@
  *    top-k reduction with unit weights in a fixed slot order.
  *  - "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling ...", commit
  *    "deterministic per-row top-k": score descending, exact ties by ascending
- *    index, -0.0 canonicalised to +0.0, ranking on a monotone int32 key.
+ *    index, -0.0 canonicalised to +0.0, ranking on a monotone int32 key; and
+ *    for the windowed (indexer) top-k the same commit plus the masked-lane,
+ *    sentinel and validity-first ranking commits that follow it.
  */
 #include <math.h>
 #include <stdint.h>
@@ -105,6 +107,61 @@ ORACLE_API void oracle_topk(const float *scores, int64_t M, int64_t E,
         }
     }
     free(taken);
+}
+
+/* --------------------------------------------------------- windowed top-k --
+ * The sparse-MLA indexer's per-row top-k ("[BI][DSv4] Pin sparse-MLA decode
+ * and prefill scheduling under batch invariance", commit log: the
+ * deterministic per-row top-k commit, then the masked-lane, sentinel and
+ * validity-first ranking commits).  Row i of scores (row stride ld, num_cols
+ * columns) has the window [rs, re) with rs = clamp(row_start[i], 0,
+ * num_cols) and re = clamp(row_end[i], 0, num_cols) (empty when re <= rs);
+ * row_start / row_end NULL means the whole row.  Only columns inside the
+ * window can be chosen (validity ranks before any score, so no key value is
+ * reserved as a sentinel).  Inside the window columns are ranked by the
+ * monotone key descending, equal keys by ascending column; the first
+ * min(k, window size) are chosen.  out[i, 0..] holds the chosen columns in
+ * ascending column order as window-relative indices (column - rs), then -1
+ * up to k.  Written as: collect the window, sort by rank, keep k, sort the
+ * kept columns. */
+typedef struct { int32_t key; int64_t col; } oracle_kc;
+
+static int by_rank(const void *a, const void *b) {
+    const oracle_kc *x = (const oracle_kc *)a, *y = (const oracle_kc *)b;
+    if (x->key != y->key) return x->key > y->key ? -1 : 1;
+    return x->col < y->col ? -1 : (x->col > y->col ? 1 : 0);
+}
+static int by_col(const void *a, const void *b) {
+    const int64_t x = *(const int64_t *)a, y = *(const int64_t *)b;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+static int64_t clamp64(int64_t v, int64_t lo, int64_t hi) {
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+ORACLE_API void oracle_topk_window(const float *scores, int64_t ld, const int64_t *row_start,
+                                   const int64_t *row_end, int64_t n_rows, int64_t num_cols,
+                                   int32_t k, int32_t *out) {
+    oracle_kc *cand = (oracle_kc *)malloc(sizeof(oracle_kc) * (size_t)(num_cols > 0 ? num_cols : 1));
+    int64_t *kept = (int64_t *)malloc(sizeof(int64_t) * (size_t)(k > 0 ? k : 1));
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t rs = row_start ? clamp64(row_start[i], 0, num_cols) : 0;
+        const int64_t re = row_end ? clamp64(row_end[i], 0, num_cols) : num_cols;
+        int64_t n = 0;
+        for (int64_t c = rs; c < re; ++c) {
+            cand[n].key = oracle_score_key(scores[i * ld + c]);
+            cand[n].col = c;
+            ++n;
+        }
+        qsort(cand, (size_t)n, sizeof(oracle_kc), by_rank);
+        const int64_t m = n < k ? n : k;
+        for (int64_t j = 0; j < m; ++j) kept[j] = cand[j].col;
+        qsort(kept, (size_t)m, sizeof(int64_t), by_col);
+        for (int64_t j = 0; j < k; ++j)
+            out[i * k + j] = j < m ? (int32_t)(kept[j] - rs) : -1;
+    }
+    free(kept);
+    free(cand);
 }
 
 /* ---------------------------------------------------------------- permute --

@@ -319,3 +319,108 @@ def test_combine_is_slot_sum(oracle_mod):
     c = rng.standard_normal((M * k, H)).astype(np.float32)
     out = oracle_mod.combine(c, k)
     assert np.allclose(out, c.astype(np.float64).reshape(M, k, H).sum(axis=1), rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------- windowed top-k --
+# The sparse-MLA indexer's per-row top-k ("[BI][DSv4] Pin sparse-MLA decode
+# and prefill scheduling under batch invariance", commit log).  For rows with
+# no NaN the rank (key desc, column asc) is numpy's stable argsort of the
+# negated values, since the monotone key orders non-NaN floats numerically
+# and makes -0.0 equal to +0.0.
+def f32_bits(bits):
+    return np.array(bits, dtype=np.uint32).view(np.float32)
+
+
+def stable_topk_ref(row, k):
+    """Chosen columns, ascending, by numpy's stable sort of -value."""
+    order = np.argsort(-row.astype(np.float64), kind="stable")[:k]
+    return np.sort(order)
+
+
+@pytest.mark.parametrize("k", [1, 7, 512])
+def test_topk_window_matches_stable_sort(oracle_mod, k):
+    rng = np.random.default_rng(k)
+    for trial in range(40):
+        width = int(rng.integers(1, 1400))
+        row = rng.normal(size=width).astype(np.float32)
+        if trial % 2:   # quantised values: tie plateaus at the cutoff
+            row = np.round(row * 4) / 4
+        if trial % 3 == 0:   # relu plateaus of exact zeros, both signs
+            row = np.maximum(row, 0) * np.where(rng.random(width) < 0.5, -1, 1).astype(np.float32)
+        rs = int(rng.integers(0, width))
+        re = int(rng.integers(rs, width + 1))
+        got = oracle_mod.topk_window(row[None], k, [rs], [re])[0]
+        ref = stable_topk_ref(row[rs:re], k)
+        assert np.array_equal(got[: len(ref)], ref)
+        assert np.all(got[len(ref):] == -1)
+
+
+def test_topk_window_closed_forms(oracle_mod):
+    k = 512
+    # all-equal and all -inf rows: the first k columns of the window
+    for v in (0.5, -np.inf, 0.0):
+        out = oracle_mod.topk_window(np.full((1, 3000), v, np.float32), k, [100], [2900])[0]
+        assert np.array_equal(out, np.arange(k))
+    # window narrower than k: all of it, then -1
+    out = oracle_mod.topk_window(np.random.default_rng(1).normal(size=(1, 630)).astype(np.float32),
+                                 k, [5], [35])[0]
+    assert np.array_equal(out[:30], np.arange(30)) and np.all(out[30:] == -1)
+    # empty windows
+    for rs, re in ((10, 10), (20, 3), (700, 800)):
+        out = oracle_mod.topk_window(np.ones((1, 630), np.float32), 4, [rs], [re])[0]
+        assert np.all(out == -1)
+
+
+def test_topk_window_shift_invariance(oracle_mod):
+    """The same logical row at six window offsets selects the same local
+    indices, whatever the masked lanes around it hold (the masked-lane fix)."""
+    rng = np.random.default_rng(5)
+    logical = np.round(rng.normal(size=600) * 2).astype(np.float32) / 2
+    logical[::7] = -np.inf
+    base = None
+    for off in (0, 1, 17, 100, 511, 1400):
+        buf = np.full((1, 2100), np.inf, np.float32)   # out-of-window lanes would win on score
+        buf[0, off:off + 600] = logical
+        out = oracle_mod.topk_window(buf, 512, [off], [off + 600])[0]
+        base = out if base is None else base
+        assert np.array_equal(out, base), off
+    assert np.array_equal(base, stable_topk_ref(logical, 512))
+
+
+def test_topk_window_signed_zero_and_nan_patterns(oracle_mod):
+    # -0.0 ties +0.0: the lower column wins
+    row = np.array([-0.0, 0.0, -1.0], np.float32)
+    assert list(oracle_mod.topk_window(row[None], 1)[0]) == [0]
+    row = np.array([-1.0, 0.0, -0.0], np.float32)
+    assert list(oracle_mod.topk_window(row[None], 1)[0]) == [1]
+    # the two sentinel-adjacent negative NaNs are distinct keys: 0xfffffffe
+    # (INT32_MIN + 1) ranks above 0xffffffff (INT32_MIN)
+    row = f32_bits([0xFFFFFFFF, 0xFFFFFFFE, 0xFFFFFFFF])
+    assert list(oracle_mod.topk_window(row[None], 1)[0]) == [1]
+    # validity first: a window of 30 negative NaNs inside a wider row never
+    # gives up a slot to an out-of-window lane, whatever that lane holds
+    row = np.concatenate([np.full(300, np.inf, np.float32), f32_bits([0xFFFFFFFF] * 30),
+                          np.full(300, np.inf, np.float32)])
+    out = oracle_mod.topk_window(row[None], 512, [300], [330])[0]
+    assert np.array_equal(out[:30], np.arange(30)) and np.all(out[30:] == -1)
+    # the class ladder: +NaN > +inf > max > min denormal > +0 = -0 > -min denormal > -inf > -NaN
+    ladder = f32_bits([0xFF800000, 0x00000001, 0x7FC00000, 0x80000000, 0x7F800000,
+                       0x80000001, 0xFFC00000, 0x7F7FFFFF, 0x00000000])
+    ranked = [int(c) for c in oracle_mod.topk_window(ladder[None], 9)[0]]
+    assert ranked == list(range(9))   # all chosen, ascending
+    # top-1 is +NaN (col 2), top-2 adds +inf (col 4), top-3 adds max normal (col 7)
+    assert [oracle_mod.topk_window(ladder[None], j)[0].tolist() for j in (1, 2, 3)] == \
+        [[2], [2, 4], [2, 4, 7]]
+
+
+def test_topk_window_bounds_and_stride(oracle_mod):
+    rng = np.random.default_rng(9)
+    buf = rng.normal(size=(3, 1000)).astype(np.float32)
+    # bounds clamp to [0, num_cols]: negative start, end past the end, past int32
+    out = oracle_mod.topk_window(buf, 8, [-50, 0, -(2 ** 40)], [2000, 2 ** 40, 2 ** 41], num_cols=900)
+    for i in range(3):
+        assert np.array_equal(out[i], stable_topk_ref(buf[i, :900], 8))
+    # columns past num_cols (row padding) are never chosen even if they would win
+    buf[:, 900:] = np.inf
+    out2 = oracle_mod.topk_window(buf, 8, None, None, num_cols=900)
+    assert np.array_equal(out2, out)
