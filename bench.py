@@ -337,6 +337,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_extras:
         extras["router_us_vs_M"] = router_sweep(dev)
         extras["moe_layer_us_vs_M"] = moe_sweep(dev, args.workload)
+        extras["topk_window_us"] = topk_window_sweep(dev)
 
     if rank != 0:
         return None
@@ -561,6 +562,48 @@ def moe_sweep(dev, workload, Ms=(1, 16, 64, 256, 1024, 4096)):
     return res
 
 
+def topk_window_sweep(dev, ns=(1, 8, 64), ks=(512, 1024, 2048), num_cols=8192):
+    """Windowed per-row top-k (the sparse-MLA indexer's selection) device time
+    per call, CUDA-graph replay of 20 calls, on relu-plateau rows (about half
+    the scores exactly zero) with each row's window the whole row."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    g = torch.Generator().manual_seed(77)
+    x = torch.randn(max(ns), num_cols, generator=g).clamp_min(0.0).to(dev)
+    stream = torch.cuda.Stream(dev)
+    n_calls = 20
+    res = {"num_cols": num_cols, "scores": "relu(N(0,1)): about half exact zeros"}
+    for n in ns:
+        for k in ks:
+            out = torch.empty(n, k, dtype=torch.int32, device=dev)
+            xs = x[:n].contiguous()
+
+            def calls():
+                for _ in range(n_calls):
+                    bm.bi_topk_window(xs, k, out=out, stream=stream)
+
+            with torch.cuda.stream(stream):
+                calls()
+                stream.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=stream):
+                    calls()
+                gr.replay()
+                stream.synchronize()
+                ts = []
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    gr.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+            res[f"n{n}_k{k}_us"] = round(statistics.median(ts), 2)
+    return res
+
+
 # ------------------------------------------------------ oracle (CPU) arm --
 def oracle_tokens(args, n_tokens, seed=21):
     """Run the fp64 oracle on n_tokens of the workload; returns seconds."""
@@ -633,6 +676,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router-sweep", action="store_true",
                     help="only print the router device-time sweep (DSv4 router shape)")
+    ap.add_argument("--topk-window-sweep", action="store_true",
+                    help="only print the windowed top-k device-time sweep")
     ap.add_argument("--moe-sweep", action="store_true",
                     help="only print the whole-layer device-time sweep over M for --workload")
     args = ap.parse_args(argv)
@@ -643,6 +688,11 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(local)
         print(json.dumps({"router_us_vs_M": router_sweep(torch.device("cuda", local))}), flush=True)
+        return
+    if args.topk_window_sweep:
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps({"topk_window_us": topk_window_sweep(torch.device("cuda", local))}), flush=True)
         return
     if args.moe_sweep:
         import torch

@@ -163,6 +163,32 @@ BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts,
                          bi_stream_t stream);
 
 /*
+ * bi_topk_window -- deterministic per-row top-k over a column window (the
+ * sparse-MLA indexer's selection): "[BI][DSv4] Pin sparse-MLA decode and
+ * prefill scheduling under batch invariance", commit log (the deterministic
+ * per-row top-k commit, the masked-lane fix and the validity-first ranking
+ * commits).
+ *   scores    [n_rows, ld] fp32 (device), the first num_cols columns used;
+ *   row_start, row_end  [n_rows] int64 (device) or NULL (whole rows); the
+ *             window of row i is [rs, re) with rs = clamp(row_start[i], 0,
+ *             num_cols), re = clamp(row_end[i], 0, num_cols), empty if re <= rs;
+ *   out       [n_rows, k] int32 (device, written): the chosen columns as
+ *             window-relative indices (column - rs) in ascending order, then
+ *             -1 up to k.
+ * Chosen: the min(k, window size) in-window columns ranked first by the
+ * monotone int32 key of the fp32 score (descending; -0.0 equals +0.0; NaN
+ * patterns are ordered by their bits, +NaN above +inf, -NaN below -inf), equal
+ * keys by ascending column.  Out-of-window columns are never chosen, whatever
+ * they hold.  A pure function of each row: no atomics decide ties.
+ * Limits: num_cols <= 8192 (else BI_ERR_UNSUPPORTED), 1 <= k <= 8192,
+ * ld >= num_cols.  n_rows == 0 is a no-op.
+ */
+BI_API bi_status bi_topk_window(const float *scores, int64_t ld,
+                                const int64_t *row_start, const int64_t *row_end,
+                                int64_t n_rows, int64_t num_cols, int32_t k,
+                                int32_t *out, bi_stream_t stream);
+
+/*
  * bi_router_topk -- bi_router_gemm followed by bi_topk on its scores, as one
  * call for the decode path.  The scores y are exactly bi_router_gemm's (same
  * recipe, same bits) and ids / wts / probs exactly bi_topk's on y.  The

@@ -35,6 +35,7 @@ EXPORTS = [
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
+    "bi_topk_window",
 ]
 
 
@@ -82,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_gemm_variant": ([I32, P], ST),
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
+            "bi_topk_window": ([P, I64, P, P, I64, I64, I32, P, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
         }
@@ -309,6 +311,25 @@ def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=
           _ptr(probs, torch.float32, "probs", dev), _ptr(ids, torch.int32, "ids", dev),
           _ptr(wts, torch.float32, "wts", dev), M, K, N, top_k, schedule, _stream(stream))
     return y, ids, wts, probs
+
+
+def bi_topk_window(scores, k, row_start=None, row_end=None, num_cols=None, out=None, stream=None):
+    """Windowed per-row top-k: int32 [n_rows, k] window-relative columns of
+    the k best in-window scores, ascending, -1 tail.  scores is fp32
+    [n_rows, ld] with unit column stride (row stride ld >= num_cols)."""
+    if scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be 2-D with unit column stride")
+    n_rows = scores.shape[0]
+    ld = scores.stride(0) if n_rows > 1 else scores.shape[1]
+    num_cols = scores.shape[1] if num_cols is None else num_cols
+    dev = scores.device
+    if scores.dtype != torch.float32 or not scores.is_cuda:
+        raise TypeError("scores must be a CUDA float32 tensor")
+    out = out if out is not None else torch.empty(n_rows, k, dtype=torch.int32, device=dev)
+    _call("bi_topk_window", ctypes.c_void_p(scores.data_ptr()), ld,
+          _ptr(row_start, torch.int64, "row_start", dev), _ptr(row_end, torch.int64, "row_end", dev),
+          n_rows, num_cols, k, _ptr(out, torch.int32, "out", dev), _stream(stream))
+    return out
 
 
 def bi_moe_gemm_variant(variant):

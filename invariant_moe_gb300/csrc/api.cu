@@ -14,6 +14,8 @@ bi_status launch_router(const float *, const float *, const float *, float *, in
                         int64_t, int, cudaStream_t);
 bi_status launch_topk_dependent(const float *, int32_t *, float *, float *, int64_t, int64_t,
                                 int32_t, cudaStream_t);
+bi_status launch_topk_window(const float *, int64_t, const int64_t *, const int64_t *, int64_t,
+                             int64_t, int32_t, int32_t *, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
                                int64_t, int64_t, cudaStream_t);
 bi_status launch_cast_bf16_f32(const void *, float *, int64_t, cudaStream_t);
@@ -313,6 +315,22 @@ BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bia
                                 float *probs, int32_t *ids, float *wts, int64_t M, int64_t K,
                                 int64_t N, int32_t top_k, bi_stream_t stream) {
   return bi_router_topk_schedule(x, w, bias, y, probs, ids, wts, M, K, N, top_k, 0, stream);
+}
+
+BI_API bi_status bi_topk_window(const float *scores, int64_t ld, const int64_t *row_start,
+                                const int64_t *row_end, int64_t n_rows, int64_t num_cols,
+                                int32_t k, int32_t *out, bi_stream_t stream) {
+  BI_REQUIRE(n_rows >= 0 && num_cols >= 0 && ld >= num_cols, BI_ERR_INVALID_ARG,
+             "bad sizes n_rows=%lld num_cols=%lld ld=%lld", (long long)n_rows,
+             (long long)num_cols, (long long)ld);
+  BI_REQUIRE(num_cols <= 8192, BI_ERR_UNSUPPORTED, "num_cols=%lld > 8192", (long long)num_cols);
+  BI_REQUIRE(k >= 1 && k <= 8192, BI_ERR_INVALID_ARG, "k=%d outside [1, 8192]", k);
+  BI_REQUIRE(n_rows < (int64_t(1) << 31) && n_rows * ld < (int64_t(1) << 62), BI_ERR_UNSUPPORTED,
+             "sizes exceed the index range");
+  if (n_rows == 0) return BI_OK;
+  BI_REQUIRE(out && (scores || num_cols == 0), BI_ERR_INVALID_ARG, "null pointer");
+  return launch_topk_window(scores, ld, row_start, row_end, n_rows, num_cols, k, out,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, bi_stream_t stream) {

@@ -64,6 +64,16 @@ def test_router_topk_host_checks(lib):
     assert lib.bi_router_topk(nul, nul, nul, nul, nul, nul, nul, 0, 4096, 256, 8, nul) == 0
 
 
+def test_topk_window_host_checks(lib):
+    nul = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.bi_topk_window(fake, 9000, nul, nul, 4, 9000, 512, fake, nul) == 2   # > 8192 columns
+    assert lib.bi_topk_window(fake, 100, nul, nul, 4, 200, 512, fake, nul) == 1     # ld < num_cols
+    assert lib.bi_topk_window(fake, 8192, nul, nul, 4, 8192, 0, fake, nul) == 1     # k < 1
+    assert lib.bi_topk_window(fake, 8192, nul, nul, 4, 8192, 512, nul, nul) == 1    # no output
+    assert lib.bi_topk_window(nul, 8192, nul, nul, 0, 8192, 512, nul, nul) == 0     # no rows
+
+
 def test_gemm_variant_setting(lib):
     """The expert-GEMM variant is a host-side setting: no GPU needed."""
     prev = ctypes.c_int32(-1)
