@@ -12,8 +12,6 @@ namespace bimoe {
 
 bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
                         int64_t, int, cudaStream_t);
-bi_status launch_topk_dependent(const float *, int32_t *, float *, float *, int64_t, int64_t,
-                                int32_t, cudaStream_t);
 bi_status launch_topk_window(const float *, int64_t, const int64_t *, const int64_t *, int64_t,
                              int64_t, int32_t, int32_t *, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
@@ -308,7 +306,7 @@ BI_API bi_status bi_router_topk_schedule(const float *x, const float *w, const f
   BI_REQUIRE(ids && wts, BI_ERR_INVALID_ARG, "null pointer");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_router(x, w, bias, y, M, K, N, schedule, s)) != BI_OK) return st;
-  return launch_topk_dependent(y, ids, wts, probs, M, N, top_k, s);
+  return launch_topk(y, ids, wts, probs, M, N, top_k, s);
 }
 
 BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bias, float *y,

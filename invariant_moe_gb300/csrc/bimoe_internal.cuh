@@ -35,6 +35,43 @@ bool make_tma_2d_f32(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
                      uint32_t box_rows);
 void set_error(const char *fmt, ...);
 
+// Launches `kernel` as a programmatic dependent of the previous work on the
+// stream (programmatic stream serialization) and, for cluster_x > 1, in
+// clusters of cluster_x CTAs.  Every kernel of this library begins with
+// griddep_wait(), so its launch overlaps the end of its predecessor while
+// every memory access still follows it.  The kernels do not trigger their
+// dependents early (the trigger is each CTA's exit): CTAs of a dependent
+// grid parked on the SMs while a long kernel runs were measured to slow it.
+template <typename... KArgs, typename... Args>
+bi_status launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) {
+    set_error("kernel launch: %s", cudaGetErrorString(e));
+    return BI_ERR_CUDA;
+  }
+  return BI_OK;
+}
+
 #define BI_CHECK_LAUNCH()                                                  \
   do {                                                                     \
     cudaError_t e_ = cudaGetLastError();                                   \

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
   using C = GemmCfg<GATE_UP, PAIR>;
+  griddep_wait();  // the offsets, permutation and operands come from earlier kernels
   constexpr int kBN = C::kBN;
   constexpr int kStages = C::kStages;
   constexpr int kStageBytes = C::kStageBytes;
@@ -542,6 +543,15 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   const int64_t ub = static_cast<int64_t>(p.n_wb) * (std::min<int64_t>(p.E, P) + P / C::kBN + 1);
   const int units = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_units[dev], ub)));
   cfg.gridDim = dim3(PAIR ? 2 * units : units);
+  // a programmatic dependent of the previous kernel on the stream (every
+  // kernel of the library waits for its predecessors before reading)
+  cudaLaunchAttribute attr2[2];
+  attr2[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr2[0].val.programmaticStreamSerializationAllowed = 1;
+  int nattr = 1;
+  if (PAIR) attr2[nattr++] = attr[0];
+  cfg.attrs = attr2;
+  cfg.numAttrs = nattr;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR>, tmA, tmB, p);
   if (e != cudaSuccess) {
     set_error("moe_gemm launch: %s", cudaGetErrorString(e));

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kTokBlock) moe_count_kernel(const int32_t *__r
                                                               int M, int E, int top_k,
                                                               int32_t *__restrict__ blkcnt,
                                                               int *err) {
+  griddep_wait();
   extern __shared__ int s_cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restric
                                                         int nblk, int E,
                                                         int32_t *__restrict__ blkoff,
                                                         int32_t *__restrict__ offsets) {
+  griddep_wait();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   int run = 0;
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *_
                                                                 int M, int E, int top_k,
                                                                 const int32_t *__restrict__ blkoff,
                                                                 int32_t *__restrict__ perm) {
+  griddep_wait();
   constexpr int W = kTokBlock / 32;
   extern __shared__ uint32_t s_bits[];  // [E][W]
   for (int i = threadIdx.x; i < E * W; i += blockDim.x) s_bits[i] = 0u;
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
                                                          const int32_t *__restrict__ offsets,
                                                          int E, int top_k, int row_vec,
                                                          uint4 *__restrict__ xp) {
+  griddep_wait();
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= offsets[E]) return;
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
                                                           __nv_bfloat16 *__restrict__ out, int M,
                                                           int H4, int top_k) {
+  griddep_wait();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(M) * H4) return;
   const int64_t m = idx / H4;
@@ -186,36 +191,33 @@ bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, in
   int32_t *blkcnt = static_cast<int32_t *>(scratch);
   int32_t *blkoff = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + one);
   int *err = device_error_word();
-  moe_count_kernel<<<nblk, kTokBlock, E * sizeof(int), stream>>>(ids, (int)M, (int)E, top_k,
-                                                                 blkcnt, err);
-  BI_CHECK_LAUNCH();
-  moe_scan_kernel<<<1, 1024, 0, stream>>>(blkcnt, nblk, (int)E, blkoff, offsets);
-  BI_CHECK_LAUNCH();
-  moe_scatter_kernel<<<nblk, kTokBlock, E * (kTokBlock / 32) * sizeof(uint32_t), stream>>>(
-      ids, (int)M, (int)E, top_k, blkoff, perm);
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  bi_status st;
+  if ((st = launch_chained(moe_count_kernel, dim3(nblk), dim3(kTokBlock), E * sizeof(int), stream, 1,
+                           ids, (int)M, (int)E, top_k, blkcnt, err)) != BI_OK)
+    return st;
+  if ((st = launch_chained(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, 1, blkcnt, nblk, (int)E,
+                           blkoff, offsets)) != BI_OK)
+    return st;
+  return launch_chained(moe_scatter_kernel, dim3(nblk), dim3(kTokBlock),
+                        E * (kTokBlock / 32) * sizeof(uint32_t), stream, 1, ids, (int)M, (int)E,
+                        top_k, blkoff, perm);
 }
 
 bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offsets, int64_t P,
                         int64_t H, int64_t E, int32_t top_k, void *xp, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((P + 7) / 8);
-  moe_gather_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(x), perm, offsets,
-                                                (int)E, top_k, (int)(H / 8),
-                                                static_cast<uint4 *>(xp));
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  return launch_chained(moe_gather_kernel, dim3(blocks), dim3(256), 0, stream, 1,
+                        static_cast<const uint4 *>(x), perm, offsets, (int)E, top_k, (int)(H / 8),
+                        static_cast<uint4 *>(xp));
 }
 
 bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, int32_t top_k,
                          cudaStream_t stream) {
   const int64_t total = M * (H / 4);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
-  moe_combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(contrib),
-                                                 static_cast<__nv_bfloat16 *>(out), (int)M,
-                                                 (int)(H / 4), top_k);
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  return launch_chained(moe_combine_kernel, dim3(blocks), dim3(256), 0, stream, 1,
+                        reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
+                        (int)M, (int)(H / 4), top_k);
 }
 
 }  // namespace bimoe

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
   float *part = xs + MR * 32 * kSlicePad;      // [MR][S]
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
-  griddep_launch_dependents();
+  griddep_wait();
   const int S = K / kSlice;
   const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
   float *part = sm + 2 * kSlStage;               // [G][MT][NT]
   __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
-  griddep_launch_dependents();
+  griddep_wait();
   const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
   const int rounds = (S + kSlG - 1) / kSlG;
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(256, (TMR > 4 ? 1 : 2)) router_tiled_kernel(co
   float *ws = smem_f + kTStages * XS;        // [kTStages][BN][kTLd]
 
   const int tid = threadIdx.x;
-  griddep_launch_dependents();
+  griddep_wait();
   const int warp = tid >> 5, lane = tid & 31;
   const int rb = warp / CB, cb = warp % CB;
   const int r = lane >> 3, c = lane & 7;
@@ -388,8 +388,8 @@ static bi_status launch_tiled_t(const float *x, const float *w, const float *b, 
     attr_done[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((M + BM - 1) / BM), static_cast<unsigned>((N + BN - 1) / BN));
-  router_tiled_kernel<TMR, CB><<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N);
-  return BI_OK;
+  return launch_chained(router_tiled_kernel<TMR, CB>, grid, dim3(256), smem, stream, 1, x, w, b, y,
+                        (int)M, (int)K, (int)N);
 }
 
 // Tile shape for the tiled schedule: the (column blocks, rows per thread)
@@ -451,6 +451,7 @@ __global__ void router_negctl_kernel(const float *__restrict__ x, const float *_
 // -------------------------------------------------------------------- cast --
 __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float *__restrict__ y,
                                      int64_t n) {
+  griddep_wait();
   const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
   if (i0 + 8 <= n && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
       (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
@@ -490,7 +491,9 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
       cudaFuncSetAttribute(router_rows_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
       attr[dv] = true;                                                                                 \
     }                                                                                                  \
-    router_rows_kernel<R><<<grid, 32, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, device_error_word());            \
+    const bi_status st_ = launch_chained(router_rows_kernel<R>, grid, dim3(32), smem, stream, 1, x, w, \
+                                         b, y, (int)M, (int)K, (int)N, device_error_word());          \
+    if (st_ != BI_OK) return st_;                                                                    \
   }
     if (mr == 1) BI_ROWS(1) else if (mr == 2) BI_ROWS(2) else BI_ROWS(4)
 #undef BI_ROWS
@@ -508,7 +511,9 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
       cudaFuncSetAttribute(router_sliced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       attr[dv] = true;
     }
-    router_sliced_kernel<<<grid, 256, smem, stream>>>(x, w, b, y, (int)M, (int)K, (int)N, device_error_word());
+    const bi_status st = launch_chained(router_sliced_kernel, grid, dim3(256), smem, stream, 1, x, w, b,
+                                        y, (int)M, (int)K, (int)N, device_error_word());
+    if (st != BI_OK) return st;
   } else if (schedule == 3) {
     if ((M + 3) / 4 > 65535LL * 8 * 4) {
       set_error("router tiled schedule: M=%lld too large for it", (long long)M);
@@ -538,10 +543,8 @@ bi_status launch_router_negctl(const float *x, const float *w, const float *b, f
 bi_status launch_cast_bf16_f32(const void *x, float *y, int64_t n, cudaStream_t stream) {
   const int threads = 256;
   const int64_t blocks = (n + threads * 8 - 1) / (threads * 8);
-  cast_bf16_f32_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(x), y, n);
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  return launch_chained(cast_bf16_f32_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                        stream, 1, static_cast<const __nv_bfloat16 *>(x), y, n);
 }
 
 }  // namespace bimoe

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
   __shared__ uint32_t s_digit, s_kk;
   __shared__ uint32_t pre_gt[kTwVT * kTwWarps], pre_tie[kTwVT * kTwWarps];
 
+  griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int64_t rs = row_start ? tw_clamp(row_start[row], 0, num_cols) : 0;
@@ -169,10 +170,8 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
 bi_status launch_topk_window(const float *scores, int64_t ld, const int64_t *row_start,
                              const int64_t *row_end, int64_t n_rows, int64_t num_cols, int32_t k,
                              int32_t *out, cudaStream_t stream) {
-  topk_window_kernel<<<static_cast<unsigned>(n_rows), kTwThreads, 0, stream>>>(
-      scores, ld, row_start, row_end, static_cast<int>(num_cols), k, out);
-  BI_CHECK_LAUNCH();
-  return BI_OK;
+  return launch_chained(topk_window_kernel, dim3(static_cast<unsigned>(n_rows)), dim3(kTwThreads), 0,
+                        stream, 1, scores, ld, row_start, row_end, static_cast<int>(num_cols), k, out);
 }
 
 }  // namespace bimoe
