@@ -522,6 +522,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
       cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) {
+        cudaGetLastError();  // do not leave the error for an unrelated later check
         set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return BI_ERR_CUDA;
       }
@@ -531,6 +532,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR>, &cfg);
         if (e != cudaSuccess || clusters <= 0) {
+          cudaGetLastError();
           set_error("cudaOccupancyMaxActiveClusters: %s (%d clusters)", cudaGetErrorString(e), clusters);
           return BI_ERR_CUDA;
         }

@@ -120,8 +120,10 @@ def test_one_hot_rows(cuda):
 
 
 def test_no_bias_and_other_shapes(oracle_mod, cuda):
-    """Qwen-shaped router (K=2048, N=128), a ragged N, and no bias."""
-    for (M, K, N) in ((50, 2048, 128), (9, 1024, 200), (600, 2048, 100)):
+    """Qwen-shaped router (K=2048, N=128, up to M=4096 where the tiled
+    schedule splits its slices over two thread groups), a ragged N, and no
+    bias."""
+    for (M, K, N) in ((50, 2048, 128), (9, 1024, 200), (600, 2048, 100), (4096, 2048, 128)):
         x = syn.normal((M, K), 1.0, 21)
         w = syn.normal((N, K), K ** -0.5, 22)
         y = run(x.to(cuda), w.to(cuda), None, M).cpu().numpy()
