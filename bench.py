@@ -217,7 +217,6 @@ def run_ours(args, rank, world, local):
     w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
     x = syn.moe_tokens(M, H, seed=21 + rank, device=str(dev))
     # step buffers (allocated once, reused)
-    x32 = torch.empty(M, H, dtype=torch.float32, device=dev)
     scores = torch.empty(M, E, dtype=torch.float32, device=dev)
     ids = torch.empty(M, k, dtype=torch.int32, device=dev)
     wts = torch.empty(M, k, dtype=torch.float32, device=dev)
@@ -233,8 +232,7 @@ def run_ours(args, rank, world, local):
     ev = {n: [] for n in ("gate_up", "down")}
 
     def step(record=False):
-        bm.bi_cast_bf16_to_f32(x, out=x32)
-        bm.bi_router_gemm(x32, w.w_router, None, out=scores)
+        bm.bi_router_gemm(x, w.w_router, None, out=scores)   # bf16 tokens, read as fp32
         bm.bi_topk(scores, k, ids=ids, wts=wts)
         bm.bi_moe_permute(ids, E, offsets=offsets, perm=perm, workspace=ws_perm)
         bm.bi_moe_gather(x, offsets, perm, k, x_perm=x_perm)
@@ -253,7 +251,7 @@ def run_ours(args, rank, world, local):
             ev["down"].append((e1, e2))
         bm.bi_moe_combine(contrib, M, k, out=out)
 
-    launches_per_step = 1 + 1 + 1 + 3 + 2 + 1 + 1  # cast router topk permute(3) gather+gate/up down combine
+    launches_per_step = 1 + 1 + 3 + 2 + 1 + 1  # router topk permute(3) gather+gate/up down combine
 
     for _ in range(args.warmup):
         step()
@@ -446,12 +444,21 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
 
         warm = graph_time(calls) / n
         cold = (graph_time(cold_calls) - t_flush) / n
+        xb = xm.to(torch.bfloat16)
+
+        def bf16_calls():
+            for _ in range(n):
+                bm.bi_router_gemm(xb, w, b, out=y, stream=stream)
+
+        warm_bf16 = graph_time(bf16_calls) / n
         flops = 2.0 * M * 4096 * 256
         bytes_ = 4.0 * (256 * 4096 + 256 + M * (4096 + 256))
         res[str(M)] = {"warm_us": round(warm, 2), "cold_us": round(cold, 2),
                        "cold_hbm_frac": round(bytes_ / (cold * 1e-6) / 1e9 / measured_peaks()[0], 3),
                        "warm_tflops": round(flops / (warm * 1e-6) / 1e12, 2),
-                       "warm_fp32_frac": round(flops / (warm * 1e-6) / 1e12 / fp32_peak, 3)}
+                       "warm_fp32_frac": round(flops / (warm * 1e-6) / 1e12 / fp32_peak, 3),
+                       "bf16x_warm_us": round(warm_bf16, 2),
+                       "bf16x_warm_fp32_frac": round(flops / (warm_bf16 * 1e-6) / 1e12 / fp32_peak, 3)}
         # router + selection: two launches (bi_router_gemm, bi_topk) against
         # the fused bi_router_topk, top-8 of the 256 scores
         ids = torch.empty(M, 8, dtype=torch.int32, device=dev)

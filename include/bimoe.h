@@ -119,6 +119,26 @@ BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,
                                          bi_stream_t stream);
 
 /*
+ * bi_router_gemm_bf16 -- bi_router_gemm with bf16 x: y[i,n] from the fp32
+ * values of x[i,:] (a bf16 value converts to fp32 exactly), so the result is
+ * bit for bit bi_router_gemm(float(x)) under every schedule.  The MoE layer's
+ * tokens are bf16 and the router wants fp32 scores ("[BI][DSv4]
+ * Batch-invariant GateLinear router with fp32 persistent matmul", section
+ * "What": routing through bf16 would round the scores): reading x as bf16
+ * removes the separate fp32 copy of the tokens and halves their reads.
+ *   x [M,K] bf16 row-major (device, 16-byte aligned); w, bias, y, M, K, N and
+ *   errors as bi_router_gemm.
+ */
+BI_API bi_status bi_router_gemm_bf16(const bi_bf16 *x, const float *w, const float *bias,
+                                     float *y, int64_t M, int64_t K, int64_t N,
+                                     bi_stream_t stream);
+/* test hook: bi_router_gemm_bf16 with the schedule forced (as bi_router_gemm_schedule) */
+BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w,
+                                              const float *bias, float *y, int64_t M,
+                                              int64_t K, int64_t N, int32_t schedule,
+                                              bi_stream_t stream);
+
+/*
  * bi_router_gemm_splitk_negctl -- NEGATIVE CONTROL, test use only.  Same
  * signature as bi_router_gemm but its K split depends on M (one chain over
  * all of K for M > 16, sixteen 256-long slices for M <= 16), the kind of
@@ -208,6 +228,14 @@ BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bia
                                 float *y, float *probs, int32_t *ids, float *wts,
                                 int64_t M, int64_t K, int64_t N, int32_t top_k,
                                 bi_stream_t stream);
+/*
+ * bi_router_topk_bf16 -- bi_router_topk with bf16 x, i.e. bi_router_gemm_bf16
+ * followed by bi_topk on its scores (same bits as bi_router_topk(float(x))).
+ */
+BI_API bi_status bi_router_topk_bf16(const bi_bf16 *x, const float *w, const float *bias,
+                                     float *y, float *probs, int32_t *ids, float *wts,
+                                     int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                     bi_stream_t stream);
 /*
  * bi_router_topk_schedule -- test hook: bi_router_topk with the router
  * schedule forced as in bi_router_gemm_schedule.

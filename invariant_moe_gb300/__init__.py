@@ -35,7 +35,7 @@ EXPORTS = [
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
-    "bi_topk_window",
+    "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
 ]
 
 
@@ -84,6 +84,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
             "bi_topk_window": ([P, I64, P, P, I64, I64, I32, P, P], ST),
+            "bi_router_gemm_bf16": ([P, P, P, P, I64, I64, I64, P], ST),
+            "bi_router_gemm_bf16_schedule": ([P, P, P, P, I64, I64, I64, I32, P], ST),
+            "bi_router_topk_bf16": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
         }
@@ -142,7 +145,8 @@ def bi_cast_bf16_to_f32(x, out=None, stream=None):
 
 
 def bi_router_gemm(x, w, bias=None, out=None, schedule=0, stream=None):
-    """y[M,N] = x[M,K] @ w[N,K]^T (+ bias), fp32, batch-invariant recipe."""
+    """y[M,N] = x[M,K] @ w[N,K]^T (+ bias), fp32, batch-invariant recipe.  x is
+    fp32 or bf16 (bf16 values are read as their exact fp32 values)."""
     M, K = x.shape
     N = w.shape[0]
     if w.shape[1] != K:
@@ -150,13 +154,15 @@ def bi_router_gemm(x, w, bias=None, out=None, schedule=0, stream=None):
     out = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
     if out.shape != (M, N):
         raise ValueError("out must be [M, N]")
-    args = (_ptr(x, torch.float32, "x"), _ptr(w, torch.float32, "w", x.device),
+    bf16 = x.dtype == torch.bfloat16
+    args = (_ptr(x, torch.bfloat16 if bf16 else torch.float32, "x"), _ptr(w, torch.float32, "w", x.device),
             _ptr(bias, torch.float32, "bias", x.device), _ptr(out, torch.float32, "out", x.device),
             M, K, N)
+    name = "bi_router_gemm_bf16" if bf16 else "bi_router_gemm"
     if schedule:
-        _call("bi_router_gemm_schedule", *args, schedule, _stream(stream))
+        _call(name + "_schedule", *args, schedule, _stream(stream))
     else:
-        _call("bi_router_gemm", *args, _stream(stream))
+        _call(name, *args, _stream(stream))
     return out
 
 
@@ -306,10 +312,16 @@ def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=
     ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
     wts = torch.empty(M, top_k, dtype=torch.float32, device=dev)
     probs = torch.empty(M, N, dtype=torch.float32, device=dev) if want_probs else None
-    _call("bi_router_topk_schedule", _ptr(x, torch.float32, "x"), _ptr(w, torch.float32, "w", dev),
-          _ptr(bias, torch.float32, "bias", dev), _ptr(y, torch.float32, "out", dev),
-          _ptr(probs, torch.float32, "probs", dev), _ptr(ids, torch.int32, "ids", dev),
-          _ptr(wts, torch.float32, "wts", dev), M, K, N, top_k, schedule, _stream(stream))
+    ptrs = (_ptr(w, torch.float32, "w", dev), _ptr(bias, torch.float32, "bias", dev),
+            _ptr(y, torch.float32, "out", dev), _ptr(probs, torch.float32, "probs", dev),
+            _ptr(ids, torch.int32, "ids", dev), _ptr(wts, torch.float32, "wts", dev))
+    if x.dtype == torch.bfloat16:
+        if schedule:
+            raise ValueError("bf16 x takes the automatic router schedule")
+        _call("bi_router_topk_bf16", _ptr(x, torch.bfloat16, "x"), *ptrs, M, K, N, top_k, _stream(stream))
+    else:
+        _call("bi_router_topk_schedule", _ptr(x, torch.float32, "x"), *ptrs, M, K, N, top_k, schedule,
+              _stream(stream))
     return y, ids, wts, probs
 
 
@@ -348,14 +360,13 @@ def bi_fp32_fma_probe(blocks, iters, stream=None):
 
 
 def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
-    """Whole hot path of one MoE layer: cast -> router -> top-k -> experts.
-    Returns (out, scores, ids, wts)."""
-    x32 = bi_cast_bf16_to_f32(x_bf16, stream=stream)
+    """Whole hot path of one MoE layer: router (on the bf16 tokens, read as
+    their exact fp32 values) -> top-k -> experts.  Returns (out, scores, ids, wts)."""
+    # the router reads the bf16 tokens as their exact fp32 values
     if x_bf16.shape[0] < 1024:
-        # decode-size batches: the selection grid overlaps the router's launch
-        scores, ids, wts, _ = bi_router_topk(x32, w_router, top_k, bias=bias, stream=stream)
+        scores, ids, wts, _ = bi_router_topk(x_bf16, w_router, top_k, bias=bias, stream=stream)
     else:
-        scores = bi_router_gemm(x32, w_router, bias, stream=stream)
+        scores = bi_router_gemm(x_bf16, w_router, bias, stream=stream)
         ids, wts, _ = bi_topk(scores, top_k, stream=stream)
     out = bi_moe_forward(x_bf16, ids, wts, w13, w2, stream=stream)
     return out, scores, ids, wts

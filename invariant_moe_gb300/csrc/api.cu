@@ -12,6 +12,8 @@ namespace bimoe {
 
 bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
                         int64_t, int, cudaStream_t);
+bi_status launch_router_bf16(const void *, const float *, const float *, float *, int64_t, int64_t,
+                             int64_t, int, cudaStream_t);
 bi_status launch_topk_window(const float *, int64_t, const int64_t *, const int64_t *, int64_t,
                              int64_t, int32_t, int32_t *, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
@@ -241,7 +243,7 @@ BI_API bi_status bi_cast_bf16_to_f32(const bi_bf16 *x, float *y, int64_t n, bi_s
   return launch_cast_bf16_f32(x, y, n, reinterpret_cast<cudaStream_t>(stream));
 }
 
-static bi_status router_checks(const float *x, const float *w, float *y, int64_t M, int64_t K,
+static bi_status router_checks(const void *x, const float *w, float *y, int64_t M, int64_t K,
                                int64_t N) {
   BI_REQUIRE(M >= 0 && K > 0 && N > 0, BI_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld N=%lld",
              (long long)M, (long long)K, (long long)N);
@@ -269,6 +271,21 @@ BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w, const f
 BI_API bi_status bi_router_gemm(const float *x, const float *w, const float *bias, float *y,
                                 int64_t M, int64_t K, int64_t N, bi_stream_t stream) {
   return bi_router_gemm_schedule(x, w, bias, y, M, K, N, 0, stream);
+}
+
+BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w, const float *bias,
+                                              float *y, int64_t M, int64_t K, int64_t N,
+                                              int32_t schedule, bi_stream_t stream) {
+  bi_status st = router_checks(x, w, y, M, K, N);
+  if (st != BI_OK) return st;
+  BI_REQUIRE(schedule >= 0 && schedule <= 3, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  if (M == 0) return BI_OK;
+  return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_router_gemm_bf16(const bi_bf16 *x, const float *w, const float *bias, float *y,
+                                     int64_t M, int64_t K, int64_t N, bi_stream_t stream) {
+  return bi_router_gemm_bf16_schedule(x, w, bias, y, M, K, N, 0, stream);
 }
 
 BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w, const float *bias,
@@ -313,6 +330,21 @@ BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bia
                                 float *probs, int32_t *ids, float *wts, int64_t M, int64_t K,
                                 int64_t N, int32_t top_k, bi_stream_t stream) {
   return bi_router_topk_schedule(x, w, bias, y, probs, ids, wts, M, K, N, top_k, 0, stream);
+}
+
+BI_API bi_status bi_router_topk_bf16(const bi_bf16 *x, const float *w, const float *bias, float *y,
+                                     float *probs, int32_t *ids, float *wts, int64_t M, int64_t K,
+                                     int64_t N, int32_t top_k, bi_stream_t stream) {
+  bi_status st = router_checks(x, w, y, M, K, N);
+  if (st != BI_OK) return st;
+  BI_REQUIRE(N <= 512, BI_ERR_UNSUPPORTED, "selection needs N <= 512 (N=%lld)", (long long)N);
+  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= N, BI_ERR_INVALID_ARG,
+             "top_k=%d outside [1, min(16, N)]", top_k);
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(ids && wts, BI_ERR_INVALID_ARG, "null pointer");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_router_bf16(x, w, bias, y, M, K, N, 0, s)) != BI_OK) return st;
+  return launch_topk(y, ids, wts, probs, M, N, top_k, s);
 }
 
 BI_API bi_status bi_topk_window(const float *scores, int64_t ld, const int64_t *row_start,

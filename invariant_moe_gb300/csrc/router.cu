@@ -32,6 +32,22 @@ constexpr int kSlice = 128;
 // slices along k then read distinct banks.
 constexpr int kSlicePad = kSlice + 4;
 
+// x may be fp32 or bf16 (the MoE layer's tokens); a bf16 value converts to
+// fp32 exactly (its bits are the high half of the fp32's), so both give the
+// same per-element sequence.  Shared-memory row pitches (elements) keep every
+// row 16-byte aligned for the bulk / cp.async copies.
+template <typename XT> struct XPitch;
+template <> struct XPitch<float> { static constexpr int slice = kSlicePad, round = 8 * kSlice + 4, chunk = 36; };
+template <> struct XPitch<__nv_bfloat16> { static constexpr int slice = kSlice + 8, round = 8 * kSlice + 8, chunk = 40; };
+
+// Four consecutive x values from shared memory, as fp32.
+__device__ __forceinline__ float4 ld_x4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld_x4(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -58,16 +74,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // the MR x rows (512 B each) into padded shared rows, then runs its MR
 // chains from there; the partials meet in shared memory and lane i < MR adds
 // them in slice order.
-template <int MR>
-__global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict__ x,
+template <int MR, typename XT>
+__global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ x,
                                                          const float *__restrict__ w,
                                                          const float *__restrict__ bias,
                                                          float *__restrict__ y, int M, int K,
                                                          int N, int *err) {
+  constexpr int XP = XPitch<XT>::slice;
   extern __shared__ __align__(16) float sm[];
-  float *ws = sm;                              // [32][kSlicePad]
-  float *xs = sm + 32 * kSlicePad;             // [MR][32][kSlicePad]
-  float *part = xs + MR * 32 * kSlicePad;      // [MR][S]
+  float *ws = sm;                                              // [32][kSlicePad]
+  XT *xs = reinterpret_cast<XT *>(sm + 32 * kSlicePad);        // [MR][32][XP]
+  float *part = reinterpret_cast<float *>(xs + MR * 32 * XP);  // [MR][S]
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   griddep_wait();
@@ -84,15 +101,16 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
   uint32_t phase = 0;
   for (int g0 = 0; g0 < S; g0 += 32) {
     const int ns = min(32, S - g0);
-    if (lane == 0) mbar_arrive_expect_tx(b, static_cast<uint32_t>(ns) * kSlice * 4 * (1 + MR));
+    if (lane == 0)
+      mbar_arrive_expect_tx(b, static_cast<uint32_t>(ns) * kSlice * (4 + MR * sizeof(XT)));
     __syncwarp();
     if (lane < ns) {
       const int k0 = (g0 + lane) * kSlice;
       bulk_g2s(smem_u32(ws + lane * kSlicePad), wrow + k0, kSlice * 4, b);
 #pragma unroll
       for (int i = 0; i < MR; ++i)
-        bulk_g2s(smem_u32(xs + (i * 32 + lane) * kSlicePad),
-                 x + static_cast<size_t>(min(m0 + i, M - 1)) * K + k0, kSlice * 4, b);
+        bulk_g2s(smem_u32(xs + (i * 32 + lane) * XP),
+                 x + static_cast<size_t>(min(m0 + i, M - 1)) * K + k0, kSlice * sizeof(XT), b);
     }
     const bool got = mbar_wait(b, phase, nullptr, err);
     if (!__all_sync(0xffffffffu, got)) {
@@ -110,7 +128,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
         const float4 wv = *reinterpret_cast<const float4 *>(wl + k);
 #pragma unroll
         for (int i = 0; i < MR; ++i) {
-          const float4 xv = *reinterpret_cast<const float4 *>(xs + (i * 32 + lane) * kSlicePad + k);
+          const float4 xv = ld_x4(xs + (i * 32 + lane) * XP + k);
           p[i] = __fmaf_rn(xv.x, wv.x, p[i]);
           p[i] = __fmaf_rn(xv.y, wv.y, p[i]);
           p[i] = __fmaf_rn(xv.z, wv.z, p[i]);
@@ -142,17 +160,30 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const float *__restrict
 // computes.  Partials meet in shared memory and thread (i, j) adds them to
 // its running sum in slice order.
 constexpr int kSlMT = 8, kSlNT = 16, kSlG = 8;
-constexpr int kSlRow = kSlG * kSlice + 4;  // floats per staged row
-constexpr int kSlStage = (kSlMT + kSlNT) * kSlRow;
+constexpr int kSlRow = kSlG * kSlice + 4;  // floats per staged W row
+// bytes of one stage: MT x rows (element type XT) then NT W rows
+template <typename XT>
+__host__ __device__ constexpr int sl_stage_bytes() {
+  return kSlMT * XPitch<XT>::round * static_cast<int>(sizeof(XT)) + kSlNT * kSlRow * 4;
+}
 
-__global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restrict__ x,
+template <typename XT>
+__global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict__ x,
                                                             const float *__restrict__ w,
                                                             const float *__restrict__ bias,
                                                             float *__restrict__ y, int M, int K,
                                                             int N, int *err) {
+  constexpr int XP = XPitch<XT>::round;
+  constexpr int kStageB = sl_stage_bytes<XT>();
   extern __shared__ __align__(16) float sm[];
-  float *stage_buf = sm;                         // [2][MT + NT][kSlRow]
-  float *part = sm + 2 * kSlStage;               // [G][MT][NT]
+  uint8_t *stage_buf = reinterpret_cast<uint8_t *>(sm);                     // [2] x [MT][XP] XT, W [NT][kSlRow]
+  float *part = reinterpret_cast<float *>(stage_buf + 2 * kStageB);         // [G][MT][NT]
+  auto xrow = [&](int buf, int row) {
+    return reinterpret_cast<XT *>(stage_buf + buf * kStageB) + row * XP;
+  };
+  auto wrow = [&](int buf, int row) {
+    return reinterpret_cast<float *>(stage_buf + buf * kStageB + kSlMT * XP * sizeof(XT)) + row * kSlRow;
+  };
   __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
   griddep_wait();
@@ -173,13 +204,16 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
     const int buf = rd & 1;
     const uint32_t b = smem_u32(&bars[buf]);
     const int ns = min(kSlG, S - rd * kSlG);
-    const uint32_t bytes = static_cast<uint32_t>(ns) * kSlice * 4;
-    if (lane == 0) mbar_arrive_expect_tx(b, bytes * (kSlMT + kSlNT));
+    const uint32_t xbytes = static_cast<uint32_t>(ns) * kSlice * sizeof(XT);
+    const uint32_t wbytes = static_cast<uint32_t>(ns) * kSlice * 4;
+    if (lane == 0) mbar_arrive_expect_tx(b, xbytes * kSlMT + wbytes * kSlNT);
     __syncwarp();
-    if (lane < kSlMT + kSlNT) {
-      const float *src = lane < kSlMT ? x + static_cast<size_t>(min(m0 + lane, M - 1)) * K
-                                      : w + static_cast<size_t>(min(n0 + lane - kSlMT, N - 1)) * K;
-      bulk_g2s(smem_u32(stage_buf + buf * kSlStage + lane * kSlRow), src + rd * kSlG * kSlice, bytes, b);
+    if (lane < kSlMT) {
+      bulk_g2s(smem_u32(xrow(buf, lane)),
+               x + static_cast<size_t>(min(m0 + lane, M - 1)) * K + rd * kSlG * kSlice, xbytes, b);
+    } else if (lane < kSlMT + kSlNT) {
+      bulk_g2s(smem_u32(wrow(buf, lane - kSlMT)),
+               w + static_cast<size_t>(min(n0 + lane - kSlMT, N - 1)) * K + rd * kSlG * kSlice, wbytes, b);
     }
   };
 
@@ -195,18 +229,17 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const float *__restr
     if (!mbar_wait(smem_u32(&bars[buf]), (phases >> buf) & 1u, nullptr, err)) ok = false;
     phases ^= 1u << buf;
     if (__syncthreads_or(!ok)) break;
-    const float *sb = stage_buf + buf * kSlStage;
     const int sl = rd * kSlG + g;
     if (sl < S) {
       float p00 = 0.0f, p01 = 0.0f, p10 = 0.0f, p11 = 0.0f;
-      const float *x0 = sb + cr * kSlRow + g * kSlice;
-      const float *x1 = x0 + 4 * kSlRow;
-      const float *w0 = sb + (kSlMT + cc) * kSlRow + g * kSlice;
-      const float *w1 = w0 + 8 * kSlRow;
+      const XT *x0 = xrow(buf, cr) + g * kSlice;
+      const XT *x1 = xrow(buf, cr + 4) + g * kSlice;
+      const float *w0 = wrow(buf, cc) + g * kSlice;
+      const float *w1 = wrow(buf, cc + 8) + g * kSlice;
 #pragma unroll 8
       for (int k = 0; k < kSlice; k += 4) {
-        const float4 a0 = *reinterpret_cast<const float4 *>(x0 + k);
-        const float4 a1 = *reinterpret_cast<const float4 *>(x1 + k);
+        const float4 a0 = ld_x4(x0 + k);
+        const float4 a1 = ld_x4(x1 + k);
         const float4 b0 = *reinterpret_cast<const float4 *>(w0 + k);
         const float4 b1 = *reinterpret_cast<const float4 *>(w1 + k);
         p00 = __fmaf_rn(a0.x, b0.x, p00); p01 = __fmaf_rn(a0.x, b1.x, p01);
@@ -261,14 +294,16 @@ constexpr int kTBK = 32;              // k per chunk
 constexpr int kTLd = kTBK + 4;        // padded smem row length (floats)
 constexpr int kTStages = 3;
 
-template <int TMR, int CB, int G>
+template <int TMR, int CB, int G, typename XT>
 __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_tiled_kernel(
-    const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
+    const XT *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
     float *__restrict__ y, int M, int K, int N) {
   constexpr int RB = 8 / CB;                 // row blocks per CTA
   constexpr int BM = RB * 4 * TMR;           // rows per CTA
   constexpr int BN = CB * 32;                // columns per CTA
-  constexpr int XS = BM * kTLd, WS = BN * kTLd;  // floats per stage
+  constexpr int XLd = XPitch<XT>::chunk;     // x row pitch in the stage (elements)
+  constexpr int XS = BM * XLd * static_cast<int>(sizeof(XT)) / 4;  // x floats-worth per stage
+  constexpr int WS = BN * kTLd;              // W floats per stage
   constexpr int GS = kTStages * (XS + WS);   // floats of one group's ring
   extern __shared__ __align__(16) float smem_f[];
 
@@ -277,8 +312,8 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
   // CTA's whole output tile; group 0 keeps the running sums
   const int grp = threadIdx.x >> 8;
   const int tid = threadIdx.x & 255;
-  float *xs = smem_f + grp * GS;             // [kTStages][BM][kTLd]
-  float *ws = xs + kTStages * XS;            // [kTStages][BN][kTLd]
+  XT *xs = reinterpret_cast<XT *>(smem_f + grp * GS);       // [kTStages][BM][XLd]
+  float *ws = smem_f + grp * GS + kTStages * XS;            // [kTStages][BN][kTLd]
   float *pb = smem_f + G * GS;               // [G-1][TMR*4][256] slice partials of groups >= 1
   const int warp = tid >> 5, lane = tid & 31;
   const int rb = warp / CB, cb = warp % CB;
@@ -290,14 +325,17 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
   // rows past M / N read a clamped valid row and are never stored)
   auto load_chunk = [&](int lc, int stage) {
     const int k0 = ((lc / kCPS) * G + grp) * kSlice + (lc % kCPS) * kTBK;
-    for (int q = tid; q < (BM + BN) * (kTBK / 4); q += 256) {
-      const int row = q / (kTBK / 4), piece = q % (kTBK / 4);
-      if (row < BM) {
+    constexpr int XE = 16 / static_cast<int>(sizeof(XT));  // x elements per 16-byte piece
+    constexpr int XPC = kTBK / XE, WPC = kTBK / 4;         // pieces per row
+    XT *xst = xs + stage * (BM * XLd);
+    for (int q = tid; q < BM * XPC + BN * WPC; q += 256) {
+      if (q < BM * XPC) {
+        const int row = q / XPC, piece = q % XPC;
         const int gm = min(m0 + row, M - 1);
-        cp_async16(smem_u32(xs + stage * XS + row * kTLd + piece * 4),
-                   x + static_cast<size_t>(gm) * K + k0 + piece * 4);
+        cp_async16(smem_u32(xst + row * XLd + piece * XE),
+                   x + static_cast<size_t>(gm) * K + k0 + piece * XE);
       } else {
-        const int wr = row - BM;
+        const int wr = (q - BM * XPC) / WPC, piece = (q - BM * XPC) % WPC;
         const int gn = min(n0 + wr, N - 1);
         cp_async16(smem_u32(ws + stage * WS + wr * kTLd + piece * 4),
                    w + static_cast<size_t>(gn) * K + k0 + piece * 4);
@@ -327,14 +365,14 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
     __syncthreads();
     if (ch + kTStages - 1 < nchunks) load_chunk(ch + kTStages - 1, (ch + kTStages - 1) % kTStages);
     cp_async_commit();
-    const float *xb = xs + (ch % kTStages) * XS;
+    const XT *xb = xs + (ch % kTStages) * (BM * XLd);
     const float *wb = ws + (ch % kTStages) * WS;
 #pragma unroll
     for (int kk = 0; kk < kTBK; kk += 4) {
       float4 xv[TMR], wv[4];
 #pragma unroll
       for (int i = 0; i < TMR; ++i)
-        xv[i] = *reinterpret_cast<const float4 *>(xb + (xrow0 + 4 * i) * kTLd + kk);
+        xv[i] = ld_x4(xb + (xrow0 + 4 * i) * XLd + kk);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         wv[j] = *reinterpret_cast<const float4 *>(wb + (wrow0 + 8 * j) * kTLd + kk);
@@ -395,17 +433,19 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
   }
 }
 
-template <int TMR, int CB, int G>
-static bi_status launch_tiled_t(const float *x, const float *w, const float *b, float *y, int64_t M,
+template <int TMR, int CB, int G, typename XT>
+static bi_status launch_tiled_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, cudaStream_t stream) {
   constexpr int RB = 8 / CB, BM = RB * 4 * TMR, BN = CB * 32;
-  const size_t smem = (static_cast<size_t>(G) * kTStages * (BM + BN) * kTLd +
-                       static_cast<size_t>(G - 1) * TMR * 4 * 256) * sizeof(float);
+  const size_t stage = static_cast<size_t>(BM) * XPitch<XT>::chunk * sizeof(XT) +
+                       static_cast<size_t>(BN) * kTLd * sizeof(float);
+  const size_t smem = static_cast<size_t>(G) * kTStages * stage +
+                      static_cast<size_t>(G - 1) * TMR * 4 * 256 * sizeof(float);
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(router_tiled_kernel<TMR, CB, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(router_tiled_kernel<TMR, CB, G, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess) {
       cudaGetLastError();  // do not leave the error for an unrelated later check
       set_error("router tiled: cannot reserve %zu bytes of shared memory", smem);
@@ -414,15 +454,16 @@ static bi_status launch_tiled_t(const float *x, const float *w, const float *b, 
     attr_done[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((M + BM - 1) / BM), static_cast<unsigned>((N + BN - 1) / BN));
-  return launch_chained(router_tiled_kernel<TMR, CB, G>, grid, dim3(256 * G), smem, stream, 1, x, w,
-                        b, y, (int)M, (int)K, (int)N);
+  return launch_chained(router_tiled_kernel<TMR, CB, G, XT>, grid, dim3(256 * G), smem, stream, 1, x,
+                        w, b, y, (int)M, (int)K, (int)N);
 }
 
 // Tile shape for the tiled schedule: the (column blocks, rows per thread)
 // pair with the smallest per-SM load ceil(CTAs / SMs) * TMR, taking the first
 // of a preference list on ties (measured on GB300: a full-width 7-row tile
 // for the widest batches, 128-column tiles with fewer rows otherwise).
-static bi_status launch_tiled(const float *x, const float *w, const float *b, float *y, int64_t M,
+template <typename XT>
+static bi_status launch_tiled(const XT *x, const float *w, const float *b, float *y, int64_t M,
                               int64_t K, int64_t N, cudaStream_t stream) {
   struct Shape { int cb, tmr; };
   static const Shape wide[] = {{8, 7}, {8, 8}, {4, 4}, {4, 3}, {4, 2}, {4, 1}};
@@ -453,20 +494,20 @@ static bi_status launch_tiled(const float *x, const float *w, const float *b, fl
     const int64_t ctas = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     if (pick.tmr <= 4 && ctas < sms && (K / kSlice) % 2 == 0) {
       switch (pick.cb * 16 + pick.tmr) {
-        case 4 * 16 + 4: return launch_tiled_t<4, 4, 2>(x, w, b, y, M, K, N, stream);
-        case 4 * 16 + 3: return launch_tiled_t<3, 4, 2>(x, w, b, y, M, K, N, stream);
-        case 4 * 16 + 2: return launch_tiled_t<2, 4, 2>(x, w, b, y, M, K, N, stream);
-        default: return launch_tiled_t<1, 4, 2>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 4: return launch_tiled_t<4, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 3: return launch_tiled_t<3, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 2: return launch_tiled_t<2, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        default: return launch_tiled_t<1, 4, 2, XT>(x, w, b, y, M, K, N, stream);
       }
     }
   }
   switch (pick.cb * 16 + pick.tmr) {
-    case 8 * 16 + 7: return launch_tiled_t<7, 8, 1>(x, w, b, y, M, K, N, stream);
-    case 8 * 16 + 8: return launch_tiled_t<8, 8, 1>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 4: return launch_tiled_t<4, 4, 1>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 3: return launch_tiled_t<3, 4, 1>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 2: return launch_tiled_t<2, 4, 1>(x, w, b, y, M, K, N, stream);
-    default: return launch_tiled_t<1, 4, 1>(x, w, b, y, M, K, N, stream);
+    case 8 * 16 + 7: return launch_tiled_t<7, 8, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 8 * 16 + 8: return launch_tiled_t<8, 8, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 4: return launch_tiled_t<4, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 3: return launch_tiled_t<3, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 2: return launch_tiled_t<2, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    default: return launch_tiled_t<1, 4, 1, XT>(x, w, b, y, M, K, N, stream);
   }
 }
 
@@ -513,14 +554,17 @@ __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float 
 }
 
 // ------------------------------------------------------------------- host --
-bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
-                        int64_t K, int64_t N, int schedule, cudaStream_t stream) {
+template <typename XT>
+static bi_status launch_router_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                                 int64_t K, int64_t N, int schedule, cudaStream_t stream) {
   const int S = static_cast<int>(K / kSlice);
   if (schedule == 0) schedule = (M <= 4) ? 1 : (M < 384 ? 2 : 3);
   if (schedule == 1) {
     const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
     dim3 grid(static_cast<unsigned>(N), static_cast<unsigned>((M + mr - 1) / mr));
-    const size_t smem = (static_cast<size_t>(1 + mr) * 32 * kSlicePad + static_cast<size_t>(mr) * S) * sizeof(float);
+    const size_t smem = static_cast<size_t>(32) * kSlicePad * sizeof(float) +
+                        static_cast<size_t>(mr) * 32 * XPitch<XT>::slice * sizeof(XT) +
+                        static_cast<size_t>(mr) * S * sizeof(float);
     if (grid.y > 65535u) {
       set_error("router rows schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
@@ -531,10 +575,10 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
     int dv = 0;                                                                                        \
     cudaGetDevice(&dv);                                                                                \
     if (dv < 64 && !attr[dv]) {                                                                        \
-      cudaFuncSetAttribute(router_rows_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
+      cudaFuncSetAttribute(router_rows_kernel<R, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
       attr[dv] = true;                                                                                 \
     }                                                                                                  \
-    const bi_status st_ = launch_chained(router_rows_kernel<R>, grid, dim3(32), smem, stream, 1, x, w, \
+    const bi_status st_ = launch_chained(router_rows_kernel<R, XT>, grid, dim3(32), smem, stream, 1, x, w, \
                                          b, y, (int)M, (int)K, (int)N, device_error_word());          \
     if (st_ != BI_OK) return st_;                                                                    \
   }
@@ -542,7 +586,7 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
 #undef BI_ROWS
   } else if (schedule == 2) {
     dim3 grid(static_cast<unsigned>((N + kSlNT - 1) / kSlNT), static_cast<unsigned>((M + kSlMT - 1) / kSlMT));
-    const size_t smem = (2 * static_cast<size_t>(kSlStage) + kSlG * kSlMT * kSlNT) * sizeof(float);
+    const size_t smem = 2 * static_cast<size_t>(sl_stage_bytes<XT>()) + kSlG * kSlMT * kSlNT * sizeof(float);
     if (grid.y > 65535u) {
       set_error("router sliced schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
@@ -551,10 +595,10 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
     int dv = 0;
     cudaGetDevice(&dv);
     if (dv < 64 && !attr[dv]) {
-      cudaFuncSetAttribute(router_sliced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      cudaFuncSetAttribute(router_sliced_kernel<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       attr[dv] = true;
     }
-    const bi_status st = launch_chained(router_sliced_kernel, grid, dim3(256), smem, stream, 1, x, w, b,
+    const bi_status st = launch_chained(router_sliced_kernel<XT>, grid, dim3(256), smem, stream, 1, x, w, b,
                                         y, (int)M, (int)K, (int)N, device_error_word());
     if (st != BI_OK) return st;
   } else if (schedule == 3) {
@@ -570,6 +614,18 @@ bi_status launch_router(const float *x, const float *w, const float *b, float *y
   }
   BI_CHECK_LAUNCH();
   return BI_OK;
+}
+
+bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
+                        int64_t K, int64_t N, int schedule, cudaStream_t stream) {
+  return launch_router_t<float>(x, w, b, y, M, K, N, schedule, stream);
+}
+
+// The same router on bf16 x (converted exactly to fp32 as it is read).
+bi_status launch_router_bf16(const void *x, const float *w, const float *b, float *y, int64_t M,
+                             int64_t K, int64_t N, int schedule, cudaStream_t stream) {
+  return launch_router_t<__nv_bfloat16>(static_cast<const __nv_bfloat16 *>(x), w, b, y, M, K, N,
+                                        schedule, stream);
 }
 
 bi_status launch_router_negctl(const float *x, const float *w, const float *b, float *y,

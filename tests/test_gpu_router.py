@@ -156,3 +156,36 @@ def test_bf16_cast_exact(cuda):
     assert torch.equal(y, x.float())
     xo = x.flatten()[3:3 + 1001]  # misaligned, ragged
     assert torch.equal(bm.bi_cast_bf16_to_f32(xo), xo.float())
+
+
+@pytest.mark.parametrize("M", [1, 3, 9, 64, 130, 700, 4096])
+def test_bf16_x_equals_fp32_of_it(dev_inputs, M):
+    """The router on bf16 x gives the bits of the router on float(x), under
+    every schedule (the conversion is exact and happens as x is read)."""
+    import invariant_moe_gb300 as bm
+    x, w, b = dev_inputs
+    xb = x[:M].to(torch.bfloat16)
+    xf = xb.float()
+    for s in ((1, 2, 3) if M <= 700 else (2, 3)):
+        y32 = bm.bi_router_gemm(xf, w, b, schedule=s)
+        y16 = bm.bi_router_gemm(xb, w, b, schedule=s)
+        torch.cuda.synchronize()
+        assert torch.equal(y32, y16), f"M={M} schedule={s}"
+    assert torch.equal(bm.bi_router_gemm(xb, w, b), bm.bi_router_gemm(xf, w, b))
+
+
+def test_bf16_x_qwen_shape_and_topk(cuda):
+    """K=2048, N=128, no bias (the Qwen3-30B-A3B router): bf16 x through the
+    router and router+top-k calls equals the fp32 path on float(x)."""
+    import invariant_moe_gb300 as bm
+    g = syn.gen(81)
+    x = torch.randn(4096, 2048, generator=g).to(torch.bfloat16).to(cuda)
+    w = (torch.randn(128, 2048, generator=g) * 0.02).to(cuda)
+    for M in (1, 5, 300, 1000, 4096):
+        xb = x[:M].contiguous()
+        assert torch.equal(bm.bi_router_gemm(xb, w), bm.bi_router_gemm(xb.float(), w)), M
+        a = bm.bi_router_topk(xb, w, 8)
+        c = bm.bi_router_topk(xb.float(), w, 8)
+        torch.cuda.synchronize()
+        for u, v in zip(a[:3], c[:3]):
+            assert torch.equal(u, v), M
