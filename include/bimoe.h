@@ -349,12 +349,16 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
  * the whole process, from the next call on:
  *   0  automatic (the default): CTA pairs whenever the GEMM's output
  *      features (I for gate/up, H for down) are a multiple of 256, else one
- *      CTA per tile;
+ *      CTA per tile; for gate/up with H >= 4096, CTA pairs with interleaved
+ *      gate/up rows;
  *   1  one CTA per tile (128 weight rows), tcgen05 cta_group::1;
  *   2  CTA pairs (256 weight rows over two SMs of a cluster), cta_group::2;
  *      a call whose output features are not a multiple of 256 then fails
- *      with BI_ERR_UNSUPPORTED.
- * Both variants evaluate the same per-element K order, so the bits do not
+ *      with BI_ERR_UNSUPPORTED;
+ *   3  gate/up: CTA pairs whose CTAs each hold 64 gate rows and the matching
+ *      64 up rows (one M=256 x N=256 MMA per K step, any I % 128 == 0);
+ *      down: as 2.
+ * All variants evaluate the same per-element K order, so the bits do not
  * depend on the choice (tests compare them).  *previous (may be NULL)
  * receives the old setting.  Other values: BI_ERR_INVALID_ARG.  Not
  * synchronised with calls in flight on other host threads.

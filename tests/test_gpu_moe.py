@@ -145,7 +145,8 @@ def gemm_variant():
 
 @pytest.mark.parametrize("M,kind", [(1, "rand"), (17, "rand"), (300, "skew"), (4096, "rand")])
 def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
-    """One CTA per tile (M=128 MMAs) and CTA pairs (M=256 MMAs over two SMs)
+    """One CTA per tile (M=128 MMAs), CTA pairs (M=256 MMAs over two SMs) and
+    CTA pairs with interleaved gate/up rows (one M=256 x N=256 MMA per K step)
     evaluate the same K order, so act, the fp32 contributions and the layer
     output agree bit for bit, ragged token blocks included."""
     import invariant_moe_gb300 as bm
@@ -158,7 +159,7 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
     off, perm = bm.bi_moe_permute(ids, E)
     xp = bm.bi_moe_gather(x, off, perm, k)
     res = {}
-    for v in (1, 2):
+    for v in (1, 2, 3):
         gemm_variant(v)
         act = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
         contrib = bm.bi_moe_down(act, off, perm, w2, M, k)
@@ -166,8 +167,29 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
         torch.cuda.synchronize()
         res[v] = (act, contrib, out)
     assert bm.device_error() == 0
-    for a, b in zip(res[1], res[2]):
-        assert torch.equal(a, b)
+    for v in (2, 3):
+        for a, b in zip(res[1], res[v]):
+            assert torch.equal(a, b), f"variant {v}"
+
+
+@pytest.mark.parametrize("M,H,E,I,k", [(40, 256, 8, 128, 2), (333, 512, 16, 384, 4), (1, 2048, 128, 768, 8)])
+def test_interleaved_gate_up_same_bits(cuda, gemm_variant, M, H, E, I, k):
+    """The interleaved gate/up variant (any I % 128 == 0, including I=128 and
+    I=384 where plain CTA pairs do not apply) gives the bits of one CTA per
+    tile."""
+    import invariant_moe_gb300 as bm
+    w, x, ids, wts = stage_inputs(M, H, E, I, k, seed=M + I, unit=True)
+    x, ids, wts = x.to(cuda), ids.to(cuda), wts.to(cuda)
+    w13 = w.w13.to(cuda)
+    off, perm = bm.bi_moe_permute(ids, E)
+    xp = bm.bi_moe_gather(x, off, perm, k)
+    gemm_variant(1)
+    a1 = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
+    gemm_variant(3)
+    a3 = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
+    torch.cuda.synchronize()
+    assert bm.device_error() == 0
+    assert torch.equal(a1, a3)
 
 
 def test_gemm_pair_variant_rejects_unaligned_features(cuda, gemm_variant):
