@@ -1,19 +1,23 @@
 """Benchmark of the batch-invariant MoE hot path on GB300.
 
 One step = one pass of the whole hot path over one batch of M synthetic
-tokens: bf16->fp32 cast, fp32 router GEMM, sigmoid top-k, token permute,
-gate/up grouped GEMM with SwiGLU x probability, down grouped GEMM, slot-order
-combine.  Default workload: Qwen3-30B-A3B-shaped MoE layer (H=2048, E=128,
-top-8, I=768, router K=2048 N=128), M=4096 tokens per GPU per step, bf16
+tokens: fp32 router GEMM on the bf16 tokens (read as their exact fp32
+values), sigmoid top-k, token permute and row gather, gate/up grouped GEMM
+with SwiGLU x probability, down grouped GEMM, slot-order combine.  Default
+workload: Qwen3-30B-A3B-shaped MoE layer (H=2048, E=128, top-8, I=768,
+router K=2048 N=128), M=4096 tokens per GPU per step, bf16
 weights/activations ~ N(0, 0.02), fp32 router.  The expert weights (1.2 GB)
 are larger than L2, so every step streams them from HBM (no explicit flush).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload qwen|dsv4] [--tokens M] [--no-extras]
+                  [--no-cpu-baseline]
+  python bench.py --router-sweep | --moe-sweep [--workload ...] | --topk-window-sweep
 
 Prints one JSON line (rank 0).  N > 1: launched by torchrun, one rank per
 GPU, every rank runs its own M tokens (weak scaling, no collective on the
-data path); the time is the max over ranks.
+data path); the time is the max over ranks.  The sweeps print one JSON
+object each (device time vs batch size, CUDA-graph replay).
 """
 from __future__ import annotations
 

@@ -8,38 +8,39 @@
 // gate|up half split, single final bf16 round).
 //
 // Design (sm_103a):
-//   * swap-AB: weight rows are the MMA "M" side (128 rows), the tokens routed
-//     to one expert are the "N" side (up to 256 per tile), K runs over the
-//     hidden (gate/up) or intermediate (down) dimension.
-//   * one tcgen05.mma.cta_group::1.kind::f16 per K=16 step: M=128, N = the
-//     tile's token count rounded up to 16, bf16 operands, fp32 accumulator in
-//     tensor memory.  K advances in steps of 64 (one 128-byte swizzle atom,
-//     four MMAs) in increasing k into the same accumulator, no split-K: each
-//     output element sees the same K order whatever the batch is (the N of
-//     the instruction only decides how many token columns are computed; the
-//     tests check that a token's bits do not depend on it).
-//   * gate/up: a tile is 128 gate rows j0.. and the 128 matching up rows
-//     I+j0.. against up to 128 tokens: two MMAs per K step share the token
-//     tile, into two accumulators (gate, up); the epilogue computes
-//     act = bf16(silu(g) * u * p).  (Interleaving 64 gate + 64 up rows into
-//     one MMA with 256 tokens was measured slower: twice the weight blocks
-//     re-read each token tile, and the kernel is bound by memory traffic.)
-//   * down: 128 rows of W2 (h) against up to 256 tokens per tile; the
-//     epilogue writes fp32 contributions to row token*top_k + slot.
+//   * swap-AB: weight rows are the MMA "M" side, the tokens routed to one
+//     expert are the "N" side (up to 256 per tile), K runs over the hidden
+//     (gate/up) or intermediate (down) dimension.
+//   * tcgen05.mma kind::f16 per K=16 step: bf16 operands, fp32 accumulator in
+//     tensor memory, N = the tile's token count rounded up to 16.  K advances
+//     in steps of 64 (one 128-byte swizzle atom, four MMAs) in increasing k
+//     into the same accumulator, no split-K: each output element sees the
+//     same K order whatever the batch is (the instruction's M and N only
+//     decide how many rows and token columns are computed; the tests check
+//     that neither the batch nor the variant below changes a bit).
+//   * three variants of one kernel template (bi_moe_gemm_variant selects;
+//     automatic by shape):
+//       - one CTA per tile, cta_group::1, M=128 weight rows.  gate/up: 128
+//         gate rows j0.. and the 128 matching up rows I+j0.. against up to
+//         128 tokens, two MMAs per K step sharing the token tile into two
+//         accumulators; down: 128 rows of W2 against up to 256 tokens.
+//       - CTA pairs, cta_group::2 (output features a multiple of 256): two
+//         SMs of a cluster share a tile of 256 weight rows; each stages its
+//         own 128 rows and HALF of the token rows, and one thread of the even
+//         CTA issues M=256 MMAs reading the token rows from both SMs, so each
+//         SM stages 40 KB (gate/up) or 32 KB (down) per K step instead of 48.
+//       - CTA pairs with interleaved gate/up rows (gate/up, H >= 4096): each
+//         CTA holds 64 gate rows and the matching 64 up rows against up to
+//         256 tokens, one M=256 x N=256 MMA per K step; the epilogue swaps
+//         half of each chunk between the gate and up warps.
+//   * the epilogue computes act = bf16(silu(g) * u * p) (gate/up) or writes
+//     fp32 contributions to row token*top_k + slot (down).
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a ring of stages;
 //     accumulators are double buffered (2 x 256 tensor-memory columns) so the
 //     epilogue of one tile overlaps the MMAs of the next.
-//   * CTA pairs (cta_group::2, the default when the output features are a
-//     multiple of 256): two SMs of a cluster share one tile of 256 weight
-//     rows.  Each SM stages its own 128 weight rows and HALF of the token
-//     rows; one thread of the even CTA issues M=256 MMAs that read the token
-//     rows from both SMs, so each SM receives 32 KB (down) or 40 KB
-//     (gate/up) per K step instead of 48 KB for the same MMA work per SM.
-//     The kernels are bound by how many bytes each SM can keep in flight,
-//     so this is the lever.  Every output element still sees the same K
-//     order (64-wide steps of four K=16 MMAs, increasing k).
 //   * warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues the
-//     MMAs from one thread, warps 2-5 drain the accumulator (tcgen05.ld).
+//     MMAs (both warp-uniform, one elected lane issuing), warps 2-5 drain the
+//     accumulator (tcgen05.ld).  Every mbarrier wait is bounded.
 //   * persistent grid (one CTA, or CTA pair, per SM or SM pair); tiles are
 //     ordered expert, weight block, token block, so the token blocks of a
 //     weight block run back to back and share it through L2.

@@ -21,7 +21,11 @@
 //                         partials combined in slice order through smem
 //   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over 128 or
 //                         256 columns, TMR x 4 outputs per thread, cp.async
-//                         3-stage ring, slices summed into a running sum
+//                         3-stage ring, slices summed into a running sum;
+//                         a second group of 8 warps splits the slices of
+//                         small tiles (partials joined in slice order)
+// x is fp32, or bf16 (the MoE layer's tokens) read as its exact fp32 values;
+// both give the same bits.
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
