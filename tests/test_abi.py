@@ -64,6 +64,17 @@ def test_router_topk_host_checks(lib):
     assert lib.bi_router_topk(nul, nul, nul, nul, nul, nul, nul, 0, 4096, 256, 8, nul) == 0
 
 
+def test_router_bf16_host_checks(lib):
+    nul = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)   # 8-byte but not 16-byte aligned
+    assert lib.bi_router_gemm_bf16(fake, fake, nul, fake, 4, 100, 256, nul) == 2   # K % 128
+    assert lib.bi_router_gemm_bf16(odd, fake, nul, fake, 4, 128, 256, nul) == 1    # misaligned x
+    assert lib.bi_router_gemm_bf16_schedule(fake, fake, nul, fake, 4, 128, 256, 7, nul) == 1
+    assert lib.bi_router_topk_bf16(fake, fake, nul, fake, nul, fake, fake, 4, 128, 600, 8, nul) == 2
+    assert lib.bi_router_gemm_bf16(nul, nul, nul, nul, 0, 128, 256, nul) == 0      # M == 0
+
+
 def test_topk_window_host_checks(lib):
     nul = ctypes.c_void_p(None)
     fake = ctypes.c_void_p(0x10000)
