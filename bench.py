@@ -390,7 +390,7 @@ def fp32_fma_peak(dev):
     return blocks * 256 * 16 * 2 * iters / min(ts) / 1e12
 
 
-def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
+def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)):
     """Device us per router call (DSv4 router: K=4096, N=256, fp32, bias) vs M,
     from CUDA-graph replays so host launch cost is excluded.
     warm: a graph of 20 back-to-back calls (W stays in L2);
@@ -477,6 +477,15 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
             for _ in range(n):
                 bm.bi_router_topk(xm, w, 8, bias=b, out=y, stream=stream)
 
+        # every schedule on the same rows (1 rows, 2 sliced, 3 tiled, 4 split
+        # with the tile picked from M, 5..8 split with each lane tile)
+        sched = {}
+        for s_ in ((1,) if M <= 64 else ()) + (2, 3, 4, 5, 6, 7, 8):
+            def scalls(s_=s_):
+                for _ in range(n):
+                    bm.bi_router_gemm(xm, w, b, out=y, schedule=s_, stream=stream)
+            sched[str(s_)] = round(graph_time(scalls) / n, 2)
+        res[str(M)]["schedule_warm_us"] = sched
         res[str(M)]["router_plus_topk_warm_us"] = round(graph_time(two_calls) / n, 2)
         res[str(M)]["fused_router_topk_warm_us"] = round(graph_time(fused_calls) / n, 2)
         # the library default on the same shape: cuBLAS through torch.matmul,
@@ -501,6 +510,23 @@ def router_sweep(dev, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096)):
                     (part.view(torch.int32) != full[:M].view(torch.int32)).any(dim=1).sum().item())
             finally:
                 torch.backends.cuda.matmul.allow_tf32 = prev
+    # the Qwen3-30B-A3B-shaped router (K=2048, N=128, no bias) on bf16 tokens,
+    # as the MoE layer calls it
+    g = torch.Generator().manual_seed(5)
+    xq = torch.randn(4096, 2048, generator=g).to(torch.bfloat16).to(dev)
+    wq = (torch.randn(128, 2048, generator=g) * 0.02).to(dev)
+    qres = {}
+    for M in (16, 64, 256, 1024, 2048, 4096):
+        xm = xq[:M].contiguous()
+        yq = torch.empty(M, 128, dtype=torch.float32, device=dev)
+        sched = {}
+        for s_ in (0, 2, 3, 4, 5, 6, 7, 8):
+            def qcalls(s_=s_):
+                for _ in range(n):
+                    bm.bi_router_gemm(xm, wq, None, out=yq, schedule=s_, stream=stream)
+            sched[str(s_)] = round(graph_time(qcalls) / n, 2)
+        qres[str(M)] = sched
+    res["qwen_bf16_schedule_warm_us"] = qres
     return res
 
 

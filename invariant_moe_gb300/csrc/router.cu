@@ -15,15 +15,20 @@
 // contraction or reassociation freedom.  Schedules differ only in which
 // thread evaluates which p_s and in tile sizes; they are chosen from M for
 // speed:
-//   rows    (M <= 4)      one warp per weight row and up to 4 token rows,
-//                         lanes own slices: streams W for decode batches
-//   sliced  (4 < M < 384) 8x16 output tile per CTA, one warp per slice, the
-//                         partials combined in slice order through smem
-//   tiled   (M >= 384)    register-tiled FFMA kernel, 8 warps over 128 or
-//                         256 columns, TMR x 4 outputs per thread, cp.async
-//                         3-stage ring, slices summed into a running sum;
-//                         a second group of 8 warps splits the slices of
-//                         small tiles (partials joined in slice order)
+//   rows    (M <= 2; M <= 4 where split does not apply) one warp per weight
+//           row and up to 4 token rows, lanes own slices: streams W
+//   split   (2 < M < 3072) the slices spread over a cluster of 2..8 CTAs,
+//           one slice per warp, lane tiles of 2x2 .. 8x4 outputs picked from
+//           M; the slice partials meet in shared memory and are summed in
+//           slice order across the cluster (distributed shared memory)
+//   sliced  (4 < M < 384 where split does not apply) 8x16 output tile per
+//           CTA, one warp per slice, partials combined through smem
+//   tiled   (M >= 3072; M >= 384 where split does not apply) register-tiled
+//           FFMA kernel, 8 warps over 128 or 256 columns, TMR x 4 outputs per
+//           thread, cp.async 3-stage ring, slices summed into a running sum;
+//           a second group of 8 warps splits the slices of small tiles
+//           (partials joined in slice order)
+// split applies when K/128 splits into 2..8 CTAs of 4 or 8 slices.
 // x is fp32, or bf16 (the MoE layer's tokens) read as its exact fp32 values;
 // both give the same bits.
 #include "bimoe_internal.cuh"
@@ -515,6 +520,238 @@ static bi_status launch_tiled(const XT *x, const float *w, const float *b, float
   }
 }
 
+// ------------------------------------------------------------------- split --
+// Slice-parallel kernel for small and medium M.  The S slices of every output
+// are spread over a cluster of C = S / L CTAs of L warps, one slice per warp,
+// so a batch of a few rows still keeps most SMs busy and each warp's lane
+// tile can be as large as the batch allows.  Warp w of cluster rank r
+// evaluates slice s = rL + w for the CTA's whole BM x BN block: lane (a, b)
+// owns rows a + 4i (i < TM) and columns b + 8j (j < TN).  The warp streams its
+// slice of x and W through a warp-private ring of NST chunks of 32 k
+// (cp.async, 16-byte pieces, padded rows as in the tiled kernel), so no warp
+// waits for another.  After the chain the warp parks its slice partials in
+// its own shared memory; a cluster barrier; then each CTA takes 1/C of the
+// block's outputs and sums, for each, the S partials in slice order (rank r's
+// shared memory holds slices rL .. rL+L-1), then adds the bias.  The sum order
+// is the recipe's; only the placement of the chains differs.
+constexpr int kSpLM = 4, kSpLN = 8;  // lanes along rows x lanes along columns
+constexpr int kSpMaxC = 8;           // portable cluster size
+
+template <int TM, int TN, int NST, typename XT>
+struct SplitCfg {
+  static constexpr int BM = kSpLM * TM, BN = kSpLN * TN;
+  static constexpr int XLd = XPitch<XT>::chunk;  // x row pitch of a chunk (elements)
+  static constexpr int XB = BM * XLd * static_cast<int>(sizeof(XT));  // bytes of one x chunk
+  static constexpr int WB = BN * kTLd * 4;                            // bytes of one W chunk
+  static constexpr int WARP_BYTES = NST * (XB + WB);                  // one warp's ring
+  static_assert(BM * BN * 4 <= WARP_BYTES, "a warp's partials must fit in its ring");
+};
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
+  return v;
+}
+
+template <int TM, int TN, int NST, int L, typename XT>
+__global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restrict__ x,
+                                                              const float *__restrict__ w,
+                                                              const float *__restrict__ bias,
+                                                              float *__restrict__ y, int M, int K,
+                                                              int N) {
+  using Cf = SplitCfg<TM, TN, NST, XT>;
+  constexpr int BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd;
+  constexpr int kChunks = kSlice / kTBK;
+  extern __shared__ __align__(16) uint8_t sp_smem[];
+
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = K / kSlice / L;  // CTAs per cluster (the launch's cluster size)
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int n0 = (blockIdx.x / C) * BN, m0 = blockIdx.y * BM;
+  const int s = rank * L + warp;  // this warp's slice
+  uint8_t *mine = sp_smem + warp * Cf::WARP_BYTES;
+  XT *xr = reinterpret_cast<XT *>(mine);                   // [NST][BM][XLd]
+  float *wr = reinterpret_cast<float *>(mine + NST * Cf::XB);  // [NST][BN][kTLd]
+
+  // chunk q (k = 128 s + 32 q ...) of the warp's x rows and W rows into stage st
+  auto load = [&](int q, int st) {
+    const int k0 = s * kSlice + q * kTBK;
+    constexpr int XE = 16 / static_cast<int>(sizeof(XT));  // x elements per piece
+    constexpr int XPC = kTBK / XE, WPC = kTBK / 4;         // pieces per row
+    static_assert((BM * XPC) % 32 == 0 && (BN * WPC) % 32 == 0, "whole warps of pieces");
+#pragma unroll
+    for (int t = 0; t < BM * XPC / 32; ++t) {
+      const int i = lane + 32 * t, row = i / XPC, pc = i % XPC;
+      const int gm = min(m0 + row, M - 1);
+      cp_async16(smem_u32(xr + (st * BM + row) * XLd + pc * XE),
+                 x + static_cast<size_t>(gm) * K + k0 + pc * XE);
+    }
+#pragma unroll
+    for (int t = 0; t < BN * WPC / 32; ++t) {
+      const int i = lane + 32 * t, row = i / WPC, pc = i % WPC;
+      const int gn = min(n0 + row, N - 1);
+      cp_async16(smem_u32(wr + (st * BN + row) * kTLd + pc * 4),
+                 w + static_cast<size_t>(gn) * K + k0 + pc * 4);
+    }
+  };
+
+  float p[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) p[i][j] = 0.0f;
+
+#pragma unroll
+  for (int q = 0; q < NST - 1; ++q) {
+    if (q < kChunks) load(q, q);
+    cp_async_commit();
+  }
+  const int a = lane / kSpLN, b = lane % kSpLN;
+#pragma unroll
+  for (int q = 0; q < kChunks; ++q) {
+    cp_async_wait<NST - 2>();
+    __syncwarp();  // every lane's pieces of chunk q landed; stage of q-1 free
+    if (q + NST - 1 < kChunks) load(q + NST - 1, (q + NST - 1) % NST);
+    cp_async_commit();
+    const XT *xb = xr + (q % NST) * BM * XLd;
+    const float *wb = wr + (q % NST) * BN * kTLd;
+#pragma unroll
+    for (int kk = 0; kk < kTBK; kk += 4) {
+      float4 xv[TM], wv[TN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) xv[i] = ld_x4(xb + (a + kSpLM * i) * XLd + kk);
+#pragma unroll
+      for (int j = 0; j < TN; ++j)
+        wv[j] = *reinterpret_cast<const float4 *>(wb + (b + kSpLN * j) * kTLd + kk);
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+          p[i][j] = __fmaf_rn(xv[i].x, wv[j].x, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].y, wv[j].y, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].z, wv[j].z, p[i][j]);
+          p[i][j] = __fmaf_rn(xv[i].w, wv[j].w, p[i][j]);
+        }
+    }
+  }
+  cp_async_wait<0>();
+  __syncwarp();  // the ring is read out: the warp's partials go over it
+  float *part = reinterpret_cast<float *>(mine);  // [BM][BN]
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) part[(a + kSpLM * i) * BN + b + kSpLN * j] = p[i][j];
+
+  cluster_sync_all();  // every slice partial of the block is in place
+
+  // this CTA's share of the block's outputs, each summed over all S slices
+  constexpr int E = BM * BN;
+  const int per = (E + C - 1) / C;
+  const int e_end = min(E, (rank + 1) * per);
+  const uint32_t base = smem_u32(sp_smem);
+  for (int e = rank * per + static_cast<int>(threadIdx.x); e < e_end; e += 32 * L) {
+    float v[kSpMaxC][L];
+#pragma unroll
+    for (int r = 0; r < kSpMaxC; ++r) {
+      if (r < C) {
+        const uint32_t rb = mapa_shared(base, static_cast<uint32_t>(r)) + static_cast<uint32_t>(e) * 4u;
+#pragma unroll
+        for (int l = 0; l < L; ++l) v[r][l] = ld_dsmem_f32(rb + static_cast<uint32_t>(l * Cf::WARP_BYTES));
+      }
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kSpMaxC; ++r) {
+      if (r < C) {
+#pragma unroll
+        for (int l = 0; l < L; ++l) acc = __fadd_rn(acc, v[r][l]);
+      }
+    }
+    const int m = m0 + e / BN, n = n0 + e % BN;
+    if (m < M && n < N) {
+      if (bias) acc = __fadd_rn(acc, bias[n]);
+      y[static_cast<size_t>(m) * N + n] = acc;
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while a peer still reads its partials
+}
+
+template <int TM, int TN, int NST, int L, typename XT>
+static bi_status launch_split_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                                int64_t K, int64_t N, cudaStream_t stream) {
+  using Cf = SplitCfg<TM, TN, NST, XT>;
+  const int C = static_cast<int>(K / kSlice) / L;
+  const size_t smem = static_cast<size_t>(L) * Cf::WARP_BYTES;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      set_error("router split: cannot reserve %zu bytes of shared memory", smem);
+      return BI_ERR_CUDA;
+    }
+    attr_done[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
+            static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
+  return launch_chained(router_split_kernel<TM, TN, NST, L, XT>, grid, dim3(32 * L), smem, stream, C,
+                        x, w, b, y, (int)M, (int)K, (int)N);
+}
+
+// Lane tiles of the split schedule (outputs per thread TM x TN, ring depth).
+struct SplitTile { int tm, tn, nst; };
+constexpr SplitTile kSplitTiles[] = {{2, 2, 4}, {4, 2, 4}, {4, 4, 3}, {8, 4, 2}};
+constexpr int kNumSplitTiles = 4;
+
+// Warps per CTA for the split schedule (slices per CTA), 0 if the slice count
+// does not split into 2..8 CTAs of 4 or 8 warps.
+static int split_warps(int64_t K) {
+  const int64_t S = K / kSlice;
+  if (S % 4 == 0 && S / 4 >= 2 && S / 4 <= kSpMaxC) return 4;
+  if (S % 8 == 0 && S / 8 >= 2 && S / 8 <= kSpMaxC) return 8;
+  return 0;
+}
+
+// Tile for M: the largest lane tile that still gives at least 1.5 CTAs per
+// SM, else the smallest.  A CTA of few warps is latency-bound, so spreading
+// the work over more CTAs beats the better load/FMA ratio of a larger tile
+// until the SMs are covered (measured on GB300 for K=4096/N=256 and
+// K=2048/N=128, M = 1 .. 1024).
+static int split_pick(int64_t M, int64_t N, int C) {
+  const int64_t want = 3 * static_cast<int64_t>(num_sms()) / 2;
+  for (int t = kNumSplitTiles - 1; t > 0; --t) {
+    const int64_t bm = kSpLM * kSplitTiles[t].tm, bn = kSpLN * kSplitTiles[t].tn;
+    if (C * ((N + bn - 1) / bn) * ((M + bm - 1) / bm) >= want) return t;
+  }
+  return 0;
+}
+
+template <int L, typename XT>
+static bi_status launch_split_l(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                                int64_t K, int64_t N, int tile, cudaStream_t stream) {
+  switch (tile) {
+    case 0: return launch_split_t<2, 2, 4, L, XT>(x, w, b, y, M, K, N, stream);
+    case 1: return launch_split_t<4, 2, 4, L, XT>(x, w, b, y, M, K, N, stream);
+    case 2: return launch_split_t<4, 4, 3, L, XT>(x, w, b, y, M, K, N, stream);
+    default: return launch_split_t<8, 4, 2, L, XT>(x, w, b, y, M, K, N, stream);
+  }
+}
+
+// tile < 0: chosen from M.  Needs split_warps(K) != 0.
+template <typename XT>
+static bi_status launch_split(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                              int64_t K, int64_t N, int tile, cudaStream_t stream) {
+  const int L = split_warps(K);
+  const int C = static_cast<int>(K / kSlice) / L;
+  if (tile < 0) tile = split_pick(M, N, C);
+  return L == 4 ? launch_split_l<4, XT>(x, w, b, y, M, K, N, tile, stream)
+                : launch_split_l<8, XT>(x, w, b, y, M, K, N, tile, stream);
+}
+
 // ------------------------------------------------------- negative control --
 // One thread per output; the K split depends on M (the defect the recipe
 // above exists to rule out).  Test use only.
@@ -562,8 +799,29 @@ template <typename XT>
 static bi_status launch_router_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                  int64_t K, int64_t N, int schedule, cudaStream_t stream) {
   const int S = static_cast<int>(K / kSlice);
-  if (schedule == 0) schedule = (M <= 4) ? 1 : (M < 384 ? 2 : 3);
-  if (schedule == 1) {
+  // automatic: rows for one or two tokens, the cluster split up to ~3K rows,
+  // the tiled kernel beyond (measured crossover on GB300: the split is 27 %
+  // faster at M=2048 for K=2048/N=128 and level for K=4096/N=256; the tiled
+  // kernel is level or faster at M=4096)
+  if (schedule == 0) {
+    if (M <= 2) schedule = 1;
+    else if (M < 3072 && split_warps(K)) schedule = 4;
+    else if (M < 384) schedule = (M <= 4) ? 1 : 2;
+    else schedule = 3;
+  }
+  if (schedule >= 4 && schedule <= 4 + kNumSplitTiles) {  // 4 auto tile, 5.. forced
+    if (!split_warps(K)) {
+      set_error("router split schedule: K=%lld does not split into 2..8 CTAs of 4 or 8 slices",
+                (long long)K);
+      return BI_ERR_UNSUPPORTED;
+    }
+    if ((M + 7) / 8 > 65535) {
+      set_error("router split schedule: M=%lld too large for it", (long long)M);
+      return BI_ERR_UNSUPPORTED;
+    }
+    const bi_status st = launch_split(x, w, b, y, M, K, N, schedule - 5, stream);
+    if (st != BI_OK) return st;
+  } else if (schedule == 1) {
     const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
     dim3 grid(static_cast<unsigned>(N), static_cast<unsigned>((M + mr - 1) / mr));
     const size_t smem = static_cast<size_t>(32) * kSlicePad * sizeof(float) +

@@ -51,16 +51,21 @@ def test_parity_config1(oracle_mod, inputs, dev_inputs):
 def test_row_bits_invariant_over_M(dev_inputs):
     x, w, b = dev_inputs
     full = run(x, w, b, 4096)
-    for M in syn.batch_sizes(4096) + [2, 3, 4, 5, 6, 7, 100, 383, 384, 385, 1000]:
+    for M in syn.batch_sizes(4096) + [2, 3, 4, 5, 6, 7, 100, 383, 384, 385, 1000, 2047, 2048, 3071, 3072]:
         y = run(x, w, b, M)
         assert torch.equal(y, full[:M]), f"M={M}: rows differ from the M=4096 run"
 
 
-@pytest.mark.parametrize("M", [1, 5, 9, 64, 130, 700])
+# 1 rows, 2 sliced, 3 tiled, 4 split (tile from M), 5..8 split with each lane tile
+ALL_SCHEDULES = (1, 2, 3, 4, 5, 6, 7, 8)
+
+
+@pytest.mark.parametrize("M", [1, 5, 9, 31, 64, 130, 700])
 def test_forced_schedules_agree(dev_inputs, M):
     x, w, b = dev_inputs
-    ys = [run(x, w, b, M, schedule=s) for s in (1, 2, 3)]
-    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+    ys = [run(x, w, b, M, schedule=s) for s in ALL_SCHEDULES]
+    for s, y in zip(ALL_SCHEDULES[1:], ys[1:]):
+        assert torch.equal(ys[0], y), f"M={M}: schedule {s} differs from schedule 1"
 
 
 def test_same_row_at_any_position(dev_inputs):
@@ -100,7 +105,7 @@ def test_exact_integer_case(oracle_mod, cuda):
     wi = torch.randint(-64, 65, (N, K), generator=g)
     bi = torch.randint(-64, 65, (N,), generator=g)
     x, w, b = xi.float() / 8, wi.float() / 64, bi.float() / 64
-    for s in (1, 2, 3):
+    for s in ALL_SCHEDULES:
         y = run(x.to(cuda), w.to(cuda), b.to(cuda), M, schedule=s).cpu().numpy()
         r = oracle_mod.router(x.numpy(), w.numpy(), b.numpy())
         assert np.array_equal(y.astype(np.float64), r)
@@ -121,16 +126,19 @@ def test_one_hot_rows(cuda):
 
 def test_no_bias_and_other_shapes(oracle_mod, cuda):
     """Qwen-shaped router (K=2048, N=128, up to M=4096 where the tiled
-    schedule splits its slices over two thread groups), a ragged N, and no
-    bias."""
-    for (M, K, N) in ((50, 2048, 128), (9, 1024, 200), (600, 2048, 100), (4096, 2048, 128)):
+    schedule splits its slices over two thread groups), a ragged N, no bias,
+    and K whose slices split into clusters of 2, 4, 6 and 8 CTAs (K = 1024,
+    2048, 6144 with 8 slices per CTA, 8192)."""
+    for (M, K, N) in ((50, 2048, 128), (9, 1024, 200), (600, 2048, 100), (4096, 2048, 128),
+                      (20, 6144, 64), (40, 8192, 96)):
         x = syn.normal((M, K), 1.0, 21)
         w = syn.normal((N, K), K ** -0.5, 22)
         y = run(x.to(cuda), w.to(cuda), None, M).cpu().numpy()
         r = oracle_mod.router(x.numpy(), w.numpy(), None)
         check_parity(y, r)
-        ys = [run(x.to(cuda), w.to(cuda), None, M, schedule=s) for s in (1, 2, 3)]
-        assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+        ys = [run(x.to(cuda), w.to(cuda), None, M, schedule=s) for s in ALL_SCHEDULES]
+        for s, yy in zip(ALL_SCHEDULES[1:], ys[1:]):
+            assert torch.equal(ys[0], yy), f"M={M} K={K} N={N}: schedule {s}"
 
 
 def test_full_size_sampled_parity(oracle_mod, inputs, dev_inputs):
@@ -166,7 +174,7 @@ def test_bf16_x_equals_fp32_of_it(dev_inputs, M):
     x, w, b = dev_inputs
     xb = x[:M].to(torch.bfloat16)
     xf = xb.float()
-    for s in ((1, 2, 3) if M <= 700 else (2, 3)):
+    for s in (ALL_SCHEDULES if M <= 700 else (2, 3, 4, 8)):
         y32 = bm.bi_router_gemm(xf, w, b, schedule=s)
         y16 = bm.bi_router_gemm(xb, w, b, schedule=s)
         torch.cuda.synchronize()

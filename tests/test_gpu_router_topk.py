@@ -29,7 +29,7 @@ def dsv4(cuda):
     return inp, inp.x.to(cuda), inp.w.to(cuda), inp.b.to(cuda)
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2, 3])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4, 7])
 def test_fused_equals_two_launch_dsv4(cuda, dsv4, schedule):
     import invariant_moe_gb300 as bm
     _, x, w, b = dsv4
