@@ -59,7 +59,7 @@ constexpr int kAccCols = 256;               // tensor-memory columns per accumul
 constexpr int kNumAcc = 2;                  // double-buffered
 constexpr int kTmemCols = kNumAcc * kAccCols;
 constexpr int kGemmThreads = 192;
-constexpr int kAuxBytes = 8192;             // barriers, tile prefix
+constexpr int kAuxBytes = 12288;            // barriers, tile prefix, expert offsets
 
 // gate/up: A = gate + up tiles (32 KB), up to 128 tokens, two 128-column
 // accumulators per buffer.  down: A = one tile (16 KB), up to 256 tokens, one
@@ -71,18 +71,26 @@ constexpr int kAuxBytes = 8192;             // barriers, tile prefix
 // (128 token rows per SM): one M=256 x N=256 MMA per K step; gate and up of
 // a feature land in different tensor-memory lane quarters and the epilogue
 // swaps half of them between the two warps through shared memory.
-template <bool GATE_UP, bool PAIR, bool INTER = false>
+// NARROW (decode-sized batches): tiles of at most 32 tokens, so a stage is
+// almost all weight bytes and the ring is as deep as shared memory allows;
+// with few tokens per expert a CTA's time is the weight stream, and the
+// bytes it keeps in flight set its rate.
+constexpr int kSmemLimit = 227 * 1024;
+
+template <bool GATE_UP, bool PAIR, bool INTER = false, bool NARROW = false>
 struct GemmCfg {
   static_assert(!INTER || (GATE_UP && PAIR), "interleaved rows are a gate/up CTA-pair layout");
-  static constexpr int kBN = (GATE_UP && !INTER) ? 128 : 256;  // tokens per tile (largest MMA N)
+  static constexpr int kBN = NARROW ? 32 : ((GATE_UP && !INTER) ? 128 : 256);  // tokens per tile (largest MMA N)
   static constexpr int kBNc = PAIR ? kBN / 2 : kBN; // token rows staged per CTA
   static constexpr int kABytes = (GATE_UP && !INTER ? 2 : 1) * kTileBytes;
   static constexpr int kStageBytes = kABytes + kBNc * kBK * 2;
-  static constexpr int kStages = PAIR ? (GATE_UP && !INTER ? 5 : 6) : 4;
   // 2 warp pairs x (g, u) halves of 16 x 32 fp32, then one decision flag per epilogue warp
   static constexpr int kXchgBytes = INTER ? 2 * 2 * 16 * 32 * 4 + 16 : 0;
+  static constexpr int kNarrowStages = (kSmemLimit - 1024 - kAuxBytes - kXchgBytes) / kStageBytes;
+  static constexpr int kStages =
+      NARROW ? (kNarrowStages < 16 ? kNarrowStages : 16) : (PAIR ? (GATE_UP && !INTER ? 5 : 6) : 4);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAuxBytes + kXchgBytes;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
 };
 
@@ -107,7 +115,7 @@ struct TileInfo {
 
 template <int kBN>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix,
-                                                const GemmParams &p) {
+                                                const int *offs, const GemmParams &p) {
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -117,8 +125,8 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix
   TileInfo t;
   t.e = lo;
   const int local = tile - tile_prefix[lo];
-  const int beg = __ldg(p.offsets + lo);
-  const int cnt = __ldg(p.offsets + lo + 1) - beg;
+  const int beg = offs[lo];
+  const int cnt = offs[lo + 1] - beg;
   const int ntt = (cnt + kBN - 1) / kBN;
   t.wb = local / ntt;
   const int tt = local - t.wb * ntt;
@@ -133,11 +141,11 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
   return __float2bfloat16_rn(__fmul_rn(__fmul_rn(sg, u), p));
 }
 
-template <bool GATE_UP, bool PAIR, bool INTER>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
-  using C = GemmCfg<GATE_UP, PAIR, INTER>;
+  using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   griddep_wait();  // the offsets, permutation and operands come from earlier kernels
   constexpr int kBN = C::kBN;
   constexpr int kStages = C::kStages;
@@ -156,6 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *tile_prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [E+1]
+  int *offs = tile_prefix + prm.E + 1;                        // [E+1] copy of prm.offsets
   // INTER: [warp pair][g half, u half][16 columns][32 lanes] fp32
   float *xchg = reinterpret_cast<float *>(smem + kStages * kStageBytes + kAuxBytes);
 
@@ -185,10 +194,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // the expert offsets in shared memory: one global round trip for all
+  // threads instead of a chain of dependent loads in the tile scan below
+  for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  __syncthreads();
   if (warp == 1) {
     if (PAIR) {
       if (lane == 0) *tmem_slot = 0u;
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int e0 = min(lane * per, prm.E), e1 = min(e0 + per, prm.E);
     int local = 0;
     for (int e = e0; e < e1; ++e) {
-      const int cnt = __ldg(prm.offsets + e + 1) - __ldg(prm.offsets + e);
+      const int cnt = offs[e + 1] - offs[e];
       local += prm.n_wb * ((cnt + kBN - 1) / kBN);
     }
     int incl = local;
@@ -218,7 +231,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int run = incl - local;
     for (int e = e0; e < e1; ++e) {
       tile_prefix[e] = run;
-      const int cnt = __ldg(prm.offsets + e + 1) - __ldg(prm.offsets + e);
+      const int cnt = offs[e + 1] - offs[e];
       run += prm.n_wb * ((cnt + kBN - 1) / kBN);
     }
     if (lane == 31) tile_prefix[prm.E] = incl;
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
-      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
       const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
                         static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
       // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
         // the MMA N covers the tile's real tokens (a multiple of 16), so a
         // ragged last tile of an expert does not pay for padding columns
-        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
         const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, (ti.ntok + 15) & ~15);
         if (!wait_u(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int nx_pair[kBN / 32];
     float nx_p[kBN / 32];
     auto prefetch = [&](int tile) {
-      const TileInfo t = decode_tile<kBN>(tile, tile_prefix, prm);
+      const TileInfo t = decode_tile<kBN>(tile, tile_prefix, offs, prm);
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         const int c = 32 * i + lane;
@@ -432,7 +445,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     if (unit0 < total_tiles) prefetch(unit0);
     for (int tile = unit0; tile < total_tiles; tile += nunits) {
-      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, prm);
+      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
       int my_pair[kBN / 32];
       float my_p[kBN / 32];
 #pragma unroll
@@ -549,10 +562,10 @@ static std::atomic<int> g_gemm_variant{0};
 
 int set_gemm_variant(int v) { return g_gemm_variant.exchange(v); }
 
-template <bool GATE_UP, bool PAIR, bool INTER = false>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
 static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                              int64_t P, cudaStream_t stream) {
-  using C = GemmCfg<GATE_UP, PAIR, INTER>;
+  using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   static std::mutex mu;
   static int max_units[64] = {};  // CTAs (or CTA pairs) resident at once, per device
   int dev = 0;
@@ -577,7 +590,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   {
     std::lock_guard<std::mutex> lk(mu);
     if (max_units[dev] == 0) {
-      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER>,
+      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) {
         cudaGetLastError();  // do not leave the error for an unrelated later check
@@ -588,7 +601,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
       if (PAIR) {
         cfg.gridDim = dim3(2 * (num_sms() / 2));
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>, &cfg);
         if (e != cudaSuccess || clusters <= 0) {
           cudaGetLastError();
           set_error("cudaOccupancyMaxActiveClusters: %s (%d clusters)", cudaGetErrorString(e), clusters);
@@ -612,7 +625,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   if (PAIR) attr2[nattr++] = attr[0];
   cfg.attrs = attr2;
   cfg.numAttrs = nattr;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER>, tmA, tmB, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>, tmA, tmB, p);
   if (e != cudaSuccess) {
     set_error("moe_gemm launch: %s", cudaGetErrorString(e));
     return BI_ERR_CUDA;
@@ -628,9 +641,14 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
 // average 64 or more rows (P >= 64 E); measured on GB300 for the DSv4-shaped
 // layer (H=4096, E=256, I=2048): 3 % faster at M=4096 (128 rows per
 // expert), 3-5 % slower at M <= 1024, where plain pairs win.
+static bool use_narrow(int64_t P, int64_t E);
+
 static int pick_variant(int64_t features, bool gate_up, int64_t K, int64_t P, int64_t E) {
   const int v = g_gemm_variant.load();
   const bool fits = features % (2 * kBM) == 0;
+  // NARROW tiles: one CTA per tile (measured on GB300: 2-6 % faster than
+  // CTA pairs at M <= 256 on both the Qwen- and DSv4-shaped layers)
+  if (v == 0 && use_narrow(P, E)) return 1;
   if (gate_up && (v == 3 || (v == 0 && K >= 4096 && P >= 64 * E)))
     return 3;  // 128 features per CTA pair: any I % 128 == 0
   if (v >= 2 && !fits) {
@@ -641,27 +659,44 @@ static int pick_variant(int64_t features, bool gate_up, int64_t K, int64_t P, in
   return (v == 1 || !fits) ? 1 : 2;
 }
 
+// Batches of at most 8 (token, expert) pairs per expert on average run the
+// NARROW tiles (measured on GB300: the DSv4-shaped layer at M = 1 / 16 / 64 /
+// 256 went from 135 / 878 / 1829 / 2139 us to 112 / 810 / 1727 / 2003 us,
+// 94-96 % of the copy bandwidth over the touched weights for M >= 16).
+static bool use_narrow(int64_t P, int64_t E) { return P <= 8 * E; }
+
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
+static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const void *tok, int64_t P,
+                          int64_t K, const GemmParams &p, cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  if (!make_tma_2d_bf16(&tmA, wt, static_cast<uint64_t>(w_rows), static_cast<uint64_t>(K), box_a) ||
+      !make_tma_2d_bf16(&tmB, tok, static_cast<uint64_t>(P), static_cast<uint64_t>(K),
+                        GemmCfg<GATE_UP, PAIR, INTER, NARROW>::kBNc))
+    return BI_ERR_CUDA;
+  return launch_gemm<GATE_UP, PAIR, INTER, NARROW>(tmA, tmB, p, P, stream);
+}
+
 bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32_t *perm,
                          const float *wts, const void *w13, void *act, int64_t P, int64_t H,
                          int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
   (void)top_k;
   const int v = pick_variant(I, true, H, P, E);
   if (v < 0) return BI_ERR_UNSUPPORTED;
-  const bool pair = v >= 2, inter = v == 3;
+  const bool pair = v >= 2, inter = v == 3, narrow = use_narrow(P, E);
   // features per tile: 128 (one CTA), 256 (pair), 128 (pair, interleaved: 64 per CTA)
   const int wb_rows = inter ? kBM : (pair ? 2 * kBM : kBM);
-  CUtensorMap tmA, tmB;
   const uint32_t box_a = inter ? kBM / 2 : kBM;
-  const uint32_t box_tokens = inter ? GemmCfg<true, true, true>::kBNc
-                                    : (pair ? GemmCfg<true, true>::kBNc : GemmCfg<true, false>::kBNc);
-  if (!make_tma_2d_bf16(&tmA, w13, static_cast<uint64_t>(E * 2 * I), static_cast<uint64_t>(H), box_a) ||
-      !make_tma_2d_bf16(&tmB, x_perm, static_cast<uint64_t>(P), static_cast<uint64_t>(H), box_tokens))
-    return BI_ERR_CUDA;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
                (int)(2 * I), (int)I, device_error_word()};
-  if (inter) return launch_gemm<true, true, true>(tmA, tmB, p, P, stream);
-  return pair ? launch_gemm<true, true>(tmA, tmB, p, P, stream)
-              : launch_gemm<true, false>(tmA, tmB, p, P, stream);
+  const int64_t wr = E * 2 * I;
+  if (inter)
+    return narrow ? run_gemm<true, true, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
+                  : run_gemm<true, true, true, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+  if (pair)
+    return narrow ? run_gemm<true, true, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
+                  : run_gemm<true, true, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+  return narrow ? run_gemm<true, false, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
+                : run_gemm<true, false, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
 }
 
 bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *perm, const void *w2,
@@ -670,17 +705,15 @@ bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *pe
   (void)top_k;
   const int v = pick_variant(H, false, I, P, E);
   if (v < 0) return BI_ERR_UNSUPPORTED;
-  const bool pair = v >= 2;
+  const bool pair = v >= 2, narrow = use_narrow(P, E);
   const int wb_rows = pair ? 2 * kBM : kBM;
-  CUtensorMap tmA, tmB;
-  const uint32_t box_tokens = pair ? GemmCfg<false, true>::kBNc : GemmCfg<false, false>::kBNc;
-  if (!make_tma_2d_bf16(&tmA, w2, static_cast<uint64_t>(E * H), static_cast<uint64_t>(I), kBM) ||
-      !make_tma_2d_bf16(&tmB, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I), box_tokens))
-    return BI_ERR_CUDA;
   GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / wb_rows), wb_rows, (int)H,
                (int)H, 0, device_error_word()};
-  return pair ? launch_gemm<false, true>(tmA, tmB, p, P, stream)
-              : launch_gemm<false, false>(tmA, tmB, p, P, stream);
+  if (pair)
+    return narrow ? run_gemm<false, true, false, true>(w2, E * H, kBM, act, P, I, p, stream)
+                  : run_gemm<false, true, false, false>(w2, E * H, kBM, act, P, I, p, stream);
+  return narrow ? run_gemm<false, false, false, true>(w2, E * H, kBM, act, P, I, p, stream)
+                : run_gemm<false, false, false, false>(w2, E * H, kBM, act, P, I, p, stream);
 }
 
 }  // namespace bimoe

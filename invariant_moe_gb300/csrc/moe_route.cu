@@ -7,8 +7,9 @@
 // contributions reduced with unit weights in a fixed `for t in range(topk)`
 // order).
 //
-// Permutation = stable grouping of the (token, slot) pairs by expert, in
-// three launches with integer arithmetic only:
+// Permutation = stable grouping of the (token, slot) pairs by expert, with
+// integer arithmetic only; up to 1024 tokens in one single-CTA launch, beyond
+// that in three launches:
 //   count   per 256-token block, per-expert pair counts (shared-memory
 //           counters: a count does not depend on the order of increments)
 //   scan    per expert, exclusive scan over blocks; exclusive scan over
@@ -109,27 +110,103 @@ __global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *_
                                                                 const int32_t *__restrict__ blkoff,
                                                                 int32_t *__restrict__ perm) {
   griddep_wait();
-  constexpr int W = kTokBlock / 32;
-  extern __shared__ uint32_t s_bits[];  // [E][W]
-  for (int i = threadIdx.x; i < E * W; i += blockDim.x) s_bits[i] = 0u;
+  constexpr int W = kTokBlock / 32, WP = W + 1;  // odd pitch: conflict-free rank loads
+  extern __shared__ uint32_t s_bits[];  // [E][WP]
+  for (int i = threadIdx.x; i < E * WP; i += blockDim.x) s_bits[i] = 0u;
   __syncthreads();
   const int lm = threadIdx.x;
   const int m = blockIdx.x * kTokBlock + lm;
   const int32_t *r = ids + static_cast<size_t>(m) * top_k;
   if (m < M)
     for (int t = 0; t < top_k; ++t)
-      if (pair_ok(r, t, E, nullptr)) atomicOr(&s_bits[r[t] * W + (lm >> 5)], 1u << (lm & 31));
+      if (pair_ok(r, t, E, nullptr)) atomicOr(&s_bits[r[t] * WP + (lm >> 5)], 1u << (lm & 31));
   __syncthreads();
   if (m < M) {
     for (int t = 0; t < top_k; ++t) {
       if (!pair_ok(r, t, E, nullptr)) continue;
       const int e = r[t];
       int rank = 0;
-      for (int w = 0; w < (lm >> 5); ++w) rank += __popc(s_bits[e * W + w]);
-      rank += __popc(s_bits[e * W + (lm >> 5)] & ((1u << (lm & 31)) - 1u));
+      for (int w = 0; w < (lm >> 5); ++w) rank += __popc(s_bits[e * WP + w]);
+      rank += __popc(s_bits[e * WP + (lm >> 5)] & ((1u << (lm & 31)) - 1u));
       const int pos = blkoff[static_cast<size_t>(blockIdx.x) * E + e] + rank;
       perm[pos] = m * top_k + t;
     }
+  }
+}
+
+// Single-CTA permutation for M <= 1024 tokens (one thread per token): the
+// count, scan and scatter above in one launch.  The positions are the same:
+// inside an expert the pairs are in token order, and a pair's rank is the
+// number of lower tokens holding that expert (popcounts of a bit matrix).
+constexpr int kSmallPermuteMaxM = 1024;
+
+__device__ __forceinline__ int block_excl_scan_int(int v, int *s_warp, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  int base = 0, all = 0;
+  for (int i = 0; i < nw; ++i) {
+    const int t = s_warp[i];
+    if (i < w) base += t;
+    all += t;
+  }
+  *total = all;
+  return base + incl - v;
+}
+
+__global__ void __launch_bounds__(kSmallPermuteMaxM) moe_permute_small_kernel(
+    const int32_t *__restrict__ ids, int M, int E, int top_k, int32_t *__restrict__ offsets,
+    int32_t *__restrict__ perm, int *err) {
+  griddep_wait();
+  extern __shared__ int s_pm[];
+  __shared__ int s_warp[32];
+  // bit rows padded to an odd pitch: lanes reading word w of different
+  // experts' rows then hit different banks
+  const int T = blockDim.x, W = T >> 5, WP = W + 1, tid = threadIdx.x;
+  int *s_cnt = s_pm;                                          // [E]
+  int *s_off = s_pm + E;                                      // [E]
+  uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_pm + 2 * E);  // [E][WP]
+  for (int i = tid; i < E * WP; i += T) s_bits[i] = 0u;
+  for (int e = tid; e < E; e += T) s_cnt[e] = 0;
+  __syncthreads();
+  const int m = tid;
+  const int32_t *r = ids + static_cast<size_t>(m) * top_k;
+  uint32_t ok = 0u;  // bit t: slot t is a valid pair
+  if (m < M)
+    for (int t = 0; t < top_k; ++t)
+      if (pair_ok(r, t, E, err)) {
+        ok |= 1u << t;
+        atomicAdd(&s_cnt[r[t]], 1);
+        atomicOr(&s_bits[r[t] * WP + (m >> 5)], 1u << (m & 31));
+      }
+  __syncthreads();
+  // exclusive scan over experts: thread tid owns experts [tid*c, tid*c + c)
+  const int c = (E + T - 1) / T;
+  const int e0 = min(E, tid * c), e1 = min(E, e0 + c);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += s_cnt[e];
+  int total;
+  int run = block_excl_scan_int(local, s_warp, &total);
+  for (int e = e0; e < e1; ++e) {
+    s_off[e] = run;
+    offsets[e] = run;
+    run += s_cnt[e];
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  for (int t = 0; t < top_k; ++t) {
+    if (!((ok >> t) & 1u)) continue;
+    const int e = r[t];
+    const uint32_t *row = s_bits + e * WP;
+    int rank = __popc(row[m >> 5] & ((1u << (m & 31)) - 1u));
+    for (int w = 0; w < (m >> 5); ++w) rank += __popc(row[w]);
+    perm[s_off[e] + rank] = m * top_k + t;
   }
 }
 
@@ -186,6 +263,13 @@ size_t permute_scratch_bytes(int64_t M, int64_t E) {
 
 bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, int64_t M,
                          int64_t E, int32_t top_k, void *scratch, cudaStream_t stream) {
+  if (M <= kSmallPermuteMaxM) {
+    const int T = static_cast<int>((M + 255) / 256 * 256);
+    const size_t smem = static_cast<size_t>(E) * (2 * sizeof(int) + (T / 32 + 1) * sizeof(uint32_t));
+    if (smem <= 48 * 1024)
+      return launch_chained(moe_permute_small_kernel, dim3(1), dim3(T), smem, stream, 1, ids, (int)M,
+                            (int)E, top_k, offsets, perm, device_error_word());
+  }
   const int nblk = static_cast<int>((M + kTokBlock - 1) / kTokBlock);
   const size_t one = (static_cast<size_t>(nblk) * E * sizeof(int32_t) + 255) / 256 * 256;
   int32_t *blkcnt = static_cast<int32_t *>(scratch);
@@ -199,7 +283,7 @@ bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, in
                            blkoff, offsets)) != BI_OK)
     return st;
   return launch_chained(moe_scatter_kernel, dim3(nblk), dim3(kTokBlock),
-                        E * (kTokBlock / 32) * sizeof(uint32_t), stream, 1, ids, (int)M, (int)E,
+                        E * (kTokBlock / 32 + 1) * sizeof(uint32_t), stream, 1, ids, (int)M, (int)E,
                         top_k, blkoff, perm);
 }
 

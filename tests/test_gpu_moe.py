@@ -48,9 +48,13 @@ def check_layer(out, ref):
 
 
 # ------------------------------------------------------------------ stages --
+# M <= 1024 runs the single-CTA permutation (unless E is too large for its
+# shared memory, as E=1024 here), larger M the three-launch one
 @pytest.mark.parametrize("M,E,k,kind", [(1, 128, 8, "rand"), (300, 128, 8, "rand"),
                                         (4096, 256, 8, "rand"), (777, 16, 4, "skew"),
-                                        (5, 8, 1, "rand"), (2000, 1024, 16, "rand")])
+                                        (5, 8, 1, "rand"), (2000, 1024, 16, "rand"),
+                                        (1024, 256, 8, "skew"), (1025, 256, 8, "skew"),
+                                        (300, 1024, 4, "rand"), (256, 512, 16, "rand")])
 def test_permute_bit_exact(oracle_mod, cuda, M, E, k, kind):
     import invariant_moe_gb300 as bm
     f = syn.random_routing if kind == "rand" else syn.skewed_routing
@@ -70,6 +74,11 @@ def test_permute_reports_bad_ids(cuda, request):
     ids = torch.tensor([[0, 5]], dtype=torch.int32, device=cuda)
     bm.bi_moe_permute(ids, 4)
     assert bm.device_error() == 1   # id out of range
+    # the three-launch path (more than 1024 tokens) reports the same
+    ids = torch.arange(2, dtype=torch.int32).repeat(1500, 1)
+    ids[700, 1] = 0
+    bm.bi_moe_permute(ids.to(cuda), 4)
+    assert bm.device_error() == 2
 
 
 def stage_inputs(M, H, E, I, k, seed, unit=False):
