@@ -152,7 +152,7 @@ def gemm_variant():
     bm.bi_moe_gemm_variant(0)
 
 
-@pytest.mark.parametrize("M,kind", [(1, "rand"), (17, "rand"), (300, "skew"), (4096, "rand")])
+@pytest.mark.parametrize("M,kind", [(1, "rand"), (17, "rand"), (100, "skew"), (300, "skew"), (4096, "rand")])
 def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
     """One CTA per tile (M=128 MMAs), CTA pairs (M=256 MMAs over two SMs) and
     CTA pairs with interleaved gate/up rows (one M=256 x N=256 MMA per K step)
