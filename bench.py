@@ -478,9 +478,10 @@ def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 
                 bm.bi_router_topk(xm, w, 8, bias=b, out=y, stream=stream)
 
         # every schedule on the same rows (1 rows, 2 sliced, 3 tiled, 4 split
-        # with the tile picked from M, 5..8 split with each lane tile)
+        # with the tile picked from M, 5..8 split with each lane tile, 9 tiled
+        # with 7x8 lane tiles)
         sched = {}
-        for s_ in ((1,) if M <= 64 else ()) + (2, 3, 4, 5, 6, 7, 8):
+        for s_ in ((1,) if M <= 64 else ()) + (2, 3, 4, 5, 6, 7, 8, 9):
             def scalls(s_=s_):
                 for _ in range(n):
                     bm.bi_router_gemm(xm, w, b, out=y, schedule=s_, stream=stream)
@@ -520,7 +521,7 @@ def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 
         xm = xq[:M].contiguous()
         yq = torch.empty(M, 128, dtype=torch.float32, device=dev)
         sched = {}
-        for s_ in (0, 2, 3, 4, 5, 6, 7, 8):
+        for s_ in (0, 2, 3, 4, 5, 6, 7, 8, 9):
             def qcalls(s_=s_):
                 for _ in range(n):
                     bm.bi_router_gemm(xm, wq, None, out=yq, schedule=s_, stream=stream)

@@ -112,9 +112,10 @@ BI_API bi_status bi_router_gemm(const float *x, const float *w, const float *bia
  * forced (0 = automatic by M, 1 = per-row warp kernel, 2 = slice-parallel
  * tile kernel, 3 = register-tiled kernel, 4 = slices spread over a cluster
  * of CTAs with the lane tile picked from M, 5..8 = the same with the lane
- * tile forced to 2x2, 4x2, 4x4, 8x4 outputs).  Schedules 4..8 need
- * K/128 to split into 2..8 CTAs of 4 or 8 slices (else
- * BI_ERR_UNSUPPORTED).  Every schedule computes the same recipe; tests use
+ * tile forced to 2x2, 4x2, 4x4, 8x4 outputs, 9 = register-tiled kernel
+ * with 7x8 outputs per thread).  Schedules 4..8 need K/128 to split into
+ * 2..8 CTAs of 4 or 8 slices, schedule 9 K/128 even (N > 128) or a multiple
+ * of 4 (N <= 128) (else BI_ERR_UNSUPPORTED).  Every schedule computes the same recipe; tests use
  * this to show that the bits do not depend on it.
  */
 BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,

@@ -263,7 +263,7 @@ BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w, const f
                                          int32_t schedule, bi_stream_t stream) {
   bi_status st = router_checks(x, w, y, M, K, N);
   if (st != BI_OK) return st;
-  BI_REQUIRE(schedule >= 0 && schedule <= 8, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   if (M == 0) return BI_OK;
   return launch_router(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -278,7 +278,7 @@ BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w, 
                                               int32_t schedule, bi_stream_t stream) {
   bi_status st = router_checks(x, w, y, M, K, N);
   if (st != BI_OK) return st;
-  BI_REQUIRE(schedule >= 0 && schedule <= 8, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   if (M == 0) return BI_OK;
   return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -315,7 +315,7 @@ BI_API bi_status bi_router_topk_schedule(const float *x, const float *w, const f
                                          int32_t schedule, bi_stream_t stream) {
   bi_status st = router_checks(x, w, y, M, K, N);
   if (st != BI_OK) return st;
-  BI_REQUIRE(schedule >= 0 && schedule <= 8, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   BI_REQUIRE(N <= 512, BI_ERR_UNSUPPORTED, "selection needs N <= 512 (N=%lld)", (long long)N);
   BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= N, BI_ERR_INVALID_ARG,
              "top_k=%d outside [1, min(16, N)]", top_k);

@@ -24,10 +24,11 @@
 //   sliced  (4 < M < 384 where split does not apply) 8x16 output tile per
 //           CTA, one warp per slice, partials combined through smem
 //   tiled   (M >= 3072; M >= 384 where split does not apply) register-tiled
-//           FFMA kernel, 8 warps over 128 or 256 columns, TMR x 4 outputs per
-//           thread, cp.async 3-stage ring, slices summed into a running sum;
-//           a second group of 8 warps splits the slices of small tiles
-//           (partials joined in slice order)
+//           FFMA kernel over 128 or 256 columns, TMR x TN outputs per thread
+//           (7x8 once the 28-row tiles cover 70 % of the SMs, else 7x4 or
+//           smaller), cp.async ring, slices summed into a running sum; extra
+//           groups of warps split the slices of a tile (partials joined in
+//           slice order)
 // split applies when K/128 splits into 2..8 CTAs of 4 or 8 slices.
 // x is fp32, or bf16 (the MoE layer's tokens) read as its exact fp32 values;
 // both give the same bits.
@@ -289,41 +290,52 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict
 }
 
 // ------------------------------------------------------------------- tiled --
-// Register-tiled FFMA kernel for large M.  A CTA is 8 warps arranged as RB
-// row blocks x CB column blocks (32 columns each, CB <= 8); thread (r, c)
-// of a warp owns rows base + 4i + r
-// (i < TMR) and columns base + 8j + c (j < 4).  K advances in chunks of 32
-// through a 3-stage cp.async ring of [rows][32 + 4] fp32 tiles (k
-// contiguous, padded so the 16-byte loads along k are bank-conflict free);
-// each chunk is consumed four k at a time, each output's chain in increasing
-// k.  Every 128 k (4 chunks) the chain value is added to the running sum and
-// restarted from +0.0f.  TMR <= 4 keeps a thread under 128 registers so two
-// CTAs can share an SM; TMR 7 and 8 take one CTA per SM.
+// Register-tiled FFMA kernel for large M.  A group of RB x CB warps (row
+// blocks x column blocks of 8*TN columns) covers a BM x BN output tile;
+// thread (r, c) of a warp owns rows base + 4i + r (i < TMR) and columns
+// base + 8j + c (j < TN).  K advances in chunks of 32 through an NSTG-stage
+// cp.async ring of [rows][32 + 4] fp32 tiles (k contiguous, padded so the
+// 16-byte loads along k are bank-conflict free); each chunk is consumed four
+// k at a time, each output's chain in increasing k.  Every 128 k (4 chunks)
+// the chain value is added to the running sum and restarted from +0.0f.
+// A CTA holds G groups over the same tile: group g evaluates slices g, g+G,
+// ... and after each round of G slices group 0 adds the round's partials to
+// the running sum in slice order through shared memory.  A thread loads
+// TMR + TN values per k for TMR x TN FMAs, so the FMA pipe can be at most
+// TMR*TN / (4 (TMR + TN)) busy under the shared-memory load rate (one
+// wavefront per loaded register per warp): 64 % for 7x4, 93 % for 7x8.
 constexpr int kTBK = 32;              // k per chunk
 constexpr int kTLd = kTBK + 4;        // padded smem row length (floats)
-constexpr int kTStages = 3;
 
-template <int TMR, int CB, int G, typename XT>
-__global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_tiled_kernel(
-    const XT *__restrict__ x, const float *__restrict__ w, const float *__restrict__ bias,
-    float *__restrict__ y, int M, int K, int N) {
-  constexpr int RB = 8 / CB;                 // row blocks per CTA
-  constexpr int BM = RB * 4 * TMR;           // rows per CTA
-  constexpr int BN = CB * 32;                // columns per CTA
-  constexpr int XLd = XPitch<XT>::chunk;     // x row pitch in the stage (elements)
-  constexpr int XS = BM * XLd * static_cast<int>(sizeof(XT)) / 4;  // x floats-worth per stage
-  constexpr int WS = BN * kTLd;              // W floats per stage
-  constexpr int GS = kTStages * (XS + WS);   // floats of one group's ring
+template <int TMR, int TN, int RB, int CB, int G, int NSTG, typename XT>
+struct TiledCfg {
+  static constexpr int GT = 32 * RB * CB;  // threads per group
+  static constexpr int BM = RB * 4 * TMR, BN = CB * 8 * TN;
+  static constexpr int XLd = XPitch<XT>::chunk;
+  static constexpr int XS = BM * XLd * static_cast<int>(sizeof(XT)) / 4;  // x floats-worth per stage
+  static constexpr int WS = BN * kTLd;                                    // W floats per stage
+  static constexpr int GS = NSTG * (XS + WS);                             // floats of one group's ring
+  static constexpr int PB = (G - 1) * TMR * TN * GT;                      // partial floats
+  static constexpr size_t kSmem = (static_cast<size_t>(G) * GS + PB) * sizeof(float);
+  static constexpr int kMinBlocks = (TMR > 4 || G > 1 || TN > 4) ? 1 : 2;
+};
+
+template <int TMR, int TN, int RB, int CB, int G, int NSTG, typename XT>
+__global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G,
+                                  TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::kMinBlocks)
+    router_tiled_kernel(const XT *__restrict__ x, const float *__restrict__ w,
+                        const float *__restrict__ bias, float *__restrict__ y, int M, int K, int N) {
+  using Cf = TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>;
+  constexpr int GT = Cf::GT, BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd;
+  constexpr int XS = Cf::XS, WS = Cf::WS, GS = Cf::GS;
   extern __shared__ __align__(16) float smem_f[];
 
   griddep_wait();
-  // slice groups: group g (256 threads) evaluates slices g, g+G, ... of the
-  // CTA's whole output tile; group 0 keeps the running sums
-  const int grp = threadIdx.x >> 8;
-  const int tid = threadIdx.x & 255;
-  XT *xs = reinterpret_cast<XT *>(smem_f + grp * GS);       // [kTStages][BM][XLd]
-  float *ws = smem_f + grp * GS + kTStages * XS;            // [kTStages][BN][kTLd]
-  float *pb = smem_f + G * GS;               // [G-1][TMR*4][256] slice partials of groups >= 1
+  const int grp = threadIdx.x / GT;
+  const int tid = threadIdx.x % GT;
+  XT *xs = reinterpret_cast<XT *>(smem_f + grp * GS);       // [NSTG][BM][XLd]
+  float *ws = smem_f + grp * GS + NSTG * XS;                // [NSTG][BN][kTLd]
+  float *pb = smem_f + G * GS;               // [G-1][TMR*TN][GT] slice partials of groups >= 1
   const int warp = tid >> 5, lane = tid & 31;
   const int rb = warp / CB, cb = warp % CB;
   const int r = lane >> 3, c = lane & 7;
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
     constexpr int XE = 16 / static_cast<int>(sizeof(XT));  // x elements per 16-byte piece
     constexpr int XPC = kTBK / XE, WPC = kTBK / 4;         // pieces per row
     XT *xst = xs + stage * (BM * XLd);
-    for (int q = tid; q < BM * XPC + BN * WPC; q += 256) {
+    for (int q = tid; q < BM * XPC + BN * WPC; q += GT) {
       if (q < BM * XPC) {
         const int row = q / XPC, piece = q % XPC;
         const int gm = min(m0 + row, M - 1);
@@ -352,43 +364,43 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
     }
   };
 
-  float p[TMR][4], acc[TMR][4];
+  float p[TMR][TN], acc[TMR][TN];
 #pragma unroll
   for (int i = 0; i < TMR; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < TN; ++j) {
       p[i][j] = 0.0f;
       acc[i][j] = 0.0f;
     }
 
   const int nchunks = K / kTBK / G;  // per group (G divides the slice count)
 #pragma unroll
-  for (int s = 0; s < kTStages - 1; ++s) {
+  for (int s = 0; s < NSTG - 1; ++s) {
     if (s < nchunks) load_chunk(s, s);
     cp_async_commit();
   }
   const int xrow0 = rb * 4 * TMR + r;  // + 4i
-  const int wrow0 = cb * 32 + c;       // + 8j
+  const int wrow0 = cb * 8 * TN + c;   // + 8j
   for (int ch = 0; ch < nchunks; ++ch) {
-    cp_async_wait<kTStages - 2>();
+    cp_async_wait<NSTG - 2>();
     __syncthreads();
-    if (ch + kTStages - 1 < nchunks) load_chunk(ch + kTStages - 1, (ch + kTStages - 1) % kTStages);
+    if (ch + NSTG - 1 < nchunks) load_chunk(ch + NSTG - 1, (ch + NSTG - 1) % NSTG);
     cp_async_commit();
-    const XT *xb = xs + (ch % kTStages) * (BM * XLd);
-    const float *wb = ws + (ch % kTStages) * WS;
+    const XT *xb = xs + (ch % NSTG) * (BM * XLd);
+    const float *wb = ws + (ch % NSTG) * WS;
 #pragma unroll
     for (int kk = 0; kk < kTBK; kk += 4) {
-      float4 xv[TMR], wv[4];
+      float4 xv[TMR], wv[TN];
 #pragma unroll
       for (int i = 0; i < TMR; ++i)
         xv[i] = ld_x4(xb + (xrow0 + 4 * i) * XLd + kk);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < TN; ++j)
         wv[j] = *reinterpret_cast<const float4 *>(wb + (wrow0 + 8 * j) * kTLd + kk);
 #pragma unroll
       for (int i = 0; i < TMR; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < TN; ++j) {
           p[i][j] = __fmaf_rn(xv[i].x, wv[j].x, p[i][j]);
           p[i][j] = __fmaf_rn(xv[i].y, wv[j].y, p[i][j]);
           p[i][j] = __fmaf_rn(xv[i].z, wv[j].z, p[i][j]);
@@ -403,7 +415,7 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
 #pragma unroll
           for (int i = 0; i < TMR; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) pb[((grp - 1) * TMR * 4 + i * 4 + j) * 256 + tid] = p[i][j];
+            for (int j = 0; j < TN; ++j) pb[((grp - 1) * TMR * TN + i * TN + j) * GT + tid] = p[i][j];
         }
         __syncthreads();
       }
@@ -411,17 +423,17 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
 #pragma unroll
         for (int i = 0; i < TMR; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < TN; ++j) {
             float a = __fadd_rn(acc[i][j], p[i][j]);
 #pragma unroll
-            for (int g2 = 1; g2 < G; ++g2) a = __fadd_rn(a, pb[((g2 - 1) * TMR * 4 + i * 4 + j) * 256 + tid]);
+            for (int g2 = 1; g2 < G; ++g2) a = __fadd_rn(a, pb[((g2 - 1) * TMR * TN + i * TN + j) * GT + tid]);
             acc[i][j] = a;
           }
       }
 #pragma unroll
       for (int i = 0; i < TMR; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) p[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) p[i][j] = 0.0f;
     }
   }
   cp_async_wait<0>();
@@ -432,7 +444,7 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
     const int m = m0 + xrow0 + 4 * i;
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < TN; ++j) {
       const int n = n0 + wrow0 + 8 * j;
       if (n >= N) continue;
       float v = acc[i][j];
@@ -442,29 +454,64 @@ __global__ void __launch_bounds__(256 * G, (TMR > 4 || G > 1) ? 1 : 2) router_ti
   }
 }
 
-template <int TMR, int CB, int G, typename XT>
+template <int TMR, int TN, int RB, int CB, int G, int NSTG, typename XT>
 static bi_status launch_tiled_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, cudaStream_t stream) {
-  constexpr int RB = 8 / CB, BM = RB * 4 * TMR, BN = CB * 32;
-  const size_t stage = static_cast<size_t>(BM) * XPitch<XT>::chunk * sizeof(XT) +
-                       static_cast<size_t>(BN) * kTLd * sizeof(float);
-  const size_t smem = static_cast<size_t>(G) * kTStages * stage +
-                      static_cast<size_t>(G - 1) * TMR * 4 * 256 * sizeof(float);
+  using Cf = TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>;
+  static_assert(Cf::kSmem <= 227 * 1024, "shared memory");
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(router_tiled_kernel<TMR, CB, G, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
+    if (cudaFuncSetAttribute(router_tiled_kernel<TMR, TN, RB, CB, G, NSTG, XT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cf::kSmem)) !=
+        cudaSuccess) {
       cudaGetLastError();  // do not leave the error for an unrelated later check
-      set_error("router tiled: cannot reserve %zu bytes of shared memory", smem);
+      set_error("router tiled: cannot reserve %zu bytes of shared memory", Cf::kSmem);
       return BI_ERR_CUDA;
     }
     attr_done[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>((M + BM - 1) / BM), static_cast<unsigned>((N + BN - 1) / BN));
-  return launch_chained(router_tiled_kernel<TMR, CB, G, XT>, grid, dim3(256 * G), smem, stream, 1, x,
-                        w, b, y, (int)M, (int)K, (int)N);
+  dim3 grid(static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM), static_cast<unsigned>((N + Cf::BN - 1) / Cf::BN));
+  return launch_chained(router_tiled_kernel<TMR, TN, RB, CB, G, NSTG, XT>, grid, dim3(Cf::GT * G), Cf::kSmem,
+                        stream, 1, x, w, b, y, (int)M, (int)K, (int)N);
+}
+
+// The classic shapes: 8 warps per group, 4 columns per thread, 3 stages.
+template <int TMR, int CB, int G, typename XT>
+static bi_status launch_tiled4(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                               int64_t K, int64_t N, cudaStream_t stream) {
+  return launch_tiled_t<TMR, 4, 8 / CB, CB, G, 3, XT>(x, w, b, y, M, K, N, stream);
+}
+
+// Wide lane tiles (7 rows x 8 columns per thread): groups of 4 warps over 256
+// columns with two slice groups, or of 2 warps over 128 columns with four;
+// either way 28-row CTA tiles of 256 threads (147 CTAs at M = 4096).  A CTA
+// runs its whole K loop in about the same time at any M (255 registers, two
+// warps per scheduler), so the schedule pays once the 28-row tiles cover
+// most SMs: measured on GB300 at M = 4096, 62.5 vs 75.0 us (K=2048, N=128,
+// bf16 x) and 226.5 vs 233.8 us (K=4096, N=256) against the 7x4 tiles.
+static bool wide_ok(int64_t K, int64_t N) {
+  const int64_t S = K / kSlice;
+  return N <= 128 ? S % 4 == 0 : S % 2 == 0;
+}
+
+template <typename XT>
+static bi_status launch_tiled_wide(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                                   int64_t K, int64_t N, cudaStream_t stream) {
+  const int64_t S = K / kSlice;
+  if (N <= 128) {
+    if (S % 4 != 0) {
+      set_error("router wide tiles: K/128 = %lld slices do not split over 4 groups", (long long)S);
+      return BI_ERR_UNSUPPORTED;
+    }
+    return launch_tiled_t<7, 8, 1, 2, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+  }
+  if (S % 2 != 0) {
+    set_error("router wide tiles: K/128 = %lld slices do not split over 2 groups", (long long)S);
+    return BI_ERR_UNSUPPORTED;
+  }
+  return launch_tiled_t<7, 8, 1, 4, 2, 2, XT>(x, w, b, y, M, K, N, stream);
 }
 
 // Tile shape for the tiled schedule: the (column blocks, rows per thread)
@@ -503,20 +550,20 @@ static bi_status launch_tiled(const XT *x, const float *w, const float *b, float
     const int64_t ctas = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     if (pick.tmr <= 4 && ctas < sms && (K / kSlice) % 2 == 0) {
       switch (pick.cb * 16 + pick.tmr) {
-        case 4 * 16 + 4: return launch_tiled_t<4, 4, 2, XT>(x, w, b, y, M, K, N, stream);
-        case 4 * 16 + 3: return launch_tiled_t<3, 4, 2, XT>(x, w, b, y, M, K, N, stream);
-        case 4 * 16 + 2: return launch_tiled_t<2, 4, 2, XT>(x, w, b, y, M, K, N, stream);
-        default: return launch_tiled_t<1, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 4: return launch_tiled4<4, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 3: return launch_tiled4<3, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        case 4 * 16 + 2: return launch_tiled4<2, 4, 2, XT>(x, w, b, y, M, K, N, stream);
+        default: return launch_tiled4<1, 4, 2, XT>(x, w, b, y, M, K, N, stream);
       }
     }
   }
   switch (pick.cb * 16 + pick.tmr) {
-    case 8 * 16 + 7: return launch_tiled_t<7, 8, 1, XT>(x, w, b, y, M, K, N, stream);
-    case 8 * 16 + 8: return launch_tiled_t<8, 8, 1, XT>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 4: return launch_tiled_t<4, 4, 1, XT>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 3: return launch_tiled_t<3, 4, 1, XT>(x, w, b, y, M, K, N, stream);
-    case 4 * 16 + 2: return launch_tiled_t<2, 4, 1, XT>(x, w, b, y, M, K, N, stream);
-    default: return launch_tiled_t<1, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 8 * 16 + 7: return launch_tiled4<7, 8, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 8 * 16 + 8: return launch_tiled4<8, 8, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 4: return launch_tiled4<4, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 3: return launch_tiled4<3, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    case 4 * 16 + 2: return launch_tiled4<2, 4, 1, XT>(x, w, b, y, M, K, N, stream);
+    default: return launch_tiled4<1, 4, 1, XT>(x, w, b, y, M, K, N, stream);
   }
 }
 
@@ -807,7 +854,7 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
     if (M <= 2) schedule = 1;
     else if (M < 3072 && split_warps(K)) schedule = 4;
     else if (M < 384) schedule = (M <= 4) ? 1 : 2;
-    else schedule = 3;
+    else schedule = (wide_ok(K, N) && (M + 27) / 28 >= 7 * num_sms() / 10) ? 9 : 3;
   }
   if (schedule >= 4 && schedule <= 4 + kNumSplitTiles) {  // 4 auto tile, 5.. forced
     if (!split_warps(K)) {
@@ -862,6 +909,13 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
     }
     const bi_status st = launch_chained(router_sliced_kernel<XT>, grid, dim3(256), smem, stream, 1, x, w, b,
                                         y, (int)M, (int)K, (int)N, device_error_word());
+    if (st != BI_OK) return st;
+  } else if (schedule == 9) {
+    if ((M + 27) / 28 > 2147483647LL) {
+      set_error("router wide schedule: M=%lld too large for it", (long long)M);
+      return BI_ERR_UNSUPPORTED;
+    }
+    const bi_status st = launch_tiled_wide(x, w, b, y, M, K, N, stream);
     if (st != BI_OK) return st;
   } else if (schedule == 3) {
     if ((M + 3) / 4 > 65535LL * 8 * 4) {

@@ -70,7 +70,7 @@ def test_router_bf16_host_checks(lib):
     odd = ctypes.c_void_p(0x10008)   # 8-byte but not 16-byte aligned
     assert lib.bi_router_gemm_bf16(fake, fake, nul, fake, 4, 100, 256, nul) == 2   # K % 128
     assert lib.bi_router_gemm_bf16(odd, fake, nul, fake, 4, 128, 256, nul) == 1    # misaligned x
-    assert lib.bi_router_gemm_bf16_schedule(fake, fake, nul, fake, 4, 128, 256, 9, nul) == 1
+    assert lib.bi_router_gemm_bf16_schedule(fake, fake, nul, fake, 4, 128, 256, 10, nul) == 1
     # the cluster-split schedules need K/128 to split into 2..8 CTAs of 4 or 8 slices
     assert lib.bi_router_gemm_bf16_schedule(fake, fake, nul, fake, 4, 512, 256, 4, nul) == 2
     assert lib.bi_router_gemm_schedule(fake, fake, nul, fake, 4, 36 * 128, 256, 8, nul) == 2

@@ -56,8 +56,9 @@ def test_row_bits_invariant_over_M(dev_inputs):
         assert torch.equal(y, full[:M]), f"M={M}: rows differ from the M=4096 run"
 
 
-# 1 rows, 2 sliced, 3 tiled, 4 split (tile from M), 5..8 split with each lane tile
-ALL_SCHEDULES = (1, 2, 3, 4, 5, 6, 7, 8)
+# 1 rows, 2 sliced, 3 tiled, 4 split (tile from M), 5..8 split with each lane
+# tile, 9 tiled with 7x8 lane tiles
+ALL_SCHEDULES = (1, 2, 3, 4, 5, 6, 7, 8, 9)
 
 
 @pytest.mark.parametrize("M", [1, 5, 9, 31, 64, 130, 700])
@@ -174,7 +175,7 @@ def test_bf16_x_equals_fp32_of_it(dev_inputs, M):
     x, w, b = dev_inputs
     xb = x[:M].to(torch.bfloat16)
     xf = xb.float()
-    for s in (ALL_SCHEDULES if M <= 700 else (2, 3, 4, 8)):
+    for s in (ALL_SCHEDULES if M <= 700 else (2, 3, 4, 8, 9)):
         y32 = bm.bi_router_gemm(xf, w, b, schedule=s)
         y16 = bm.bi_router_gemm(xb, w, b, schedule=s)
         torch.cuda.synchronize()
