@@ -311,8 +311,10 @@ template <int TMR, int TN, int RB, int CB, int G, int NSTG, typename XT>
 struct TiledCfg {
   static constexpr int GT = 32 * RB * CB;  // threads per group
   static constexpr int BM = RB * 4 * TMR, BN = CB * 8 * TN;
-  static constexpr int XLd = XPitch<XT>::chunk;
-  static constexpr int XS = BM * XLd * static_cast<int>(sizeof(XT)) / 4;  // x floats-worth per stage
+  // x is staged as fp32 whatever its type: bf16 x is widened once as it is
+  // written to shared memory instead of at every use
+  static constexpr int XLd = kTLd;
+  static constexpr int XS = BM * XLd;                                     // x floats per stage
   static constexpr int WS = BN * kTLd;                                    // W floats per stage
   static constexpr int GS = NSTG * (XS + WS);                             // floats of one group's ring
   static constexpr int PB = (G - 1) * TMR * TN * GT;                      // partial floats
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G
   griddep_wait();
   const int grp = threadIdx.x / GT;
   const int tid = threadIdx.x % GT;
-  XT *xs = reinterpret_cast<XT *>(smem_f + grp * GS);       // [NSTG][BM][XLd]
+  float *xs = smem_f + grp * GS;                            // [NSTG][BM][XLd] fp32
   float *ws = smem_f + grp * GS + NSTG * XS;                // [NSTG][BN][kTLd]
   float *pb = smem_f + G * GS;               // [G-1][TMR*TN][GT] slice partials of groups >= 1
   const int warp = tid >> 5, lane = tid & 31;
@@ -341,25 +343,56 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G
   const int r = lane >> 3, c = lane & 7;
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   constexpr int kCPS = kSlice / kTBK;        // chunks per slice
+  constexpr bool kBf16 = sizeof(XT) == 2;
+  // first k of the group's local chunk lc
+  auto chunk_k0 = [&](int lc) { return ((lc / kCPS) * G + grp) * kSlice + (lc % kCPS) * kTBK; };
 
   // global -> shared copy of the group's local chunk lc (16-byte pieces;
-  // rows past M / N read a clamped valid row and are never stored)
+  // rows past M / N read a clamped valid row and are never stored); bf16 x
+  // goes through registers (xload / xstore) instead
   auto load_chunk = [&](int lc, int stage) {
-    const int k0 = ((lc / kCPS) * G + grp) * kSlice + (lc % kCPS) * kTBK;
-    constexpr int XE = 16 / static_cast<int>(sizeof(XT));  // x elements per 16-byte piece
-    constexpr int XPC = kTBK / XE, WPC = kTBK / 4;         // pieces per row
-    XT *xst = xs + stage * (BM * XLd);
+    const int k0 = chunk_k0(lc);
+    constexpr int XPC = kBf16 ? 0 : kTBK / 4, WPC = kTBK / 4;  // pieces per row
+    float *xst = xs + stage * (BM * XLd);
     for (int q = tid; q < BM * XPC + BN * WPC; q += GT) {
       if (q < BM * XPC) {
         const int row = q / XPC, piece = q % XPC;
         const int gm = min(m0 + row, M - 1);
-        cp_async16(smem_u32(xst + row * XLd + piece * XE),
-                   x + static_cast<size_t>(gm) * K + k0 + piece * XE);
+        cp_async16(smem_u32(xst + row * XLd + piece * 4),
+                   reinterpret_cast<const float *>(x) + static_cast<size_t>(gm) * K + k0 + piece * 4);
       } else {
         const int wr = (q - BM * XPC) / WPC, piece = (q - BM * XPC) % WPC;
         const int gn = min(n0 + wr, N - 1);
         cp_async16(smem_u32(ws + stage * WS + wr * kTLd + piece * 4),
                    w + static_cast<size_t>(gn) * K + k0 + piece * 4);
+      }
+    }
+  };
+  constexpr int XPT = kBf16 ? (BM * 4 + GT - 1) / GT : 1;  // 16-byte bf16 pieces per thread
+  uint4 xreg[XPT];
+  auto xload = [&](int lc) {  // bf16 x of chunk lc into registers
+    const int k0 = chunk_k0(lc);
+#pragma unroll
+    for (int t = 0; t < XPT; ++t) {
+      const int q = tid + t * GT;
+      if (q < BM * 4) {
+        const int gm = min(m0 + q / 4, M - 1);
+        xreg[t] = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(gm) * K + k0 + (q % 4) * 8));
+      }
+    }
+  };
+  auto xstore = [&](int stage) {  // ... widened to fp32 into the stage
+    float *xst = xs + stage * (BM * XLd);
+#pragma unroll
+    for (int t = 0; t < XPT; ++t) {
+      const int q = tid + t * GT;
+      if (q < BM * 4) {
+        const uint4 u = xreg[t];
+        float4 *d = reinterpret_cast<float4 *>(xst + (q / 4) * XLd + (q % 4) * 8);
+        d[0] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        d[1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u),
+                           __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
       }
     }
   };
@@ -376,7 +409,13 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G
   const int nchunks = K / kTBK / G;  // per group (G divides the slice count)
 #pragma unroll
   for (int s = 0; s < NSTG - 1; ++s) {
-    if (s < nchunks) load_chunk(s, s);
+    if (s < nchunks) {
+      load_chunk(s, s);
+      if (kBf16) {
+        xload(s);
+        xstore(s);
+      }
+    }
     cp_async_commit();
   }
   const int xrow0 = rb * 4 * TMR + r;  // + 4i
@@ -384,9 +423,13 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G
   for (int ch = 0; ch < nchunks; ++ch) {
     cp_async_wait<NSTG - 2>();
     __syncthreads();
-    if (ch + NSTG - 1 < nchunks) load_chunk(ch + NSTG - 1, (ch + NSTG - 1) % NSTG);
+    const int nx = ch + NSTG - 1;  // the chunk staged during this one
+    if (nx < nchunks) {
+      load_chunk(nx, nx % NSTG);
+      if (kBf16) xload(nx);  // lands in registers while this chunk computes
+    }
     cp_async_commit();
-    const XT *xb = xs + (ch % NSTG) * (BM * XLd);
+    const float *xb = xs + (ch % NSTG) * (BM * XLd);
     const float *wb = ws + (ch % NSTG) * WS;
 #pragma unroll
     for (int kk = 0; kk < kTBK; kk += 4) {
@@ -407,6 +450,9 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>::GT * G
           p[i][j] = __fmaf_rn(xv[i].w, wv[j].w, p[i][j]);
         }
     }
+    // the stage of chunk nx held chunk ch - 1, which every thread finished
+    // before this iteration's barrier
+    if (kBf16 && nx < nchunks) xstore(nx % NSTG);
     if ((ch + 1) % kCPS == 0) {
       // end of a round of G slices: the slice partials join the running sum
       // in slice order (group 0's slice first, then group 1's, ...)
