@@ -250,6 +250,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Relaxed arrivals: no release of the thread's earlier memory writes.  For
+// signals that order only tensor-memory reads (already complete after
+// tcgen05.wait::ld and fenced by tcgen05.fence::before_thread_sync), so the
+// arriving thread does not wait for its global stores to drain.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 // Every thread of every CTA of the cluster; used only at kernel entry and
 // exit, which all threads reach on every path.
 __device__ __forceinline__ void cluster_sync_all() {

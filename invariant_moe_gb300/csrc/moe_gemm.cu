@@ -525,12 +525,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
+      // the accumulator is free once its tensor-memory loads have completed
+      // (tcgen05.wait::ld above); the arrival does not wait for this tile's
+      // global stores, which only later kernels read
       tc_fence_before();
       if (PAIR) {
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tempty[acc]), 0));
       } else {
-        mbar_arrive(smem_u32(&tempty[acc]));
+        mbar_arrive_relaxed(smem_u32(&tempty[acc]));
       }
       if (++acc == kNumAcc) {
         acc = 0;
