@@ -390,6 +390,11 @@ def fp32_fma_peak(dev):
     return blocks * 256 * 16 * 2 * iters / min(ts) / 1e12
 
 
+def num_sms_of(dev):
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
 def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)):
     """Device us per router call (DSv4 router: K=4096, N=256, fp32, bias) vs M,
     from CUDA-graph replays so host launch cost is excluded.
@@ -433,6 +438,15 @@ def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 
     t_flush = graph_time(flushes)
     fp32_peak = fp32_fma_peak(dev)
     res = {"fp32_fma_peak_tflops_measured": round(fp32_peak, 2)}
+    # the floor of one kernel in this measurement: a grid of one 256-thread
+    # CTA per SM doing next to nothing (the FP32 probe with one step)
+    probe_out = torch.empty(num_sms_of(dev) * 256, dtype=torch.float32, device=dev)
+
+    def empty_calls():
+        for _ in range(n):
+            bm.bi_fp32_fma_probe(num_sms_of(dev), 1, stream=stream, out=probe_out)
+
+    res["empty_kernel_floor_us"] = round(graph_time(empty_calls) / n, 2)
     for M in Ms:
         xm = x[:M].contiguous()
         y = torch.empty(M, 256, dtype=torch.float32, device=dev)

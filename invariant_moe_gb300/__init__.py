@@ -353,9 +353,12 @@ def bi_moe_gemm_variant(variant):
     return prev.value
 
 
-def bi_fp32_fma_probe(blocks, iters, stream=None):
+def bi_fp32_fma_probe(blocks, iters, stream=None, out=None):
     """Run the FP32 FMA throughput probe; returns its output tensor."""
-    out = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    if out is None:
+        out = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    elif out.numel() < blocks * 256:
+        raise ValueError("out holds fewer than blocks * 256 floats")
     _call("bi_fp32_fma_probe", _ptr(out, torch.float32, "out"), blocks, iters, _stream(stream))
     return out
 
