@@ -236,8 +236,8 @@ def run_ours(args, rank, world, local):
     ev = {n: [] for n in ("gate_up", "down")}
 
     def step(record=False):
-        bm.bi_router_gemm(x, w.w_router, None, out=scores)   # bf16 tokens, read as fp32
-        bm.bi_topk(scores, k, ids=ids, wts=wts)
+        # router on the bf16 tokens (read as fp32) and top-k selection
+        bm.bi_router_topk(x, w.w_router, k, out=scores, ids=ids, wts=wts)
         bm.bi_moe_permute(ids, E, offsets=offsets, perm=perm, workspace=ws_perm)
         bm.bi_moe_gather(x, offsets, perm, k, x_perm=x_perm)
         if record:
@@ -255,7 +255,10 @@ def run_ours(args, rank, world, local):
             ev["down"].append((e1, e2))
         bm.bi_moe_combine(contrib, M, k, out=out)
 
-    launches_per_step = 1 + 1 + 3 + 2 + 1 + 1  # router topk permute(3) gather+gate/up down combine
+    # router + top-k (2), permute (1 up to 1024 tokens, else 3; both bench
+    # workloads fit the one-CTA permutation's shared memory), gather, gate/up,
+    # down, combine
+    launches_per_step = 2 + (1 if M <= 1024 else 3) + 4
 
     for _ in range(args.warmup):
         step()

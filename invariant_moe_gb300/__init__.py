@@ -301,7 +301,8 @@ def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
     return out
 
 
-def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=0, stream=None):
+def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=0, stream=None,
+                   ids=None, wts=None):
     """Router scores and top-k selection in one call (the selection grid is a
     programmatic dependent of the router grid).  Returns
     (scores [M,N] fp32, ids [M,top_k] int32, wts [M,top_k] fp32, probs or None)."""
@@ -309,8 +310,10 @@ def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=
     N = w.shape[0]
     dev = x.device
     y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=dev)
-    ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
-    wts = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    ids = ids if ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    wts = wts if wts is not None else torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    if ids.shape != (M, top_k) or wts.shape != (M, top_k):
+        raise ValueError("ids and wts must be [M, top_k]")
     probs = torch.empty(M, N, dtype=torch.float32, device=dev) if want_probs else None
     ptrs = (_ptr(w, torch.float32, "w", dev), _ptr(bias, torch.float32, "bias", dev),
             _ptr(y, torch.float32, "out", dev), _ptr(probs, torch.float32, "probs", dev),
@@ -366,11 +369,6 @@ def bi_fp32_fma_probe(blocks, iters, stream=None, out=None):
 def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
     """Whole hot path of one MoE layer: router (on the bf16 tokens, read as
     their exact fp32 values) -> top-k -> experts.  Returns (out, scores, ids, wts)."""
-    # the router reads the bf16 tokens as their exact fp32 values
-    if x_bf16.shape[0] < 1024:
-        scores, ids, wts, _ = bi_router_topk(x_bf16, w_router, top_k, bias=bias, stream=stream)
-    else:
-        scores = bi_router_gemm(x_bf16, w_router, bias, stream=stream)
-        ids, wts, _ = bi_topk(scores, top_k, stream=stream)
+    scores, ids, wts, _ = bi_router_topk(x_bf16, w_router, top_k, bias=bias, stream=stream)
     out = bi_moe_forward(x_bf16, ids, wts, w13, w2, stream=stream)
     return out, scores, ids, wts

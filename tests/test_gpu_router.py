@@ -195,6 +195,11 @@ def test_bf16_x_qwen_shape_and_topk(cuda):
         assert torch.equal(bm.bi_router_gemm(xb, w), bm.bi_router_gemm(xb.float(), w)), M
         a = bm.bi_router_topk(xb, w, 8)
         c = bm.bi_router_topk(xb.float(), w, 8)
+        s2 = bm.bi_router_gemm(xb, w)
+        ids2, wts2, _ = bm.bi_topk(s2, 8)
         torch.cuda.synchronize()
         for u, v in zip(a[:3], c[:3]):
+            assert torch.equal(u, v), M
+        # the same bits as the separate calls
+        for u, v in zip(a[:3], (s2, ids2, wts2)):
             assert torch.equal(u, v), M

@@ -29,7 +29,7 @@ def dsv4(cuda):
     return inp, inp.x.to(cuda), inp.w.to(cuda), inp.b.to(cuda)
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4, 7])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4, 7, 9])
 def test_fused_equals_two_launch_dsv4(cuda, dsv4, schedule):
     import invariant_moe_gb300 as bm
     _, x, w, b = dsv4
@@ -54,10 +54,10 @@ def test_fused_equals_two_launch_qwen_shape(cuda, k):
     g = syn.gen(71)
     x = torch.randn(1500, 2048, generator=g).to(cuda)
     w = (torch.randn(128, 2048, generator=g) * 0.02).to(cuda)
-    for M in (1, 4, 9, 300, 1500):
+    for M, sched in ((1, 0), (4, 0), (9, 0), (300, 0), (1500, 0), (33, 9), (1500, 9)):
         xm = x[:M].contiguous()
-        y1, i1, w1, _ = two_launch(bm, xm, w, None, k, 0)
-        y2, i2, w2, _ = bm.bi_router_topk(xm, w, k)
+        y1, i1, w1, _ = two_launch(bm, xm, w, None, k, sched)
+        y2, i2, w2, _ = bm.bi_router_topk(xm, w, k, schedule=sched)
         torch.cuda.synchronize()
         assert torch.equal(y1, y2) and torch.equal(i1, i2) and torch.equal(w1, w2), f"M={M}"
 
