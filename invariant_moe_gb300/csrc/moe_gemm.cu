@@ -19,7 +19,7 @@
 //     decide how many rows and token columns are computed; the tests check
 //     that neither the batch nor the variant below changes a bit).
 //   * three variants of one kernel template (bi_moe_gemm_variant selects;
-//     automatic by shape):
+//     automatic by shape and batch):
 //       - one CTA per tile, cta_group::1, M=128 weight rows.  gate/up: 128
 //         gate rows j0.. and the 128 matching up rows I+j0.. against up to
 //         128 tokens, two MMAs per K step sharing the token tile into two
@@ -29,10 +29,15 @@
 //         own 128 rows and HALF of the token rows, and one thread of the even
 //         CTA issues M=256 MMAs reading the token rows from both SMs, so each
 //         SM stages 40 KB (gate/up) or 32 KB (down) per K step instead of 48.
-//       - CTA pairs with interleaved gate/up rows (gate/up, H >= 4096): each
-//         CTA holds 64 gate rows and the matching 64 up rows against up to
-//         256 tokens, one M=256 x N=256 MMA per K step; the epilogue swaps
-//         half of each chunk between the gate and up warps.
+//       - CTA pairs with interleaved gate/up rows (gate/up; automatic for
+//         H >= 4096 once the experts average 64 or more rows): each CTA
+//         holds 64 gate rows and the matching 64 up rows against up to 256
+//         tokens, one M=256 x N=256 MMA per K step; the epilogue swaps half
+//         of each chunk between the gate and up warps.
+//     and two token-tile widths: up to 128/256 tokens, or NARROW tiles of up
+//     to 32 tokens with the deepest ring shared memory allows, for batches of
+//     at most 8 rows per expert on average (decode), where the weight stream
+//     is the whole cost (automatic choice there: one CTA per tile).
 //   * the epilogue computes act = bf16(silu(g) * u * p) (gate/up) or writes
 //     fp32 contributions to row token*top_k + slot (down).
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a ring of stages;
@@ -556,11 +561,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------------- host --
 // 0 = automatic, 1 = one CTA per tile, 2 = CTA pairs, 3 = CTA pairs with
-// interleaved gate/up rows for the gate/up GEMM (CTA pairs for down).
-// Automatic: CTA pairs whenever the output features are a multiple of 256;
-// for gate/up with K = H >= 4096 the interleaved rows (measured on GB300:
-// 4 % faster on an H=4096, I=2048, E=256 layer, but 20 % slower at H=2048,
-// where the shorter K loop no longer hides the epilogue's exchange).
+// interleaved gate/up rows for the gate/up GEMM (CTA pairs for down); the
+// automatic choice is pick_variant below.  The interleaved rows lose at
+// H=2048 (20 % slower on the gate/up GEMM), where the shorter K loop no
+// longer hides the epilogue's exchange.
 static std::atomic<int> g_gemm_variant{0};
 
 int set_gemm_variant(int v) { return g_gemm_variant.exchange(v); }
