@@ -73,14 +73,16 @@ constexpr int kAuxBytes = 12288;            // barriers, tile prefix, expert off
 // (40 KB x 5 for gate/up, 32 KB x 6 for down).
 // INTER (gate/up with CTA pairs only): each CTA stages 64 gate rows and the
 // matching 64 up rows as one 128-row A operand, against up to 256 tokens
-// (128 token rows per SM): one M=256 x N=256 MMA per K step; gate and up of
-// a feature land in different tensor-memory lane quarters and the epilogue
-// swaps half of them between the two warps through shared memory.
+// (128 token rows per SM): one M=256 x N=256 MMA per K step.  The rows go in
+// 16-row groups, gate rows of 16 features then the up rows of the same 16,
+// so each tensor-memory lane quarter (one epilogue warp) holds both halves of
+// its features and a lane swaps half of a chunk with lane ^ 16 by shuffle.
 // NARROW (decode-sized batches): tiles of at most 32 tokens, so a stage is
 // almost all weight bytes and the ring is as deep as shared memory allows;
 // with few tokens per expert a CTA's time is the weight stream, and the
 // bytes it keeps in flight set its rate.
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kInterBox = 16 * kBK * 2;  // INTER: bytes of one 16-row A box
 
 template <bool GATE_UP, bool PAIR, bool INTER = false, bool NARROW = false>
 struct GemmCfg {
@@ -90,7 +92,7 @@ struct GemmCfg {
   static constexpr int kABytes = (GATE_UP && !INTER ? 2 : 1) * kTileBytes;
   static constexpr int kStageBytes = kABytes + kBNc * kBK * 2;
   // 2 warp pairs x (g, u) halves of 16 x 32 fp32, then one decision flag per epilogue warp
-  static constexpr int kXchgBytes = INTER ? 2 * 2 * 16 * 32 * 4 + 16 : 0;
+  static constexpr int kXchgBytes = 0;
   static constexpr int kNarrowStages = (kSmemLimit - 1024 - kAuxBytes - kXchgBytes) / kStageBytes;
   static constexpr int kStages =
       NARROW ? (kNarrowStages < 16 ? kNarrowStages : 16) : (PAIR ? (GATE_UP && !INTER ? 5 : 6) : 4);
@@ -170,8 +172,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *tile_prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [E+1]
   int *offs = tile_prefix + prm.E + 1;                        // [E+1] copy of prm.offsets
-  // INTER: [warp pair][g half, u half][16 columns][32 lanes] fp32
-  float *xchg = reinterpret_cast<float *>(smem + kStages * kStageBytes + kAuxBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -284,9 +284,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (elect_one()) {
             if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * kStageBytes);
             if (INTER) {
-              // 64 gate rows, then the 64 up rows of the same features
-              tma_load_2d_pair(smem_u32(st), &tmA, fb, kb * kBK, a_row);
-              tma_load_2d_pair(smem_u32(st + kTileBytes / 2), &tmA, fb, kb * kBK, a_row + prm.up_offset);
+              // 16 gate rows, the 16 up rows of the same features, and so on
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                tma_load_2d_pair(smem_u32(st + (2 * g) * kInterBox), &tmA, fb, kb * kBK, a_row + 16 * g);
+                tma_load_2d_pair(smem_u32(st + (2 * g + 1) * kInterBox), &tmA, fb, kb * kBK,
+                                 a_row + prm.up_offset + 16 * g);
+              }
             } else {
               tma_load_2d_pair(smem_u32(st), &tmA, fb, kb * kBK, a_row);
               if (GATE_UP)
@@ -459,22 +463,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         my_p[i] = nx_p[i];
       }
       if (tile + nunits < total_tiles) prefetch(tile + nunits);
-      // one decision per warp (lanes can disagree at the instant a wait gives
-      // up), and for INTER one per warp pair: the pair meets at a named
-      // barrier every chunk, so neither may continue without the other
-      bool okw = __all_sync(0xffffffffu, wait(smem_u32(&tfull[acc]), acc_phase, abort_flag) ? 1 : 0) != 0;
-      if (INTER) {
-        volatile int *pflag = reinterpret_cast<volatile int *>(xchg + 2 * 2 * 16 * 32);
-        if (lane == 0) pflag[q] = okw ? 1 : 0;
-        named_bar_sync(1 + (q & 1), 64);
-        okw = pflag[q] != 0 && pflag[q ^ 2] != 0;
-        named_bar_sync(1 + (q & 1), 64);  // the flags are rewritten at the next tile
-      }
+      // one decision per warp (lanes can disagree at the instant a wait gives up)
+      const bool okw = __all_sync(0xffffffffu, wait(smem_u32(&tfull[acc]), acc_phase, abort_flag) ? 1 : 0) != 0;
       if (!okw) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
-      const int col = INTER ? ti.wb * prm.wb_rows + static_cast<int>(rank) * (kBM / 2) + (q & 1) * 32 + lane
+      const int col = INTER ? ti.wb * prm.wb_rows + static_cast<int>(rank) * (kBM / 2) + 16 * q + (lane & 15)
                             : ti.wb * prm.wb_rows + static_cast<int>(rank) * kBM + row;
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
@@ -483,30 +478,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t d[32];
         tmem_ld32(tbase + c0, d);
         if (INTER) {
-          // warps q and q^2 hold gate and up of the same 32 features: the gate
-          // warp keeps tokens 0-15 of the chunk and sends 16-31, the up warp
-          // the reverse; each then finishes its 16 tokens
+          // lanes 0-15 hold the gate rows of 16 features, lanes 16-31 the up
+          // rows of the same features: the gate lane keeps tokens 0-15 of the
+          // chunk and hands 16-31 to its partner (lane ^ 16), which hands
+          // back the up values of tokens 0-15; each finishes 16 tokens
           tmem_ld_wait();
-          const bool is_gate = q < 2;
-          float *xg = xchg + (q & 1) * (2 * 16 * 32);   // gate values for tokens 16..31
-          float *xu = xg + 16 * 32;                     // up values for tokens 0..15
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (is_gate) xg[j * 32 + lane] = __uint_as_float(d[16 + j]);
-            else xu[j * 32 + lane] = __uint_as_float(d[j]);
-          }
-          named_bar_sync(1 + (q & 1), 64);
+          const bool is_gate = lane < 16;
           __nv_bfloat16 *act = static_cast<__nv_bfloat16 *>(prm.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
+            const float mine = __uint_as_float(is_gate ? d[j] : d[16 + j]);
+            const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(is_gate ? d[16 + j] : d[j]), 16);
             const int c = is_gate ? j : 16 + j;
             const float pc = __shfl_sync(0xffffffffu, my_p[i], c);
-            const float g = is_gate ? __uint_as_float(d[j]) : xg[j * 32 + lane];
-            const float u = is_gate ? xu[j * 32 + lane] : __uint_as_float(d[16 + j]);
+            const float g = is_gate ? mine : other;
+            const float u = is_gate ? other : mine;
             if (c0 + c < ti.ntok)
               act[static_cast<size_t>(ti.tok0 + c0 + c) * prm.out_ld + col] = swiglu_p(g, u, pc);
           }
-          named_bar_sync(1 + (q & 1), 64);  // the buffers are refilled by the next chunk
         } else if (GATE_UP) {
           uint32_t u[32];
           tmem_ld32(tbase + kBN + c0, u);
@@ -692,7 +681,7 @@ bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32
   const bool pair = v >= 2, inter = v == 3, narrow = use_narrow(P, E);
   // features per tile: 128 (one CTA), 256 (pair), 128 (pair, interleaved: 64 per CTA)
   const int wb_rows = inter ? kBM : (pair ? 2 * kBM : kBM);
-  const uint32_t box_a = inter ? kBM / 2 : kBM;
+  const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
                (int)(2 * I), (int)I, device_error_word()};
   const int64_t wr = E * 2 * I;
