@@ -352,8 +352,8 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
  * bi_moe_gemm_variant -- selects how the expert GEMMs (bi_moe_gate_up,
  * bi_moe_down and the two GEMMs inside bi_moe_forward) are scheduled, for
  * the whole process, from the next call on:
- *   0  automatic (the default): for batches of at most 8 (token, expert)
- *      pairs per expert on average (M * top_k <= 8 E), one CTA per tile
+ *   0  automatic (the default): for batches of at most 16 (token, expert)
+ *      pairs per expert on average (M * top_k <= 16 E), one CTA per tile
  *      with narrow token tiles; otherwise CTA pairs whenever the GEMM's
  *      output features (I for gate/up, H for down) are a multiple of 256,
  *      else one CTA per tile, and for gate/up with H >= 4096 and at least

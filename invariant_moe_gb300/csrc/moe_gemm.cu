@@ -655,11 +655,13 @@ static int pick_variant(int64_t features, bool gate_up, int64_t K, int64_t P, in
   return (v == 1 || !fits) ? 1 : 2;
 }
 
-// Batches of at most 8 (token, expert) pairs per expert on average run the
+// Batches of at most 16 (token, expert) pairs per expert on average run the
 // NARROW tiles (measured on GB300: the DSv4-shaped layer at M = 1 / 16 / 64 /
 // 256 went from 135 / 878 / 1829 / 2139 us to 112 / 810 / 1727 / 2003 us,
-// 94-96 % of the copy bandwidth over the touched weights for M >= 16).
-static bool use_narrow(int64_t P, int64_t E) { return P <= 8 * E; }
+// 94-96 % of the copy bandwidth over the touched weights for M >= 16; the
+// Qwen-shaped layer at M=256, 16 pairs per expert, from 260 to 251 us; at 32
+// and 64 pairs per expert the wide tiles win by 15-40 %).
+static bool use_narrow(int64_t P, int64_t E) { return P <= 16 * E; }
 
 template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
 static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const void *tok, int64_t P,
