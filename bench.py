@@ -636,6 +636,7 @@ def topk_window_sweep(dev, ns=(1, 8, 64), ks=(512, 1024, 2048), num_cols=8192):
     import invariant_moe_gb300 as bm
     g = torch.Generator().manual_seed(77)
     x = torch.randn(max(ns), num_cols, generator=g).clamp_min(0.0).to(dev)
+    flat = torch.zeros(max(ns), num_cols, device=dev)  # the worst case: one plateau
     stream = torch.cuda.Stream(dev)
     n_calls = 20
     res = {"num_cols": num_cols, "scores": "relu(N(0,1)): about half exact zeros"}
@@ -666,6 +667,32 @@ def topk_window_sweep(dev, ns=(1, 8, 64), ks=(512, 1024, 2048), num_cols=8192):
                     e1.synchronize()
                     ts.append(e0.elapsed_time(e1) * 1e3 / n_calls)
             res[f"n{n}_k{k}_us"] = round(statistics.median(ts), 2)
+    # every score equal: each radix pass puts the whole row in one bin
+    out = torch.empty(max(ns), 1024, dtype=torch.int32, device=dev)
+    xs = flat.contiguous()
+
+    def flat_calls():
+        for _ in range(n_calls):
+            bm.bi_topk_window(xs, 1024, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        flat_calls()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            flat_calls()
+        gr.replay()
+        stream.synchronize()
+        ts = []
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+    res[f"all_equal_n{max(ns)}_k1024_us"] = round(statistics.median(ts), 2)
     return res
 
 

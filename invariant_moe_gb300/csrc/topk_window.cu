@@ -13,9 +13,12 @@
 // One CTA of 512 threads per row, up to 8192 columns: thread t holds columns
 // t, t+512, ... (coalesced loads) as unsigned keys (the int32 key with its sign
 // bit flipped, so unsigned order is key order).  The exact k-th largest key T
-// is found by a 4-pass radix select, 8 bits per pass, on shared-memory
-// histograms (warp-aggregated atomics, so plateaus of equal keys do not
-// serialise).  Then one pass in column order: a chosen column's output slot is
+// is found by a 4-pass radix select, 8 bits per pass, on a shared-memory
+// histogram, one atomic per key.  (Aggregating a warp's equal digits first
+// with match.any, or a shuffle-and-vote plateau test, puts a dependent
+// instruction in front of every atomic and cost more than the same-bin
+// conflicts it saves: 13.2 and 12.0 us per row on GB300 against 9.0 us, and a
+// row whose scores are all equal, every key in one bin, takes 9.4 us.)  Then one pass in column order: a chosen column's output slot is
 // (keys > T before it) + min(ties before it, budget), from warp ballots and a
 // block scan.  Everything is integer counting: the result is a pure function
 // of the row.
@@ -110,9 +113,10 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
 #pragma unroll
     for (int j = 0; j < kTwVT; ++j) {
       const bool in = ((valid >> j) & 1u) && (key[j] & pmask) == prefix;
-      const uint32_t d = in ? (key[j] >> shift) & 255u : 256u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+      // one atomic per key, results unused, so the 16 of a pass issue back
+      // to back (lanes of a warp hitting one bin are merged by the shared
+      // memory atomic unit)
+      if (in) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
     }
     __syncthreads();
     // thread t < 256 holds bin 255 - t: bins in descending digit order
