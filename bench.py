@@ -613,9 +613,10 @@ def moe_sweep(dev, workload, Ms=(1, 16, 64, 256, 1024, 4096)):
                        "cold_tokens_per_s": round(M / (cold * 1e-6), 1),
                        "cold_hbm_frac": round(bytes_ / (cold * 1e-6) / 1e9 / measured_peaks()[0], 3)}
         # the same layer with each expert-GEMM variant forced (1 one CTA per
-        # tile, 2 CTA pairs, 3 CTA pairs with interleaved gate/up rows)
+        # tile, 2 CTA pairs, 3 CTA pairs with interleaved gate/up rows, 4 one
+        # CTA per tile with interleaved gate/up rows)
         var = {}
-        for v in (1, 2, 3):
+        for v in (1, 2, 3, 4):
             prev = bm.bi_moe_gemm_variant(v)
             try:
                 var[str(v)] = round((graph_time(cold_calls) - t_flush) / n, 2)

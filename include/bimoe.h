@@ -354,7 +354,8 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
  * the whole process, from the next call on:
  *   0  automatic (the default): for batches of at most 16 (token, expert)
  *      pairs per expert on average (M * top_k <= 16 E), one CTA per tile
- *      with narrow token tiles; otherwise CTA pairs whenever the GEMM's
+ *      with narrow token tiles (for gate/up with interleaved rows, as 4,
+ *      when min(E, M * top_k) * I / 64 tiles fit on the SMs); otherwise CTA pairs whenever the GEMM's
  *      output features (I for gate/up, H for down) are a multiple of 256,
  *      else one CTA per tile, and for gate/up with H >= 4096 and at least
  *      64 pairs per expert on average, CTA pairs with interleaved gate/up
@@ -365,7 +366,9 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
  *      with BI_ERR_UNSUPPORTED;
  *   3  gate/up: CTA pairs whose CTAs each hold 64 gate rows and the matching
  *      64 up rows (one M=256 x N=256 MMA per K step, any I % 128 == 0);
- *      down: as 2.
+ *      down: as 2;
+ *   4  gate/up: one CTA per tile holding 64 gate rows and the matching 64 up
+ *      rows (one M=128 MMA per K step, any I % 64 == 0); down: as 1.
  * All variants evaluate the same per-element K order, so the bits do not
  * depend on the choice (tests compare them).  *previous (may be NULL)
  * receives the old setting.  Other values: BI_ERR_INVALID_ARG.  Not

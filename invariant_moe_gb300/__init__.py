@@ -350,7 +350,8 @@ def bi_topk_window(scores, k, row_start=None, row_end=None, num_cols=None, out=N
 def bi_moe_gemm_variant(variant):
     """Select the expert-GEMM schedule for the process (0 automatic, 1 one CTA
     per tile, 2 CTA pairs, 3 CTA pairs with interleaved gate/up rows for the
-    gate/up GEMM); returns the previous setting."""
+    gate/up GEMM, 4 one CTA per tile with interleaved gate/up rows); returns
+    the previous setting."""
     prev = ctypes.c_int32(0)
     _call("bi_moe_gemm_variant", int(variant), ctypes.byref(prev))
     return prev.value

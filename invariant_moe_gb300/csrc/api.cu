@@ -486,7 +486,7 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
 }  // extern "C"
 
 BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous) {
-  BI_REQUIRE(variant >= 0 && variant <= 3, BI_ERR_INVALID_ARG, "variant %d not in {0, 1, 2, 3}", variant);
+  BI_REQUIRE(variant >= 0 && variant <= 4, BI_ERR_INVALID_ARG, "variant %d not in {0, ..., 4}", variant);
   const int old = bimoe::set_gemm_variant(variant);
   if (previous) *previous = old;
   return BI_OK;

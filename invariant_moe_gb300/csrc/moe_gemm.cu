@@ -86,7 +86,7 @@ constexpr int kInterBox = 16 * kBK * 2;  // INTER: bytes of one 16-row A box
 
 template <bool GATE_UP, bool PAIR, bool INTER = false, bool NARROW = false>
 struct GemmCfg {
-  static_assert(!INTER || (GATE_UP && PAIR), "interleaved rows are a gate/up CTA-pair layout");
+  static_assert(!INTER || GATE_UP, "interleaved rows are a gate/up layout");
   static constexpr int kBN = NARROW ? 32 : ((GATE_UP && !INTER) ? 128 : 256);  // tokens per tile (largest MMA N)
   static constexpr int kBNc = PAIR ? kBN / 2 : kBN; // token rows staged per CTA
   static constexpr int kABytes = (GATE_UP && !INTER ? 2 : 1) * kTileBytes;
@@ -302,8 +302,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = smem_u32(&full[stage]);
           if (elect_one()) {
             mbar_arrive_expect_tx(fb, kStageBytes);
-            tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
-            if (GATE_UP) tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
+            if (INTER) {
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                tma_load_2d(smem_u32(st + (2 * g) * kInterBox), &tmA, fb, kb * kBK, a_row + 16 * g);
+                tma_load_2d(smem_u32(st + (2 * g + 1) * kInterBox), &tmA, fb, kb * kBK,
+                            a_row + prm.up_offset + 16 * g);
+              }
+            } else {
+              tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
+            }
+            if (GATE_UP && !INTER)
+              tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
             tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
           }
         }
@@ -379,7 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (GATE_UP && !INTER) umma_f16_pair(d0 + kBN, udesc, bdesc, idesc, acc_in);
               } else {
                 umma_f16(d0, adesc, bdesc, idesc, acc_in);
-                if (GATE_UP) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
+                if (GATE_UP && !INTER) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
               }
             }
             __syncwarp();
@@ -643,10 +653,16 @@ static int pick_variant(int64_t features, bool gate_up, int64_t K, int64_t P, in
   const int v = g_gemm_variant.load();
   const bool fits = features % (2 * kBM) == 0;
   // NARROW tiles: one CTA per tile (measured on GB300: 2-6 % faster than
-  // CTA pairs at M <= 256 on both the Qwen- and DSv4-shaped layers)
-  if (v == 0 && use_narrow(P, E)) return 1;
+  // CTA pairs at M <= 256 on both the Qwen- and DSv4-shaped layers); for
+  // gate/up, 64-feature tiles with interleaved rows when even those fit in
+  // one wave on the SMs (twice the CTAs streaming the touched weights: the
+  // Qwen-shaped layer at M=1, 96 tiles, 44.1 vs 47.9 us; a second wave,
+  // as for the DSv4-shaped layer at M=1, makes them slower)
+  if (v == 0 && use_narrow(P, E))
+    return (gate_up && std::min(E, P) * (features / (kBM / 2)) <= num_sms()) ? 4 : 1;
   if (gate_up && (v == 3 || (v == 0 && K >= 4096 && P >= 64 * E)))
     return 3;  // 128 features per CTA pair: any I % 128 == 0
+  if (v == 4) return gate_up ? 4 : 1;  // 64 features per CTA (gate/up); down: one CTA per tile
   if (v >= 2 && !fits) {
     set_error("CTA-pair expert GEMMs need output features %% 256 == 0 (got %lld)",
               static_cast<long long>(features));
@@ -680,19 +696,23 @@ bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32
   (void)top_k;
   const int v = pick_variant(I, true, H, P, E);
   if (v < 0) return BI_ERR_UNSUPPORTED;
-  const bool pair = v >= 2, inter = v == 3, narrow = use_narrow(P, E);
-  // features per tile: 128 (one CTA), 256 (pair), 128 (pair, interleaved: 64 per CTA)
-  const int wb_rows = inter ? kBM : (pair ? 2 * kBM : kBM);
+  const bool pair = v == 2 || v == 3, inter = v == 3 || v == 4, narrow = use_narrow(P, E);
+  // features per tile: 128 (one CTA), 256 (pair), 128 (pair, interleaved:
+  // 64 per CTA), 64 (one CTA, interleaved)
+  const int wb_rows = inter ? (pair ? kBM : kBM / 2) : (pair ? 2 * kBM : kBM);
   const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
                (int)(2 * I), (int)I, device_error_word()};
   const int64_t wr = E * 2 * I;
-  if (inter)
+  if (inter && pair)
     return narrow ? run_gemm<true, true, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
                   : run_gemm<true, true, true, false>(w13, wr, box_a, x_perm, P, H, p, stream);
   if (pair)
     return narrow ? run_gemm<true, true, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
                   : run_gemm<true, true, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+  if (inter)
+    return narrow ? run_gemm<true, false, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
+                  : run_gemm<true, false, true, false>(w13, wr, box_a, x_perm, P, H, p, stream);
   return narrow ? run_gemm<true, false, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
                 : run_gemm<true, false, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
 }

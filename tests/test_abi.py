@@ -91,7 +91,7 @@ def test_topk_window_host_checks(lib):
 def test_gemm_variant_setting(lib):
     """The expert-GEMM variant is a host-side setting: no GPU needed."""
     prev = ctypes.c_int32(-1)
-    assert lib.bi_moe_gemm_variant(4, None) == 1
+    assert lib.bi_moe_gemm_variant(5, None) == 1
     assert lib.bi_moe_gemm_variant(-1, None) == 1
     assert lib.bi_moe_gemm_variant(1, ctypes.byref(prev)) == 0 and prev.value == 0
     assert lib.bi_moe_gemm_variant(0, ctypes.byref(prev)) == 0 and prev.value == 1

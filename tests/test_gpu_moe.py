@@ -168,7 +168,7 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
     off, perm = bm.bi_moe_permute(ids, E)
     xp = bm.bi_moe_gather(x, off, perm, k)
     res = {}
-    for v in (1, 2, 3):
+    for v in (1, 2, 3, 4):
         gemm_variant(v)
         act = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
         contrib = bm.bi_moe_down(act, off, perm, w2, M, k)
@@ -176,7 +176,7 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
         torch.cuda.synchronize()
         res[v] = (act, contrib, out)
     assert bm.device_error() == 0
-    for v in (2, 3):
+    for v in (2, 3, 4):
         for a, b in zip(res[1], res[v]):
             assert torch.equal(a, b), f"variant {v}"
 
@@ -196,9 +196,12 @@ def test_interleaved_gate_up_same_bits(cuda, gemm_variant, M, H, E, I, k):
     a1 = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
     gemm_variant(3)
     a3 = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
+    gemm_variant(4)
+    a4 = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
     torch.cuda.synchronize()
     assert bm.device_error() == 0
     assert torch.equal(a1, a3)
+    assert torch.equal(a1, a4)
 
 
 def test_gemm_pair_variant_rejects_unaligned_features(cuda, gemm_variant):
