@@ -29,15 +29,15 @@
 //         own 128 rows and HALF of the token rows, and one thread of the even
 //         CTA issues M=256 MMAs reading the token rows from both SMs, so each
 //         SM stages 40 KB (gate/up) or 32 KB (down) per K step instead of 48.
-//       - CTA pairs with interleaved gate/up rows (gate/up; automatic for
-//         H >= 4096 once the experts average 64 or more rows): each CTA
+//       - interleaved gate/up rows (gate/up), in CTA pairs (automatic for
+//         H >= 4096 once the experts average 64 or more rows) or one CTA
+//         per tile (automatic for the smallest decode batches): each CTA
 //         holds 64 gate rows and the matching 64 up rows against up to 256
-//         tokens, one M=256 x N=256 MMA per K step; the epilogue swaps half
-//         of each chunk between the gate and up warps.
+//         tokens; a lane and its partner lane swap half of each chunk.
 //     and two token-tile widths: up to 128/256 tokens, or NARROW tiles of up
 //     to 32 tokens with the deepest ring shared memory allows, for batches of
-//     at most 8 rows per expert on average (decode), where the weight stream
-//     is the whole cost (automatic choice there: one CTA per tile).
+//     at most 16 rows per expert on average (decode), where the weight
+//     stream is the whole cost (automatic choice there: one CTA per tile).
 //   * the epilogue computes act = bf16(silu(g) * u * p) (gate/up) or writes
 //     fp32 contributions to row token*top_k + slot (down).
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) fills a ring of stages;
@@ -71,12 +71,13 @@ constexpr int kAuxBytes = 12288;            // barriers, tile prefix, expert off
 // 256-column accumulator per buffer.  One CTA per tile stages all the tile's
 // token rows (48 KB stages, 4 deep); a CTA pair stages half of them per SM
 // (40 KB x 5 for gate/up, 32 KB x 6 for down).
-// INTER (gate/up with CTA pairs only): each CTA stages 64 gate rows and the
-// matching 64 up rows as one 128-row A operand, against up to 256 tokens
-// (128 token rows per SM): one M=256 x N=256 MMA per K step.  The rows go in
-// 16-row groups, gate rows of 16 features then the up rows of the same 16,
-// so each tensor-memory lane quarter (one epilogue warp) holds both halves of
-// its features and a lane swaps half of a chunk with lane ^ 16 by shuffle.
+// INTER (gate/up): each CTA stages 64 gate rows and the matching 64 up rows
+// as one 128-row A operand, against up to 256 tokens (for a pair, 128 token
+// rows per SM and one M=256 x N=256 MMA per K step; alone, one M=128 MMA).
+// The rows go in 16-row groups, gate rows of 16 features then the up rows of
+// the same 16, so each tensor-memory lane quarter (one epilogue warp) holds
+// both halves of its features and a lane swaps half of a chunk with
+// lane ^ 16 by shuffle.
 // NARROW (decode-sized batches): tiles of at most 32 tokens, so a stage is
 // almost all weight bytes and the ring is as deep as shared memory allows;
 // with few tokens per expert a CTA's time is the weight stream, and the
