@@ -620,9 +620,9 @@ static bi_status launch_tiled(const XT *x, const float *w, const float *b, float
 // tile can be as large as the batch allows.  Warp w of cluster rank r
 // evaluates slice s = rL + w for the CTA's whole BM x BN block: lane (a, b)
 // owns rows a + 4i (i < TM) and columns b + 8j (j < TN).  The warp streams its
-// slice of x and W through a warp-private ring of NST chunks of 32 k
-// (cp.async, 16-byte pieces, padded rows as in the tiled kernel), so no warp
-// waits for another.  After the chain the warp parks its slice partials in
+// slice of x and W through a warp-private ring of NST chunks of CK k
+// (cp.async, 16-byte pieces, rows padded by 16 bytes so lanes reading
+// different rows at one k hit different banks), so no warp waits for another.  After the chain the warp parks its slice partials in
 // its own shared memory; a cluster barrier; then each CTA takes 1/C of the
 // block's outputs and sums, for each, the S partials in slice order (rank r's
 // shared memory holds slices rL .. rL+L-1), then adds the bias.  The sum order
@@ -630,12 +630,13 @@ static bi_status launch_tiled(const XT *x, const float *w, const float *b, float
 constexpr int kSpLM = 4, kSpLN = 8;  // lanes along rows x lanes along columns
 constexpr int kSpMaxC = 8;           // portable cluster size
 
-template <int TM, int TN, int NST, typename XT>
+template <int TM, int TN, int NST, typename XT, int CK>
 struct SplitCfg {
   static constexpr int BM = kSpLM * TM, BN = kSpLN * TN;
-  static constexpr int XLd = XPitch<XT>::chunk;  // x row pitch of a chunk (elements)
+  static constexpr int XLd = CK + 16 / static_cast<int>(sizeof(XT));  // x row pitch (elements)
+  static constexpr int WLd = CK + 4;                                  // W row pitch (floats)
   static constexpr int XB = BM * XLd * static_cast<int>(sizeof(XT));  // bytes of one x chunk
-  static constexpr int WB = BN * kTLd * 4;                            // bytes of one W chunk
+  static constexpr int WB = BN * WLd * 4;                             // bytes of one W chunk
   static constexpr int WARP_BYTES = NST * (XB + WB);                  // one warp's ring
   static_assert(BM * BN * 4 <= WARP_BYTES, "a warp's partials must fit in its ring");
 };
@@ -646,15 +647,15 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   return v;
 }
 
-template <int TM, int TN, int NST, int L, typename XT>
+template <int TM, int TN, int NST, int L, typename XT, int CK>
 __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restrict__ x,
                                                               const float *__restrict__ w,
                                                               const float *__restrict__ bias,
                                                               float *__restrict__ y, int M, int K,
                                                               int N) {
-  using Cf = SplitCfg<TM, TN, NST, XT>;
-  constexpr int BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd;
-  constexpr int kChunks = kSlice / kTBK;
+  using Cf = SplitCfg<TM, TN, NST, XT, CK>;
+  constexpr int BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd, WLd = Cf::WLd;
+  constexpr int kChunks = kSlice / CK;
   extern __shared__ __align__(16) uint8_t sp_smem[];
 
   griddep_wait();
@@ -665,13 +666,13 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
   const int s = rank * L + warp;  // this warp's slice
   uint8_t *mine = sp_smem + warp * Cf::WARP_BYTES;
   XT *xr = reinterpret_cast<XT *>(mine);                   // [NST][BM][XLd]
-  float *wr = reinterpret_cast<float *>(mine + NST * Cf::XB);  // [NST][BN][kTLd]
+  float *wr = reinterpret_cast<float *>(mine + NST * Cf::XB);  // [NST][BN][WLd]
 
-  // chunk q (k = 128 s + 32 q ...) of the warp's x rows and W rows into stage st
+  // chunk q (k = 128 s + CK q ...) of the warp's x rows and W rows into stage st
   auto load = [&](int q, int st) {
-    const int k0 = s * kSlice + q * kTBK;
+    const int k0 = s * kSlice + q * CK;
     constexpr int XE = 16 / static_cast<int>(sizeof(XT));  // x elements per piece
-    constexpr int XPC = kTBK / XE, WPC = kTBK / 4;         // pieces per row
+    constexpr int XPC = CK / XE, WPC = CK / 4;             // pieces per row
     static_assert((BM * XPC) % 32 == 0 && (BN * WPC) % 32 == 0, "whole warps of pieces");
 #pragma unroll
     for (int t = 0; t < BM * XPC / 32; ++t) {
@@ -684,7 +685,7 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
     for (int t = 0; t < BN * WPC / 32; ++t) {
       const int i = lane + 32 * t, row = i / WPC, pc = i % WPC;
       const int gn = min(n0 + row, N - 1);
-      cp_async16(smem_u32(wr + (st * BN + row) * kTLd + pc * 4),
+      cp_async16(smem_u32(wr + (st * BN + row) * WLd + pc * 4),
                  w + static_cast<size_t>(gn) * K + k0 + pc * 4);
     }
   };
@@ -708,15 +709,15 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
     if (q + NST - 1 < kChunks) load(q + NST - 1, (q + NST - 1) % NST);
     cp_async_commit();
     const XT *xb = xr + (q % NST) * BM * XLd;
-    const float *wb = wr + (q % NST) * BN * kTLd;
+    const float *wb = wr + (q % NST) * BN * WLd;
 #pragma unroll
-    for (int kk = 0; kk < kTBK; kk += 4) {
+    for (int kk = 0; kk < CK; kk += 4) {
       float4 xv[TM], wv[TN];
 #pragma unroll
       for (int i = 0; i < TM; ++i) xv[i] = ld_x4(xb + (a + kSpLM * i) * XLd + kk);
 #pragma unroll
       for (int j = 0; j < TN; ++j)
-        wv[j] = *reinterpret_cast<const float4 *>(wb + (b + kSpLN * j) * kTLd + kk);
+        wv[j] = *reinterpret_cast<const float4 *>(wb + (b + kSpLN * j) * WLd + kk);
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -770,17 +771,17 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
   cluster_sync_all();  // no CTA leaves while a peer still reads its partials
 }
 
-template <int TM, int TN, int NST, int L, typename XT>
+template <int TM, int TN, int NST, int CK, int L, typename XT>
 static bi_status launch_split_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, cudaStream_t stream) {
-  using Cf = SplitCfg<TM, TN, NST, XT>;
+  using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   const int C = static_cast<int>(K / kSlice) / L;
   const size_t smem = static_cast<size_t>(L) * Cf::WARP_BYTES;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT>,
+    if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT, CK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -791,13 +792,15 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   }
   dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
             static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
-  return launch_chained(router_split_kernel<TM, TN, NST, L, XT>, grid, dim3(32 * L), smem, stream, C,
+  return launch_chained(router_split_kernel<TM, TN, NST, L, XT, CK>, grid, dim3(32 * L), smem, stream, C,
                         x, w, b, y, (int)M, (int)K, (int)N);
 }
 
-// Lane tiles of the split schedule (outputs per thread TM x TN, ring depth).
-struct SplitTile { int tm, tn, nst; };
-constexpr SplitTile kSplitTiles[] = {{2, 2, 4}, {4, 2, 4}, {4, 4, 3}, {8, 4, 2}};
+// Lane tiles of the split schedule (outputs per thread TM x TN, ring depth,
+// k per chunk).  The 8x4 tile streams 16-k chunks: 40 KB per CTA instead of
+// 74, so four of its CTAs share an SM (register-limited) instead of three.
+struct SplitTile { int tm, tn, nst, ck; };
+constexpr SplitTile kSplitTiles[] = {{2, 2, 4, 32}, {4, 2, 4, 32}, {4, 4, 3, 32}, {8, 4, 2, 16}};
 constexpr int kNumSplitTiles = 4;
 
 // Warps per CTA for the split schedule (slices per CTA), 0 if the slice count
@@ -827,10 +830,10 @@ template <int L, typename XT>
 static bi_status launch_split_l(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, int tile, cudaStream_t stream) {
   switch (tile) {
-    case 0: return launch_split_t<2, 2, 4, L, XT>(x, w, b, y, M, K, N, stream);
-    case 1: return launch_split_t<4, 2, 4, L, XT>(x, w, b, y, M, K, N, stream);
-    case 2: return launch_split_t<4, 4, 3, L, XT>(x, w, b, y, M, K, N, stream);
-    default: return launch_split_t<8, 4, 2, L, XT>(x, w, b, y, M, K, N, stream);
+    case 0: return launch_split_t<2, 2, 4, 32, L, XT>(x, w, b, y, M, K, N, stream);
+    case 1: return launch_split_t<4, 2, 4, 32, L, XT>(x, w, b, y, M, K, N, stream);
+    case 2: return launch_split_t<4, 4, 3, 32, L, XT>(x, w, b, y, M, K, N, stream);
+    default: return launch_split_t<8, 4, 2, 16, L, XT>(x, w, b, y, M, K, N, stream);
   }
 }
 
