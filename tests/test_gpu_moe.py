@@ -240,10 +240,12 @@ def test_forward_parity_qwen(oracle_mod, cuda, qwen_w, M, unit):
 
 
 def test_forward_skewed_and_small_shapes(oracle_mod, cuda):
-    """Load skew (four hot experts, most experts empty), top_k=1, E=1."""
+    """Load skew (four hot experts, most experts empty), top_k=1, E=1, and
+    the largest expert count and top_k the call accepts (E=1024, top_k=16)."""
     import invariant_moe_gb300 as bm
     for (M, H, E, I, k, kind) in ((333, 256, 32, 128, 8, "skew"), (50, 128, 1, 128, 1, "rand"),
-                                  (129, 384, 6, 256, 2, "rand")):
+                                  (129, 384, 6, 256, 2, "rand"),
+                                  (64, 256, 1024, 128, 16, "rand")):  # the largest E and top_k
         w = syn.moe_weights(H, E, I, seed=M, unit=True)
         x = syn.moe_tokens(M, H, seed=M + 1, unit=True)
         f = syn.random_routing if kind == "rand" else syn.skewed_routing

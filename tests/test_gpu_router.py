@@ -142,6 +142,29 @@ def test_no_bias_and_other_shapes(oracle_mod, cuda):
             assert torch.equal(ys[0], yy), f"M={M} K={K} N={N}: schedule {s}"
 
 
+def test_largest_shapes(oracle_mod, cuda):
+    """The largest K (32768: 256 slices, no cluster split, so rows / sliced /
+    tiled) and the largest N (4096) the call accepts: parity with the oracle
+    and the same bits under every schedule that takes the shape."""
+    import invariant_moe_gb300 as bm
+    for (M, K, N) in ((5, 32768, 256), (7, 4096, 4096)):
+        x = syn.normal((M, K), 1.0, 31)
+        w = syn.normal((N, K), K ** -0.5, 32)
+        b = syn.normal((N,), 0.01, 33)
+        xd, wd, bd = x.to(cuda), w.to(cuda), b.to(cuda)
+        y = run(xd, wd, bd, M).cpu().numpy()
+        check_parity(y, oracle_mod.router(x.numpy(), w.numpy(), b.numpy()))
+        ys = {}
+        for s in ALL_SCHEDULES:
+            try:
+                ys[s] = run(xd, wd, bd, M, schedule=s)
+            except RuntimeError as e:  # schedules that do not take this K report it
+                assert "BI_ERR_UNSUPPORTED" in str(e) and s in (4, 5, 6, 7, 8), (s, e)
+        assert set(ys) >= {1, 2, 3, 9}
+        for s, yy in ys.items():
+            assert torch.equal(ys[1], yy), f"M={M} K={K} N={N}: schedule {s}"
+
+
 def test_full_size_sampled_parity(oracle_mod, inputs, dev_inputs):
     """M=4096 (the largest batch) on sampled rows the oracle can afford."""
     x, w, b = dev_inputs
