@@ -47,8 +47,8 @@ constexpr int kSlicePad = kSlice + 4;
 // same per-element sequence.  Shared-memory row pitches (elements) keep every
 // row 16-byte aligned for the bulk / cp.async copies.
 template <typename XT> struct XPitch;
-template <> struct XPitch<float> { static constexpr int slice = kSlicePad, round = 8 * kSlice + 4, chunk = 36; };
-template <> struct XPitch<__nv_bfloat16> { static constexpr int slice = kSlice + 8, round = 8 * kSlice + 8, chunk = 40; };
+template <> struct XPitch<float> { static constexpr int slice = kSlicePad, round = 8 * kSlice + 4; };
+template <> struct XPitch<__nv_bfloat16> { static constexpr int slice = kSlice + 8, round = 8 * kSlice + 8; };
 
 // Four consecutive x values from shared memory, as fp32.
 __device__ __forceinline__ float4 ld_x4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
