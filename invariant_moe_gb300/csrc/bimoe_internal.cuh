@@ -39,9 +39,10 @@ void set_error(const char *fmt, ...);
 // stream (programmatic stream serialization) and, for cluster_x > 1, in
 // clusters of cluster_x CTAs.  Every kernel of this library begins with
 // griddep_wait(), so its launch overlaps the end of its predecessor while
-// every memory access still follows it.  The kernels do not trigger their
-// dependents early (the trigger is each CTA's exit): CTAs of a dependent
-// grid parked on the SMs while a long kernel runs were measured to slow it.
+// every memory access still follows it.  Only the short kernels with small
+// grids (griddep_wait_small_release) trigger their dependents early; for the
+// rest the trigger is each CTA's exit: CTAs of a dependent grid parked on the
+// SMs while a large grid runs were measured to slow it.
 template <typename... KArgs, typename... Args>
 bi_status launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                          cudaStream_t stream, int cluster_x, Args... args) {
@@ -95,6 +96,16 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// For the short kernels of the path: wait for the predecessor and, when this
+// grid is small (a decode-sized batch: at most 64 CTAs, most SMs idle), let
+// the successor grid launch at once; its CTAs park at their own
+// griddep_wait until this grid has finished, and a GEMM successor sets up its
+// barriers and tensor memory meanwhile.  Larger grids leave the trigger to
+// CTA exit (parked successor CTAs were measured to slow them).
+__device__ __forceinline__ void griddep_wait_small_release() {
+  griddep_wait();
+  if (gridDim.x * gridDim.y * gridDim.z <= 64u) griddep_launch_dependents();
+}
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;

@@ -154,7 +154,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
-  griddep_wait();  // the offsets, permutation and operands come from earlier kernels
   constexpr int kBN = C::kBN;
   constexpr int kStages = C::kStages;
   constexpr int kStageBytes = C::kStageBytes;
@@ -200,14 +199,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // the expert offsets in shared memory: one global round trip for all
-  // threads instead of a chain of dependent loads in the tile scan below
-  for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  __syncthreads();
   if (warp == 1) {
     if (PAIR) {
       if (lane == 0) *tmem_slot = 0u;
@@ -219,6 +214,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tmem_relinquish();
     }
   }
+  // Nothing above reads what earlier kernels write (the tensor maps are
+  // parameters), so it overlaps their end; from here on the offsets,
+  // permutation and operands are read.  (Tensor memory is never held by a
+  // predecessor on the same SM: only these GEMM kernels allocate it and their
+  // CTAs need most of an SM's shared memory.)
+  griddep_wait();
+  // the expert offsets in shared memory: one global round trip for all
+  // threads instead of a chain of dependent loads in the tile scan below
+  for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
+  __syncthreads();
   if (warp == 2) {
     // tile_prefix[e] = tiles of experts < e; each lane scans a contiguous chunk
     const int per = (prm.E + 31) / 32;

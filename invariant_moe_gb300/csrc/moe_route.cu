@@ -163,7 +163,7 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *s_warp, int *tota
 __global__ void __launch_bounds__(kSmallPermuteMaxM) moe_permute_small_kernel(
     const int32_t *__restrict__ ids, int M, int E, int top_k, int32_t *__restrict__ offsets,
     int32_t *__restrict__ perm, int *err) {
-  griddep_wait();
+  griddep_wait_small_release();
   extern __shared__ int s_pm[];
   __shared__ int s_warp[32];
   // bit rows padded to an odd pitch: lanes reading word w of different
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
                                                          const int32_t *__restrict__ offsets,
                                                          int E, int top_k, int row_vec,
                                                          uint4 *__restrict__ xp) {
-  griddep_wait();
+  griddep_wait_small_release();
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= offsets[E]) return;
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
                                                           __nv_bfloat16 *__restrict__ out, int M,
                                                           int H4, int top_k) {
-  griddep_wait();
+  griddep_wait_small_release();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(M) * H4) return;
   const int64_t m = idx / H4;

@@ -10,7 +10,7 @@ __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ sco
                                                    float *__restrict__ wts,
                                                    float *__restrict__ probs, int M, int E,
                                                    int top_k) {
-  griddep_wait();
+  griddep_wait_small_release();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= M) return;  // whole warp leaves together
