@@ -13,14 +13,16 @@
 // One CTA of 512 threads per row, up to 8192 columns: thread t holds columns
 // t, t+512, ... (coalesced loads) as unsigned keys (the int32 key with its sign
 // bit flipped, so unsigned order is key order).  The exact k-th largest key T
-// is found by a 4-pass radix select, 8 bits per pass, on a shared-memory
-// histogram, one atomic per key.  (Aggregating a warp's equal digits first
-// with match.any, or a shuffle-and-vote plateau test, puts a dependent
-// instruction in front of every atomic and cost more than the same-bin
-// conflicts it saves: 13.2 and 12.0 us per row on GB300 against 9.0 us, and a
-// row whose scores are all equal, every key in one bin, takes 9.4 us.)  Then one pass in column order: a chosen column's output slot is
-// (keys > T before it) + min(ties before it, budget), from warp ballots and a
-// block scan.  Everything is integer counting: the result is a pure function
+// is found by a 3-pass radix select on digits of 11, 11 and 10 bits, on a
+// 2048-bin shared-memory histogram, one atomic per key; each thread owns a
+// quad of bins for the descending scan, and the next pass's clear rides on
+// the scan's own barrier, so a pass costs three barriers.  (Aggregating a
+// warp's equal digits first with match.any, or a shuffle-and-vote plateau
+// test, puts a dependent instruction in front of every atomic and cost more
+// than the same-bin conflicts it saves.)  Then one pass in column order: a
+// chosen column's output slot is (keys > T before it) + min(ties before it,
+// budget), from warp ballots and one block scan of both counts packed in a
+// word.  Everything is integer counting: the result is a pure function
 // of the row.
 #include "bimoe_internal.cuh"
 
@@ -30,6 +32,8 @@ constexpr int kTwThreads = 512;
 constexpr int kTwWarps = kTwThreads / 32;
 constexpr int kTwMaxCols = 8192;
 constexpr int kTwVT = kTwMaxCols / kTwThreads;  // columns per thread
+constexpr int kTwBins = 2048;                  // 11-bit digits
+static_assert(kTwThreads * 4 == kTwBins, "one bin quad per thread");
 
 __device__ __forceinline__ uint32_t tw_ukey(float v) {
   uint32_t u = __float_as_uint(v);
@@ -43,9 +47,10 @@ __device__ __forceinline__ int64_t tw_clamp(int64_t v, int64_t lo, int64_t hi) {
 }
 
 // Exclusive prefix sum of one value per thread over the whole CTA (thread
-// order).  Every thread must call it; scratch holds kTwWarps words.
-__device__ __forceinline__ uint32_t tw_block_excl_scan(uint32_t v, uint32_t *scratch,
-                                                       uint32_t *total) {
+// order).  Every thread must call it; scratch holds kTwWarps words.  There is
+// one barrier inside and none at the end: the caller puts a barrier between
+// this call's return and the next write of scratch.
+__device__ __forceinline__ uint32_t tw_block_excl_scan(uint32_t v, uint32_t *scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -55,25 +60,21 @@ __device__ __forceinline__ uint32_t tw_block_excl_scan(uint32_t v, uint32_t *scr
   }
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
-  uint32_t base = 0, all = 0;
+  uint32_t base = 0;
 #pragma unroll
-  for (int w = 0; w < kTwWarps; ++w) {
-    const uint32_t s = scratch[w];
-    if (w < warp) base += s;
-    all += s;
-  }
-  __syncthreads();  // scratch is reused by the next call
-  if (total) *total = all;
+  for (int w = 0; w < kTwWarps; ++w)
+    if (w < warp) base += scratch[w];
   return base + incl - v;
 }
 
 __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
     const float *__restrict__ scores, int64_t ld, const int64_t *__restrict__ row_start,
     const int64_t *__restrict__ row_end, int num_cols, int k, int32_t *__restrict__ out) {
-  __shared__ uint32_t hist[256];
+  __shared__ __align__(16) uint32_t hist[kTwBins];
   __shared__ uint32_t scratch[kTwWarps];
   __shared__ uint32_t s_digit, s_kk;
-  __shared__ uint32_t pre_gt[kTwVT * kTwWarps], pre_tie[kTwVT * kTwWarps];
+  // per (column block, warp): keys above T in the low half, ties in the high
+  __shared__ uint32_t pre[kTwVT * kTwWarps];
 
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -90,6 +91,9 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
     return;
   }
 
+  uint4 *hist4 = reinterpret_cast<uint4 *>(hist);
+  hist4[tid] = make_uint4(0u, 0u, 0u, 0u);  // kTwThreads * 4 == kTwBins
+
   uint32_t key[kTwVT];
   uint32_t valid = 0;  // bit j: column j*512 + tid is in the window
 #pragma unroll
@@ -101,34 +105,49 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
       valid |= 1u << j;
     }
   }
+  __syncthreads();
 
-  // ---- radix select: T = the k-th largest key, kk = how many of the keys
-  // equal to T are chosen (the tie budget)
+  // ---- radix select over digits of 11, 11 and 10 bits: T = the k-th largest
+  // key, kk = how many of the keys equal to T are chosen (the tie budget)
   uint32_t prefix = 0u, pmask = 0u, kk = static_cast<uint32_t>(k);
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0u;
-    __syncthreads();
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+    const int nq = static_cast<int>(dmask + 1u) / 4;  // bin quads in use
 #pragma unroll
     for (int j = 0; j < kTwVT; ++j) {
       const bool in = ((valid >> j) & 1u) && (key[j] & pmask) == prefix;
       // one atomic per key, results unused, so the 16 of a pass issue back
       // to back (lanes of a warp hitting one bin are merged by the shared
       // memory atomic unit)
-      if (in) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
+      if (in) atomicAdd(&hist[(key[j] >> shift) & dmask], 1u);
     }
     __syncthreads();
-    // thread t < 256 holds bin 255 - t: bins in descending digit order
-    const uint32_t v = tid < 256 ? hist[255 - tid] : 0u;
-    const uint32_t excl = tw_block_excl_scan(v, scratch, nullptr);
-    if (tid < 256 && excl < kk && excl + v >= kk) {
-      s_digit = 255u - static_cast<uint32_t>(tid);
-      s_kk = kk - excl;
+    // thread t < nq holds the quad of bins 4(nq-1-t) .. 4(nq-1-t)+3, so the
+    // threads walk the bins in descending digit order
+    const uint4 q = tid < nq ? hist4[nq - 1 - tid] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t sum = q.x + q.y + q.z + q.w;
+    const uint32_t excl = tw_block_excl_scan(sum, scratch);
+    // every thread has read its quad (the scan's barrier): clear for the next
+    // pass
+    if (pass < 2) hist4[tid] = make_uint4(0u, 0u, 0u, 0u);
+    if (excl < kk && excl + sum >= kk) {
+      const uint32_t top = 4u * static_cast<uint32_t>(nq - 1 - tid) + 3u;
+      const uint32_t v[4] = {q.w, q.z, q.y, q.x};
+      uint32_t c = excl;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (c < kk && c + v[i] >= kk) {
+          s_digit = top - static_cast<uint32_t>(i);
+          s_kk = kk - c;
+        }
+        c += v[i];
+      }
     }
     __syncthreads();
     prefix |= s_digit << shift;
-    pmask |= 255u << shift;
+    pmask |= dmask << shift;
     kk = s_kk;
   }
   const uint32_t T = prefix, budget = kk;
@@ -140,21 +159,15 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
     const bool v_ = (valid >> j) & 1u;
     const uint32_t bg = __ballot_sync(0xffffffffu, v_ && key[j] > T);
     const uint32_t bt = __ballot_sync(0xffffffffu, v_ && key[j] == T);
-    if (lane == 0) {
-      pre_gt[j * kTwWarps + warp] = __popc(bg);
-      pre_tie[j * kTwWarps + warp] = __popc(bt);
-    }
+    if (lane == 0) pre[j * kTwWarps + warp] = __popc(bg) | (__popc(bt) << 16);
   }
   __syncthreads();
-  // exclusive prefixes of the kTwVT * kTwWarps = 256 (block, warp) counts
-  const uint32_t cg = tid < kTwVT * kTwWarps ? pre_gt[tid] : 0u;
-  const uint32_t ct = tid < kTwVT * kTwWarps ? pre_tie[tid] : 0u;
-  const uint32_t eg = tw_block_excl_scan(cg, scratch, nullptr);
-  const uint32_t et = tw_block_excl_scan(ct, scratch, nullptr);
-  if (tid < kTwVT * kTwWarps) {
-    pre_gt[tid] = eg;
-    pre_tie[tid] = et;
-  }
+  // exclusive prefixes of the kTwVT * kTwWarps = 256 (block, warp) counts,
+  // both halves in one scan: each half's total is at most 8192, so the low
+  // half never carries into the high one
+  const uint32_t cnt = tid < kTwVT * kTwWarps ? pre[tid] : 0u;
+  const uint32_t ex = tw_block_excl_scan(cnt, scratch);
+  if (tid < kTwVT * kTwWarps) pre[tid] = ex;
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < kTwVT; ++j) {
@@ -162,8 +175,9 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
     const bool gt = v_ && key[j] > T, tie = v_ && key[j] == T;
     const uint32_t bg = __ballot_sync(0xffffffffu, gt);
     const uint32_t bt = __ballot_sync(0xffffffffu, tie);
-    const uint32_t gb = pre_gt[j * kTwWarps + warp] + __popc(bg & lt);
-    const uint32_t tb = pre_tie[j * kTwWarps + warp] + __popc(bt & lt);
+    const uint32_t pw = pre[j * kTwWarps + warp];
+    const uint32_t gb = (pw & 0xffffu) + __popc(bg & lt);
+    const uint32_t tb = (pw >> 16) + __popc(bt & lt);
     if (gt || (tie && tb < budget)) {
       const uint32_t pos = gb + min(tb, budget);
       orow[pos] = j * kTwThreads + tid - static_cast<int>(rs);
