@@ -35,8 +35,8 @@ constexpr int kTwVT = kTwMaxCols / kTwThreads;  // columns per thread
 constexpr int kTwBins = 2048;                  // 11-bit digits
 static_assert(kTwThreads * 4 == kTwBins, "one bin quad per thread");
 
-__device__ __forceinline__ uint32_t tw_ukey(float v) {
-  uint32_t u = __float_as_uint(v);
+// the score's bits, read as an integer so that no float operation touches them
+__device__ __forceinline__ uint32_t tw_ukey(uint32_t u) {
   if (u == 0x80000000u) u = 0u;           // -0.0 ranks as +0.0
   if (u & 0x80000000u) u ^= 0x7fffffffu;  // the monotone int32 key ...
   return u ^ 0x80000000u;                 // ... in unsigned order
@@ -60,10 +60,16 @@ __device__ __forceinline__ uint32_t tw_block_excl_scan(uint32_t v, uint32_t *scr
   }
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
-  uint32_t base = 0;
+  // prefix over the warp totals: lane w < kTwWarps scans total w, and warp w
+  // takes the exclusive prefix held by its lane w
+  const uint32_t wt = lane < kTwWarps ? scratch[lane] : 0u;
+  uint32_t wincl = wt;
 #pragma unroll
-  for (int w = 0; w < kTwWarps; ++w)
-    if (w < warp) base += scratch[w];
+  for (int off = 1; off < kTwWarps; off <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, wincl, off);
+    if (lane >= off) wincl += o;
+  }
+  const uint32_t base = __shfl_sync(0xffffffffu, wincl - wt, warp);
   return base + incl - v;
 }
 
@@ -79,10 +85,21 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
-  const int64_t rs = row_start ? tw_clamp(row_start[row], 0, num_cols) : 0;
-  const int64_t re = row_end ? tw_clamp(row_end[row], 0, num_cols) : num_cols;
+  // the row bounds and the scores are loaded together: every column below
+  // num_cols is readable whatever the window, so the score loads do not wait
+  // for the bounds
+  const int64_t rs_in = row_start ? row_start[row] : 0;
+  const int64_t re_in = row_end ? row_end[row] : num_cols;
+  const uint32_t *srow = reinterpret_cast<const uint32_t *>(scores + row * ld);
+  uint32_t sv[kTwVT];
+#pragma unroll
+  for (int j = 0; j < kTwVT; ++j) {
+    const int c = j * kTwThreads + tid;
+    sv[j] = c < num_cols ? srow[c] : 0u;
+  }
+  const int64_t rs = tw_clamp(rs_in, 0, num_cols);
+  const int64_t re = tw_clamp(re_in, 0, num_cols);
   const int nvalid = re > rs ? static_cast<int>(re - rs) : 0;
-  const float *srow = scores + row * ld;
   int32_t *orow = out + row * static_cast<int64_t>(k);
 
   if (nvalid <= k) {
@@ -101,7 +118,7 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
     const int c = j * kTwThreads + tid;
     key[j] = 0u;
     if (c >= rs && c < re) {
-      key[j] = tw_ukey(srow[c]);
+      key[j] = tw_ukey(sv[j]);
       valid |= 1u << j;
     }
   }
@@ -154,12 +171,13 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
 
   // ---- emission in column order (block j, then warp, then lane)
   const uint32_t lt = (1u << lane) - 1u;
+  uint32_t bgt[kTwVT], btie[kTwVT];  // warp ballots of "key > T" and "key == T"
 #pragma unroll
   for (int j = 0; j < kTwVT; ++j) {
     const bool v_ = (valid >> j) & 1u;
-    const uint32_t bg = __ballot_sync(0xffffffffu, v_ && key[j] > T);
-    const uint32_t bt = __ballot_sync(0xffffffffu, v_ && key[j] == T);
-    if (lane == 0) pre[j * kTwWarps + warp] = __popc(bg) | (__popc(bt) << 16);
+    bgt[j] = __ballot_sync(0xffffffffu, v_ && key[j] > T);
+    btie[j] = __ballot_sync(0xffffffffu, v_ && key[j] == T);
+    if (lane == 0) pre[j * kTwWarps + warp] = __popc(bgt[j]) | (__popc(btie[j]) << 16);
   }
   __syncthreads();
   // exclusive prefixes of the kTwVT * kTwWarps = 256 (block, warp) counts,
@@ -171,13 +189,10 @@ __global__ void __launch_bounds__(kTwThreads) topk_window_kernel(
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < kTwVT; ++j) {
-    const bool v_ = (valid >> j) & 1u;
-    const bool gt = v_ && key[j] > T, tie = v_ && key[j] == T;
-    const uint32_t bg = __ballot_sync(0xffffffffu, gt);
-    const uint32_t bt = __ballot_sync(0xffffffffu, tie);
+    const bool gt = (bgt[j] >> lane) & 1u, tie = (btie[j] >> lane) & 1u;
     const uint32_t pw = pre[j * kTwWarps + warp];
-    const uint32_t gb = (pw & 0xffffu) + __popc(bg & lt);
-    const uint32_t tb = (pw >> 16) + __popc(bt & lt);
+    const uint32_t gb = (pw & 0xffffu) + __popc(bgt[j] & lt);
+    const uint32_t tb = (pw >> 16) + __popc(btie[j] & lt);
     if (gt || (tie && tb < budget)) {
       const uint32_t pos = gb + min(tb, budget);
       orow[pos] = j * kTwThreads + tid - static_cast<int>(rs);
