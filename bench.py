@@ -253,7 +253,7 @@ def run_ours(args, rank, world, local):
             e2.record(stream)
             ev["gate_up"].append((e0, e1))
             ev["down"].append((e1, e2))
-        bm.bi_moe_combine(contrib, M, k, out=out)
+        bm.bi_moe_combine_consume(contrib, M, k, out=out)
 
     # router + top-k (2), permute (1 up to 1024 tokens, else 3; both bench
     # workloads fit the one-CTA permutation's shared memory), gather, gate/up,

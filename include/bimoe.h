@@ -349,6 +349,20 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
                                 int64_t H, int32_t top_k, bi_stream_t stream);
 
 /*
+ * bi_moe_combine_consume -- bi_moe_combine (same arguments, checks and
+ * result bits) for a caller that never reads contrib again: once a line of
+ * contrib has been summed it is dropped from L2 without being written back
+ * to memory (discard.global.L2), so contributions still cached when the
+ * combine runs cost no DRAM write.  contrib's contents are indeterminate
+ * afterwards.  The drop applies when H is a multiple of 32 and contrib is
+ * 128-byte aligned (each 128-byte line then belongs to one (token, slot)
+ * row); otherwise the call is exactly bi_moe_combine.  bi_moe_forward
+ * combines this way into its own workspace.
+ */
+BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M,
+                                        int64_t H, int32_t top_k, bi_stream_t stream);
+
+/*
  * bi_moe_gemm_variant -- selects how the expert GEMMs (bi_moe_gate_up,
  * bi_moe_down and the two GEMMs inside bi_moe_forward) are scheduled, for
  * the whole process, from the next call on:

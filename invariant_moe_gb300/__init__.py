@@ -33,7 +33,7 @@ EXPORTS = [
     "bi_cast_bf16_to_f32", "bi_router_gemm", "bi_router_gemm_schedule",
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
-    "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_forward_noalloc",
+    "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_combine_consume", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
 ]
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_gate_up": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_down": ([P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
+            "bi_moe_combine_consume": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_gemm_variant": ([I32, P], ST),
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
@@ -298,6 +299,18 @@ def bi_moe_combine(contrib, M, top_k, out=None, stream=None):
     out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     _call("bi_moe_combine", _ptr(contrib, torch.float32, "contrib"), _ptr(out, torch.bfloat16, "out", dev),
           M, H, top_k, _stream(stream))
+    return out
+
+
+def bi_moe_combine_consume(contrib, M, top_k, out=None, stream=None):
+    """bi_moe_combine for a caller that never reads ``contrib`` again: its
+    lines are dropped from L2 once summed, and its contents are indeterminate
+    afterwards."""
+    H = contrib.shape[-1]
+    dev = contrib.device
+    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_combine_consume", _ptr(contrib, torch.float32, "contrib"),
+          _ptr(out, torch.bfloat16, "out", dev), M, H, top_k, _stream(stream))
     return out
 
 

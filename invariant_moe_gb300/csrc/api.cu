@@ -26,7 +26,7 @@ bi_status launch_permute(const int32_t *, int32_t *, int32_t *, int64_t, int64_t
                          cudaStream_t);
 bi_status launch_gather(const void *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
                         int32_t, void *, cudaStream_t);
-bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, cudaStream_t);
+bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, bool, cudaStream_t);
 bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const float *,
                          const void *, void *, int64_t, int64_t, int64_t, int32_t, int64_t,
                          cudaStream_t);
@@ -450,7 +450,18 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M, i
   BI_REQUIRE(contrib && out, BI_ERR_INVALID_ARG, "null pointer");
   BI_REQUIRE(aligned(contrib, 16) && aligned(out, 8), BI_ERR_INVALID_ARG,
              "contrib must be 16-byte and out 8-byte aligned");
-  return launch_combine(contrib, out, M, H, top_k, reinterpret_cast<cudaStream_t>(stream));
+  return launch_combine(contrib, out, M, H, top_k, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M, int64_t H,
+                                        int32_t top_k, bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && H > 0 && H % 4 == 0, BI_ERR_INVALID_ARG, "bad sizes (H %% 4 == 0 needed)");
+  BI_REQUIRE(top_k >= 1 && top_k <= 16, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(contrib && out, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(contrib, 16) && aligned(out, 8), BI_ERR_INVALID_ARG,
+             "contrib must be 16-byte and out 8-byte aligned");
+  return launch_combine(contrib, out, M, H, top_k, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const float *wts,
@@ -480,7 +491,7 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
   if ((st = launch_gate_up(xperm, offsets, perm, wts, w13, act, P, H, E, top_k, I, s)) != BI_OK)
     return st;
   if ((st = launch_down(act, offsets, perm, w2, contrib, P, H, E, top_k, I, s)) != BI_OK) return st;
-  return launch_combine(contrib, out, M, H, top_k, s);
+  return launch_combine(contrib, out, M, H, top_k, true, s);
 }
 
 }  // extern "C"

@@ -107,6 +107,13 @@ __device__ __forceinline__ void griddep_wait_small_release() {
   if (gridDim.x * gridDim.y * gridDim.z <= 64u) griddep_launch_dependents();
 }
 
+// ---- L2
+// Drops the 128-byte line at p (128-byte aligned) from L2 without writing it
+// back: its contents become indeterminate.  Only for data nothing reads again.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

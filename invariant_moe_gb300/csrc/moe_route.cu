@@ -229,29 +229,41 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
 
 // out[m, h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) + c[m,k-1,h]), fp32 adds in
 // slot order; four consecutive h per thread.
+template <bool CONSUME>
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
                                                           __nv_bfloat16 *__restrict__ out, int M,
                                                           int H4, int top_k) {
   griddep_wait_small_release();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(M) * H4) return;
-  const int64_t m = idx / H4;
+  const bool active = idx < static_cast<int64_t>(M) * H4;
+  const int64_t m = active ? idx / H4 : 0;
   const int h4 = static_cast<int>(idx % H4);
   const float4 *c = contrib + m * top_k * H4 + h4;
-  float4 s = c[0];
-  for (int t = 1; t < top_k; ++t) {
-    const float4 v = c[static_cast<int64_t>(t) * H4];
-    s.x = __fadd_rn(s.x, v.x);
-    s.y = __fadd_rn(s.y, v.y);
-    s.z = __fadd_rn(s.z, v.z);
-    s.w = __fadd_rn(s.w, v.w);
+  if (active) {
+    float4 s = c[0];
+    for (int t = 1; t < top_k; ++t) {
+      const float4 v = c[static_cast<int64_t>(t) * H4];
+      s.x = __fadd_rn(s.x, v.x);
+      s.y = __fadd_rn(s.y, v.y);
+      s.z = __fadd_rn(s.z, v.z);
+      s.w = __fadd_rn(s.w, v.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(s.z, s.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(out + idx * 4) = pk;
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(s.z, s.w);
-  uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t *>(&lo);
-  pk.y = *reinterpret_cast<uint32_t *>(&hi);
-  *reinterpret_cast<uint2 *>(out + idx * 4) = pk;
+  if (CONSUME) {
+    // every contribution line has been read (by the eight lanes that share
+    // it, all in this warp): drop it from L2 without a write-back.  The host
+    // takes this path only when H is a multiple of 32 and contrib is 128-byte
+    // aligned, so lines never straddle two rows.
+    __syncwarp();
+    if (active && (h4 & 7) == 0)
+      for (int t = 0; t < top_k; ++t) discard_l2_line(c + static_cast<int64_t>(t) * H4);
+  }
 }
 
 // ------------------------------------------------------------------- host --
@@ -296,10 +308,14 @@ bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offse
 }
 
 bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, int32_t top_k,
-                         cudaStream_t stream) {
+                         bool consume, cudaStream_t stream) {
   const int64_t total = M * (H / 4);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
-  return launch_chained(moe_combine_kernel, dim3(blocks), dim3(256), 0, stream, 1,
+  if (consume && H % 32 == 0 && reinterpret_cast<uintptr_t>(contrib) % 128 == 0)
+    return launch_chained(moe_combine_kernel<true>, dim3(blocks), dim3(256), 0, stream, 1,
+                          reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
+                          (int)M, (int)(H / 4), top_k);
+  return launch_chained(moe_combine_kernel<false>, dim3(blocks), dim3(256), 0, stream, 1,
                         reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
                         (int)M, (int)(H / 4), top_k);
 }

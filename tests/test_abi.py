@@ -122,6 +122,9 @@ def test_host_side_rejections(lib):
     assert lib.bi_moe_forward(nul, nul, nul, nul, nul, nul, 0, 2048, 128, 8, 768,
                               nul, 0, nul) == 0
     assert lib.bi_moe_combine(fake, fake, 4, 2046, 8, nul) == 1
+    assert lib.bi_moe_combine_consume(fake, fake, 4, 2046, 8, nul) == 1
+    assert lib.bi_moe_combine_consume(fake, fake, 4, 2048, 17, nul) == 1
+    assert lib.bi_moe_combine_consume(nul, nul, 0, 2048, 8, nul) == 0
 
 
 def test_binding_rejects_cpu_tensors():

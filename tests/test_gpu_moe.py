@@ -144,6 +144,26 @@ def test_combine_stage(oracle_mod, cuda):
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * rms(ref))
 
 
+@pytest.mark.parametrize("M,H,offset", [(513, 2048, 0), (7, 4096, 0), (33, 2048, 4), (5, 1000, 0)])
+def test_combine_consume_same_bits(cuda, M, H, offset):
+    """The consuming combine (contribution lines dropped from L2 once summed)
+    gives the plain combine's bits: line-aligned rows (H % 32 == 0, aligned
+    base) take the dropping path, a base 16 bytes off a line or H = 1000 the
+    plain one."""
+    import invariant_moe_gb300 as bm
+    k = 8
+    c = syn.normal((M * k * H + offset,), 1.0, 56).to(cuda)
+    want = bm.bi_moe_combine(c[offset:].view(M * k, H), M, k)
+    buf = c.clone()  # same offset from an aligned allocation as c
+    got = bm.bi_moe_combine_consume(buf[offset:].view(M * k, H), M, k)
+    # the buffer rewritten and consumed again, as a layer loop does with its
+    # workspace
+    buf.copy_(c)
+    again = bm.bi_moe_combine_consume(buf[offset:].view(M * k, H), M, k)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want) and torch.equal(again, want)
+
+
 @pytest.fixture
 def gemm_variant():
     """Set the expert-GEMM variant for one test; restores automatic after."""
