@@ -168,6 +168,16 @@ BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
                                    bi_stream_t stream);
 
 /*
+ * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path: one CTA
+ * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
+ * barrier phase that nothing completes.  The wait gives up after its limit
+ * (one second of the GPU's global timer), records BI_DEVERR_WAIT_TIMEOUT in
+ * the device error word and the kernel returns; nothing faults or traps and
+ * the context stays usable.  Read the outcome with bi_device_error.
+ */
+BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream);
+
+/*
  * bi_topk -- sigmoid scoring and deterministic top-k expert selection.
  * Source: "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling under
  * batch invariance", commit log, deterministic per-row top-k commit: score

@@ -34,7 +34,7 @@ EXPORTS = [
     "bi_router_gemm_splitk_negctl", "bi_topk", "bi_moe_workspace_bytes", "bi_moe_forward",
     "bi_moe_permute_workspace_bytes", "bi_moe_permute", "bi_moe_gather",
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_combine_consume", "bi_moe_forward_noalloc",
-    "bi_fp32_fma_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
+    "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
 ]
 
@@ -90,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_router_topk_bf16": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
+            "bi_wait_timeout_probe": ([P], ST),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -378,6 +379,12 @@ def bi_fp32_fma_probe(blocks, iters, stream=None, out=None):
         raise ValueError("out holds fewer than blocks * 256 floats")
     _call("bi_fp32_fma_probe", _ptr(out, torch.float32, "out"), blocks, iters, _stream(stream))
     return out
+
+
+def bi_wait_timeout_probe(stream=None):
+    """Test use only: a kernel whose bounded mbarrier wait runs out (about one
+    second); read the recorded BI_DEVERR_WAIT_TIMEOUT with device_error()."""
+    _call("bi_wait_timeout_probe", _stream(stream))
 
 
 def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):

@@ -34,6 +34,7 @@ int set_gemm_variant(int v);
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
+bi_status launch_wait_timeout_probe(cudaStream_t);
 
 // ------------------------------------------------------------ error state --
 static thread_local char g_msg[512] = "";
@@ -367,6 +368,10 @@ BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, bi
   BI_REQUIRE(out && blocks > 0 && blocks < (int64_t(1) << 31) && iters > 0, BI_ERR_INVALID_ARG,
              "bad probe arguments");
   return launch_fp32_fma_probe(out, blocks, iters, reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream) {
+  return launch_wait_timeout_probe(reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {

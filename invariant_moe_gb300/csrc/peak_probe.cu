@@ -1,5 +1,6 @@
 // peak_probe.cu -- FP32 FMA throughput probe used by the benchmark to
-// measure the FP32 (non-tensor) roofline denominator of this GPU.
+// measure the FP32 (non-tensor) roofline denominator of this GPU, and the
+// wait-timeout probe the tests use to exercise the bounded-wait discipline.
 //
 // Every thread runs kChains independent __fmaf_rn chains for `iters` steps
 // (no memory traffic inside the loop), so the kernel is bound by the FP32
@@ -24,6 +25,24 @@ __global__ void __launch_bounds__(256) fp32_fma_probe_kernel(float *__restrict__
 #pragma unroll
   for (int c = 0; c < kChains; ++c) s = __fadd_rn(s, v[c]);
   out[static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x] = s;
+}
+
+// One thread waits, through the library's bounded mbarrier wait, for a phase
+// of a barrier that nothing arrives on: the wait gives up after its limit,
+// records BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel
+// returns normally.
+__global__ void wait_timeout_probe_kernel(int *err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_barrier_init();
+  (void)mbar_wait(smem_u32(&bar), 0, nullptr, err);
+}
+
+bi_status launch_wait_timeout_probe(cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(device_error_word());
+  BI_CHECK_LAUNCH();
+  return BI_OK;
 }
 
 bi_status launch_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, cudaStream_t stream) {
