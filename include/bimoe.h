@@ -64,6 +64,8 @@ typedef enum {
 #define BI_DEVERR_BAD_EXPERT_ID 1   /* id outside [0,E) */
 #define BI_DEVERR_REPEATED_EXPERT 2 /* one row routed twice to one expert */
 #define BI_DEVERR_WAIT_TIMEOUT 3    /* an mbarrier wait exceeded its limit */
+#define BI_DEVERR_BAD_PERMUTATION 4 /* offsets / perm given to a stage call are not
+                                       a grouping of the M*top_k pairs */
 
 BI_API const char *bi_status_str(bi_status s);
 BI_API const char *bi_last_error_message(void);
@@ -318,6 +320,9 @@ BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets,
  * gate/up GEMM can stream them with TMA.  x [M,H] bf16; x_perm [M*top_k, H]
  * bf16 (device, written; 16-byte aligned).  Rows at positions >= offsets[E]
  * are left untouched.
+ * Bad grouping (offsets[E] outside [0, M*top_k], or a perm entry outside
+ * [0, M*top_k)): those positions are not copied and BI_DEVERR_BAD_PERMUTATION
+ * is recorded in the device error word.
  */
 BI_API bi_status bi_moe_gather(const bi_bf16 *x, const int32_t *offsets,
                                const int32_t *perm, bi_bf16 *x_perm, int64_t M,
@@ -332,6 +337,10 @@ BI_API bi_status bi_moe_gather(const bi_bf16 *x, const int32_t *offsets,
  *   x_perm [M*top_k, H] bf16 from bi_moe_gather (16-byte aligned);
  *   offsets/perm from bi_moe_permute; wts [M,top_k] fp32;
  *   w13 [E,2I,H] bf16 (16-byte aligned); act [M*top_k, I] bf16 (written).
+ * Bad grouping: offsets that are not non-decreasing inside [0, M*top_k]
+ * make the kernel compute nothing; a perm entry outside [0, M*top_k) gets
+ * probability 0.  Either records BI_DEVERR_BAD_PERMUTATION (device error
+ * word); nothing is read or written outside the arguments' extents.
  */
 BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets,
                                 const int32_t *perm, const float *wts,
@@ -344,6 +353,9 @@ BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets,
  * permuted position p (tcgen05 bf16 MMA, fp32 accumulation, K step 64, no
  * split-K).  act [M*top_k, I] bf16 (16-byte aligned); w2 [E,H,I] bf16;
  * contrib [M*top_k, H] fp32 (row = token*top_k + slot), written.
+ * Bad grouping: offsets that are not non-decreasing inside [0, M*top_k]
+ * make the kernel compute nothing; a position whose perm entry is outside
+ * [0, M*top_k) is not stored.  Either records BI_DEVERR_BAD_PERMUTATION.
  */
 BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets,
                              const int32_t *perm, const bi_bf16 *w2,

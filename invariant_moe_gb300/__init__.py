@@ -25,7 +25,7 @@ BI_OK = 0
 STATUS = {0: "BI_OK", 1: "BI_ERR_INVALID_ARG", 2: "BI_ERR_UNSUPPORTED", 3: "BI_ERR_WORKSPACE",
           4: "BI_ERR_CUDA", 5: "BI_ERR_DEVICE"}
 DEVERR = {0: "none", 1: "expert id out of range", 2: "repeated expert in a row",
-          3: "bounded wait timed out"}
+          3: "bounded wait timed out", 4: "offsets / perm are not a grouping of the pairs"}
 
 # every symbol include/bimoe.h declares (checked by the CPU test-suite)
 EXPORTS = [

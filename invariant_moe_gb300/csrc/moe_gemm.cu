@@ -115,6 +115,7 @@ struct GemmParams {
   int a_rows_per_expert;   // rows of the weight tensor per expert (2I or H)
   int up_offset;           // row offset of the up half (I), gate/up only
   int *err;
+  int P;                   // (token, slot) pairs: rows of the token operand and of the output
 };
 
 struct TileInfo {
@@ -228,11 +229,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // tile_prefix[e] = tiles of experts < e; each lane scans a contiguous chunk
     const int per = (prm.E + 31) / 32;
     const int e0 = min(lane * per, prm.E), e1 = min(e0 + per, prm.E);
+    // offsets that are not non-decreasing inside [0, P] would put tiles
+    // outside the operands: then the kernel does no tile and records the error
+    bool bad = lane == 0 && (offs[0] < 0 || offs[prm.E] > prm.P);
     int local = 0;
     for (int e = e0; e < e1; ++e) {
       const int cnt = offs[e + 1] - offs[e];
-      local += prm.n_wb * ((cnt + kBN - 1) / kBN);
+      bad = bad || cnt < 0;
+      local += prm.n_wb * ((max(cnt, 0) + kBN - 1) / kBN);
     }
+    bad = __any_sync(0xffffffffu, bad);
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -243,9 +249,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int e = e0; e < e1; ++e) {
       tile_prefix[e] = run;
       const int cnt = offs[e + 1] - offs[e];
-      run += prm.n_wb * ((cnt + kBN - 1) / kBN);
+      run += prm.n_wb * ((max(cnt, 0) + kBN - 1) / kBN);
     }
-    if (lane == 31) tile_prefix[prm.E] = incl;
+    if (lane == 31) tile_prefix[prm.E] = bad ? 0 : incl;
+    if (bad && lane == 0) report_error(prm.err, BI_DEVERR_BAD_PERMUTATION);
   }
   tc_fence_before();
   __syncthreads();
@@ -461,10 +468,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         nx_p[i] = 0.0f;
       }
       if (GATE_UP) {
+        // a perm entry that is not a pair id reads no probability (checked
+        // again, and reported, when the tile is stored)
 #pragma unroll
         for (int i = 0; i < kBN / 32; ++i) {
           const int c = 32 * i + lane;
-          nx_p[i] = c < t.ntok ? __ldg(prm.wts + nx_pair[i]) : 0.0f;
+          const bool ok = static_cast<unsigned>(nx_pair[i]) < static_cast<unsigned>(prm.P);
+          nx_p[i] = c < t.ntok && ok ? __ldg(prm.wts + nx_pair[i]) : 0.0f;
         }
       }
     };
@@ -482,6 +492,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // one decision per warp (lanes can disagree at the instant a wait gives up)
       const bool okw = __all_sync(0xffffffffu, wait(smem_u32(&tfull[acc]), acc_phase, abort_flag) ? 1 : 0) != 0;
       if (!okw) break;
+      {
+        // perm entries of this tile that are not pair ids (the loads landed
+        // long ago): reported once; nothing is stored through them below
+        bool badp = false;
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i)
+          badp = badp || (32 * i + lane < ti.ntok &&
+                          static_cast<unsigned>(my_pair[i]) >= static_cast<unsigned>(prm.P));
+        if (badp) report_error(prm.err, BI_DEVERR_BAD_PERMUTATION);
+      }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
@@ -530,7 +550,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int pair = __shfl_sync(0xffffffffu, my_pair[i], c);
-            if (c0 + c < ti.ntok)
+            if (c0 + c < ti.ntok && static_cast<unsigned>(pair) < static_cast<unsigned>(prm.P))
               contrib[static_cast<size_t>(pair) * prm.out_ld + col] = __uint_as_float(d[c]);
           }
         }
@@ -708,7 +728,7 @@ bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32
   const int wb_rows = inter ? (pair ? kBM : kBM / 2) : (pair ? 2 * kBM : kBM);
   const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
-               (int)(2 * I), (int)I, device_error_word()};
+               (int)(2 * I), (int)I, device_error_word(), (int)P};
   const int64_t wr = E * 2 * I;
   if (inter && pair)
     return narrow ? run_gemm<true, true, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
@@ -732,7 +752,7 @@ bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *pe
   const bool pair = v >= 2, narrow = use_narrow(P, E);
   const int wb_rows = pair ? 2 * kBM : kBM;
   GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / wb_rows), wb_rows, (int)H,
-               (int)H, 0, device_error_word()};
+               (int)H, 0, device_error_word(), (int)P};
   if (pair)
     return narrow ? run_gemm<false, true, false, true>(w2, E * H, kBM, act, P, I, p, stream)
                   : run_gemm<false, true, false, false>(w2, E * H, kBM, act, P, I, p, stream);

@@ -215,13 +215,20 @@ __global__ void __launch_bounds__(kSmallPermuteMaxM) moe_permute_small_kernel(
 __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict__ x,
                                                          const int32_t *__restrict__ perm,
                                                          const int32_t *__restrict__ offsets,
-                                                         int E, int top_k, int row_vec,
-                                                         uint4 *__restrict__ xp) {
+                                                         int E, int top_k, int P, int row_vec,
+                                                         uint4 *__restrict__ xp, int *err) {
   griddep_wait_small_release();
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (p >= offsets[E]) return;
-  const int m = perm[p] / top_k;
+  const int npos = offsets[E];
+  if (p == 0 && lane == 0 && (npos < 0 || npos > P)) report_error(err, BI_DEVERR_BAD_PERMUTATION);
+  if (p >= min(npos, P)) return;
+  const int pair = perm[p];
+  if (static_cast<unsigned>(pair) >= static_cast<unsigned>(P)) {  // not a pair id: no copy
+    if (lane == 0) report_error(err, BI_DEVERR_BAD_PERMUTATION);
+    return;
+  }
+  const int m = pair / top_k;
   const uint4 *src = x + static_cast<size_t>(m) * row_vec;
   uint4 *dst = xp + static_cast<size_t>(p) * row_vec;
   for (int c = lane; c < row_vec; c += 32) dst[c] = src[c];
@@ -303,8 +310,8 @@ bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offse
                         int64_t H, int64_t E, int32_t top_k, void *xp, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((P + 7) / 8);
   return launch_chained(moe_gather_kernel, dim3(blocks), dim3(256), 0, stream, 1,
-                        static_cast<const uint4 *>(x), perm, offsets, (int)E, top_k, (int)(H / 8),
-                        static_cast<uint4 *>(xp));
+                        static_cast<const uint4 *>(x), perm, offsets, (int)E, top_k, (int)P,
+                        (int)(H / 8), static_cast<uint4 *>(xp), device_error_word());
 }
 
 bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, int32_t top_k,

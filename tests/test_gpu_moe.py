@@ -81,6 +81,71 @@ def test_permute_reports_bad_ids(cuda, request):
     assert bm.device_error() == 2
 
 
+def test_stage_calls_reject_bad_grouping(cuda):
+    """offsets / perm handed to the stage calls that are not a grouping of
+    the pairs: nothing is read or written outside the arguments' extents and
+    the device error word says BI_DEVERR_BAD_PERMUTATION (4).  Every buffer is
+    padded with rows past its extent, so the checks are observed without any
+    access leaving the allocations even if one were missing."""
+    import invariant_moe_gb300 as bm
+    M, H, E, I, k, pad = 64, 256, 8, 128, 2, 64
+    P = M * k
+    w = syn.moe_weights(H, E, I, seed=71, device=str(cuda))
+    x = syn.moe_tokens(M, H, seed=72).to(cuda)
+    ids, wts = syn.random_routing(M, E, k, seed=73)
+    offsets, perm = bm.bi_moe_permute(ids.to(cuda), E)
+    x_pad = torch.zeros(M + pad, H, dtype=torch.bfloat16, device=cuda)
+    x_pad[:M] = x
+    xp_pad = torch.zeros(P + pad, H, dtype=torch.bfloat16, device=cuda)
+    wts_pad = torch.zeros(P + pad, dtype=torch.float32, device=cuda)
+    wts_pad[:P] = wts.flatten().to(cuda)
+    act_pad = torch.zeros(P + pad, I, dtype=torch.bfloat16, device=cuda)
+    con_pad = torch.zeros(P + pad, H, dtype=torch.float32, device=cuda)
+    assert bm.device_error() == 0
+
+    # a perm entry outside [0, P)
+    bad_perm = perm.clone()
+    bad_perm[5] = P + 3
+    bm.bi_moe_gather(x_pad[:M], offsets, bad_perm, k, x_perm=xp_pad[:P])
+    assert bm.device_error() == 4
+    bm.bi_moe_gate_up(xp_pad[:P], offsets, bad_perm, wts_pad[:P].view(M, k), w.w13, k, act=act_pad[:P])
+    assert bm.device_error() == 4
+    bm.bi_moe_down(act_pad[:P], offsets, bad_perm, w.w2, M, k, contrib=con_pad[:P])
+    assert bm.device_error() == 4
+    torch.cuda.synchronize()
+    assert not xp_pad[P:].any() and not act_pad[P:].any() and not con_pad[P:].any()
+
+    # offsets past P (and so not a grouping): the GEMMs compute nothing
+    perm_pad = torch.zeros(P + pad, dtype=torch.int32, device=cuda)
+    perm_pad[:P] = perm
+    bad_off = offsets.clone()
+    bad_off[E] = P + 32
+    act_pad.fill_(7.0)
+    con_pad.fill_(7.0)
+    bm.bi_moe_gate_up(xp_pad[:P], bad_off, perm_pad[:P], wts_pad[:P].view(M, k), w.w13, k, act=act_pad[:P])
+    assert bm.device_error() == 4
+    bm.bi_moe_down(act_pad[:P], bad_off, perm_pad[:P], w.w2, M, k, contrib=con_pad[:P])
+    assert bm.device_error() == 4
+    torch.cuda.synchronize()
+    assert bool((act_pad == 7.0).all()) and bool((con_pad == 7.0).all())
+    # offsets that decrease
+    bad_off = offsets.clone()
+    bad_off[3] = bad_off[4] + 5
+    bm.bi_moe_down(act_pad[:P], bad_off, perm_pad[:P], w.w2, M, k, contrib=con_pad[:P])
+    assert bm.device_error() == 4
+    torch.cuda.synchronize()
+    assert bool((con_pad == 7.0).all())
+    bm.bi_moe_gather(x_pad[:M], bad_off, perm, k, x_perm=xp_pad[:P])  # copies by offsets[E] only
+    assert bm.device_error() == 0
+
+    # the good grouping still gives the layer's stages their normal result
+    xp = bm.bi_moe_gather(x, offsets, perm, k)
+    act = bm.bi_moe_gate_up(xp, offsets, perm, wts.to(cuda), w.w13, k)
+    con = bm.bi_moe_down(act, offsets, perm, w.w2, M, k)
+    torch.cuda.synchronize()
+    assert bm.device_error() == 0 and torch.isfinite(con).all()
+
+
 def stage_inputs(M, H, E, I, k, seed, unit=False):
     w = syn.moe_weights(H, E, I, seed=seed, unit=unit)
     x = syn.moe_tokens(M, H, seed=seed + 5, unit=unit)
