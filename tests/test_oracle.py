@@ -89,6 +89,26 @@ def test_router_invariants(oracle_mod):
     assert np.all(np.abs(r - ref) <= bound)
 
 
+def test_router_within_bound_of_correctly_rounded_sum(oracle_mod):
+    """Against math.fsum of the exact products (fp32 x fp32 is exact in fp64):
+    the oracle's fp64 sum in increasing k, bias last, stays within the
+    recursive-summation bound (K+1) u sum|terms| of the correctly rounded
+    sum, at the router's K = 4096."""
+    rng = np.random.default_rng(21)
+    M, K, N = 3, 4096, 5
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) / 64).astype(np.float32)
+    b = (rng.standard_normal(N) * 0.01).astype(np.float32)
+    r = oracle_mod.router(x, w, b)
+    u = 2.0 ** -53
+    for i in range(M):
+        for n in range(N):
+            terms = [float(x[i, k]) * float(w[n, k]) for k in range(K)] + [float(b[n])]
+            exact = math.fsum(terms)
+            mag = math.fsum(abs(t) for t in terms)
+            assert abs(r[i, n] - exact) <= (K + 1) * u * mag
+
+
 def test_sigmoid_closed_forms(oracle_mod):
     assert oracle_mod.sigmoid(np.array([0.0]))[0] == 0.5
     v = np.array([-3.5, -1.0, 0.25, 1.0, 2.0, 7.0], np.float32)
