@@ -27,6 +27,16 @@ def test_header_and_binding_agree():
     assert declared_symbols() == sorted(bm.EXPORTS)
 
 
+def test_status_and_device_error_codes_agree():
+    """The binding's names for the status and device error codes are the
+    header's values."""
+    import invariant_moe_gb300 as bm
+    src = open(os.path.join(ROOT, "include", "bimoe.h")).read()
+    deverr = {int(v): n for n, v in re.findall(r"#define\s+BI_DEVERR_(\w+)\s+(\d+)", src)}
+    assert sorted(deverr) == sorted(bm.DEVERR)
+    assert deverr[0] == "NONE" and deverr[3] == "WAIT_TIMEOUT" and deverr[4] == "BAD_PERMUTATION"
+
+
 def test_every_declared_symbol_is_exported(lib):
     names = declared_symbols()
     assert len(names) >= 15
