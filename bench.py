@@ -339,7 +339,9 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device error during the timed region")
 
     extras = {}
-    if rank == 0 and not args.no_extras:
+    # the sweeps characterise one GPU: the N=1 run reports them, and a
+    # multi-GPU run does not hold the other GPUs idle while rank 0 sweeps
+    if rank == 0 and world == 1 and not args.no_extras:
         extras["router_us_vs_M"] = router_sweep(dev)
         extras["moe_layer_us_vs_M"] = moe_sweep(dev, args.workload)
         extras["topk_window_us"] = topk_window_sweep(dev)
@@ -797,7 +799,8 @@ def main(argv=None):
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world, local)
-        if line is not None and not args.no_cpu_baseline:
+        # the oracle's CPU baseline is timed at N=1 only
+        if line is not None and world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args)
     if line is not None:
         print(json.dumps(line), flush=True)
