@@ -24,8 +24,10 @@
  * never falls back to another recipe); BI_ERR_WORKSPACE for a workspace that
  * is too small; BI_ERR_CUDA when a launch fails.  M == 0 returns BI_OK and
  * launches nothing.  A kernel that detects bad data (an expert id outside
- * [0,E), repeated experts in one row) or whose bounded wait times out
- * records a code in a device-side error word; bi_device_error() reads it.
+ * [0,E), repeated experts in one row, offsets / perm handed to a stage call
+ * that are not a grouping of the pairs) or whose bounded wait times out
+ * records a code in a device-side error word and skips what it cannot do
+ * safely; bi_device_error() reads it.
  * bi_last_error_message() returns a human-readable detail of the last
  * failing call on this host thread.
  */
@@ -170,7 +172,8 @@ BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
                                    bi_stream_t stream);
 
 /*
- * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path: one CTA
+ * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path and not on
+ * the pages (it exercises this library's bounded-wait discipline): one CTA
  * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
  * barrier phase that nothing completes.  The wait gives up after its limit
  * (one second of the GPU's global timer), records BI_DEVERR_WAIT_TIMEOUT in
@@ -364,7 +367,9 @@ BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets,
 
 /*
  * bi_moe_combine -- out[m,h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) +
- * c[m,top_k-1,h]) in fp32, slot order, unit weights.
+ * c[m,top_k-1,h]) in fp32, slot order, unit weights (the top-k sum of the
+ * fused-MoE page, section "What's included": a fixed `for t in range(topk)`
+ * order, the probabilities already applied at the activation).
  * contrib [M,top_k,H] fp32; out [M,H] bf16 (device, written).
  */
 BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
