@@ -112,22 +112,6 @@ BI_API bi_status bi_router_gemm(const float *x, const float *w, const float *bia
                                 bi_stream_t stream);
 
 /*
- * bi_router_gemm_schedule -- test hook: bi_router_gemm with the schedule
- * forced (0 = automatic by M, 1 = per-row warp kernel, 2 = slice-parallel
- * tile kernel, 3 = register-tiled kernel, 4 = slices spread over a cluster
- * of CTAs with the lane tile picked from M, 5..8 = the same with the lane
- * tile forced to 2x2, 4x2, 4x4, 8x4 outputs, 9 = register-tiled kernel
- * with 7x8 outputs per thread).  Schedules 4..8 need K/128 to split into
- * 2..8 CTAs of 4 or 8 slices, schedule 9 K/128 even (N > 128) or a multiple
- * of 4 (N <= 128) (else BI_ERR_UNSUPPORTED).  Every schedule computes the same recipe; tests use
- * this to show that the bits do not depend on it.
- */
-BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,
-                                         const float *bias, float *y, int64_t M,
-                                         int64_t K, int64_t N, int32_t schedule,
-                                         bi_stream_t stream);
-
-/*
  * bi_router_gemm_bf16 -- bi_router_gemm with bf16 x: y[i,n] from the fp32
  * values of x[i,:] (a bf16 value converts to fp32 exactly), so the result is
  * bit for bit bi_router_gemm(float(x)) under every schedule.  The MoE layer's
@@ -141,47 +125,6 @@ BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,
 BI_API bi_status bi_router_gemm_bf16(const bi_bf16 *x, const float *w, const float *bias,
                                      float *y, int64_t M, int64_t K, int64_t N,
                                      bi_stream_t stream);
-/* test hook: bi_router_gemm_bf16 with the schedule forced (as bi_router_gemm_schedule) */
-BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w,
-                                              const float *bias, float *y, int64_t M,
-                                              int64_t K, int64_t N, int32_t schedule,
-                                              bi_stream_t stream);
-
-/*
- * bi_router_gemm_splitk_negctl -- NEGATIVE CONTROL, test use only.  Same
- * signature as bi_router_gemm but its K split depends on M (one chain over
- * all of K for M > 16, sixteen 256-long slices for M <= 16), the kind of
- * batch-dependent reduction the GateLinear page diagnoses in the default
- * route.  Row bits change across that boundary; the tests assert that they
- * do, to prove the invariance tests can fail.
- */
-BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w,
-                                              const float *bias, float *y,
-                                              int64_t M, int64_t K, int64_t N,
-                                              bi_stream_t stream);
-
-/*
- * bi_fp32_fma_probe -- MEASUREMENT ONLY, not part of the MoE path: blocks x
- * 256 threads, each running 16 independent fp32 FMA chains for `iters`
- * steps (2 * 16 * iters flop per thread, no memory traffic in the loop).
- * The benchmark times it to measure the FP32 (non-tensor) peak that the
- * router's FFMA roofline is reported against.  out: blocks * 256 floats
- * (device), written.
- */
-BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
-                                   bi_stream_t stream);
-
-/*
- * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path and not on
- * the pages (it exercises this library's bounded-wait discipline): one CTA
- * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
- * barrier phase that nothing completes.  The wait gives up after its limit
- * (one second of the GPU's global timer), records BI_DEVERR_WAIT_TIMEOUT in
- * the device error word and the kernel returns; nothing faults or traps and
- * the context stays usable.  Read the outcome with bi_device_error.
- */
-BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream);
-
 /*
  * bi_topk -- sigmoid scoring and deterministic top-k expert selection.
  * Source: "[BI][DSv4] Pin sparse-MLA decode and prefill scheduling under
@@ -190,16 +133,16 @@ BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream);
  * ranking on a monotone int32 key of the fp32 score, no shared-memory
  * atomics.
  *   scores [M,E] fp32 (device): router outputs
+ *   probs  [M,E] fp32 (device) or NULL: sigmoid of every score, written
  *   ids    [M,top_k] int32 (device), written: ids[m,t] = rank-t expert
  *   wts    [M,top_k] fp32 (device), written: sigmoid(scores[m, ids[m,t]])
- *   probs  [M,E] fp32 (device) or NULL: sigmoid of every score
  * Selection is on the fp32 score (sigmoid is monotone, so this is the
  * selection by probability without ties manufactured by rounding the
  * sigmoid).  One warp per row.  Requirements: 1 <= E <= 512,
  * 1 <= top_k <= min(E, 16).
  */
-BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts,
-                         float *probs, int64_t M, int64_t E, int32_t top_k,
+BI_API bi_status bi_topk(const float *scores, float *probs, int32_t *ids,
+                         float *wts, int64_t M, int64_t E, int32_t top_k,
                          bi_stream_t stream);
 
 /*
@@ -257,18 +200,13 @@ BI_API bi_status bi_router_topk_bf16(const bi_bf16 *x, const float *w, const flo
                                      int64_t M, int64_t K, int64_t N, int32_t top_k,
                                      bi_stream_t stream);
 /*
- * bi_router_topk_schedule -- test hook: bi_router_topk with the router
- * schedule forced as in bi_router_gemm_schedule.
- */
-BI_API bi_status bi_router_topk_schedule(const float *x, const float *w,
-                                         const float *bias, float *y, float *probs,
-                                         int32_t *ids, float *wts, int64_t M, int64_t K,
-                                         int64_t N, int32_t top_k, int32_t schedule,
-                                         bi_stream_t stream);
-
-/*
  * bi_moe_workspace_bytes -- bytes of device workspace bi_moe_forward needs
- * for these sizes (a multiple of 256).  Returns 0 for invalid sizes.
+ * for these sizes (a multiple of 256).  Returns 0 for invalid sizes.  The
+ * pages have no counterpart: their fused-MoE keeps its buffers inside the
+ * framework; this library leaves every allocation to the caller, so it states
+ * the size.  The workspace holds the permutation (offsets, pair ids, a mask of
+ * valid slots per token), the gathered token rows, the activations and the
+ * fp32 per-slot contributions.
  */
 BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E,
                                      int32_t top_k, int64_t I);
@@ -293,6 +231,10 @@ BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E,
  *   256-byte aligned, owned by the caller, contents need not be initialised.
  * Requirements: H % 128 == 0, I % 128 == 0, 1 <= E <= 1024,
  * 1 <= top_k <= 16, M * top_k < 2^31.
+ * Bad routing data: a slot whose expert id is outside [0,E), or repeats an
+ * earlier slot of its row, is skipped (BI_DEVERR_BAD_EXPERT_ID /
+ * BI_DEVERR_REPEATED_EXPERT in the device error word) and adds nothing: that
+ * token's output is the slot-order sum over its valid slots (+0 if none).
  */
 BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids,
                                 const float *wts, const bi_bf16 *w13,
@@ -389,6 +331,143 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M,
 BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M,
                                         int64_t H, int32_t top_k, bi_stream_t stream);
 
+/* ---- expert parallelism: the two data-layout steps around the exchange --
+ *
+ * With the experts split over R ranks (rank r owns experts
+ * [r*E/R, (r+1)*E/R)), a token's k contributions are computed on the ranks
+ * that own its experts and must return to the token's home rank, where they
+ * are summed in slot order: then every output bit is the single-GPU layer's
+ * ("Batch-invariance generation with vLLM fused-MoE backend at improved
+ * performance", sections "Summary" and "Usage": expert parallelism over 8
+ * GPUs with the fused-MoE backend).  The home rank groups its pairs by expert
+ * (bi_moe_permute, which also groups them by destination rank), gathers the
+ * token rows (bi_moe_gather) and their routing (bi_moe_gather_routing), and
+ * sends each rank its contiguous range of positions; the receiving rank runs
+ * the expert GEMMs on the rows it received (top_k = 1, pair id = row) and
+ * sends the fp32 contribution rows back in the order it received them; the
+ * home rank puts them back in (token, slot) order (bi_moe_scatter_contrib)
+ * and combines them in slot order (bi_moe_combine).
+ *
+ * bi_moe_gather_routing -- for every permuted position p < offsets[E]:
+ *   lid[p] = ids[perm[p]] % experts_per_rank   (the expert's index on its rank)
+ *   pw[p]  = wts[perm[p]]                      (the routing probability)
+ *   ids [M,top_k] int32, wts [M,top_k] fp32, offsets [E+1] / perm [M*top_k]
+ *   from bi_moe_permute; lid [M*top_k] int32 and pw [M*top_k] fp32 (device,
+ *   written for p < offsets[E]).  experts_per_rank must divide E.
+ *   A perm entry outside [0, M*top_k) or offsets[E] outside that range:
+ *   the position is skipped and BI_DEVERR_BAD_PERMUTATION recorded.
+ */
+BI_API bi_status bi_moe_gather_routing(const int32_t *ids, const float *wts,
+                                       const int32_t *offsets, const int32_t *perm,
+                                       int32_t *lid, float *pw, int64_t M, int64_t E,
+                                       int32_t top_k, int64_t experts_per_rank,
+                                       bi_stream_t stream);
+
+/*
+ * bi_moe_scatter_contrib -- contrib[perm[p], :] = rows[p, :] for every
+ * permuted position p < offsets[E]: fp32 contribution rows that came back in
+ * the permuted order, put back at row token*top_k + slot.
+ *   rows [M*top_k, H] fp32, contrib [M*top_k, H] fp32 (device, 16-byte
+ *   aligned; rows of pairs that were skipped are not written).  H % 4 == 0.
+ *   Bad grouping as bi_moe_gather_routing.
+ */
+BI_API bi_status bi_moe_scatter_contrib(const float *rows, const int32_t *offsets,
+                                        const int32_t *perm, float *contrib, int64_t M,
+                                        int64_t H, int64_t E, int32_t top_k,
+                                        bi_stream_t stream);
+
+/*
+ * bi_moe_forward_noalloc -- bi_moe_forward without a caller-provided
+ * workspace, for callers that cannot allocate device memory where they run
+ * the layer (code inside an allocator or memory-pool callback, runtimes that
+ * own all device memory and forbid allocations behind their back).  This
+ * entry point has no counterpart in the papers; it exists only for such
+ * callers.
+ *
+ * Arguments, layouts, requirements and results are those of bi_moe_forward
+ * (same kernels, same bits).  The scratch space is a fixed array of
+ * BI_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device code: every
+ * GPU that loads the library holds it until the process exits.  Sizes whose
+ * bi_moe_workspace_bytes() exceeds it are rejected with BI_ERR_WORKSPACE and
+ * a message naming both sizes (64 MiB covers e.g. 606 tokens of H=2048,
+ * E=128, top-8, I=768, or 292 tokens of H=4096, E=256, top-8, I=2048).
+ * The call never allocates or frees device memory.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it for the
+ * current CUDA context; the first call after the context changes (after a
+ * cudaDeviceReset, or from a context other than the device's primary one)
+ * looks it up again.  Make the first call of each context before any stream
+ * capture begins.
+ *
+ * All calls on a device share the one array and it keeps the previous
+ * call's contents; nothing in it needs to start at zero, because every call
+ * writes each scratch byte it reads before reading it.  Calls whose
+ * executions overlap on the GPU (different streams, or host threads issuing
+ * concurrently without ordering) race on the array and give undefined
+ * results: order them on one stream.
+ */
+#define BI_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+BI_API bi_status bi_moe_forward_noalloc(const bi_bf16 *x, const int32_t *ids,
+                                        const float *wts, const bi_bf16 *w13,
+                                        const bi_bf16 *w2, bi_bf16 *out,
+                                        int64_t M, int64_t H, int64_t E,
+                                        int32_t top_k, int64_t I,
+                                        bi_stream_t stream);
+
+/* ======================================================================
+ * TEST AND MEASUREMENT HOOKS.  Not part of the hot path and not needed to
+ * use it: the test-suite and the benchmark call these to force schedules
+ * (and show the bits do not depend on them), to run the negative control,
+ * to measure the FP32 peak and to exercise the bounded-wait discipline.
+ * ====================================================================== */
+
+/*
+ * bi_router_gemm_schedule -- test hook: bi_router_gemm with the schedule
+ * forced (0 = automatic by M, 1 = per-row warp kernel, 2 = slice-parallel
+ * tile kernel, 3 = register-tiled kernel, 4 = slices spread over a cluster
+ * of CTAs with the lane tile picked from M, 5..8 = the same with the lane
+ * tile forced to 2x2, 4x2, 4x4, 8x4 outputs, 9 = register-tiled kernel
+ * with 7x8 outputs per thread).  Schedules 4..8 need K/128 to split into
+ * 2..8 CTAs of 4 or 8 slices, schedule 9 K/128 even (N > 128) or a multiple
+ * of 4 (N <= 128) (else BI_ERR_UNSUPPORTED).  Every schedule computes the same recipe; tests use
+ * this to show that the bits do not depend on it.
+ */
+BI_API bi_status bi_router_gemm_schedule(const float *x, const float *w,
+                                         const float *bias, float *y, int64_t M,
+                                         int64_t K, int64_t N, int32_t schedule,
+                                         bi_stream_t stream);
+
+/* test hook: bi_router_gemm_bf16 with the schedule forced (as bi_router_gemm_schedule) */
+BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w,
+                                              const float *bias, float *y, int64_t M,
+                                              int64_t K, int64_t N, int32_t schedule,
+                                              bi_stream_t stream);
+
+
+/*
+ * bi_router_gemm_splitk_negctl -- NEGATIVE CONTROL, test use only.  Same
+ * signature as bi_router_gemm but its K split depends on M (one chain over
+ * all of K for M > 16, sixteen 256-long slices for M <= 16), the kind of
+ * batch-dependent reduction the GateLinear page diagnoses in the default
+ * route.  Row bits change across that boundary; the tests assert that they
+ * do, to prove the invariance tests can fail.
+ */
+BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w,
+                                              const float *bias, float *y,
+                                              int64_t M, int64_t K, int64_t N,
+                                              bi_stream_t stream);
+
+/*
+ * bi_router_topk_schedule -- test hook: bi_router_topk with the router
+ * schedule forced as in bi_router_gemm_schedule.
+ */
+BI_API bi_status bi_router_topk_schedule(const float *x, const float *w,
+                                         const float *bias, float *y, float *probs,
+                                         int32_t *ids, float *wts, int64_t M, int64_t K,
+                                         int64_t N, int32_t top_k, int32_t schedule,
+                                         bi_stream_t stream);
+
 /*
  * bi_moe_gemm_variant -- selects how the expert GEMMs (bi_moe_gate_up,
  * bi_moe_down and the two GEMMs inside bi_moe_forward) are scheduled, for
@@ -418,40 +497,27 @@ BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M,
 BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous);
 
 /*
- * bi_moe_forward_noalloc -- bi_moe_forward without a caller-provided
- * workspace, for callers that cannot allocate device memory where they run
- * the layer (code inside an allocator or memory-pool callback, runtimes that
- * own all device memory and forbid allocations behind their back).  This
- * entry point has no counterpart in the papers; it exists only for such
- * callers.
- *
- * Arguments, layouts, requirements and results are those of bi_moe_forward
- * (same kernels, same bits).  The scratch space is a fixed array of
- * BI_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device code: every
- * GPU that loads the library holds it until the process exits.  Sizes whose
- * bi_moe_workspace_bytes() exceeds it are rejected with BI_ERR_WORKSPACE and
- * a message naming both sizes (64 MiB covers e.g. 606 tokens of H=2048,
- * E=128, top-8, I=768, or 292 tokens of H=4096, E=256, top-8, I=2048).
- * The call never allocates or frees device memory.
- *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture begins.
- *
- * All calls on a device share the one array and it keeps the previous
- * call's contents; nothing in it needs to start at zero, because every call
- * writes each scratch byte it reads before reading it.  Calls whose
- * executions overlap on the GPU (different streams, or host threads issuing
- * concurrently without ordering) race on the array and give undefined
- * results: order them on one stream.
+ * bi_fp32_fma_probe -- MEASUREMENT ONLY, not part of the MoE path: blocks x
+ * 256 threads, each running 16 independent fp32 FMA chains for `iters`
+ * steps (2 * 16 * iters flop per thread, no memory traffic in the loop).
+ * The benchmark times it to measure the FP32 (non-tensor) peak that the
+ * router's FFMA roofline is reported against.  out: blocks * 256 floats
+ * (device), written.
  */
-#define BI_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
-BI_API bi_status bi_moe_forward_noalloc(const bi_bf16 *x, const int32_t *ids,
-                                        const float *wts, const bi_bf16 *w13,
-                                        const bi_bf16 *w2, bi_bf16 *out,
-                                        int64_t M, int64_t H, int64_t E,
-                                        int32_t top_k, int64_t I,
-                                        bi_stream_t stream);
+BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
+                                   bi_stream_t stream);
+
+/*
+ * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path and not on
+ * the pages (it exercises this library's bounded-wait discipline): one CTA
+ * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
+ * barrier phase that nothing completes.  The wait gives up after its limit
+ * (one second of the GPU's global timer), records BI_DEVERR_WAIT_TIMEOUT in
+ * the device error word and the kernel returns; nothing faults or traps and
+ * the context stays usable.  Read the outcome with bi_device_error.
+ */
+BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream);
+
 
 #ifdef __cplusplus
 }

@@ -36,6 +36,7 @@ EXPORTS = [
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_combine_consume", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
+    "bi_moe_gather_routing", "bi_moe_scatter_contrib",
 ]
 
 
@@ -91,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
             "bi_wait_timeout_probe": ([P], ST),
+            "bi_moe_gather_routing": ([P, P, P, P, P, P, I64, I64, I32, I64, P], ST),
+            "bi_moe_scatter_contrib": ([P, P, P, P, I64, I64, I64, I32, P], ST),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -188,8 +191,8 @@ def bi_topk(scores, top_k, ids=None, wts=None, probs=None, want_probs=False, str
     wts = wts if wts is not None else torch.empty(M, top_k, dtype=torch.float32, device=dev)
     if want_probs and probs is None:
         probs = torch.empty(M, E, dtype=torch.float32, device=dev)
-    _call("bi_topk", _ptr(scores, torch.float32, "scores"), _ptr(ids, torch.int32, "ids", dev),
-          _ptr(wts, torch.float32, "wts", dev), _ptr(probs, torch.float32, "probs", dev),
+    _call("bi_topk", _ptr(scores, torch.float32, "scores"), _ptr(probs, torch.float32, "probs", dev),
+          _ptr(ids, torch.int32, "ids", dev), _ptr(wts, torch.float32, "wts", dev),
           M, E, top_k, _stream(stream))
     return ids, wts, probs
 
@@ -208,12 +211,7 @@ def moe_workspace(M, H, E, top_k, I, device):
 
 def bi_moe_forward(x, ids, wts, w13, w2, out=None, workspace=None, stream=None):
     """out[M,H] bf16 = batch-invariant SwiGLU MoE of x [M,H] bf16."""
-    M, H = x.shape
-    E, twoI, H2 = w13.shape
-    I = twoI // 2
-    top_k = ids.shape[1]
-    if H2 != H or tuple(w2.shape) != (E, H, I):
-        raise ValueError("w13 must be [E, 2I, H] and w2 [E, H, I]")
+    M, H, E, I, top_k = _check_moe_shapes(x, ids, wts, w13, w2, out)
     dev = x.device
     out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     if workspace is None:
@@ -226,19 +224,36 @@ def bi_moe_forward(x, ids, wts, w13, w2, out=None, workspace=None, stream=None):
     return out
 
 
+def _check_moe_shapes(x, ids, wts, w13, w2, out):
+    M, H = x.shape
+    E, twoI, H2 = w13.shape
+    I = twoI // 2
+    if H2 != H or twoI % 2 or tuple(w2.shape) != (E, H, I):
+        raise ValueError("w13 must be [E, 2I, H] and w2 [E, H, I]")
+    if ids.dim() != 2 or ids.shape[0] != M or tuple(wts.shape) != tuple(ids.shape):
+        raise ValueError("ids and wts must be [M, top_k]")
+    if out is not None and tuple(out.shape) != (M, H):
+        raise ValueError("out must be [M, H]")
+    return M, H, E, I, ids.shape[1]
+
+
 def bi_moe_forward_noalloc(x, ids, wts, w13, w2, out=None, stream=None):
     """bi_moe_forward with the library's built-in scratch array instead of a
     caller workspace (for callers that cannot allocate device memory; the
-    output tensor, if not given, is still allocated here by torch)."""
-    M, H = x.shape
-    E, twoI, _ = w13.shape
-    I = twoI // 2
+    output tensor, if not given, is still allocated here by torch).  The call
+    runs with x's device current, whose scratch array the library uses."""
+    M, H, E, I, top_k = _check_moe_shapes(x, ids, wts, w13, w2, out)
     dev = x.device
-    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-    _call("bi_moe_forward_noalloc", _ptr(x, torch.bfloat16, "x"), _ptr(ids, torch.int32, "ids", dev),
-          _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
-          _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
-          M, H, E, ids.shape[1], I, _stream(stream))
+    if not x.is_cuda:
+        raise ValueError("x must live on a CUDA device")
+    with torch.cuda.device(dev):
+        out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        if stream is not None and stream.device != dev:
+            raise ValueError(f"stream is on {stream.device}, expected {dev}")
+        _call("bi_moe_forward_noalloc", _ptr(x, torch.bfloat16, "x"), _ptr(ids, torch.int32, "ids", dev),
+              _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+              _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
+              M, H, E, top_k, I, _stream(stream))
     return out
 
 
@@ -291,6 +306,34 @@ def bi_moe_down(act, offsets, perm, w2, M, top_k, contrib=None, stream=None):
     _call("bi_moe_down", _ptr(act, torch.bfloat16, "act"), _ptr(offsets, torch.int32, "offsets", dev),
           _ptr(perm, torch.int32, "perm", dev), _ptr(w2, torch.bfloat16, "w2", dev),
           _ptr(contrib, torch.float32, "contrib", dev), M, H, E, top_k, I, _stream(stream))
+    return contrib
+
+
+def bi_moe_gather_routing(ids, wts, offsets, perm, experts_per_rank, lid=None, pw=None, stream=None):
+    """(lid int32 [M*top_k], pw fp32 [M*top_k]): for each permuted position,
+    the expert's index on the rank that owns it and the routing probability."""
+    M, top_k = ids.shape
+    E = offsets.numel() - 1
+    dev = ids.device
+    P = M * top_k
+    lid = lid if lid is not None else torch.empty(max(P, 1), dtype=torch.int32, device=dev)
+    pw = pw if pw is not None else torch.empty(max(P, 1), dtype=torch.float32, device=dev)
+    _call("bi_moe_gather_routing", _ptr(ids, torch.int32, "ids"), _ptr(wts, torch.float32, "wts", dev),
+          _ptr(offsets, torch.int32, "offsets", dev), _ptr(perm, torch.int32, "perm", dev),
+          _ptr(lid, torch.int32, "lid", dev), _ptr(pw, torch.float32, "pw", dev), M, E, top_k,
+          experts_per_rank, _stream(stream))
+    return lid, pw
+
+
+def bi_moe_scatter_contrib(rows, offsets, perm, M, top_k, contrib=None, stream=None):
+    """contrib [M*top_k, H] fp32 with contrib[perm[p]] = rows[p] for p < offsets[E]."""
+    H = rows.shape[-1]
+    E = offsets.numel() - 1
+    dev = rows.device
+    contrib = contrib if contrib is not None else torch.empty(M * top_k, H, dtype=torch.float32, device=dev)
+    _call("bi_moe_scatter_contrib", _ptr(rows, torch.float32, "rows"), _ptr(offsets, torch.int32, "offsets", dev),
+          _ptr(perm, torch.int32, "perm", dev), _ptr(contrib, torch.float32, "contrib", dev), M, H, E, top_k,
+          _stream(stream))
     return contrib
 
 

@@ -23,10 +23,11 @@ bi_status launch_topk(const float *, int32_t *, float *, float *, int64_t, int64
                       cudaStream_t);
 size_t permute_scratch_bytes(int64_t M, int64_t E);
 bi_status launch_permute(const int32_t *, int32_t *, int32_t *, int64_t, int64_t, int32_t, void *,
-                         cudaStream_t);
+                         cudaStream_t, uint32_t *slot_mask);
 bi_status launch_gather(const void *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
                         int32_t, void *, cudaStream_t);
-bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, bool, cudaStream_t);
+bi_status launch_combine(const float *, void *, int64_t, int64_t, int32_t, bool, cudaStream_t,
+                         const uint32_t *slot_mask);
 bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const float *,
                          const void *, void *, int64_t, int64_t, int64_t, int32_t, int64_t,
                          cudaStream_t);
@@ -34,6 +35,10 @@ int set_gemm_variant(int v);
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
+bi_status launch_gather_routing(const int32_t *, const float *, const int32_t *, const int32_t *, int64_t,
+                                int64_t, int64_t, int32_t *, float *, cudaStream_t);
+bi_status launch_scatter_contrib(const float *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
+                                 float *, cudaStream_t);
 bi_status launch_wait_timeout_probe(cudaStream_t);
 
 // ------------------------------------------------------------ error state --
@@ -52,6 +57,7 @@ __device__ int g_device_error;
 constexpr int kMaxDevices = 64;
 static std::mutex g_mu;
 static int *g_err_ptr[kMaxDevices] = {};
+static ContextSetup g_err_ctx;
 static int g_sms[kMaxDevices] = {};
 
 static int current_device() {
@@ -60,13 +66,44 @@ static int current_device() {
   return d;
 }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // 0 stays "no context"
+}
+
 int *device_error_word() {
   const int d = current_device();
   if (d >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[d]) {
+  // the word's address belongs to the context the module is loaded in
+  if (!g_err_ptr[d] || g_err_ctx.pending(d)) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_ptr[d] = static_cast<int *>(p);
+    g_err_ptr[d] = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) {
+      g_err_ptr[d] = static_cast<int *>(p);
+      g_err_ctx.done(d);
+    }
   }
   return g_err_ptr[d];
 }
@@ -151,7 +188,7 @@ bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct MoeWorkspace {
-  size_t offsets, perm, scratch, xperm, act, contrib, total;
+  size_t offsets, perm, slot_mask, scratch, xperm, act, contrib, total;
 };
 
 static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
@@ -160,6 +197,7 @@ static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, i
   size_t off = 0;
   w.offsets = off; off += align256((E + 1) * sizeof(int32_t));
   w.perm = off;    off += align256(P * sizeof(int32_t));
+  w.slot_mask = off; off += align256(static_cast<size_t>(M) * sizeof(uint32_t));
   w.scratch = off; off += align256(permute_scratch_bytes(M, E));
   w.xperm = off;   off += align256(P * H * 2);
   w.act = off;     off += align256(P * I * 2);
@@ -298,7 +336,7 @@ BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w, co
   return launch_router_negctl(x, w, bias, y, M, K, N, reinterpret_cast<cudaStream_t>(stream));
 }
 
-BI_API bi_status bi_topk(const float *scores, int32_t *ids, float *wts, float *probs, int64_t M,
+BI_API bi_status bi_topk(const float *scores, float *probs, int32_t *ids, float *wts, int64_t M,
                          int64_t E, int32_t top_k, bi_stream_t stream) {
   BI_REQUIRE(M >= 0, BI_ERR_INVALID_ARG, "M < 0");
   BI_REQUIRE(E >= 1 && E <= 512, BI_ERR_UNSUPPORTED, "E=%lld outside [1, 512]", (long long)E);
@@ -403,7 +441,7 @@ BI_API bi_status bi_moe_permute(const int32_t *ids, int32_t *offsets, int32_t *p
   BI_REQUIRE(ids && perm && workspace, BI_ERR_INVALID_ARG, "null pointer");
   BI_REQUIRE(workspace_bytes >= bi_moe_permute_workspace_bytes(M, E), BI_ERR_WORKSPACE,
              "workspace %zu < %zu bytes", workspace_bytes, bi_moe_permute_workspace_bytes(M, E));
-  return launch_permute(ids, offsets, perm, M, E, top_k, workspace, s);
+  return launch_permute(ids, offsets, perm, M, E, top_k, workspace, s, nullptr);
 }
 
 BI_API bi_status bi_moe_gather(const bi_bf16 *x, const int32_t *offsets, const int32_t *perm,
@@ -455,7 +493,7 @@ BI_API bi_status bi_moe_combine(const float *contrib, bi_bf16 *out, int64_t M, i
   BI_REQUIRE(contrib && out, BI_ERR_INVALID_ARG, "null pointer");
   BI_REQUIRE(aligned(contrib, 16) && aligned(out, 8), BI_ERR_INVALID_ARG,
              "contrib must be 16-byte and out 8-byte aligned");
-  return launch_combine(contrib, out, M, H, top_k, false, reinterpret_cast<cudaStream_t>(stream));
+  return launch_combine(contrib, out, M, H, top_k, false, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M, int64_t H,
@@ -466,7 +504,37 @@ BI_API bi_status bi_moe_combine_consume(float *contrib, bi_bf16 *out, int64_t M,
   BI_REQUIRE(contrib && out, BI_ERR_INVALID_ARG, "null pointer");
   BI_REQUIRE(aligned(contrib, 16) && aligned(out, 8), BI_ERR_INVALID_ARG,
              "contrib must be 16-byte and out 8-byte aligned");
-  return launch_combine(contrib, out, M, H, top_k, true, reinterpret_cast<cudaStream_t>(stream));
+  return launch_combine(contrib, out, M, H, top_k, true, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+BI_API bi_status bi_moe_gather_routing(const int32_t *ids, const float *wts, const int32_t *offsets,
+                                       const int32_t *perm, int32_t *lid, float *pw, int64_t M, int64_t E,
+                                       int32_t top_k, int64_t experts_per_rank, bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && E >= 1 && E <= 1024, BI_ERR_INVALID_ARG, "bad sizes M=%lld E=%lld", (long long)M,
+             (long long)E);
+  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= E, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  BI_REQUIRE(experts_per_rank >= 1 && experts_per_rank <= E && E % experts_per_rank == 0, BI_ERR_INVALID_ARG,
+             "experts_per_rank=%lld must divide E=%lld", (long long)experts_per_rank, (long long)E);
+  BI_REQUIRE(M * top_k < (int64_t(1) << 31), BI_ERR_UNSUPPORTED, "M*top_k exceeds int32");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(ids && wts && offsets && perm && lid && pw, BI_ERR_INVALID_ARG, "null pointer");
+  return launch_gather_routing(ids, wts, offsets, perm, M * top_k, E, experts_per_rank, lid, pw,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+BI_API bi_status bi_moe_scatter_contrib(const float *rows, const int32_t *offsets, const int32_t *perm,
+                                        float *contrib, int64_t M, int64_t H, int64_t E, int32_t top_k,
+                                        bi_stream_t stream) {
+  BI_REQUIRE(M >= 0 && H > 0 && H % 4 == 0 && E >= 1 && E <= 1024, BI_ERR_INVALID_ARG,
+             "bad sizes (H %% 4 == 0 needed)");
+  BI_REQUIRE(top_k >= 1 && top_k <= 16, BI_ERR_INVALID_ARG, "top_k=%d", top_k);
+  BI_REQUIRE(M * top_k < (int64_t(1) << 31), BI_ERR_UNSUPPORTED, "M*top_k exceeds int32");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(rows && offsets && perm && contrib, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(rows, 16) && aligned(contrib, 16), BI_ERR_INVALID_ARG,
+             "rows and contrib must be 16-byte aligned");
+  return launch_scatter_contrib(rows, offsets, perm, M * top_k, H, E, contrib,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const float *wts,
@@ -489,14 +557,18 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
   void *xperm = ws + L.xperm;
   void *act = ws + L.act;
   float *contrib = reinterpret_cast<float *>(ws + L.contrib);
+  uint32_t *slot_mask = reinterpret_cast<uint32_t *>(ws + L.slot_mask);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t P = M * top_k;
-  if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s)) != BI_OK) return st;
+  if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s, slot_mask)) != BI_OK)
+    return st;
   if ((st = launch_gather(x, perm, offsets, P, H, E, top_k, xperm, s)) != BI_OK) return st;
   if ((st = launch_gate_up(xperm, offsets, perm, wts, w13, act, P, H, E, top_k, I, s)) != BI_OK)
     return st;
   if ((st = launch_down(act, offsets, perm, w2, contrib, P, H, E, top_k, I, s)) != BI_OK) return st;
-  return launch_combine(contrib, out, M, H, top_k, true, s);
+  // a pair skipped for a bad id (recorded in the device error word) adds
+  // nothing: the combine sums the slots the permutation marked valid
+  return launch_combine(contrib, out, M, H, top_k, true, s, slot_mask);
 }
 
 }  // extern "C"

@@ -26,6 +26,22 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 // Device error word of the current device (defined in api.cu).
 int *device_error_word();
 int num_sms();
+// Unique id of the CUDA context current on this host thread (cuCtxGetId: ids
+// are never reused within a process), or 0 when no context is current.
+// Facts that belong to a context -- device addresses of __device__ symbols,
+// per-function attributes such as the dynamic shared-memory limit -- are
+// cached under this id and redone when it changes (a cudaDeviceReset, or a
+// caller running in a context other than the device's primary one).
+unsigned long long current_context_id();
+// Per-device record of the context in which a one-time set-up was done.
+struct ContextSetup {
+  unsigned long long ctx[64] = {};
+  // true when `dev`'s set-up has not been done in the current context
+  bool pending(int dev) const { return dev >= 0 && dev < 64 && (ctx[dev] == 0 || ctx[dev] != current_context_id()); }
+  void done(int dev) {
+    if (dev >= 0 && dev < 64) ctx[dev] = current_context_id();
+  }
+};
 // Encode a 2-D bf16 TMA map over a row-major [rows, cols] tensor with a
 // [box_rows, 64]-element box and 128-byte swizzle.  Returns false on failure.
 bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,

@@ -600,6 +600,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   static std::mutex mu;
   static int max_units[64] = {};  // CTAs (or CTA pairs) resident at once, per device
+  static ContextSetup setup;      // the shared-memory attribute is per context
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) {
@@ -621,7 +622,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   }
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (max_units[dev] == 0) {
+    if (max_units[dev] == 0 || setup.pending(dev)) {
       cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) {
@@ -642,6 +643,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
         units = clusters;
       }
       max_units[dev] = units;
+      setup.done(dev);
     }
   }
   // upper bound on the number of tiles (token blocks per expert <= P/kBN + 1)

@@ -11,9 +11,12 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds kNoAllocScratchBytes of memory for it until the process exits.
 // Host code cannot use the array's name as a device address (on the host it is
-// only a stand-in symbol), so the device address is looked up once per device
-// with cudaGetSymbolAddress, with that device current, on the first call made
-// on that device.  Make that first call before any stream capture begins.
+// only a stand-in symbol), so the device address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call made on
+// that device -- and again on the first call after the current context
+// changes (a cudaDeviceReset, or a caller in a context other than the
+// device's primary one loads the module anew, possibly at another address).
+// Make the first call of each context before any stream capture begins.
 #include <mutex>
 
 #include "bimoe_internal.cuh"
@@ -31,9 +34,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 static std::mutex g_noalloc_mu;
 static void *g_noalloc_ptr[64] = {};
+static ContextSetup g_noalloc_ctx;
 
-// Device address of the scratch array on the current device (looked up once
-// per device).  Returns null and sets the error message on failure.
+// Device address of the scratch array in the current context of the current
+// device (looked up once per device and context).  Returns null and sets the
+// error message on failure.
 static void *noalloc_scratch() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -41,14 +46,17 @@ static void *noalloc_scratch() {
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx.pending(dev)) {
+    g_noalloc_ptr[dev] = nullptr;
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // do not leave the error for an unrelated later check
       set_error("bi_moe_forward_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
       return nullptr;
     }
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx.done(dev);
   }
   return g_noalloc_ptr[dev];
 }
@@ -60,10 +68,14 @@ extern "C" BI_API bi_status bi_moe_forward_noalloc(const bi_bf16 *x, const int32
                                                    const bi_bf16 *w2, bi_bf16 *out, int64_t M,
                                                    int64_t H, int64_t E, int32_t top_k, int64_t I,
                                                    bi_stream_t stream) {
-  if (M == 0) return bi_moe_forward(x, ids, wts, w13, w2, out, M, H, E, top_k, I, nullptr, 0, stream);
   const size_t need = bi_moe_workspace_bytes(M, H, E, top_k, I);
-  if (need == 0)  // invalid sizes: let the regular checks report them
-    return bi_moe_forward(x, ids, wts, w13, w2, out, M, H, E, top_k, I, nullptr, 0, stream);
+  if (need == 0) {
+    // invalid sizes (bi_moe_workspace_bytes is 0 only for those): the
+    // regular checks report them; nothing is launched
+    const bi_status st = bi_moe_forward(x, ids, wts, w13, w2, out, M, H, E, top_k, I, nullptr, 0, stream);
+    return st == BI_OK ? BI_ERR_INVALID_ARG : st;
+  }
+  if (M == 0) return BI_OK;  // valid sizes, nothing to do
   if (need > bimoe::kNoAllocScratchBytes) {
     bimoe::set_error(
         "bi_moe_forward_noalloc: these sizes need %zu bytes of scratch but the built-in array "

@@ -19,7 +19,10 @@
 //           tokens' bits, so positions never depend on thread timing.
 // A pair is skipped (and BI_DEVERR_* recorded) when its expert id is outside
 // [0,E) or repeats an earlier slot of the same row; the other pairs keep
-// their positions.
+// their positions.  When asked, the permutation also writes each token's mask
+// of valid slots (bit t set: slot t is a pair that the GEMMs compute), so the
+// layer's combine sums exactly the valid slots and a skipped pair adds
+// nothing.
 #include "bimoe_internal.cuh"
 
 namespace bimoe {
@@ -108,7 +111,8 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restric
 __global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *__restrict__ ids,
                                                                 int M, int E, int top_k,
                                                                 const int32_t *__restrict__ blkoff,
-                                                                int32_t *__restrict__ perm) {
+                                                                int32_t *__restrict__ perm,
+                                                                uint32_t *__restrict__ slot_mask) {
   griddep_wait();
   constexpr int W = kTokBlock / 32, WP = W + 1;  // odd pitch: conflict-free rank loads
   extern __shared__ uint32_t s_bits[];  // [E][WP]
@@ -122,8 +126,10 @@ __global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *_
       if (pair_ok(r, t, E, nullptr)) atomicOr(&s_bits[r[t] * WP + (lm >> 5)], 1u << (lm & 31));
   __syncthreads();
   if (m < M) {
+    uint32_t ok = 0u;
     for (int t = 0; t < top_k; ++t) {
       if (!pair_ok(r, t, E, nullptr)) continue;
+      ok |= 1u << t;
       const int e = r[t];
       int rank = 0;
       for (int w = 0; w < (lm >> 5); ++w) rank += __popc(s_bits[e * WP + w]);
@@ -131,6 +137,7 @@ __global__ void __launch_bounds__(kTokBlock) moe_scatter_kernel(const int32_t *_
       const int pos = blkoff[static_cast<size_t>(blockIdx.x) * E + e] + rank;
       perm[pos] = m * top_k + t;
     }
+    if (slot_mask) slot_mask[m] = ok;
   }
 }
 
@@ -162,7 +169,7 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *s_warp, int *tota
 
 __global__ void __launch_bounds__(kSmallPermuteMaxM) moe_permute_small_kernel(
     const int32_t *__restrict__ ids, int M, int E, int top_k, int32_t *__restrict__ offsets,
-    int32_t *__restrict__ perm, int *err) {
+    int32_t *__restrict__ perm, uint32_t *__restrict__ slot_mask, int *err) {
   griddep_wait_small_release();
   extern __shared__ int s_pm[];
   __shared__ int s_warp[32];
@@ -199,6 +206,7 @@ __global__ void __launch_bounds__(kSmallPermuteMaxM) moe_permute_small_kernel(
     run += s_cnt[e];
   }
   if (tid == 0) offsets[E] = total;
+  if (slot_mask && m < M) slot_mask[m] = ok;
   __syncthreads();
   for (int t = 0; t < top_k; ++t) {
     if (!((ok >> t) & 1u)) continue;
@@ -234,12 +242,62 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
   for (int c = lane; c < row_vec; c += 32) dst[c] = src[c];
 }
 
+// Expert-parallel dispatch: for every permuted position p < offsets[E],
+// lid[p] = ids[perm[p]] % experts_per_rank (the expert's index on the rank
+// that owns it) and pw[p] = wts[perm[p]]: the routing that travels with the
+// gathered token rows.  One thread per position.
+__global__ void __launch_bounds__(256) moe_gather_routing_kernel(
+    const int32_t *__restrict__ ids, const float *__restrict__ wts, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ perm, int E, int P, int experts_per_rank, int32_t *__restrict__ lid,
+    float *__restrict__ pw, int *err) {
+  griddep_wait_small_release();
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  const int npos = offsets[E];
+  if (p == 0 && (npos < 0 || npos > P)) report_error(err, BI_DEVERR_BAD_PERMUTATION);
+  if (p >= min(npos, P)) return;
+  const int pair = perm[p];
+  if (static_cast<unsigned>(pair) >= static_cast<unsigned>(P)) {
+    report_error(err, BI_DEVERR_BAD_PERMUTATION);
+    return;
+  }
+  const int e = ids[pair];
+  lid[p] = e >= 0 ? e % experts_per_rank : -1;
+  pw[p] = wts[pair];
+}
+
+// Expert-parallel return: contrib[perm[p], :] = rows[p, :] for p < offsets[E]
+// (the contributions computed on the experts' ranks, back in (token, slot)
+// order at the tokens' home rank).  One warp per position, 16-byte copies.
+__global__ void __launch_bounds__(256) moe_scatter_contrib_kernel(
+    const uint4 *__restrict__ rows, const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    int E, int P, int row_vec, uint4 *__restrict__ contrib, int *err) {
+  griddep_wait_small_release();
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int npos = offsets[E];
+  if (p == 0 && lane == 0 && (npos < 0 || npos > P)) report_error(err, BI_DEVERR_BAD_PERMUTATION);
+  if (p >= min(npos, P)) return;
+  const int pair = perm[p];
+  if (static_cast<unsigned>(pair) >= static_cast<unsigned>(P)) {
+    if (lane == 0) report_error(err, BI_DEVERR_BAD_PERMUTATION);
+    return;
+  }
+  const uint4 *src = rows + static_cast<size_t>(p) * row_vec;
+  uint4 *dst = contrib + static_cast<size_t>(pair) * row_vec;
+  for (int c = lane; c < row_vec; c += 32) dst[c] = src[c];
+}
+
 // out[m, h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) + c[m,k-1,h]), fp32 adds in
-// slot order; four consecutive h per thread.
+// slot order; four consecutive h per thread.  With a slot mask (the layer's
+// own permutation wrote it) only the valid slots are summed, in the same
+// order: the first valid contribution, then each later valid one added; a
+// token with no valid slot gets +0.  With every slot valid this is the same
+// sequence of adds as without a mask.
 template <bool CONSUME>
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
                                                           __nv_bfloat16 *__restrict__ out, int M,
-                                                          int H4, int top_k) {
+                                                          int H4, int top_k,
+                                                          const uint32_t *__restrict__ slot_mask) {
   griddep_wait_small_release();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool active = idx < static_cast<int64_t>(M) * H4;
@@ -247,9 +305,17 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restri
   const int h4 = static_cast<int>(idx % H4);
   const float4 *c = contrib + m * top_k * H4 + h4;
   if (active) {
-    float4 s = c[0];
-    for (int t = 1; t < top_k; ++t) {
+    const uint32_t valid = slot_mask ? slot_mask[m] : 0xffffffffu;
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    bool first = true;
+    for (int t = 0; t < top_k; ++t) {
+      if (!((valid >> t) & 1u)) continue;
       const float4 v = c[static_cast<int64_t>(t) * H4];
+      if (first) {
+        s = v;
+        first = false;
+        continue;
+      }
       s.x = __fadd_rn(s.x, v.x);
       s.y = __fadd_rn(s.y, v.y);
       s.z = __fadd_rn(s.z, v.z);
@@ -281,13 +347,14 @@ size_t permute_scratch_bytes(int64_t M, int64_t E) {
 }
 
 bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, int64_t M,
-                         int64_t E, int32_t top_k, void *scratch, cudaStream_t stream) {
+                         int64_t E, int32_t top_k, void *scratch, cudaStream_t stream,
+                         uint32_t *slot_mask) {
   if (M <= kSmallPermuteMaxM) {
     const int T = static_cast<int>((M + 255) / 256 * 256);
     const size_t smem = static_cast<size_t>(E) * (2 * sizeof(int) + (T / 32 + 1) * sizeof(uint32_t));
     if (smem <= 48 * 1024)
       return launch_chained(moe_permute_small_kernel, dim3(1), dim3(T), smem, stream, 1, ids, (int)M,
-                            (int)E, top_k, offsets, perm, device_error_word());
+                            (int)E, top_k, offsets, perm, slot_mask, device_error_word());
   }
   const int nblk = static_cast<int>((M + kTokBlock - 1) / kTokBlock);
   const size_t one = (static_cast<size_t>(nblk) * E * sizeof(int32_t) + 255) / 256 * 256;
@@ -303,7 +370,7 @@ bi_status launch_permute(const int32_t *ids, int32_t *offsets, int32_t *perm, in
     return st;
   return launch_chained(moe_scatter_kernel, dim3(nblk), dim3(kTokBlock),
                         E * (kTokBlock / 32 + 1) * sizeof(uint32_t), stream, 1, ids, (int)M, (int)E,
-                        top_k, blkoff, perm);
+                        top_k, blkoff, perm, slot_mask);
 }
 
 bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offsets, int64_t P,
@@ -314,17 +381,33 @@ bi_status launch_gather(const void *x, const int32_t *perm, const int32_t *offse
                         (int)(H / 8), static_cast<uint4 *>(xp), device_error_word());
 }
 
+bi_status launch_gather_routing(const int32_t *ids, const float *wts, const int32_t *offsets,
+                                const int32_t *perm, int64_t P, int64_t E, int64_t experts_per_rank,
+                                int32_t *lid, float *pw, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((P + 255) / 256);
+  return launch_chained(moe_gather_routing_kernel, dim3(blocks), dim3(256), 0, stream, 1, ids, wts, offsets,
+                        perm, (int)E, (int)P, (int)experts_per_rank, lid, pw, device_error_word());
+}
+
+bi_status launch_scatter_contrib(const float *rows, const int32_t *offsets, const int32_t *perm,
+                                 int64_t P, int64_t H, int64_t E, float *contrib, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((P + 7) / 8);
+  return launch_chained(moe_scatter_contrib_kernel, dim3(blocks), dim3(256), 0, stream, 1,
+                        reinterpret_cast<const uint4 *>(rows), offsets, perm, (int)E, (int)P, (int)(H / 4),
+                        reinterpret_cast<uint4 *>(contrib), device_error_word());
+}
+
 bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, int32_t top_k,
-                         bool consume, cudaStream_t stream) {
+                         bool consume, cudaStream_t stream, const uint32_t *slot_mask) {
   const int64_t total = M * (H / 4);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
   if (consume && H % 32 == 0 && reinterpret_cast<uintptr_t>(contrib) % 128 == 0)
     return launch_chained(moe_combine_kernel<true>, dim3(blocks), dim3(256), 0, stream, 1,
                           reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
-                          (int)M, (int)(H / 4), top_k);
+                          (int)M, (int)(H / 4), top_k, slot_mask);
   return launch_chained(moe_combine_kernel<false>, dim3(blocks), dim3(256), 0, stream, 1,
                         reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
-                        (int)M, (int)(H / 4), top_k);
+                        (int)M, (int)(H / 4), top_k, slot_mask);
 }
 
 }  // namespace bimoe

@@ -505,10 +505,10 @@ static bi_status launch_tiled_t(const XT *x, const float *w, const float *b, flo
                                 int64_t K, int64_t N, cudaStream_t stream) {
   using Cf = TiledCfg<TMR, TN, RB, CB, G, NSTG, XT>;
   static_assert(Cf::kSmem <= 227 * 1024, "shared memory");
-  static bool attr_done[64] = {};
+  static ContextSetup attr_done;  // the shared-memory attribute is per context
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (attr_done.pending(dev)) {
     if (cudaFuncSetAttribute(router_tiled_kernel<TMR, TN, RB, CB, G, NSTG, XT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cf::kSmem)) !=
         cudaSuccess) {
@@ -516,7 +516,7 @@ static bi_status launch_tiled_t(const XT *x, const float *w, const float *b, flo
       set_error("router tiled: cannot reserve %zu bytes of shared memory", Cf::kSmem);
       return BI_ERR_CUDA;
     }
-    attr_done[dev] = true;
+    attr_done.done(dev);
   }
   dim3 grid(static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM), static_cast<unsigned>((N + Cf::BN - 1) / Cf::BN));
   return launch_chained(router_tiled_kernel<TMR, TN, RB, CB, G, NSTG, XT>, grid, dim3(Cf::GT * G), Cf::kSmem,
@@ -777,10 +777,10 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   const int C = static_cast<int>(K / kSlice) / L;
   const size_t smem = static_cast<size_t>(L) * Cf::WARP_BYTES;
-  static bool attr_done[64] = {};
+  static ContextSetup attr_done;  // the shared-memory attribute is per context
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (attr_done.pending(dev)) {
     if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT, CK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess) {
@@ -788,7 +788,7 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
       set_error("router split: cannot reserve %zu bytes of shared memory", smem);
       return BI_ERR_CUDA;
     }
-    attr_done[dev] = true;
+    attr_done.done(dev);
   }
   dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
             static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
@@ -929,12 +929,12 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
     }
 #define BI_ROWS(R)                                                                                     \
   {                                                                                                    \
-    static bool attr[64] = {};                                                                         \
+    static ContextSetup attr;                                                                          \
     int dv = 0;                                                                                        \
     cudaGetDevice(&dv);                                                                                \
-    if (dv < 64 && !attr[dv]) {                                                                        \
+    if (attr.pending(dv)) {                                                                            \
       cudaFuncSetAttribute(router_rows_kernel<R, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100000); \
-      attr[dv] = true;                                                                                 \
+      attr.done(dv);                                                                                   \
     }                                                                                                  \
     const bi_status st_ = launch_chained(router_rows_kernel<R, XT>, grid, dim3(32), smem, stream, 1, x, w, \
                                          b, y, (int)M, (int)K, (int)N, device_error_word());          \
@@ -949,12 +949,12 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       set_error("router sliced schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    static bool attr[64] = {};
+    static ContextSetup attr;
     int dv = 0;
     cudaGetDevice(&dv);
-    if (dv < 64 && !attr[dv]) {
+    if (attr.pending(dv)) {
       cudaFuncSetAttribute(router_sliced_kernel<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      attr[dv] = true;
+      attr.done(dv);
     }
     const bi_status st = launch_chained(router_sliced_kernel<XT>, grid, dim3(256), smem, stream, 1, x, w, b,
                                         y, (int)M, (int)K, (int)N, device_error_word());

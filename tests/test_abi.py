@@ -122,8 +122,10 @@ def test_host_side_rejections(lib):
     # M == 0 is a no-op
     assert lib.bi_router_gemm(nul, nul, nul, nul, 0, 128, 256, nul) == 0
     # top_k > E, E too large
-    assert lib.bi_topk(fake, fake, fake, nul, 4, 8, 9, nul) == 1
-    assert lib.bi_topk(fake, fake, fake, nul, 4, 600, 8, nul) == 2
+    assert lib.bi_topk(fake, nul, fake, fake, 4, 8, 9, nul) == 1
+    assert lib.bi_topk(fake, nul, fake, fake, 4, 600, 8, nul) == 2
+    # null ids with M > 0 (probs may be NULL, ids and wts may not)
+    assert lib.bi_topk(fake, fake, nul, fake, 4, 256, 8, nul) == 1
     # MoE: workspace too small, unsupported H
     assert lib.bi_moe_forward(fake, fake, fake, fake, fake, fake, 4, 2048, 128, 8, 768,
                               fake, 1024, nul) == 3
@@ -135,6 +137,28 @@ def test_host_side_rejections(lib):
     assert lib.bi_moe_combine_consume(fake, fake, 4, 2046, 8, nul) == 1
     assert lib.bi_moe_combine_consume(fake, fake, 4, 2048, 17, nul) == 1
     assert lib.bi_moe_combine_consume(nul, nul, 0, 2048, 8, nul) == 0
+
+
+def test_moe_wrappers_check_shapes_first():
+    """The layer wrappers reject mismatched weight or routing shapes before
+    any pointer reaches the library (no GPU needed)."""
+    import torch
+    import invariant_moe_gb300 as bm
+    M, H, E, I, k = 4, 256, 8, 128, 2
+    x = torch.zeros(M, H, dtype=torch.bfloat16)
+    ids = torch.zeros(M, k, dtype=torch.int32)
+    wts = torch.zeros(M, k)
+    w13 = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16)
+    w2 = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    for fn in (bm.bi_moe_forward, bm.bi_moe_forward_noalloc):
+        with pytest.raises(ValueError, match="w13"):
+            fn(x, ids, wts, w13, torch.zeros(E, H, I + 128, dtype=torch.bfloat16))
+        with pytest.raises(ValueError, match="w13"):
+            fn(x, ids, wts, torch.zeros(E, 2 * I, H + 128, dtype=torch.bfloat16), w2)
+        with pytest.raises(ValueError, match="ids"):
+            fn(x, ids, torch.zeros(M, k + 1), w13, w2)
+        with pytest.raises(ValueError, match="ids"):
+            fn(x, ids[:2], wts[:2], w13, w2)
 
 
 def test_binding_rejects_cpu_tensors():
