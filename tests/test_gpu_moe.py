@@ -165,8 +165,15 @@ def test_gather_stage_exact(oracle_mod, cuda):
     assert torch.equal(xp.cpu(), x[torch.from_numpy(perm).long() // k])
 
 
+# P = M*k pairs; the automatic variant: narrow one-CTA tiles for P <= 16E,
+# else CTA pairs (I % 256 == 0), one CTA per tile (otherwise), interleaved
+# gate/up rows in CTA pairs for H >= 4096 and P >= 64E.  The last three
+# cases take the wide tiles: interleaved pairs at H=4096, plain pairs, and one
+# CTA per tile.
 @pytest.mark.parametrize("M,H,E,I,k,unit", [(64, 2048, 128, 768, 8, False), (37, 256, 8, 256, 2, True),
-                                            (1, 2048, 128, 768, 8, True), (300, 512, 4, 128, 1, True)])
+                                            (1, 2048, 128, 768, 8, True), (300, 512, 4, 128, 1, True),
+                                            (600, 4096, 8, 256, 1, True), (640, 1024, 8, 256, 1, True),
+                                            (640, 512, 4, 384, 1, True)])
 def test_gate_up_stage(oracle_mod, cuda, M, H, E, I, k, unit):
     import invariant_moe_gb300 as bm
     w, x, ids, wts = stage_inputs(M, H, E, I, k, seed=M + H, unit=unit)
@@ -181,8 +188,11 @@ def test_gate_up_stage(oracle_mod, cuda, M, H, E, I, k, unit):
     assert np.all(d <= 2.0 ** -8 * np.abs(ref) + 1e-3 * rms(ref)), f"max err {d.max():.3e}"
 
 
+# the last two cases take the wide tiles (P > 16E): CTA pairs (H % 256 == 0)
+# and one CTA per tile (H = 384)
 @pytest.mark.parametrize("M,H,E,I,k", [(64, 2048, 128, 768, 8), (37, 256, 8, 256, 2),
-                                       (1, 4096, 16, 2048, 8), (300, 512, 4, 128, 1)])
+                                       (1, 4096, 16, 2048, 8), (300, 512, 4, 128, 1),
+                                       (640, 512, 4, 256, 2), (640, 384, 4, 128, 2)])
 def test_down_stage(oracle_mod, cuda, M, H, E, I, k):
     import invariant_moe_gb300 as bm
     w = syn.moe_weights(H, E, I, seed=M + I, unit=True)
@@ -266,6 +276,34 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
             assert torch.equal(a, b), f"variant {v}"
 
 
+@pytest.mark.parametrize("M", [300, 4096])
+def test_gemm_variants_same_bits_dsv4(cuda, gemm_variant, M):
+    """The DSv4-shaped layer (H=4096, E=256, top-8, I=2048: K=4096 for
+    gate/up, the shape whose M=4096 batch takes the interleaved CTA pairs
+    automatically): every forced variant gives the automatic choice's bits
+    in act, the fp32 contributions and the layer output."""
+    import invariant_moe_gb300 as bm
+    H, E, I, k = DSV4["H"], DSV4["E"], DSV4["I"], DSV4["top_k"]
+    w = syn.moe_weights(H, E, I, seed=85, device="cuda")
+    x = syn.moe_tokens(M, H, seed=M + 86).to(cuda)
+    ids, wts = syn.random_routing(M, E, k, seed=M + 87)
+    ids, wts = ids.to(cuda), wts.to(cuda)
+    off, perm = bm.bi_moe_permute(ids, E)
+    xp = bm.bi_moe_gather(x, off, perm, k)
+    res = {}
+    for v in (0, 1, 2, 3, 4):
+        gemm_variant(v)
+        act = bm.bi_moe_gate_up(xp, off, perm, wts, w.w13, k)
+        contrib = bm.bi_moe_down(act, off, perm, w.w2, M, k)
+        out = bm.bi_moe_forward(x, ids, wts, w.w13, w.w2)
+        torch.cuda.synchronize()
+        res[v] = (act, contrib, out)
+    assert bm.device_error() == 0
+    for v in (1, 2, 3, 4):
+        for a, b, name in zip(res[0], res[v], ("act", "contrib", "out")):
+            assert torch.equal(a, b), f"variant {v}: {name} differs from the automatic choice"
+
+
 @pytest.mark.parametrize("M,H,E,I,k", [(40, 256, 8, 128, 2), (333, 512, 16, 384, 4), (1, 2048, 128, 768, 8)])
 def test_interleaved_gate_up_same_bits(cuda, gemm_variant, M, H, E, I, k):
     """The interleaved gate/up variant (any I % 128 == 0, including I=128 and
@@ -339,6 +377,43 @@ def test_forward_skewed_and_small_shapes(oracle_mod, cuda):
         torch.cuda.synchronize()
         ref = oracle_mod.moe(bits(x), ids.numpy(), wts.numpy(), bits(w.w13), bits(w.w2), E, I)
         check_layer(out.float().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("M", [40, 1500])
+def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
+    """A slot whose expert id is out of range, or repeats an earlier slot of
+    its row, is skipped (the device error word records it) and adds nothing:
+    the token's output is the sum over its valid slots, and a token with no
+    valid slot gets zeros.  M=40 takes the one-CTA permutation, M=1500 the
+    three-launch one; both write the mask of valid slots."""
+    import invariant_moe_gb300 as bm
+    H, E, I, k = 256, 8, 128, 4
+    w = syn.moe_weights(H, E, I, seed=M + 7, unit=True)
+    x = syn.moe_tokens(M, H, seed=M + 8, unit=True)
+    ids, wts = syn.random_routing(M, E, k, seed=M + 9)
+    bad = ids.clone()
+    bad[3, 1] = E + 2                 # out of range
+    bad[5, 2] = bad[5, 0]             # repeats slot 0
+    bad[7, :] = -1                    # no valid slot
+    bad[M - 1, 3] = 1 << 20           # out of range, last token
+    dropped = [(3, 1), (5, 2), (7, 0), (7, 1), (7, 2), (7, 3), (M - 1, 3)]
+    out = bm.bi_moe_forward(x.to(cuda), bad.to(cuda), wts.to(cuda), w.w13.to(cuda), w.w2.to(cuda))
+    torch.cuda.synchronize()
+    assert bm.device_error() in (1, 2)
+    # the oracle with the dropped slots given weight 0 (an fp64 product with
+    # 0 adds exactly 0) and a valid id
+    ids_o, wts_o = bad.numpy().copy(), wts.numpy().copy()
+    for m, t in dropped:
+        ids_o[m, t], wts_o[m, t] = 0, 0.0
+    ref = oracle_mod.moe(bits(x), ids_o, wts_o, bits(w.w13), bits(w.w2), E, I)
+    got = out.float().cpu().numpy()
+    check_layer(got, ref)
+    assert not got[7].any(), "a token with no valid slot must get zeros"
+    # tokens with every slot valid keep the bits of a call with clean ids
+    clean = bm.bi_moe_forward(x.to(cuda), ids.to(cuda), wts.to(cuda), w.w13.to(cuda), w.w2.to(cuda))
+    torch.cuda.synchronize()
+    keep = [m for m in range(M) if m not in (3, 5, 7, M - 1)]
+    assert torch.equal(out[keep], clean[keep])
 
 
 def test_forward_repeat_and_poisoned_workspace(cuda, qwen_w):
@@ -430,6 +505,36 @@ def test_layer_dsv4_sampled_parity(oracle_mod, cuda):
     ref = oracle_mod.moe(bits(xs[ok]), ids_c, wts_o[ok].astype(np.float32), bits(w13), bits(w2),
                          len(used), I)
     check_layer(out.float().cpu().numpy()[rows][ok], ref)
+
+
+def test_layer_dsv4_full_size_parity(oracle_mod, cuda):
+    """The largest configuration at its full batch: DSv4-router-shaped layer
+    (H=4096, E=256, top-8, I=2048), M=4096 tokens, unit scale so the stated
+    tolerance bites.  At this size the automatic choice runs the gate/up GEMM
+    as interleaved CTA pairs (K=4096) and the down GEMM as CTA pairs, the
+    permutation as three launches.  At least 16 sampled tokens are compared
+    element by element with the oracle's own end-to-end result (router in
+    fp64 from the host inputs, its own top-k, its own fp64 experts; each
+    token's oracle call gets only the experts it is routed to)."""
+    H, E, I, k, M = DSV4["H"], DSV4["E"], DSV4["I"], DSV4["top_k"], 4096
+    w = syn.moe_weights(H, E, I, seed=88, unit=True, device="cuda")
+    x = syn.moe_tokens(M, H, seed=89, unit=True)
+    out, scores, ids, wts = full_layer(x.to(cuda), w.w_router, w.w13, w.w2, k)
+    rows = torch.randperm(M, generator=syn.gen(90))[:24].numpy()
+    xs = x[rows]
+    r = oracle_mod.router(xs.float().numpy(), w.w_router.cpu().numpy())
+    assert np.all(np.abs(scores.cpu().numpy()[rows] - r) <= 2e-3 + 1e-4 * np.abs(r))
+    ids_o, wts_o = oracle_mod.topk(r.astype(np.float32), k)
+    ok = syn.unambiguous_rows(r, k)
+    assert len(ok) >= 16
+    assert np.array_equal(ids.cpu().numpy()[rows][ok], ids_o[ok])
+    got = out.float().cpu().numpy()[rows]
+    for j in ok:
+        used = np.asarray(ids_o[j], np.int64)
+        idx = torch.from_numpy(used).to(cuda)
+        ref = oracle_mod.moe(bits(xs[j:j + 1]), np.arange(k, dtype=np.int32)[None, :],
+                             wts_o[j:j + 1].astype(np.float32), bits(w.w13[idx]), bits(w.w2[idx]), k, I)
+        check_layer(got[j:j + 1], ref)
 
 
 @pytest.mark.slow

@@ -97,6 +97,35 @@ def test_negative_control_flips_bits(dev_inputs):
     assert torch.equal(run(x, w, b, 16), run(x, w, b, 17)[:16])
 
 
+def test_cublas_default_flips_row_bits(dev_inputs):
+    """The negative control on the default path: the library GEMM (cuBLAS
+    through torch.addmm, fp32, TF32 off) on this exact router shape picks its
+    reduction by M, so some row computed in a batch of M <= 256 differs in
+    bits from the same row computed in the M=4096 batch -- the failure the
+    GateLinear page's tests catch ("Tests": a negative control on the default
+    path that fails).  The batch-invariant router gives the same rows bit for
+    bit.  If cuBLAS on this image happens to pick an M-independent reduction
+    for every M tried, the control has nothing to show and the test skips."""
+    import invariant_moe_gb300 as bm
+    x, w, b = dev_inputs
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        full = torch.addmm(b, x, w.t())
+        changed = {}
+        for M in (1, 2, 8, 16, 32, 64, 128, 256):
+            part = torch.addmm(b, x[:M].contiguous(), w.t())
+            changed[M] = int((part.view(torch.int32) != full[:M].view(torch.int32)).any(dim=1).sum())
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    ours_full = run(x, w, b, 4096)
+    for M in changed:
+        assert torch.equal(run(x, w, b, M), ours_full[:M]), f"M={M}: the batch-invariant router flipped"
+    if not any(changed.values()):
+        pytest.skip(f"cuBLAS kept every row's bits for M <= 256 on this image: {changed}")
+    assert sum(changed.values()) >= 1, changed
+
+
 def test_exact_integer_case(oracle_mod, cuda):
     """x in multiples of 1/8, W and b in multiples of 1/64: every partial sum
     is exact in fp32, so GPU == oracle == integer sum, bit for bit."""
