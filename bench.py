@@ -4,10 +4,13 @@ One step = one pass of the whole hot path over one batch of M synthetic
 tokens: fp32 router GEMM on the bf16 tokens (read as their exact fp32
 values), sigmoid top-k, token permute and row gather, gate/up grouped GEMM
 with SwiGLU x probability, down grouped GEMM, slot-order combine.  Default
-workload: Qwen3-30B-A3B-shaped MoE layer (H=2048, E=128, top-8, I=768,
-router K=2048 N=128), M=4096 tokens per GPU per step, bf16
-weights/activations ~ N(0, 0.02), fp32 router.  The expert weights (1.2 GB)
-are larger than L2, so every step streams them from HBM (no explicit flush).
+workload: the largest configuration, the DSv4-router-shaped MoE layer
+(H=4096, E=256, top-8, I=2048, router K=4096 N=256), M=4096 tokens per GPU
+per step, bf16 weights/activations ~ N(0, 0.02), fp32 router.  The expert
+weights (12.9 GB) are far larger than L2, so every step streams them from
+HBM (no explicit flush).  The Qwen3-30B-A3B-shaped layer (H=2048, E=128,
+top-8, I=768) is timed as a secondary workload (--workload qwen makes it
+the headline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload qwen|dsv4] [--tokens M] [--no-extras]
@@ -146,6 +149,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our GPU arm --
 def measured_peaks():
+    """(HBM copy GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
@@ -154,11 +158,12 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def captured_traffic(kernel):
-    """DRAM bytes per launch of an expert GEMM from the committed ncu capture,
-    or None when the kernel source changed since the capture."""
+def captured_traffic(workload, M, kernel):
+    """DRAM bytes per full-size launch of an expert GEMM from the committed
+    ncu capture of this workload, or None when there is none or the kernel
+    source changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "moe_gemm_qwen4096_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"moe_gemm_{workload}_{M}_traffic.json")
     src = os.path.join(ROOT, "invariant_moe_gb300", "csrc", "moe_gemm.cu")
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
@@ -166,49 +171,156 @@ def captured_traffic(kernel):
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("kernel_source_sha256"):
         return None
     k = d.get(kernel, {})
-    return k.get("dram_read_bytes", 0) + k.get("dram_write_bytes", 0) or None
+    return k.get("dram_bytes_per_full_launch") or None
 
 
-def roofline_gate_up(args, M, H, E, I, k, gu_ms, dn_ms, hbm_gbs, tc_sust, peak_src):
-    """Roofline of the dominant kernel, the gate/up expert GEMM, against the
-    roof that binds it: its algorithmic bytes per launch (the touched experts'
-    W13, the gathered token rows read, the activations written) over the
-    measured copy bandwidth, or its flops over the sustained bf16 peak,
-    whichever floor is longer."""
+def layer_costs(M, H, E, I, k):
+    """Algorithmic bytes and flops of the method, per expert GEMM and for the
+    whole step.  'method' bytes are what the layer must move: the touched
+    experts' weights (E_t = E (1 - (1 - k/E)^M) experts), the tokens, the
+    routing (ids + wts) and the output; the router's fp32 weight and scores.
+    'impl' bytes are this implementation's workspace traffic (gathered token
+    rows, activations, fp32 per-slot contributions), reported apart."""
     P = M * k
     touched = E * (1.0 - (1.0 - k / E) ** M)
-    gu_bytes = touched * 2 * I * H * 2 + P * H * 2 + P * I * 2
-    gu_flops = 2.0 * P * 2 * I * H
-    dn_flops = 2.0 * P * H * I
-    t = gu_ms / 1e3
-    gbs, tfs = gu_bytes / t / 1e9, gu_flops / t / 1e12
-    hbm_bound = gu_bytes / (hbm_gbs * 1e9) >= gu_flops / (tc_sust * 1e12)
-    r = {"kernel": "moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)"}
+    w13, w2 = touched * 2 * I * H * 2, touched * H * I * 2
+    x = out = M * H * 2
+    routing = M * k * 8
+    router = E * H * 4 + M * E * 4
+    return {
+        "gate_up": {"method": w13 + x + routing, "impl": P * H * 2 + P * I * 2, "flops": 2.0 * P * 2 * I * H},
+        "down": {"method": w2 + out, "impl": P * I * 2 + P * H * 4, "flops": 2.0 * P * H * I},
+        "step": {"method": router + x + w13 + w2 + out + routing,
+                 "impl": P * H * 2 * 2 + P * I * 2 * 2 + P * H * 4 * 2,
+                 "flops": 2.0 * P * 3 * I * H, "fp32_flops": 2.0 * M * H * E},
+    }
+
+
+def roofline_entry(kernel, cost, ms, hbm_gbs, tc_burst, peak_src, traffic=None):
+    """Achieved method bytes (or flops) per launch over the launch's CUDA-event
+    time, against the roof that binds it: the measured copy bandwidth, or the
+    measured bf16 burst peak (these kernels run for at most milliseconds
+    inside a sub-second timed region), whichever floor is longer."""
+    t = ms / 1e3
+    gbs, tfs = cost["method"] / t / 1e9, cost["flops"] / t / 1e12
+    hbm_bound = cost["method"] / (hbm_gbs * 1e9) >= cost["flops"] / (tc_burst * 1e12)
+    r = {"kernel": kernel}
     if hbm_bound:
         r.update({"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
                   "peak_source": f"{peak_src} copy bandwidth"})
     else:
-        r.update({"bound": "tensor", "achieved": tfs, "peak": tc_sust, "unit": "TFLOP/s", "frac": tfs / tc_sust,
-                  "peak_source": f"{peak_src} bf16 sustained"})
+        r.update({"bound": "tensor", "achieved": tfs, "peak": tc_burst, "unit": "TFLOP/s",
+                  "frac": tfs / tc_burst, "peak_source": f"{peak_src} bf16 burst"})
     r.update({
-        "traffic": captured_traffic("gate_up") if args.workload == "qwen" and M == 4096 else None,
+        "traffic": traffic,
         "traffic_unit": "bytes per launch (ncu dram read+write)",
-        "algorithmic_bytes_per_launch": gu_bytes,
-        "algorithmic_flops_per_launch": gu_flops,
-        "tensor_tflops": tfs, "tensor_frac_of_sustained": tfs / tc_sust,
+        "algorithmic_bytes": cost["method"],
+        "implementation_bytes": cost["impl"],
+        "algorithmic_flops": cost["flops"],
         "hbm_gbs": gbs, "hbm_frac": gbs / hbm_gbs,
-        "ms_per_launch": gu_ms,
-        "down_ms_per_launch": dn_ms,
-        "down_tflops": dn_flops / (dn_ms / 1e3) / 1e12,
+        "tensor_tflops": tfs, "tensor_frac_of_burst": tfs / tc_burst,
+        "ms_per_launch": ms,
     })
     return r
+
+
+def setup_workload(wl, M, dev, x_seed):
+    """Weights (on the device), tokens and the step's buffers for one workload."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    from tests import synthetic as syn
+    H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
+    P = M * k
+    w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
+    lib = bm.load_library()
+    b = {
+        "w": w, "x": syn.moe_tokens(M, H, seed=x_seed, device=str(dev)),
+        "scores": torch.empty(M, E, dtype=torch.float32, device=dev),
+        "ids": torch.empty(M, k, dtype=torch.int32, device=dev),
+        "wts": torch.empty(M, k, dtype=torch.float32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "perm": torch.empty(P, dtype=torch.int32, device=dev),
+        "x_perm": torch.empty(P, H, dtype=torch.bfloat16, device=dev),
+        "act": torch.empty(P, I, dtype=torch.bfloat16, device=dev),
+        "contrib": torch.empty(P, H, dtype=torch.float32, device=dev),
+        "out": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+        "ws_perm": torch.empty(max(int(lib.bi_moe_permute_workspace_bytes(M, E)), 256),
+                               dtype=torch.uint8, device=dev),
+    }
+    return b
+
+
+def launches_per_step(M, E):
+    """Kernels one step launches: router + top-k (2), permutation (one CTA up
+    to 1024 tokens when its shared memory fits, else count / scan / scatter),
+    gather, gate/up, down, combine."""
+    small = M <= 1024 and E * (8 + ((M + 255) // 256 * 256 // 32 + 1) * 4) <= 48 * 1024
+    return 2 + (1 if small else 3) + 4
+
+
+def time_steps(wl, M, b, steps, warmup, world, stream, dev):
+    """Times `steps` steps of the whole hot path (device time, CUDA events on
+    the launching stream, barrier + synchronize on both sides) and the
+    gate/up and down GEMMs inside them.  Returns (seconds, gate/up ms, down
+    ms, clocks)."""
+    import torch
+
+    import invariant_moe_gb300 as bm
+    E, k = wl["E"], wl["top_k"]
+    w = b["w"]
+    ev = {"gate_up": [], "down": []}
+
+    def step(record=False):
+        # router on the bf16 tokens (read as fp32) and top-k selection
+        bm.bi_router_topk(b["x"], w.w_router, k, out=b["scores"], ids=b["ids"], wts=b["wts"])
+        bm.bi_moe_permute(b["ids"], E, offsets=b["offsets"], perm=b["perm"], workspace=b["ws_perm"])
+        bm.bi_moe_gather(b["x"], b["offsets"], b["perm"], k, x_perm=b["x_perm"])
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        bm.bi_moe_gate_up(b["x_perm"], b["offsets"], b["perm"], b["wts"], w.w13, k, act=b["act"])
+        if record:
+            e1.record(stream)
+        bm.bi_moe_down(b["act"], b["offsets"], b["perm"], w.w2, M, k, contrib=b["contrib"])
+        if record:
+            e2.record(stream)
+            ev["gate_up"].append((e0, e1))
+            ev["down"].append((e1, e2))
+        bm.bi_moe_combine_consume(b["contrib"], M, k, out=b["out"])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if bm.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(torch.cuda.current_device()).start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    if bm.device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    sec = t0.elapsed_time(t1) / 1e3
+    gu_ms = statistics.mean(a.elapsed_time(c) for a, c in ev["gate_up"])
+    dn_ms = statistics.mean(a.elapsed_time(c) for a, c in ev["down"])
+    return sec, gu_ms, dn_ms, clk
 
 
 def run_ours(args, rank, world, local):
     import torch
 
     import invariant_moe_gb300 as bm
-    from tests import synthetic as syn
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -216,73 +328,11 @@ def run_ours(args, rank, world, local):
     wl = WORKLOADS[args.workload]
     H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
     M = args.tokens
-    P = M * k
-
-    w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
-    x = syn.moe_tokens(M, H, seed=21 + rank, device=str(dev))
-    # step buffers (allocated once, reused)
-    scores = torch.empty(M, E, dtype=torch.float32, device=dev)
-    ids = torch.empty(M, k, dtype=torch.int32, device=dev)
-    wts = torch.empty(M, k, dtype=torch.float32, device=dev)
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(P, dtype=torch.int32, device=dev)
-    act = torch.empty(P, I, dtype=torch.bfloat16, device=dev)
-    contrib = torch.empty(P, H, dtype=torch.float32, device=dev)
-    out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-    lib = bm.load_library()
-    ws_perm = torch.empty(max(int(lib.bi_moe_permute_workspace_bytes(M, E)), 256), dtype=torch.uint8, device=dev)
-    x_perm = torch.empty(P, H, dtype=torch.bfloat16, device=dev)
+    b = setup_workload(wl, M, dev, x_seed=21 + rank)
+    w, x = b["w"], b["x"]
     stream = torch.cuda.current_stream(dev)
-    ev = {n: [] for n in ("gate_up", "down")}
-
-    def step(record=False):
-        # router on the bf16 tokens (read as fp32) and top-k selection
-        bm.bi_router_topk(x, w.w_router, k, out=scores, ids=ids, wts=wts)
-        bm.bi_moe_permute(ids, E, offsets=offsets, perm=perm, workspace=ws_perm)
-        bm.bi_moe_gather(x, offsets, perm, k, x_perm=x_perm)
-        if record:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e2 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        bm.bi_moe_gate_up(x_perm, offsets, perm, wts, w.w13, k, act=act)
-        if record:
-            e1.record(stream)
-        bm.bi_moe_down(act, offsets, perm, w.w2, M, k, contrib=contrib)
-        if record:
-            e2.record(stream)
-            ev["gate_up"].append((e0, e1))
-            ev["down"].append((e1, e2))
-        bm.bi_moe_combine_consume(contrib, M, k, out=out)
-
-    # router + top-k (2), permute (1 up to 1024 tokens, else 3; both bench
-    # workloads fit the one-CTA permutation's shared memory), gather, gate/up,
-    # down, combine
-    launches_per_step = 2 + (1 if M <= 1024 else 3) + 4
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if bm.device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-
-    clocks = ClockSampler(local).start()
-    time.sleep(0.3)  # let the sampler come up before the timed region
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clk = clocks.stop()
-    sec = t0.elapsed_time(t1) / 1e3
+    sec, gu_ms, dn_ms, clk = time_steps(wl, M, b, args.steps, args.warmup, world, stream, dev)
     sec_max = max_over_ranks(sec, world, dev)
-    gu_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["gate_up"])
-    dn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["down"])
 
     # ---- end to end through the public API from pinned host buffers.  Each
     # step uploads its tokens, runs the layer and downloads its output; the
@@ -303,21 +353,21 @@ def run_ours(args, rank, world, local):
     e2e_i = [0]
 
     def e2e_step():
-        b = e2e_i[0] % nbuf
+        i = e2e_i[0] % nbuf
         e2e_i[0] += 1
         with torch.cuda.stream(h2d_stream):
-            h2d_stream.wait_event(consumed[b])          # the layer that read x_dev[b] is done
-            x_dev[b].copy_(x_host[b], non_blocking=True)
-            uploaded[b].record(h2d_stream)
-        stream.wait_event(uploaded[b])
-        o, _, _, _ = bm.moe_layer(x_dev[b], w.w_router, w.w13, w.w2, k)
-        consumed[b].record(stream)
-        produced[b].record(stream)
+            h2d_stream.wait_event(consumed[i])          # the layer that read x_dev[i] is done
+            x_dev[i].copy_(x_host[i], non_blocking=True)
+            uploaded[i].record(h2d_stream)
+        stream.wait_event(uploaded[i])
+        o, _, _, _ = bm.moe_layer(x_dev[i], w.w_router, w.w13, w.w2, k)
+        consumed[i].record(stream)
+        produced[i].record(stream)
         with torch.cuda.stream(d2h_stream):
-            d2h_stream.wait_event(produced[b])
+            d2h_stream.wait_event(produced[i])
             o.record_stream(d2h_stream)
-            out_host[b].copy_(o, non_blocking=True)
-            downloaded[b].record(d2h_stream)
+            out_host[i].copy_(o, non_blocking=True)
+            downloaded[i].record(d2h_stream)
 
     for _ in range(3):
         e2e_step()
@@ -338,17 +388,48 @@ def run_ours(args, rank, world, local):
     if bm.device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
-    extras = {}
-    # the sweeps characterise one GPU: the N=1 run reports them, and a
-    # multi-GPU run does not hold the other GPUs idle while rank 0 sweeps
+    hbm, tc_burst, tc_sust, peak_src = measured_peaks()
+    costs = layer_costs(M, H, E, I, k)
+    rl_gu = roofline_entry("moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)",
+                           costs["gate_up"], gu_ms, hbm, tc_burst, peak_src,
+                           captured_traffic(args.workload, M, "gate_up"))
+    rl_dn = roofline_entry("moe_gemm_kernel<down> (tcgen05 grouped GEMM, fp32 per-slot contributions)",
+                           costs["down"], dn_ms, hbm, tc_burst, peak_src,
+                           captured_traffic(args.workload, M, "down"))
+    rl_step = roofline_entry("whole step (9 launches: router, top-k, permutation, gather, gate/up, down, "
+                             "combine)", costs["step"], sec_max / args.steps * 1e3, hbm, tc_burst, peak_src)
+
+    extras, summary = {}, {}
+    # the secondary workload and the sweeps characterise one GPU: the N=1
+    # run reports them, and a multi-GPU run does not hold the other GPUs idle
     if rank == 0 and world == 1 and not args.no_extras:
+        other = "qwen" if args.workload == "dsv4" else "dsv4"
+        del b, x_host, out_host, x_dev
+        torch.cuda.empty_cache()
+        wl2 = WORKLOADS[other]
+        b2 = setup_workload(wl2, M, dev, x_seed=21)
+        s2_steps = max(3, min(args.steps, 50))
+        sec2, gu2, dn2, clk2 = time_steps(wl2, M, b2, s2_steps, args.warmup, 1, stream, dev)
+        del b2
+        torch.cuda.empty_cache()
+        c2 = layer_costs(M, wl2["H"], wl2["E"], wl2["I"], wl2["top_k"])
+        extras["secondary_workload"] = {
+            "workload": wl2["name"], "tokens_per_gpu": M, "H": wl2["H"], "E": wl2["E"], "I": wl2["I"],
+            "top_k": wl2["top_k"], "steps": s2_steps, "ms_per_step": sec2 / s2_steps * 1e3,
+            "tokens_per_s": M * s2_steps / sec2, "clocks": clk2,
+            "roofline_gate_up": roofline_entry("gate/up", c2["gate_up"], gu2, hbm, tc_burst, peak_src,
+                                               captured_traffic(other, M, "gate_up")),
+            "roofline_down": roofline_entry("down", c2["down"], dn2, hbm, tc_burst, peak_src,
+                                            captured_traffic(other, M, "down")),
+        }
         extras["router_us_vs_M"] = router_sweep(dev)
         extras["moe_layer_us_vs_M"] = moe_sweep(dev, args.workload)
+        extras["moe_layer_us_vs_M_" + other] = moe_sweep(dev, other)
         extras["topk_window_us"] = topk_window_sweep(dev)
+        summary = summarize(extras, rl_gu, rl_dn, rl_step)
 
     if rank != 0:
         return None
-    hbm, tc_burst, tc_sust, peak_src = measured_peaks()
     line = {
         "metric": "BI MoE-layer tokens/s (whole hot path: router GEMM + top-k + fused experts)",
         "value": aggregate(M, args.steps, world, sec_max),
@@ -361,15 +442,48 @@ def run_ours(args, rank, world, local):
                    "router": f"fp32 [{M},{H}] x [{E},{H}]^T", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights %.2f GB streamed per step)"
                          % ((E * 3 * I * H * 2) / 1e9)},
-        "roofline": roofline_gate_up(args, M, H, E, I, k, gu_ms, dn_ms, hbm, tc_sust, peak_src),
+        "roofline": rl_gu,
+        "rooflines": {"gate_up": rl_gu, "down": rl_dn, "step": rl_step},
         "e2e": {"value": aggregate(M, e2e_steps, world, e2e_sec), "unit": "tokens/s",
                 "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
                 "steps": e2e_steps},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(M, E) * args.steps,
         "clocks": clk,
     }
     line.update(extras)
+    if summary:
+        line["summary"] = summary
     return line
+
+
+def summarize(extras, rl_gu, rl_dn, rl_step):
+    """A short digest of the line (kept last, where a truncated log still
+    shows it): kernel rooflines, router and layer time vs M, cuBLAS's row
+    flips on the router shape, the secondary workload."""
+    def rl(r):
+        return {"bound": r["bound"], "frac": round(r["frac"], 3), "achieved": round(r["achieved"], 1),
+                "unit": r["unit"], "ms": round(r["ms_per_launch"], 4),
+                "tensor_frac_of_burst": round(r["tensor_frac_of_burst"], 3)}
+    s = {"rooflines": {"gate_up": rl(rl_gu), "down": rl(rl_dn), "step": rl(rl_step)}}
+    r = extras.get("router_us_vs_M", {})
+    s["fp32_fma_peak_tflops"] = r.get("fp32_fma_peak_tflops_measured")
+    s["router_dsv4_warm_us_fp32frac"] = {m: [r[m]["warm_us"], r[m]["warm_fp32_frac"]]
+                                         for m in ("1", "8", "32", "64", "128", "1024", "4096") if m in r}
+    s["router_topk_fused_warm_us"] = {m: r[m].get("fused_router_topk_warm_us")
+                                      for m in ("1", "8", "64", "4096") if m in r}
+    s["cublas_fp32_rows_changed_vs_M4096"] = {m: r[m].get("cublas_fp32_rows_changed_vs_M4096")
+                                              for m in ("1", "8", "64", "128", "256", "1024") if m in r}
+    for key, v in extras.items():
+        if key.startswith("moe_layer_us_vs_M"):
+            s[key.replace("moe_layer_us_vs_M", "layer_cold_us_hbmfrac") or "layer"] = {
+                "workload": v.get("workload"),
+                **{m: [v[m]["cold_us"], v[m]["cold_hbm_frac"]] for m in ("1", "16", "256", "4096") if m in v}}
+    sec = extras.get("secondary_workload")
+    if sec:
+        s["secondary"] = {"workload": sec["workload"], "tokens_per_s": round(sec["tokens_per_s"]),
+                          "ms_per_step": round(sec["ms_per_step"], 4),
+                          "gate_up": rl(sec["roofline_gate_up"]), "down": rl(sec["roofline_down"])}
+    return s
 
 
 def fp32_fma_peak(dev):
@@ -700,32 +814,71 @@ def topk_window_sweep(dev, ns=(1, 8, 64), ks=(512, 1024, 2048), num_cols=8192):
 
 
 # ------------------------------------------------------ oracle (CPU) arm --
-def oracle_tokens(args, n_tokens, seed=21):
-    """Run the fp64 oracle on n_tokens of the workload; returns seconds."""
-    import oracle
-    from tests import synthetic as syn
-    wl = WORKLOADS[args.workload]
-    H, E, I, k = wl["H"], wl["E"], wl["I"], wl["top_k"]
-    if not hasattr(oracle_tokens, "_cache"):
-        oracle_tokens._cache = {}
-    key = args.workload
-    if key not in oracle_tokens._cache:
-        w = syn.moe_weights(H, E, I, seed=11)
-        oracle_tokens._cache[key] = (w.w_router.numpy(), syn.bf16_bits(w.w13), syn.bf16_bits(w.w2))
-    wr, w13, w2 = oracle_tokens._cache[key]
-    x = syn.moe_tokens(n_tokens, H, seed=seed)
-    xb = syn.bf16_bits(x)
-    t = time.perf_counter()
-    r = oracle.router(x.float().numpy(), wr)
-    ids, wts = oracle.topk(r.astype("float32"), k)
-    oracle.moe(xb, ids, wts.astype("float32"), w13, w2, E, I)
-    return time.perf_counter() - t
+class OracleSample:
+    """Times the fp64 oracle (router, top-k, experts; one host thread) on a
+    few tokens of a workload.  The weights are the bench's own, generated on
+    the GPU with the same seeds, when a GPU is present; the oracle receives
+    only the experts the sampled tokens are routed to (copied to the host
+    outside the timed part).  Without a GPU the router weight is drawn on
+    the host and each routed expert from its own seeded host stream: the same
+    shapes and distributions, other values."""
+
+    def __init__(self, workload, dev=None):
+        import oracle
+        from tests import synthetic as syn
+        oracle.build()
+        self.wl = WORKLOADS[workload]
+        H, E, I = self.wl["H"], self.wl["E"], self.wl["I"]
+        self.dev = dev
+        if dev is not None:
+            self.w = syn.moe_weights(H, E, I, seed=11, device=str(dev))
+            self.wr = self.w.w_router.cpu().numpy()
+        else:
+            self.w = None
+            self.wr = syn.normal((E, H), 0.02, 12).numpy()
+
+    def _experts(self, used):
+        """(w13 bits [n,2I,H], w2 bits [n,H,I]) of the experts in `used`."""
+        import numpy as np
+        import torch
+
+        from tests import synthetic as syn
+        H, I = self.wl["H"], self.wl["I"]
+        if self.w is not None:
+            idx = torch.from_numpy(np.asarray(used, np.int64)).to(self.w.w13.device)
+            return syn.bf16_bits(self.w.w13[idx]), syn.bf16_bits(self.w.w2[idx])
+        w13 = np.stack([syn.bf16_bits(syn.normal((2 * I, H), 0.02, 5000 + 2 * int(e), torch.bfloat16))
+                        for e in used])
+        w2 = np.stack([syn.bf16_bits(syn.normal((H, I), 0.02, 5001 + 2 * int(e), torch.bfloat16))
+                       for e in used])
+        return w13, w2
+
+    def run(self, n_tokens, seed):
+        """Seconds the oracle takes for n_tokens tokens (routing + experts)."""
+        import numpy as np
+
+        import oracle
+        from tests import synthetic as syn
+        H, I, k = self.wl["H"], self.wl["I"], self.wl["top_k"]
+        x = syn.moe_tokens(n_tokens, H, seed=seed)
+        xb = syn.bf16_bits(x)
+        t = time.perf_counter()
+        r = oracle.router(x.float().numpy(), self.wr)
+        ids, wts = oracle.topk(r.astype("float32"), k)
+        t_route = time.perf_counter() - t
+        used = np.unique(ids)
+        w13, w2 = self._experts(used)
+        remap = np.full(self.wl["E"], -1, np.int32)
+        remap[used] = np.arange(len(used), dtype=np.int32)
+        t = time.perf_counter()
+        oracle.moe(xb, remap[ids], wts.astype("float32"), w13, w2, len(used), I)
+        return t_route + time.perf_counter() - t
 
 
-def cpu_baseline(args, budget_s=12.0):
+def cpu_baseline(args, sampler, budget_s=12.0):
     n, total, tok = 2, 0.0, 0
     while total < budget_s:
-        total += oracle_tokens(args, n, seed=100 + tok)
+        total += sampler.run(n, seed=100 + tok)
         tok += n
     return {"value": tok / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{tok} tokens of the {WORKLOADS[args.workload]['name']} workload "
@@ -735,15 +888,21 @@ def cpu_baseline(args, budget_s=12.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    import oracle
-    oracle.build()
+    dev = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            dev = torch.device("cuda", 0)
+    except ImportError:
+        pass
+    sampler = OracleSample(args.workload, dev)
     wl = WORKLOADS[args.workload]
     per_step = 1  # tokens per step: a bounded sample of the workload
     for _ in range(args.warmup):
-        oracle_tokens(args, per_step)
+        sampler.run(per_step, seed=900)
     t = 0.0
     for s in range(args.steps):
-        t += oracle_tokens(args, per_step, seed=1000 + s)
+        t += sampler.run(per_step, seed=1000 + s)
     value = per_step * args.steps / t
     return {
         "impl": "reference",
@@ -765,8 +924,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=tuple(WORKLOADS), default="qwen")
+    ap.add_argument("--workload", choices=tuple(WORKLOADS), default="dsv4")
     ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the workload's expert count (a smaller case of the same "
+                         "tokens-per-expert load, for ncu captures that must stay small)")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router-sweep", action="store_true",
@@ -779,6 +941,11 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_env()
+    if args.experts is not None:
+        wl = dict(WORKLOADS[args.workload])
+        wl["E"] = args.experts
+        wl["name"] = f"{wl['name']}-E{args.experts}"
+        WORKLOADS[args.workload] = wl
     if args.router_sweep:
         import torch
         torch.cuda.set_device(local)
@@ -801,7 +968,11 @@ def main(argv=None):
         line = run_ours(args, rank, world, local)
         # the oracle's CPU baseline is timed at N=1 only
         if line is not None and world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args)
+            import torch
+            summary = line.pop("summary", None)
+            line["cpu_baseline"] = cpu_baseline(args, OracleSample(args.workload, torch.device("cuda", local)))
+            if summary is not None:
+                line["summary"] = summary
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:
