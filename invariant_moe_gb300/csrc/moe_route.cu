@@ -306,14 +306,18 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restri
   const float4 *c = contrib + m * top_k * H4 + h4;
   if (active) {
     const uint32_t valid = slot_mask ? slot_mask[m] : 0xffffffffu;
-    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    bool first = true;
-    for (int t = 0; t < top_k; ++t) {
-      if (!((valid >> t) & 1u)) continue;
+    // every slot's row is loaded whatever the mask says (a skipped slot's
+    // row holds stale but readable data and is not added), so the loads do
+    // not wait on the mask and issue back to back
+    float4 s = c[0];
+    bool any = (valid & 1u) != 0u;
+    if (!any) s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int t = 1; t < top_k; ++t) {
       const float4 v = c[static_cast<int64_t>(t) * H4];
-      if (first) {
+      if (!((valid >> t) & 1u)) continue;
+      if (!any) {
         s = v;
-        first = false;
+        any = true;
         continue;
       }
       s.x = __fadd_rn(s.x, v.x);

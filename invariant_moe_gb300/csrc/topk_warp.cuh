@@ -34,21 +34,20 @@ __device__ __forceinline__ float sigmoid_f32(float v) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-v)));
 }
 
-// Selects the top_k (<= 32) of srow[0..E) (E <= 32 * VPL) for one row, called
-// by all 32 lanes of a warp.  Writes ids_row[t], wts_row[t] = sigmoid(score)
-// for slots t < top_k and, if probs_row is non-null, sigmoid of every score.
-// L2 = true reads the scores with ld.global.cg (they were written by other
-// CTAs of the same launch); otherwise through the read-only path.
-template <int VPL, bool L2>
-__device__ __forceinline__ void topk_row_warp(const float *srow, int E, int top_k, int32_t *ids_row,
-                                              float *wts_row, float *probs_row, int lane) {
+// Selects the top_k (<= 32) of the row's E scores (E <= 32 * VPL), called by
+// all 32 lanes of a warp; load(j) returns score j.  Writes ids_row[t],
+// wts_row[t] = sigmoid(score) for slots t < top_k and, if probs_row is
+// non-null, sigmoid of every score.
+template <int VPL, typename Load>
+__device__ __forceinline__ void topk_select_warp(Load load, int E, int top_k, int32_t *ids_row,
+                                                 float *wts_row, float *probs_row, int lane) {
   int32_t key[VPL];
   uint32_t avail = 0;  // bit i: expert lane + 32 i exists and is not taken
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int j = lane + 32 * i;
     if (j < E) {
-      const float v = L2 ? __ldcg(srow + j) : __ldg(srow + j);
+      const float v = load(j);
       key[i] = score_key(v);
       avail |= 1u << i;
       if (probs_row) probs_row[j] = sigmoid_f32(v);
@@ -92,6 +91,17 @@ __device__ __forceinline__ void topk_row_warp(const float *srow, int E, int top_
     ids_row[lane] = my_id;
     wts_row[lane] = my_w;
   }
+}
+
+// The selection on a row srow[0..E) in global memory.  L2 = true reads the
+// scores with ld.global.cg (they were written by other CTAs of the same
+// launch or by the grid this one overlapped with); otherwise through the
+// read-only path.
+template <int VPL, bool L2>
+__device__ __forceinline__ void topk_row_warp(const float *srow, int E, int top_k, int32_t *ids_row,
+                                              float *wts_row, float *probs_row, int lane) {
+  topk_select_warp<VPL>([&](int j) { return L2 ? __ldcg(srow + j) : __ldg(srow + j); }, E, top_k, ids_row,
+                        wts_row, probs_row, lane);
 }
 
 // Calls topk_row_warp with the smallest VPL that holds E (E <= 512).

@@ -11,7 +11,10 @@ Tolerances.
     + 1e-6 rms.
   * whole layer: |out - ref| <= 1e-2 + 2e-2 |ref| per element (the stated
     bar) and, because that absolute term is loose at N(0, 0.02) scales,
-    max|out - ref| <= 2e-2 rms(ref) as well.
+    |out - ref| <= 2e-2 rms(ref) + 2^-8 |ref| per element as well: the rms
+    term is the scale-aware bar, the second term the output's own bf16
+    rounding (up to 2^-9 |ref|) plus that of the bf16 activations feeding
+    the down GEMM, which grow with the element, not with the rms.
 """
 import numpy as np
 import pytest
@@ -44,7 +47,8 @@ def check_layer(out, ref):
     d = np.abs(out - ref)
     ok = d <= 1e-2 + 2e-2 * np.abs(ref)
     assert ok.all(), f"{(~ok).sum()} outside rtol 2e-2 / atol 1e-2"
-    assert d.max() <= 2e-2 * rms(ref), f"max err {d.max():.3e} vs rms {rms(ref):.3e}"
+    ok = d <= 2e-2 * rms(ref) + 2.0 ** -8 * np.abs(ref)
+    assert ok.all(), f"{(~ok).sum()} outside 2e-2 rms + 2^-8 |ref|: max err {d.max():.3e} vs rms {rms(ref):.3e}"
 
 
 # ------------------------------------------------------------------ stages --
