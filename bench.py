@@ -469,8 +469,9 @@ def summarize(extras, rl_gu, rl_dn, rl_step):
     s["fp32_fma_peak_tflops"] = r.get("fp32_fma_peak_tflops_measured")
     s["router_dsv4_warm_us_fp32frac"] = {m: [r[m]["warm_us"], r[m]["warm_fp32_frac"]]
                                          for m in ("1", "8", "32", "64", "128", "1024", "4096") if m in r}
-    s["router_topk_fused_warm_us"] = {m: r[m].get("fused_router_topk_warm_us")
-                                      for m in ("1", "8", "64", "4096") if m in r}
+    s["router_topk_warm_us"] = {m: [r[m].get("fused_router_topk_warm_us"),
+                                    r[m].get("chained_router_topk_warm_us")]
+                                for m in ("1", "2", "4", "8", "64", "4096") if m in r}
     s["cublas_fp32_rows_changed_vs_M4096"] = {m: r[m].get("cublas_fp32_rows_changed_vs_M4096")
                                               for m in ("1", "8", "64", "128", "256", "1024") if m in r}
     for key, v in extras.items():
@@ -622,6 +623,19 @@ def router_sweep(dev, Ms=(1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 
         res[str(M)]["schedule_warm_us"] = sched
         res[str(M)]["router_plus_topk_warm_us"] = round(graph_time(two_calls) / n, 2)
         res[str(M)]["fused_router_topk_warm_us"] = round(graph_time(fused_calls) / n, 2)
+        if M <= 4:
+            # the one-kernel path forced (the automatic choice at these M),
+            # and the router grid chained with the selection grid
+            def one_kernel_calls():
+                for _ in range(n):
+                    bm.bi_router_topk(xm, w, 8, bias=b, out=y, schedule=10, stream=stream)
+
+            def chained_calls():
+                for _ in range(n):
+                    bm.bi_router_topk(xm, w, 8, bias=b, out=y, schedule=1 if M <= 2 else 4, stream=stream)
+
+            res[str(M)]["one_kernel_router_topk_warm_us"] = round(graph_time(one_kernel_calls) / n, 2)
+            res[str(M)]["chained_router_topk_warm_us"] = round(graph_time(chained_calls) / n, 2)
         # the library default on the same shape: cuBLAS through torch.matmul,
         # fp32 and TF32, with the rows whose bits differ from the same rows
         # computed in the M=4096 batch (ours: none, by construction)

@@ -174,15 +174,21 @@ BI_API bi_status bi_topk_window(const float *scores, int64_t ld,
 /*
  * bi_router_topk -- bi_router_gemm followed by bi_topk on its scores, as one
  * call for the decode path.  The scores y are exactly bi_router_gemm's (same
- * recipe, same bits) and ids / wts / probs exactly bi_topk's on y.  The
- * selection grid is launched as a programmatic dependent of the router grid
- * (programmatic stream serialization): its launch overlaps the router's run
- * and it waits in hardware (griddepcontrol.wait) for the router's completion
- * before reading y, which saves the launch gap between the two.  The pages
- * keep the router ("[BI][DSv4] Batch-invariant GateLinear router with fp32
- * persistent matmul", whose Perf table puts the decode-size router cost in
- * microseconds per layer) and the selection as separate ops; they have no
- * combined counterpart.
+ * recipe, same bits) and ids / wts / probs exactly bi_topk's on y.
+ * Up to 4 rows (N a multiple of 16 up to 256, K a multiple of 512) the call
+ * is ONE kernel: a thread-block cluster of N/16 CTAs owns all N scores of the
+ * rows (CTA c computes columns 16c..16c+15 with the same per-element recipe),
+ * and after a cluster barrier one warp per row selects from the scores in the
+ * cluster's shared memory, so no score goes through global memory before the
+ * selection.  If that cluster cannot be scheduled on the device, or for
+ * other shapes and larger batches, the selection grid is launched as a
+ * programmatic dependent of the router grid (programmatic stream
+ * serialization: it waits in hardware for the router's completion before
+ * reading y).  Both give the same bits.  The pages keep the router
+ * ("[BI][DSv4] Batch-invariant GateLinear router with fp32 persistent
+ * matmul", whose Perf table puts the decode-size router cost in microseconds
+ * per layer) and the selection as separate ops; they have no combined
+ * counterpart.
  *   x, w, bias, y, M, K, N  as bi_router_gemm (N <= 512);
  *   probs, ids, wts, top_k  as bi_topk on y (top_k <= min(16, N)).
  * Errors as bi_router_gemm / bi_topk.  Stream-ordered, graph-capturable.
@@ -459,14 +465,22 @@ BI_API bi_status bi_router_gemm_splitk_negctl(const float *x, const float *w,
                                               bi_stream_t stream);
 
 /*
- * bi_router_topk_schedule -- test hook: bi_router_topk with the router
- * schedule forced as in bi_router_gemm_schedule.
+ * bi_router_topk_schedule -- test hook: bi_router_topk with the path forced:
+ * 0 automatic, 1..9 the router schedule of bi_router_gemm_schedule followed
+ * by the selection grid, 10 the one-kernel cluster path (BI_ERR_UNSUPPORTED
+ * for a shape it does not take, M > 4, or a cluster the device cannot
+ * schedule).  bi_router_topk_bf16_schedule: the same for bf16 x.
  */
 BI_API bi_status bi_router_topk_schedule(const float *x, const float *w,
                                          const float *bias, float *y, float *probs,
                                          int32_t *ids, float *wts, int64_t M, int64_t K,
                                          int64_t N, int32_t top_k, int32_t schedule,
                                          bi_stream_t stream);
+BI_API bi_status bi_router_topk_bf16_schedule(const bi_bf16 *x, const float *w,
+                                              const float *bias, float *y, float *probs,
+                                              int32_t *ids, float *wts, int64_t M, int64_t K,
+                                              int64_t N, int32_t top_k, int32_t schedule,
+                                              bi_stream_t stream);
 
 /*
  * bi_moe_gemm_variant -- selects how the expert GEMMs (bi_moe_gate_up,

@@ -36,7 +36,7 @@ EXPORTS = [
     "bi_moe_gate_up", "bi_moe_down", "bi_moe_combine", "bi_moe_combine_consume", "bi_moe_forward_noalloc",
     "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
-    "bi_moe_gather_routing", "bi_moe_scatter_contrib",
+    "bi_moe_gather_routing", "bi_moe_scatter_contrib", "bi_router_topk_bf16_schedule",
 ]
 
 
@@ -89,6 +89,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_router_gemm_bf16": ([P, P, P, P, I64, I64, I64, P], ST),
             "bi_router_gemm_bf16_schedule": ([P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_bf16": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
+            "bi_router_topk_bf16_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
             "bi_wait_timeout_probe": ([P], ST),
@@ -360,8 +361,9 @@ def bi_moe_combine_consume(contrib, M, top_k, out=None, stream=None):
 
 def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=0, stream=None,
                    ids=None, wts=None):
-    """Router scores and top-k selection in one call (the selection grid is a
-    programmatic dependent of the router grid).  Returns
+    """Router scores and top-k selection in one call (up to 4 rows one
+    kernel, else the selection grid as a programmatic dependent of the router
+    grid; schedule 10 forces the one kernel, 1..9 a router schedule).  Returns
     (scores [M,N] fp32, ids [M,top_k] int32, wts [M,top_k] fp32, probs or None)."""
     M, K = x.shape
     N = w.shape[0]
@@ -376,9 +378,8 @@ def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=
             _ptr(y, torch.float32, "out", dev), _ptr(probs, torch.float32, "probs", dev),
             _ptr(ids, torch.int32, "ids", dev), _ptr(wts, torch.float32, "wts", dev))
     if x.dtype == torch.bfloat16:
-        if schedule:
-            raise ValueError("bf16 x takes the automatic router schedule")
-        _call("bi_router_topk_bf16", _ptr(x, torch.bfloat16, "x"), *ptrs, M, K, N, top_k, _stream(stream))
+        _call("bi_router_topk_bf16_schedule", _ptr(x, torch.bfloat16, "x"), *ptrs, M, K, N, top_k, schedule,
+              _stream(stream))
     else:
         _call("bi_router_topk_schedule", _ptr(x, torch.float32, "x"), *ptrs, M, K, N, top_k, schedule,
               _stream(stream))

@@ -35,6 +35,14 @@ int set_gemm_variant(int v);
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
+bool router_topk_fused_supported(int64_t M, int64_t K, int64_t N, int32_t top_k);
+template <typename XT>
+bi_status launch_router_topk_fused(const XT *, const float *, const float *, float *, float *, int32_t *,
+                                   float *, int64_t, int64_t, int64_t, int32_t, cudaStream_t);
+// Batches up to this many rows take the one-kernel router + top-k (when its
+// cluster can be scheduled); larger ones the router grid and the selection
+// grid.  Both give the same bits.
+constexpr int64_t kFusedRouterTopkMaxM = 4;
 bi_status launch_gather_routing(const int32_t *, const float *, const int32_t *, const int32_t *, int64_t,
                                 int64_t, int64_t, int32_t *, float *, cudaStream_t);
 bi_status launch_scatter_contrib(const float *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
@@ -348,21 +356,58 @@ BI_API bi_status bi_topk(const float *scores, float *probs, int32_t *ids, float 
   return launch_topk(scores, ids, wts, probs, M, E, top_k, reinterpret_cast<cudaStream_t>(stream));
 }
 
-BI_API bi_status bi_router_topk_schedule(const float *x, const float *w, const float *bias,
-                                         float *y, float *probs, int32_t *ids, float *wts,
-                                         int64_t M, int64_t K, int64_t N, int32_t top_k,
-                                         int32_t schedule, bi_stream_t stream) {
+}  // extern "C"
+
+static bi_status launch_router_any(const float *x, const float *w, const float *b, float *y, int64_t M,
+                                   int64_t K, int64_t N, int schedule, cudaStream_t s) {
+  return launch_router(x, w, b, y, M, K, N, schedule, s);
+}
+static bi_status launch_router_any(const __nv_bfloat16 *x, const float *w, const float *b, float *y,
+                                   int64_t M, int64_t K, int64_t N, int schedule, cudaStream_t s) {
+  return launch_router_bf16(x, w, b, y, M, K, N, schedule, s);
+}
+
+// Router + selection: schedule 0 picks by M (the one-kernel path for small
+// batches, else the router grid chained with the selection grid), 10 forces
+// the one-kernel path, 1..9 force a router schedule followed by the selection
+// grid.
+template <typename XT>
+static bi_status router_topk_impl(const XT *x, const float *w, const float *bias, float *y, float *probs,
+                                  int32_t *ids, float *wts, int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                  int32_t schedule, bi_stream_t stream) {
   bi_status st = router_checks(x, w, y, M, K, N);
   if (st != BI_OK) return st;
-  BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
+  BI_REQUIRE(schedule >= 0 && schedule <= 10, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   BI_REQUIRE(N <= 512, BI_ERR_UNSUPPORTED, "selection needs N <= 512 (N=%lld)", (long long)N);
   BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= N, BI_ERR_INVALID_ARG,
              "top_k=%d outside [1, min(16, N)]", top_k);
   if (M == 0) return BI_OK;
   BI_REQUIRE(ids && wts, BI_ERR_INVALID_ARG, "null pointer");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_router(x, w, bias, y, M, K, N, schedule, s)) != BI_OK) return st;
+  if (schedule == 10) return launch_router_topk_fused(x, w, bias, y, probs, ids, wts, M, K, N, top_k, s);
+  if (schedule == 0 && M <= kFusedRouterTopkMaxM && router_topk_fused_supported(M, K, N, top_k)) {
+    st = launch_router_topk_fused(x, w, bias, y, probs, ids, wts, M, K, N, top_k, s);
+    if (st != BI_ERR_UNSUPPORTED) return st;  // else its cluster cannot be scheduled: two grids
+  }
+  if ((st = launch_router_any(x, w, bias, y, M, K, N, schedule, s)) != BI_OK) return st;
   return launch_topk(y, ids, wts, probs, M, N, top_k, s);
+}
+
+extern "C" {
+
+BI_API bi_status bi_router_topk_schedule(const float *x, const float *w, const float *bias,
+                                         float *y, float *probs, int32_t *ids, float *wts,
+                                         int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                         int32_t schedule, bi_stream_t stream) {
+  return router_topk_impl(x, w, bias, y, probs, ids, wts, M, K, N, top_k, schedule, stream);
+}
+
+BI_API bi_status bi_router_topk_bf16_schedule(const bi_bf16 *x, const float *w, const float *bias,
+                                              float *y, float *probs, int32_t *ids, float *wts,
+                                              int64_t M, int64_t K, int64_t N, int32_t top_k,
+                                              int32_t schedule, bi_stream_t stream) {
+  return router_topk_impl(reinterpret_cast<const __nv_bfloat16 *>(x), w, bias, y, probs, ids, wts, M, K, N,
+                          top_k, schedule, stream);
 }
 
 BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bias, float *y,
@@ -374,16 +419,7 @@ BI_API bi_status bi_router_topk(const float *x, const float *w, const float *bia
 BI_API bi_status bi_router_topk_bf16(const bi_bf16 *x, const float *w, const float *bias, float *y,
                                      float *probs, int32_t *ids, float *wts, int64_t M, int64_t K,
                                      int64_t N, int32_t top_k, bi_stream_t stream) {
-  bi_status st = router_checks(x, w, y, M, K, N);
-  if (st != BI_OK) return st;
-  BI_REQUIRE(N <= 512, BI_ERR_UNSUPPORTED, "selection needs N <= 512 (N=%lld)", (long long)N);
-  BI_REQUIRE(top_k >= 1 && top_k <= 16 && top_k <= N, BI_ERR_INVALID_ARG,
-             "top_k=%d outside [1, min(16, N)]", top_k);
-  if (M == 0) return BI_OK;
-  BI_REQUIRE(ids && wts, BI_ERR_INVALID_ARG, "null pointer");
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_router_bf16(x, w, bias, y, M, K, N, 0, s)) != BI_OK) return st;
-  return launch_topk(y, ids, wts, probs, M, N, top_k, s);
+  return bi_router_topk_bf16_schedule(x, w, bias, y, probs, ids, wts, M, K, N, top_k, 0, stream);
 }
 
 BI_API bi_status bi_topk_window(const float *scores, int64_t ld, const int64_t *row_start,

@@ -1,7 +1,9 @@
 """Router + top-k in one call (bi_router_topk) on the GPU.
 
-The selection grid runs as a programmatic dependent of the router grid; the
-call must reproduce the two separate calls bit for bit: the same scores as
+Up to 4 rows the call is one kernel (a cluster owns all N scores and selects
+from distributed shared memory; schedule 10 forces it); beyond that the
+selection grid runs as a programmatic dependent of the router grid.  Either
+way the call must reproduce the two separate calls bit for bit: the same scores as
 bi_router_gemm under every schedule, and the same ids, wts and probs as
 bi_topk on those scores (which a missed dependency would break).  Against the oracle it is pinned through
 that equality plus a direct check of the selection on rows without near-ties,
@@ -60,6 +62,71 @@ def test_fused_equals_two_launch_qwen_shape(cuda, k):
         y2, i2, w2, _ = bm.bi_router_topk(xm, w, k, schedule=sched)
         torch.cuda.synchronize()
         assert torch.equal(y1, y2) and torch.equal(i1, i2) and torch.equal(w1, w2), f"M={M}"
+
+
+@pytest.mark.parametrize("shape", ["dsv4", "qwen", "n64"])
+@pytest.mark.parametrize("xdtype", [torch.float32, torch.bfloat16])
+def test_one_kernel_equals_two_launch(cuda, shape, xdtype):
+    """The one-kernel path (forced: schedule 10) against bi_router_gemm +
+    bi_topk: scores, ids, wts and probs bit for bit, for every batch size it
+    takes (1..4), fp32 and bf16 tokens, with and without bias, top_k 1..16,
+    and the cluster sizes 16 (N=256), 8 (N=128) and 4 (N=64)."""
+    import invariant_moe_gb300 as bm
+    K, N = {"dsv4": (4096, 256), "qwen": (2048, 128), "n64": (1536, 64)}[shape]
+    g = syn.gen(81 + N)
+    x = torch.randn(4, K, generator=g).to(xdtype).to(cuda)
+    w = (torch.randn(N, K, generator=g) / K ** 0.5).to(cuda)
+    b = (torch.randn(N, generator=g) * 0.01).to(cuda)
+    for M in (1, 2, 3, 4):
+        for bias in (b, None):
+            for k in (1, 8, 16):
+                xm = x[:M].contiguous()
+                y1 = bm.bi_router_gemm(xm, w, bias)
+                i1, w1, p1 = bm.bi_topk(y1, k, want_probs=True)
+                y2, i2, w2, p2 = bm.bi_router_topk(xm, w, k, bias=bias, want_probs=True, schedule=10)
+                torch.cuda.synchronize()
+                tag = f"{shape} M={M} k={k} bias={bias is not None} x={xdtype}"
+                assert torch.equal(y1, y2), "scores " + tag
+                assert torch.equal(i1, i2), "ids " + tag
+                assert torch.equal(w1, w2), "wts " + tag
+                assert torch.equal(p1, p2), "probs " + tag
+    assert bm.device_error() == 0
+
+
+def test_one_kernel_ties_and_rows(cuda):
+    """Exact plateaus (duplicated W rows, x on multiples of 1/8) through the
+    one-kernel path: the same ids as the separate selection, and each row's
+    result is the same alone or beside up to three other rows."""
+    import invariant_moe_gb300 as bm
+    inp, rows = syn.router_tie_inputs(M=64)
+    x, w, b = inp.x.to(cuda), inp.w.to(cuda), inp.b.to(cuda)
+    tied = torch.nonzero(rows).flatten()[:4].tolist() + [0, 1, 2, 3]
+    for r0 in tied:
+        alone = bm.bi_router_topk(x[r0:r0 + 1].contiguous(), w, 8, bias=b, schedule=10)
+        y1 = bm.bi_router_gemm(x[r0:r0 + 1].contiguous(), w, b)
+        i1, w1, _ = bm.bi_topk(y1, 8)
+        torch.cuda.synchronize()
+        assert torch.equal(alone[1], i1) and torch.equal(alone[2], w1)
+        for M in (2, 3, 4):
+            xb = x[60 - M:60].clone()
+            xb[M - 1] = x[r0]
+            got = bm.bi_router_topk(xb, w, 8, bias=b, schedule=10)
+            torch.cuda.synchronize()
+            for t in range(3):
+                assert torch.equal(got[t][M - 1], alone[t][0]), f"row {r0} beside {M - 1} others"
+
+
+def test_one_kernel_rejects_shapes_it_does_not_take(cuda):
+    """Schedule 10 on a shape the one-kernel path does not take is an error,
+    not a silent fallback: N not a multiple of 16, more than 4 rows, K not a
+    multiple of 512."""
+    import invariant_moe_gb300 as bm
+    g = syn.gen(5)
+    for M, K, N in ((1, 4096, 200), (5, 4096, 256), (2, 640, 128)):
+        x = torch.randn(M, K, generator=g).to(cuda)
+        w = torch.randn(N, K, generator=g).to(cuda)
+        with pytest.raises(RuntimeError, match="BI_ERR_UNSUPPORTED"):
+            bm.bi_router_topk(x, w, 8, schedule=10)
 
 
 def test_fused_ties_and_invariance(cuda):
