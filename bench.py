@@ -174,7 +174,7 @@ def captured_traffic(workload, M, kernel):
     return k.get("dram_bytes_per_full_launch") or None
 
 
-def layer_costs(M, H, E, I, k):
+def layer_costs(M, H, E, I, k, feed="copy"):
     """Algorithmic bytes and flops of the method, per expert GEMM and for the
     whole step.  'method' bytes are what the layer must move: the touched
     experts' weights (E_t = E (1 - (1 - k/E)^M) experts), the tokens, the
@@ -187,11 +187,12 @@ def layer_costs(M, H, E, I, k):
     x = out = M * H * 2
     routing = M * k * 8
     router = E * H * 4 + M * E * 4
+    xperm = P * H * 2 if feed == "copy" else 0   # the gathered copy, written and read back
     return {
-        "gate_up": {"method": w13 + x + routing, "impl": P * H * 2 + P * I * 2, "flops": 2.0 * P * 2 * I * H},
+        "gate_up": {"method": w13 + x + routing, "impl": xperm + P * I * 2, "flops": 2.0 * P * 2 * I * H},
         "down": {"method": w2 + out, "impl": P * I * 2 + P * H * 4, "flops": 2.0 * P * H * I},
         "step": {"method": router + x + w13 + w2 + out + routing,
-                 "impl": P * H * 2 * 2 + P * I * 2 * 2 + P * H * 4 * 2,
+                 "impl": 2 * xperm + P * I * 2 * 2 + P * H * 4 * 2,
                  "flops": 2.0 * P * 3 * I * H, "fp32_flops": 2.0 * M * H * E},
     }
 
@@ -251,15 +252,15 @@ def setup_workload(wl, M, dev, x_seed):
     return b
 
 
-def launches_per_step(M, E):
-    """Kernels one step launches: router + top-k (2), permutation (one CTA up
-    to 1024 tokens when its shared memory fits, else count / scan / scatter),
-    gather, gate/up, down, combine."""
+def launches_per_step(M, E, feed="copy"):
+    """Kernels one step launches: router + top-k (2), permutation (one CTA up to 1024 tokens when its shared memory fits,
+    else count / scan / scatter), the gather (only with feed "copy"),
+    gate/up, down, combine."""
     small = M <= 1024 and E * (8 + ((M + 255) // 256 * 256 // 32 + 1) * 4) <= 48 * 1024
-    return 2 + (1 if small else 3) + 4
+    return 2 + (1 if small else 3) + (4 if feed == "copy" else 3)
 
 
-def time_steps(wl, M, b, steps, warmup, world, stream, dev):
+def time_steps(wl, M, b, steps, warmup, world, stream, dev, feed="copy"):
     """Times `steps` steps of the whole hot path (device time, CUDA events on
     the launching stream, barrier + synchronize on both sides) and the
     gate/up and down GEMMs inside them.  Returns (seconds, gate/up ms, down
@@ -275,13 +276,17 @@ def time_steps(wl, M, b, steps, warmup, world, stream, dev):
         # router on the bf16 tokens (read as fp32) and top-k selection
         bm.bi_router_topk(b["x"], w.w_router, k, out=b["scores"], ids=b["ids"], wts=b["wts"])
         bm.bi_moe_permute(b["ids"], E, offsets=b["offsets"], perm=b["perm"], workspace=b["ws_perm"])
-        bm.bi_moe_gather(b["x"], b["offsets"], b["perm"], k, x_perm=b["x_perm"])
+        if feed == "copy":
+            bm.bi_moe_gather(b["x"], b["offsets"], b["perm"], k, x_perm=b["x_perm"])
         if record:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e2 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        bm.bi_moe_gate_up(b["x_perm"], b["offsets"], b["perm"], b["wts"], w.w13, k, act=b["act"])
+        if feed == "copy":
+            bm.bi_moe_gate_up(b["x_perm"], b["offsets"], b["perm"], b["wts"], w.w13, k, act=b["act"])
+        else:  # the GEMM gathers the token rows itself (bi_moe_gate_up_feed 2)
+            bm.bi_moe_gate_up_tokens(b["x"], b["offsets"], b["perm"], b["wts"], w.w13, k, act=b["act"])
         if record:
             e1.record(stream)
         bm.bi_moe_down(b["act"], b["offsets"], b["perm"], w.w2, M, k, contrib=b["contrib"])
@@ -331,7 +336,7 @@ def run_ours(args, rank, world, local):
     b = setup_workload(wl, M, dev, x_seed=21 + rank)
     w, x = b["w"], b["x"]
     stream = torch.cuda.current_stream(dev)
-    sec, gu_ms, dn_ms, clk = time_steps(wl, M, b, args.steps, args.warmup, world, stream, dev)
+    sec, gu_ms, dn_ms, clk = time_steps(wl, M, b, args.steps, args.warmup, world, stream, dev, args.feed)
     sec_max = max_over_ranks(sec, world, dev)
 
     # ---- end to end through the public API from pinned host buffers.  Each
@@ -389,15 +394,17 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device error during the timed region")
 
     hbm, tc_burst, tc_sust, peak_src = measured_peaks()
-    costs = layer_costs(M, H, E, I, k)
+    costs = layer_costs(M, H, E, I, k, args.feed)
     rl_gu = roofline_entry("moe_gemm_kernel<gate_up> (tcgen05 grouped GEMM + SwiGLU*p epilogue)",
                            costs["gate_up"], gu_ms, hbm, tc_burst, peak_src,
                            captured_traffic(args.workload, M, "gate_up"))
     rl_dn = roofline_entry("moe_gemm_kernel<down> (tcgen05 grouped GEMM, fp32 per-slot contributions)",
                            costs["down"], dn_ms, hbm, tc_burst, peak_src,
                            captured_traffic(args.workload, M, "down"))
-    rl_step = roofline_entry("whole step (9 launches: router, top-k, permutation, gather, gate/up, down, "
-                             "combine)", costs["step"], sec_max / args.steps * 1e3, hbm, tc_burst, peak_src)
+    rl_step = roofline_entry(f"whole step ({launches_per_step(M, E, args.feed)} launches: router + top-k, "
+                             "permutation, " + ("gather, " if args.feed == "copy" else "") +
+                             "gate/up, down, combine)", costs["step"], sec_max / args.steps * 1e3, hbm, tc_burst,
+                             peak_src)
 
     extras, summary = {}, {}
     # the secondary workload and the sweeps characterise one GPU: the N=1
@@ -409,10 +416,10 @@ def run_ours(args, rank, world, local):
         wl2 = WORKLOADS[other]
         b2 = setup_workload(wl2, M, dev, x_seed=21)
         s2_steps = max(3, min(args.steps, 50))
-        sec2, gu2, dn2, clk2 = time_steps(wl2, M, b2, s2_steps, args.warmup, 1, stream, dev)
+        sec2, gu2, dn2, clk2 = time_steps(wl2, M, b2, s2_steps, args.warmup, 1, stream, dev, args.feed)
         del b2
         torch.cuda.empty_cache()
-        c2 = layer_costs(M, wl2["H"], wl2["E"], wl2["I"], wl2["top_k"])
+        c2 = layer_costs(M, wl2["H"], wl2["E"], wl2["I"], wl2["top_k"], args.feed)
         extras["secondary_workload"] = {
             "workload": wl2["name"], "tokens_per_gpu": M, "H": wl2["H"], "E": wl2["E"], "I": wl2["I"],
             "top_k": wl2["top_k"], "steps": s2_steps, "ms_per_step": sec2 / s2_steps * 1e3,
@@ -447,7 +454,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": aggregate(M, e2e_steps, world, e2e_sec), "unit": "tokens/s",
                 "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
                 "steps": e2e_steps},
-        "gpu_launches": launches_per_step(M, E) * args.steps,
+        "gpu_launches": launches_per_step(M, E, args.feed) * args.steps,
         "clocks": clk,
     }
     line.update(extras)
@@ -940,6 +947,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="dsv4")
     ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--feed", choices=("gemm", "copy"), default="copy",
+                    help="how the gate/up GEMM gets the token rows: from the gather kernel's contiguous "
+                         "copy (the layer's path) or gathered by the GEMM itself (tile::gather4)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override the workload's expert count (a smaller case of the same "
                          "tokens-per-expert load, for ncu captures that must stay small)")

@@ -175,16 +175,15 @@ BI_API bi_status bi_topk_window(const float *scores, int64_t ld,
  * bi_router_topk -- bi_router_gemm followed by bi_topk on its scores, as one
  * call for the decode path.  The scores y are exactly bi_router_gemm's (same
  * recipe, same bits) and ids / wts / probs exactly bi_topk's on y.
- * Up to 4 rows (N a multiple of 16 up to 256, K a multiple of 512) the call
- * is ONE kernel: a thread-block cluster of N/16 CTAs owns all N scores of the
- * rows (CTA c computes columns 16c..16c+15 with the same per-element recipe),
- * and after a cluster barrier one warp per row selects from the scores in the
- * cluster's shared memory, so no score goes through global memory before the
- * selection.  If that cluster cannot be scheduled on the device, or for
- * other shapes and larger batches, the selection grid is launched as a
- * programmatic dependent of the router grid (programmatic stream
- * serialization: it waits in hardware for the router's completion before
- * reading y).  Both give the same bits.  The pages keep the router
+ * The selection grid is launched as a programmatic dependent of the router
+ * grid (programmatic stream serialization: it waits in hardware for the
+ * router's completion before reading y).  A one-kernel path exists for up
+ * to 4 rows (N a multiple of 16 up to 256, K a multiple of 1024): a
+ * thread-block cluster of N/16 CTAs owns all N scores of the rows (CTA c
+ * computes columns 16c..16c+15 with the same per-element recipe) and after a
+ * cluster barrier one warp per row selects from the scores in the cluster's
+ * shared memory (bi_router_topk_schedule, schedule 10).  Both give the same
+ * bits.  The pages keep the router
  * ("[BI][DSv4] Batch-invariant GateLinear router with fp32 persistent
  * matmul", whose Perf table puts the decode-size router cost in microseconds
  * per layer) and the selection as separate ops; they have no combined
@@ -298,6 +297,22 @@ BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets,
                                 const bi_bf16 *w13, bi_bf16 *act, int64_t M,
                                 int64_t H, int64_t E, int32_t top_k, int64_t I,
                                 bi_stream_t stream);
+
+/*
+ * bi_moe_gate_up_tokens -- bi_moe_gate_up reading the token rows straight
+ * from x [M,H] bf16 (16-byte aligned) instead of a gathered copy: the GEMM
+ * fetches row perm[p] / top_k of x for position p with TMA gather loads
+ * (tile::gather4).  Same result bits as bi_moe_gather + bi_moe_gate_up;
+ * other arguments, requirements and bad-grouping behaviour as
+ * bi_moe_gate_up.  Slower than the gathered copy for large batches (the TMA
+ * gathers 128-byte rows far slower than the MMAs consume them), so
+ * bi_moe_forward uses it only when bi_moe_gate_up_feed selects it.
+ */
+BI_API bi_status bi_moe_gate_up_tokens(const bi_bf16 *x, const int32_t *offsets,
+                                       const int32_t *perm, const float *wts,
+                                       const bi_bf16 *w13, bi_bf16 *act, int64_t M,
+                                       int64_t H, int64_t E, int32_t top_k, int64_t I,
+                                       bi_stream_t stream);
 
 /*
  * bi_moe_down -- contrib[perm[p], h] = sum_j act[p,j] * W2[e,h,j] for every
@@ -509,6 +524,17 @@ BI_API bi_status bi_router_topk_bf16_schedule(const bi_bf16 *x, const float *w,
  * synchronised with calls in flight on other host threads.
  */
 BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous);
+
+/*
+ * bi_moe_gate_up_feed -- how bi_moe_forward feeds the gate/up GEMM its token
+ * rows, for the whole process from the next call on: 0 automatic (the
+ * default: the copy), 1 a contiguous copy made by the gather kernel first
+ * (bi_moe_gather + bi_moe_gate_up), 2 gathered by the GEMM
+ * (bi_moe_gate_up_tokens).  Same bits either way (tests compare them).
+ * *previous (may be NULL) receives the old setting; other values
+ * BI_ERR_INVALID_ARG.
+ */
+BI_API bi_status bi_moe_gate_up_feed(int32_t mode, int32_t *previous);
 
 /*
  * bi_fp32_fma_probe -- MEASUREMENT ONLY, not part of the MoE path: blocks x

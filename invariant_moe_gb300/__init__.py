@@ -37,6 +37,7 @@ EXPORTS = [
     "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
     "bi_moe_gather_routing", "bi_moe_scatter_contrib", "bi_router_topk_bf16_schedule",
+    "bi_moe_gate_up_tokens", "bi_moe_gate_up_feed",
 ]
 
 
@@ -83,6 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_combine": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_combine_consume": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_gemm_variant": ([I32, P], ST),
+            "bi_moe_gate_up_feed": ([I32, P], ST),
+            "bi_moe_gate_up_tokens": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
             "bi_topk_window": ([P, I64, P, P, I64, I64, I32, P, P], ST),
@@ -300,6 +303,30 @@ def bi_moe_gate_up(x_perm, offsets, perm, wts, w13, top_k, act=None, stream=None
     return act
 
 
+def bi_moe_gate_up_tokens(x, offsets, perm, wts, w13, top_k, act=None, stream=None):
+    """act [M*top_k, I] bf16, the gate/up GEMM gathering the token rows of
+    x [M, H] itself (no gathered copy)."""
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dev = x.device
+    act = act if act is not None else torch.empty(M * top_k, I, dtype=torch.bfloat16, device=dev)
+    _call("bi_moe_gate_up_tokens", _ptr(x, torch.bfloat16, "x"),
+          _ptr(offsets, torch.int32, "offsets", dev), _ptr(perm, torch.int32, "perm", dev),
+          _ptr(wts, torch.float32, "wts", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+          _ptr(act, torch.bfloat16, "act", dev), M, H, E, top_k, I, _stream(stream))
+    return act
+
+
+def bi_moe_gate_up_feed(mode):
+    """How bi_moe_forward feeds the gate/up GEMM (0 automatic = the gathered
+    copy, 1 gathered copy, 2 gathered by the GEMM); returns the previous
+    setting."""
+    prev = ctypes.c_int32(0)
+    _call("bi_moe_gate_up_feed", int(mode), ctypes.byref(prev))
+    return prev.value
+
+
 def bi_moe_down(act, offsets, perm, w2, M, top_k, contrib=None, stream=None):
     E, H, I = w2.shape
     dev = act.device
@@ -361,9 +388,9 @@ def bi_moe_combine_consume(contrib, M, top_k, out=None, stream=None):
 
 def bi_router_topk(x, w, top_k, bias=None, out=None, want_probs=False, schedule=0, stream=None,
                    ids=None, wts=None):
-    """Router scores and top-k selection in one call (up to 4 rows one
-    kernel, else the selection grid as a programmatic dependent of the router
-    grid; schedule 10 forces the one kernel, 1..9 a router schedule).  Returns
+    """Router scores and top-k selection in one call (the selection grid as a
+    programmatic dependent of the router grid; schedule 10 forces the
+    one-kernel cluster path for up to 4 rows, 1..9 a router schedule).  Returns
     (scores [M,N] fp32, ids [M,top_k] int32, wts [M,top_k] fp32, probs or None)."""
     M, K = x.shape
     N = w.shape[0]

@@ -4,6 +4,7 @@
 // and moe_gemm.cu.
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 
 #include "bimoe_internal.cuh"
@@ -32,6 +33,17 @@ bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const f
                          const void *, void *, int64_t, int64_t, int64_t, int32_t, int64_t,
                          cudaStream_t);
 int set_gemm_variant(int v);
+bi_status launch_gate_up_tokens(const void *, int64_t, const int32_t *, const int32_t *, const float *,
+                                const void *, void *, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
+// How bi_moe_forward feeds the gate/up GEMM its token rows: 0 automatic (the
+// copy), 1 the gather kernel's contiguous copy, 2 gathered by the GEMM itself
+// (tile::gather4).  Measured on GB300 at M=4096 the GEMM gathering its own
+// rows is 3x slower (DSv4-shaped gate/up 4.31 ms against 1.45 ms; Qwen-shaped
+// 0.339 against 0.220 ms): the TMA issues the 128-byte row gathers at about
+// 20 cycles per row per SM, well below what the MMAs consume; at decode sizes
+// the two are within noise.
+static std::atomic<int> g_gate_up_feed{0};
+static bool feed_in_gemm() { return g_gate_up_feed.load() == 2; }
 bi_status launch_down(const void *, const int32_t *, const int32_t *, const void *, float *,
                       int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 bi_status launch_fp32_fma_probe(float *, int64_t, int32_t, cudaStream_t);
@@ -41,8 +53,12 @@ bi_status launch_router_topk_fused(const XT *, const float *, const float *, flo
                                    float *, int64_t, int64_t, int64_t, int32_t, cudaStream_t);
 // Batches up to this many rows take the one-kernel router + top-k (when its
 // cluster can be scheduled); larger ones the router grid and the selection
-// grid.  Both give the same bits.
-constexpr int64_t kFusedRouterTopkMaxM = 4;
+// grid.  Both give the same bits.  0: the one-kernel path runs only when
+// forced (schedule 10): measured on GB300 it is slower than the chained grids
+// (DSv4 router shape, M=1: 10.9 us against 8.6 us; the 16 SMs of one
+// cluster each stream 256 KB of the weight, and the two grids spread it over
+// all SMs).
+constexpr int64_t kFusedRouterTopkMaxM = 0;
 bi_status launch_gather_routing(const int32_t *, const float *, const int32_t *, const int32_t *, int64_t,
                                 int64_t, int64_t, int32_t *, float *, cudaStream_t);
 bi_status launch_scatter_contrib(const float *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
@@ -508,6 +524,18 @@ BI_API bi_status bi_moe_gate_up(const bi_bf16 *x_perm, const int32_t *offsets, c
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+BI_API bi_status bi_moe_gate_up_tokens(const bi_bf16 *x, const int32_t *offsets, const int32_t *perm,
+                                       const float *wts, const bi_bf16 *w13, bi_bf16 *act, int64_t M,
+                                       int64_t H, int64_t E, int32_t top_k, int64_t I, bi_stream_t stream) {
+  bi_status st = check_moe_dims(M, H, E, top_k, I);
+  if (st != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(x && offsets && perm && wts && w13 && act, BI_ERR_INVALID_ARG, "null pointer");
+  BI_REQUIRE(aligned(x, 16) && aligned(w13, 16), BI_ERR_INVALID_ARG, "x/w13 must be 16-byte aligned");
+  return launch_gate_up_tokens(x, M, offsets, perm, wts, w13, act, H, E, top_k, I,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
 BI_API bi_status bi_moe_down(const bi_bf16 *act, const int32_t *offsets, const int32_t *perm,
                              const bi_bf16 *w2, float *contrib, int64_t M, int64_t H, int64_t E,
                              int32_t top_k, int64_t I, bi_stream_t stream) {
@@ -598,9 +626,15 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
   const int64_t P = M * top_k;
   if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s, slot_mask)) != BI_OK)
     return st;
-  if ((st = launch_gather(x, perm, offsets, P, H, E, top_k, xperm, s)) != BI_OK) return st;
-  if ((st = launch_gate_up(xperm, offsets, perm, wts, w13, act, P, H, E, top_k, I, s)) != BI_OK)
-    return st;
+  if (feed_in_gemm()) {
+    // the gate/up GEMM gathers the token rows from x itself
+    if ((st = launch_gate_up_tokens(x, M, offsets, perm, wts, w13, act, H, E, top_k, I, s)) != BI_OK)
+      return st;
+  } else {
+    if ((st = launch_gather(x, perm, offsets, P, H, E, top_k, xperm, s)) != BI_OK) return st;
+    if ((st = launch_gate_up(xperm, offsets, perm, wts, w13, act, P, H, E, top_k, I, s)) != BI_OK)
+      return st;
+  }
   if ((st = launch_down(act, offsets, perm, w2, contrib, P, H, E, top_k, I, s)) != BI_OK) return st;
   // a pair skipped for a bad id (recorded in the device error word) adds
   // nothing: the combine sums the slots the permutation marked valid
@@ -608,6 +642,13 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
 }
 
 }  // extern "C"
+
+BI_API bi_status bi_moe_gate_up_feed(int32_t mode, int32_t *previous) {
+  BI_REQUIRE(mode >= 0 && mode <= 2, BI_ERR_INVALID_ARG, "feed mode %d not in {0, 1, 2}", mode);
+  const int old = g_gate_up_feed.exchange(mode);
+  if (previous) *previous = old;
+  return BI_OK;
+}
 
 BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous) {
   BI_REQUIRE(variant >= 0 && variant <= 4, BI_ERR_INVALID_ARG, "variant %d not in {0, ..., 4}", variant);

@@ -116,6 +116,7 @@ struct GemmParams {
   int up_offset;           // row offset of the up half (I), gate/up only
   int *err;
   int P;                   // (token, slot) pairs: rows of the token operand and of the output
+  int top_k;               // slots per token (GATHER: token of pair id q = q / top_k)
 };
 
 struct TileInfo {
@@ -150,10 +151,17 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
   return __float2bfloat16_rn(__fmul_rn(__fmul_rn(sg, u), p));
 }
 
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
+// GATHER (gate/up): tmB maps the token matrix x [M, H] itself with a box of
+// one row, and the producer warp gathers each tile's token rows (pair
+// perm[p] belongs to token perm[p] / top_k) with tile::gather4 loads, one
+// group of 4 rows per lane, instead of a tiled load from the gathered copy
+// x_perm.  The bytes that land in shared memory are the same rows in the same
+// swizzled layout, so the MMAs -- and the bits -- are unchanged.
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
+  static_assert(!GATHER || GATE_UP, "the token gather feeds the gate/up GEMM");
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   constexpr int kBN = C::kBN;
   constexpr int kStages = C::kStages;
@@ -283,6 +291,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
       // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
       const int b_row = ti.tok0 + (rank ? ((ti.ntok + 15) & ~15) / 2 : 0);
+      // GATHER: lane l fetches rows 4g .. 4g+3 of this CTA's token rows for
+      // g = l, l + 32, ...; rows past the tile's tokens (and any position
+      // whose perm entry is not a pair id, reported by the epilogue) fetch
+      // token 0, whose columns the epilogue never stores
+      constexpr int kGroups = C::kBNc / 4;
+      constexpr int kGPL = GATHER ? (kGroups + 31) / 32 : 1;
+      int grow[kGPL][4];
+      if (GATHER) {
+#pragma unroll
+        for (int j = 0; j < kGPL; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int pos = b_row + 4 * (lane + 32 * j) + i;
+            int tok = 0;
+            if (lane + 32 * j < kGroups && pos < ti.tok0 + ti.ntok) {
+              const int q = __ldg(prm.perm + pos);
+              if (static_cast<unsigned>(q) < static_cast<unsigned>(prm.P)) tok = q / prm.top_k;
+            }
+            grow[j][i] = tok;
+          }
+      }
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!wait_u(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
@@ -309,7 +338,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               if (GATE_UP)
                 tma_load_2d_pair(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
             }
-            tma_load_2d_pair(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
+            if (!GATHER) tma_load_2d_pair(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
+          }
+          if (GATHER) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kGPL; ++j) {
+              const int g = lane + 32 * j;
+              if (g < kGroups)
+                tma_gather4_pair(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0],
+                                 grow[j][1], grow[j][2], grow[j][3]);
+            }
           }
         } else {
           const uint32_t fb = smem_u32(&full[stage]);
@@ -327,7 +366,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (GATE_UP && !INTER)
               tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
-            tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
+            if (!GATHER) tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
+          }
+          if (GATHER) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kGPL; ++j) {
+              const int g = lane + 32 * j;
+              if (g < kGroups)
+                tma_gather4(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0], grow[j][1],
+                            grow[j][2], grow[j][3]);
+            }
           }
         }
         __syncwarp();
@@ -594,7 +643,7 @@ static std::atomic<int> g_gemm_variant{0};
 
 int set_gemm_variant(int v) { return g_gemm_variant.exchange(v); }
 
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER>
 static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                              int64_t P, cudaStream_t stream) {
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
@@ -623,7 +672,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   {
     std::lock_guard<std::mutex> lk(mu);
     if (max_units[dev] == 0 || setup.pending(dev)) {
-      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>,
+      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) {
         cudaGetLastError();  // do not leave the error for an unrelated later check
@@ -634,7 +683,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
       if (PAIR) {
         cfg.gridDim = dim3(2 * (num_sms() / 2));
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>, &cfg);
         if (e != cudaSuccess || clusters <= 0) {
           cudaGetLastError();
           set_error("cudaOccupancyMaxActiveClusters: %s (%d clusters)", cudaGetErrorString(e), clusters);
@@ -659,7 +708,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   if (PAIR) attr2[nattr++] = attr[0];
   cfg.attrs = attr2;
   cfg.numAttrs = nattr;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW>, tmA, tmB, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>, tmA, tmB, p);
   if (e != cudaSuccess) {
     set_error("moe_gemm launch: %s", cudaGetErrorString(e));
     return BI_ERR_CUDA;
@@ -707,21 +756,26 @@ static int pick_variant(int64_t features, bool gate_up, int64_t K, int64_t P, in
 // and 64 pairs per expert the wide tiles win by 15-40 %).
 static bool use_narrow(int64_t P, int64_t E) { return P <= 16 * E; }
 
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW>
+// tok: the gathered copy [P, K] (GATHER = false: tiled loads of kBNc rows),
+// or the token matrix [tok_rows = M, K] itself (GATHER: one-row box for
+// tile::gather4).
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false>
 static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const void *tok, int64_t P,
-                          int64_t K, const GemmParams &p, cudaStream_t stream) {
+                          int64_t K, const GemmParams &p, cudaStream_t stream, int64_t tok_rows = 0) {
   CUtensorMap tmA, tmB;
   if (!make_tma_2d_bf16(&tmA, wt, static_cast<uint64_t>(w_rows), static_cast<uint64_t>(K), box_a) ||
-      !make_tma_2d_bf16(&tmB, tok, static_cast<uint64_t>(P), static_cast<uint64_t>(K),
-                        GemmCfg<GATE_UP, PAIR, INTER, NARROW>::kBNc))
+      !make_tma_2d_bf16(&tmB, tok, static_cast<uint64_t>(GATHER ? tok_rows : P), static_cast<uint64_t>(K),
+                        GATHER ? 1u : static_cast<uint32_t>(GemmCfg<GATE_UP, PAIR, INTER, NARROW>::kBNc)))
     return BI_ERR_CUDA;
-  return launch_gemm<GATE_UP, PAIR, INTER, NARROW>(tmA, tmB, p, P, stream);
+  return launch_gemm<GATE_UP, PAIR, INTER, NARROW, GATHER>(tmA, tmB, p, P, stream);
 }
 
-bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32_t *perm,
-                         const float *wts, const void *w13, void *act, int64_t P, int64_t H,
-                         int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
-  (void)top_k;
+// Gate/up GEMM.  tok is the gathered copy x_perm [P, H] (GATHER = false) or
+// the token matrix x [M, H] whose rows the GEMM gathers itself (GATHER).
+template <bool GATHER>
+static bi_status gate_up_any(const void *tok, int64_t M, const int32_t *offsets, const int32_t *perm,
+                             const float *wts, const void *w13, void *act, int64_t P, int64_t H, int64_t E,
+                             int32_t top_k, int64_t I, cudaStream_t stream) {
   const int v = pick_variant(I, true, H, P, E);
   if (v < 0) return BI_ERR_UNSUPPORTED;
   const bool pair = v == 2 || v == 3, inter = v == 3 || v == 4, narrow = use_narrow(P, E);
@@ -730,31 +784,42 @@ bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32
   const int wb_rows = inter ? (pair ? kBM : kBM / 2) : (pair ? 2 * kBM : kBM);
   const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
-               (int)(2 * I), (int)I, device_error_word(), (int)P};
+               (int)(2 * I), (int)I, device_error_word(), (int)P, (int)top_k};
   const int64_t wr = E * 2 * I;
   if (inter && pair)
-    return narrow ? run_gemm<true, true, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
-                  : run_gemm<true, true, true, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+    return narrow ? run_gemm<true, true, true, true, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M)
+                  : run_gemm<true, true, true, false, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M);
   if (pair)
-    return narrow ? run_gemm<true, true, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
-                  : run_gemm<true, true, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+    return narrow ? run_gemm<true, true, false, true, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M)
+                  : run_gemm<true, true, false, false, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M);
   if (inter)
-    return narrow ? run_gemm<true, false, true, true>(w13, wr, box_a, x_perm, P, H, p, stream)
-                  : run_gemm<true, false, true, false>(w13, wr, box_a, x_perm, P, H, p, stream);
-  return narrow ? run_gemm<true, false, false, true>(w13, wr, box_a, x_perm, P, H, p, stream)
-                : run_gemm<true, false, false, false>(w13, wr, box_a, x_perm, P, H, p, stream);
+    return narrow ? run_gemm<true, false, true, true, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M)
+                  : run_gemm<true, false, true, false, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M);
+  return narrow ? run_gemm<true, false, false, true, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M)
+                : run_gemm<true, false, false, false, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M);
+}
+
+bi_status launch_gate_up(const void *x_perm, const int32_t *offsets, const int32_t *perm,
+                         const float *wts, const void *w13, void *act, int64_t P, int64_t H,
+                         int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
+  return gate_up_any<false>(x_perm, 0, offsets, perm, wts, w13, act, P, H, E, top_k, I, stream);
+}
+
+bi_status launch_gate_up_tokens(const void *x, int64_t M, const int32_t *offsets, const int32_t *perm,
+                                const float *wts, const void *w13, void *act, int64_t H, int64_t E,
+                                int32_t top_k, int64_t I, cudaStream_t stream) {
+  return gate_up_any<true>(x, M, offsets, perm, wts, w13, act, M * top_k, H, E, top_k, I, stream);
 }
 
 bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *perm, const void *w2,
                       float *contrib, int64_t P, int64_t H, int64_t E, int32_t top_k, int64_t I,
                       cudaStream_t stream) {
-  (void)top_k;
   const int v = pick_variant(H, false, I, P, E);
   if (v < 0) return BI_ERR_UNSUPPORTED;
   const bool pair = v >= 2, narrow = use_narrow(P, E);
   const int wb_rows = pair ? 2 * kBM : kBM;
   GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / wb_rows), wb_rows, (int)H,
-               (int)H, 0, device_error_word(), (int)P};
+               (int)H, 0, device_error_word(), (int)P, (int)top_k};
   if (pair)
     return narrow ? run_gemm<false, true, false, true>(w2, E * H, kBM, act, P, I, p, stream)
                   : run_gemm<false, true, false, false>(w2, E * H, kBM, act, P, I, p, stream);

@@ -22,35 +22,39 @@
 // last.  So y, ids, wts and probs are bit for bit those of bi_router_gemm
 // followed by bi_topk (the tests compare them).
 //
-// Layout of the work.  K runs in stages of 4 slices (512 k); a stage brings
-// the CTA's 16 weight-row pieces (2 KB each, 1-D bulk copies into rows padded
-// to 2064 bytes, which makes the lanes' 16-byte loads conflict free) and the
-// batch's token rows into a 5-deep ring.  Warp w evaluates slice w of the
-// stage; lane l takes column l % 16 and rows l / 16, l / 16 + 2.  After each
-// stage one thread per (row, column) adds the stage's 4 slice partials to its
-// running sum in slice order.
+// Layout of the work.  K runs in stages of 8 slices (1024 k); a stage brings
+// the CTA's 16 weight-row pieces (4 KB each, 1-D bulk copies into rows padded
+// to 4112 bytes, which makes the lanes' 16-byte loads conflict free) and the
+// batch's token rows into a ring as deep as shared memory allows (2-4
+// stages); the copies of a stage are issued by one lane each of warp 0.  Warp
+// w evaluates slice w of the stage; lane l takes column l % 16 and rows
+// l / 16, l / 16 + 2.  After each stage one thread per (row, column) adds the
+// stage's 8 slice partials to its running sum in slice order.
 #include "router_common.cuh"
 #include "topk_warp.cuh"
 
 namespace bimoe {
 
 constexpr int kRtCols = 16;                       // columns per CTA
-constexpr int kRtStageSlices = 4;                 // slices per stage (one per warp)
-constexpr int kRtStageK = kRtStageSlices * kSlice;  // 512
+constexpr int kRtStageSlices = 8;                 // slices per stage (one per warp)
+constexpr int kRtStageK = kRtStageSlices * kSlice;  // 1024
 constexpr int kRtWPitch = kRtStageK + 4;          // floats per staged weight piece
-constexpr int kRtStages = 5;                      // ring depth
-constexpr int kRtThreads = 32 * kRtStageSlices;   // 128
+constexpr int kRtThreads = 32 * kRtStageSlices;   // 256
 constexpr int kRtMaxM = 4;                        // rows per call
 constexpr int kRtMaxCluster = 16;                 // N <= 256
 
 template <int MR, typename XT>
 struct RtCfg {
-  static constexpr int kWBytes = kRtCols * kRtWPitch * 4;                 // 33,024
+  static constexpr int kWBytes = kRtCols * kRtWPitch * 4;                 // 65,792
   static constexpr int kXBytes = MR * kRtStageK * static_cast<int>(sizeof(XT));
   static constexpr int kStageBytes = kWBytes + kXBytes;
   static constexpr int kPartBytes = 2 * MR * kRtCols * kRtStageSlices * 4;
   static constexpr int kScoreBytes = MR * kRtCols * 4;
-  static constexpr int kSmem = kRtStages * kStageBytes + kPartBytes + kScoreBytes + 8 * kRtStages + 16;
+  static constexpr int kFixed = kPartBytes + kScoreBytes + 8 * 4 + 16;
+  static constexpr int kFit = (227 * 1024 - kFixed) / kStageBytes;
+  static constexpr int kStages = kFit < 4 ? kFit : 4;  // ring depth
+  static_assert(kStages >= 2, "ring");
+  static constexpr int kSmem = kStages * kStageBytes + kFixed;
   static_assert(kWBytes % 16 == 0 && kXBytes % 16 == 0, "bulk copy alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
@@ -72,7 +76,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   using C = RtCfg<MR, XT>;
   extern __shared__ __align__(16) uint8_t rt_smem[];
   uint8_t *ring = rt_smem;
-  float *part = reinterpret_cast<float *>(rt_smem + kRtStages * C::kStageBytes);  // [2][MR][16][4]
+  constexpr int kRtStages = C::kStages;
+  float *part = reinterpret_cast<float *>(rt_smem + kRtStages * C::kStageBytes);  // [2][MR][16][8]
   float *sc = part + 2 * MR * kRtCols * kRtStageSlices;                             // [MR][16]
   uint64_t *full = reinterpret_cast<uint64_t *>(sc + MR * kRtCols);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kRtStages);
@@ -91,22 +96,24 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
   griddep_wait();  // x may come from the previous kernel on the stream
 
-  // one thread issues a stage's copies: 16 weight pieces and the M token rows
+  // warp 0 issues a stage's copies, one per lane: lanes 0-15 the 16 weight
+  // pieces, lanes 16.. the M token rows
   auto issue = [&](int r) {
     const int b = r % kRtStages;
     uint8_t *st = ring + b * C::kStageBytes;
     const uint32_t bar = smem_u32(&full[b]);
     const uint32_t xbytes = kRtStageK * static_cast<uint32_t>(sizeof(XT));
-    mbar_arrive_expect_tx(bar, kRtCols * kRtStageK * 4 + static_cast<uint32_t>(M) * xbytes);
-    for (int j = 0; j < kRtCols; ++j)
-      bulk_g2s(smem_u32(st + j * kRtWPitch * 4),
-               w + static_cast<size_t>(cta * kRtCols + j) * K + static_cast<size_t>(r) * kRtStageK,
+    if (lane == 0) mbar_arrive_expect_tx(bar, kRtCols * kRtStageK * 4 + static_cast<uint32_t>(M) * xbytes);
+    __syncwarp();
+    if (lane < kRtCols)
+      bulk_g2s(smem_u32(st + lane * kRtWPitch * 4),
+               w + static_cast<size_t>(cta * kRtCols + lane) * K + static_cast<size_t>(r) * kRtStageK,
                kRtStageK * 4, bar);
-    for (int m = 0; m < M; ++m)
-      bulk_g2s(smem_u32(st + C::kWBytes + m * kRtStageK * sizeof(XT)),
-               x + static_cast<size_t>(m) * K + static_cast<size_t>(r) * kRtStageK, xbytes, bar);
+    else if (lane - kRtCols < M)
+      bulk_g2s(smem_u32(st + C::kWBytes + (lane - kRtCols) * kRtStageK * sizeof(XT)),
+               x + static_cast<size_t>(lane - kRtCols) * K + static_cast<size_t>(r) * kRtStageK, xbytes, bar);
   };
-  if (tid == 0)
+  if (warp == 0)
     for (int r = 0; r < R && r < kRtStages; ++r) issue(r);
 
   float rs = 0.0f;  // running sum of thread tid < MR*16: row tid / 16, column tid % 16
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     __syncthreads();  // the ring slot is free and the partials are in place
     done = r + 1;
-    if (tid == 0 && r + kRtStages < R) issue(r + kRtStages);
+    if (warp == 0 && r + kRtStages < R) issue(r + kRtStages);
     if (tid < MR * kRtCols) {
       const float *q = pr + tid * kRtStageSlices;
 #pragma unroll
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
   // every CTA's scores are in its shared memory before anyone reads them
   cluster_sync_all();
-  const int m = cta + ncta * warp;  // this warp's row, if any
+  const int m = cta + ncta * warp;  // this warp's row, if any (rows < 8 * ncta >= M)
   if (!aborted && m < M) {
     const uint32_t base = smem_u32(&sc[m * kRtCols]);
     auto load = [&](int j) { return ld_dsmem_f32(mapa_shared(base + 4u * (j % kRtCols), j / kRtCols)); };

@@ -116,6 +116,8 @@ def test_stage_calls_reject_bad_grouping(cuda):
     assert bm.device_error() == 4
     bm.bi_moe_down(act_pad[:P], offsets, bad_perm, w.w2, M, k, contrib=con_pad[:P])
     assert bm.device_error() == 4
+    bm.bi_moe_gate_up_tokens(x_pad[:M], offsets, bad_perm, wts_pad[:P].view(M, k), w.w13, k, act=act_pad[:P])
+    assert bm.device_error() == 4
     torch.cuda.synchronize()
     assert not xp_pad[P:].any() and not act_pad[P:].any() and not con_pad[P:].any()
 
@@ -278,6 +280,51 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
     for v in (2, 3, 4):
         for a, b in zip(res[1], res[v]):
             assert torch.equal(a, b), f"variant {v}"
+
+
+@pytest.fixture
+def gate_up_feed():
+    """Set how bi_moe_forward feeds the gate/up GEMM for one test; restores
+    automatic after."""
+    import invariant_moe_gb300 as bm
+    yield bm.bi_moe_gate_up_feed
+    bm.bi_moe_gate_up_feed(0)
+
+
+@pytest.mark.parametrize("shape,M,kind", [("qwen", 1, "rand"), ("qwen", 17, "rand"), ("qwen", 300, "skew"),
+                                          ("qwen", 4096, "rand"), ("dsv4", 4096, "rand"),
+                                          ("small", 333, "skew"), ("small", 5, "rand")])
+def test_gate_up_gathering_rows_same_bits(cuda, gemm_variant, gate_up_feed, shape, M, kind):
+    """The gate/up GEMM gathering its token rows from x (tile::gather4 in
+    the producer warp) gives the bits of the gather kernel's copy fed to the
+    plain GEMM, under every variant, ragged token blocks and skewed routing
+    included; and bi_moe_forward gives the same output with either feed."""
+    import invariant_moe_gb300 as bm
+    H, E, I, k = {"qwen": (2048, 128, 768, 8), "dsv4": (4096, 256, 2048, 8),
+                  "small": (384, 6, 256, 2)}[shape]
+    w = syn.moe_weights(H, E, I, seed=M + 91, unit=True, device="cuda")
+    x = syn.moe_tokens(M, H, seed=M + 92, unit=True).to(cuda)
+    f = syn.random_routing if kind == "rand" else syn.skewed_routing
+    ids, wts = f(M, E, k, seed=M + 93)
+    ids, wts = ids.to(cuda), wts.to(cuda)
+    off, perm = bm.bi_moe_permute(ids, E)
+    xp = bm.bi_moe_gather(x, off, perm, k)
+    for v in (0, 1, 2, 3, 4):
+        if v == 2 and I % 256:
+            continue  # plain CTA pairs need I % 256 == 0
+        gemm_variant(v)
+        a_copy = bm.bi_moe_gate_up(xp, off, perm, wts, w.w13, k)
+        a_rows = bm.bi_moe_gate_up_tokens(x, off, perm, wts, w.w13, k)
+        torch.cuda.synchronize()
+        assert torch.equal(a_copy, a_rows), f"variant {v}"
+    gemm_variant(0)
+    outs = []
+    for feed in (1, 2):
+        gate_up_feed(feed)
+        outs.append(bm.bi_moe_forward(x, ids, wts, w.w13, w.w2))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert bm.device_error() == 0
 
 
 @pytest.mark.parametrize("M", [300, 4096])

@@ -1,7 +1,7 @@
 """Router + top-k in one call (bi_router_topk) on the GPU.
 
-Up to 4 rows the call is one kernel (a cluster owns all N scores and selects
-from distributed shared memory; schedule 10 forces it); beyond that the
+With schedule 10 the call is one kernel (a cluster owns all N scores of up
+to 4 rows and selects from distributed shared memory); otherwise the
 selection grid runs as a programmatic dependent of the router grid.  Either
 way the call must reproduce the two separate calls bit for bit: the same scores as
 bi_router_gemm under every schedule, and the same ids, wts and probs as
@@ -72,7 +72,7 @@ def test_one_kernel_equals_two_launch(cuda, shape, xdtype):
     takes (1..4), fp32 and bf16 tokens, with and without bias, top_k 1..16,
     and the cluster sizes 16 (N=256), 8 (N=128) and 4 (N=64)."""
     import invariant_moe_gb300 as bm
-    K, N = {"dsv4": (4096, 256), "qwen": (2048, 128), "n64": (1536, 64)}[shape]
+    K, N = {"dsv4": (4096, 256), "qwen": (2048, 128), "n64": (3072, 64)}[shape]
     g = syn.gen(81 + N)
     x = torch.randn(4, K, generator=g).to(xdtype).to(cuda)
     w = (torch.randn(N, K, generator=g) / K ** 0.5).to(cuda)
@@ -119,7 +119,7 @@ def test_one_kernel_ties_and_rows(cuda):
 def test_one_kernel_rejects_shapes_it_does_not_take(cuda):
     """Schedule 10 on a shape the one-kernel path does not take is an error,
     not a silent fallback: N not a multiple of 16, more than 4 rows, K not a
-    multiple of 512."""
+    multiple of 1024."""
     import invariant_moe_gb300 as bm
     g = syn.gen(5)
     for M, K, N in ((1, 4096, 200), (5, 4096, 256), (2, 640, 128)):
