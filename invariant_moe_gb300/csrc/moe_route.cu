@@ -288,12 +288,14 @@ __global__ void __launch_bounds__(256) moe_scatter_contrib_kernel(
 }
 
 // out[m, h] = bf16(((c[m,0,h] + c[m,1,h]) + ...) + c[m,k-1,h]), fp32 adds in
-// slot order; four consecutive h per thread.  With a slot mask (the layer's
-// own permutation wrote it) only the valid slots are summed, in the same
-// order: the first valid contribution, then each later valid one added; a
-// token with no valid slot gets +0.  With every slot valid this is the same
-// sequence of adds as without a mask.
-template <bool CONSUME>
+// slot order; four consecutive h per thread.  MASK (the layer's own
+// permutation wrote slot_mask): only the valid slots are summed, in the same
+// order -- the first valid contribution, then each later valid one added; a
+// token with no valid slot gets +0; with every slot valid this is the same
+// sequence of adds as without a mask.  Every slot's row is loaded whatever
+// the mask says (a skipped slot's row holds stale but readable data and is
+// selected away), so the loads issue back to back in both forms.
+template <bool CONSUME, bool MASK>
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restrict__ contrib,
                                                           __nv_bfloat16 *__restrict__ out, int M,
                                                           int H4, int top_k,
@@ -305,25 +307,31 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float4 *__restri
   const int h4 = static_cast<int>(idx % H4);
   const float4 *c = contrib + m * top_k * H4 + h4;
   if (active) {
-    const uint32_t valid = slot_mask ? slot_mask[m] : 0xffffffffu;
-    // every slot's row is loaded whatever the mask says (a skipped slot's
-    // row holds stale but readable data and is not added), so the loads do
-    // not wait on the mask and issue back to back
     float4 s = c[0];
-    bool any = (valid & 1u) != 0u;
-    if (!any) s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int t = 1; t < top_k; ++t) {
-      const float4 v = c[static_cast<int64_t>(t) * H4];
-      if (!((valid >> t) & 1u)) continue;
-      if (!any) {
-        s = v;
-        any = true;
-        continue;
+    if (!MASK) {
+      for (int t = 1; t < top_k; ++t) {
+        const float4 v = c[static_cast<int64_t>(t) * H4];
+        s.x = __fadd_rn(s.x, v.x);
+        s.y = __fadd_rn(s.y, v.y);
+        s.z = __fadd_rn(s.z, v.z);
+        s.w = __fadd_rn(s.w, v.w);
       }
-      s.x = __fadd_rn(s.x, v.x);
-      s.y = __fadd_rn(s.y, v.y);
-      s.z = __fadd_rn(s.z, v.z);
-      s.w = __fadd_rn(s.w, v.w);
+    } else {
+      const uint32_t valid = slot_mask[m];
+      bool any = (valid & 1u) != 0u;
+      if (!any) s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int t = 1; t < top_k; ++t) {
+        const float4 v = c[static_cast<int64_t>(t) * H4];
+        const bool vt = ((valid >> t) & 1u) != 0u;
+        float4 a;
+        a.x = __fadd_rn(s.x, v.x);
+        a.y = __fadd_rn(s.y, v.y);
+        a.z = __fadd_rn(s.z, v.z);
+        a.w = __fadd_rn(s.w, v.w);
+        if (!any) a = v;  // the first valid slot starts the sum
+        if (vt) s = a;
+        any = any || vt;
+      }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(s.z, s.w);
@@ -405,13 +413,20 @@ bi_status launch_combine(const float *contrib, void *out, int64_t M, int64_t H, 
                          bool consume, cudaStream_t stream, const uint32_t *slot_mask) {
   const int64_t total = M * (H / 4);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
-  if (consume && H % 32 == 0 && reinterpret_cast<uintptr_t>(contrib) % 128 == 0)
-    return launch_chained(moe_combine_kernel<true>, dim3(blocks), dim3(256), 0, stream, 1,
-                          reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
-                          (int)M, (int)(H / 4), top_k, slot_mask);
-  return launch_chained(moe_combine_kernel<false>, dim3(blocks), dim3(256), 0, stream, 1,
-                        reinterpret_cast<const float4 *>(contrib), static_cast<__nv_bfloat16 *>(out),
-                        (int)M, (int)(H / 4), top_k, slot_mask);
+  const float4 *c4 = reinterpret_cast<const float4 *>(contrib);
+  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+  const bool drop = consume && H % 32 == 0 && reinterpret_cast<uintptr_t>(contrib) % 128 == 0;
+  if (drop && slot_mask)
+    return launch_chained(moe_combine_kernel<true, true>, dim3(blocks), dim3(256), 0, stream, 1, c4, o, (int)M,
+                          (int)(H / 4), top_k, slot_mask);
+  if (drop)
+    return launch_chained(moe_combine_kernel<true, false>, dim3(blocks), dim3(256), 0, stream, 1, c4, o, (int)M,
+                          (int)(H / 4), top_k, slot_mask);
+  if (slot_mask)
+    return launch_chained(moe_combine_kernel<false, true>, dim3(blocks), dim3(256), 0, stream, 1, c4, o, (int)M,
+                          (int)(H / 4), top_k, slot_mask);
+  return launch_chained(moe_combine_kernel<false, false>, dim3(blocks), dim3(256), 0, stream, 1, c4, o, (int)M,
+                        (int)(H / 4), top_k, slot_mask);
 }
 
 }  // namespace bimoe
