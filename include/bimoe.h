@@ -240,6 +240,11 @@ BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E,
  * earlier slot of its row, is skipped (BI_DEVERR_BAD_EXPERT_ID /
  * BI_DEVERR_REPEATED_EXPERT in the device error word) and adds nothing: that
  * token's output is the slot-order sum over its valid slots (+0 if none).
+ * Launches: the permutation, gather, gate/up, down and combine kernels; for
+ * decode-sized batches (M * top_k <= 64) two kernels, gate/up and down, each
+ * deriving the same routing from ids in every CTA, gate/up gathering its
+ * token rows itself and down summing each token's contributions in slot
+ * order as the last of them lands.  Same bits either way.
  */
 BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids,
                                 const float *wts, const bi_bf16 *w13,
@@ -410,8 +415,8 @@ BI_API bi_status bi_moe_scatter_contrib(const float *rows, const int32_t *offset
  * BI_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's device code: every
  * GPU that loads the library holds it until the process exits.  Sizes whose
  * bi_moe_workspace_bytes() exceeds it are rejected with BI_ERR_WORKSPACE and
- * a message naming both sizes (64 MiB covers e.g. 606 tokens of H=2048,
- * E=128, top-8, I=768, or 292 tokens of H=4096, E=256, top-8, I=2048).
+ * a message naming both sizes (64 MiB covers e.g. 605 tokens of H=2048,
+ * E=128, top-8, I=768, or 291 tokens of H=4096, E=256, top-8, I=2048).
  * The call never allocates or frees device memory.
  *
  * The first call on a device looks up the array's device address

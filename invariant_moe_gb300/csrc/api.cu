@@ -35,6 +35,10 @@ bi_status launch_gate_up(const void *, const int32_t *, const int32_t *, const f
 int set_gemm_variant(int v);
 bi_status launch_gate_up_tokens(const void *, int64_t, const int32_t *, const int32_t *, const float *,
                                 const void *, void *, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
+bool decode_path_ok(int64_t M, int64_t E, int32_t top_k);
+size_t decode_counter_count(int64_t M, int64_t H);
+bi_status launch_moe_decode(const void *, const int32_t *, const float *, const void *, const void *, void *,
+                            float *, int *, void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
 // How bi_moe_forward feeds the gate/up GEMM its token rows: 0 automatic (the
 // copy), 1 the gather kernel's contiguous copy, 2 gathered by the GEMM itself
 // (tile::gather4).  Measured on GB300 at M=4096 the GEMM gathering its own
@@ -212,7 +216,7 @@ bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct MoeWorkspace {
-  size_t offsets, perm, slot_mask, scratch, xperm, act, contrib, total;
+  size_t offsets, perm, slot_mask, scratch, xperm, act, contrib, counters, total;
 };
 
 static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
@@ -226,6 +230,7 @@ static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, i
   w.xperm = off;   off += align256(P * H * 2);
   w.act = off;     off += align256(P * I * 2);
   w.contrib = off; off += align256(P * H * sizeof(float));
+  w.counters = off; off += align256(decode_counter_count(M, H) * sizeof(int));
   w.total = off;
   return w;
 }
@@ -624,6 +629,12 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
   uint32_t *slot_mask = reinterpret_cast<uint32_t *>(ws + L.slot_mask);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t P = M * top_k;
+  if (g_gate_up_feed.load() == 0 && decode_path_ok(M, E, top_k)) {
+    // decode-sized batch: two launches, the routing derived inside the GEMMs
+    // and the combine fused into the down GEMM
+    return launch_moe_decode(x, ids, wts, w13, w2, act, contrib, reinterpret_cast<int *>(ws + L.counters), out,
+                             M, H, E, top_k, I, s);
+  }
   if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s, slot_mask)) != BI_OK)
     return st;
   if (feed_in_gemm()) {

@@ -117,7 +117,28 @@ struct GemmParams {
   int *err;
   int P;                   // (token, slot) pairs: rows of the token operand and of the output
   int top_k;               // slots per token (GATHER: token of pair id q = q / top_k)
+  // DECODE only: the kernel derives offsets / perm from the expert ids itself
+  const int32_t *ids;      // [M, top_k]
+  int M;                   // tokens
+  int *counters;           // [M, n_fb32] contributions summed per (token, 32-feature block)
+  __nv_bfloat16 *lout;     // [M, out_ld] layer output (down: the fused combine writes it)
+  int n_fb32;              // out_ld / 32
 };
+
+// Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeAutoMaxP):
+// every CTA of the two expert GEMMs derives the routing from the expert ids
+// itself, so no permutation, gather or combine kernel runs (see DECODE).
+// The routing arrays hold kDecodeMaxP pairs; the automatic choice stops at
+// 64, where the two paths cross on GB300 (layer time, CUDA-graph replay,
+// cold L2: Qwen3-30B-A3B-shaped M = 1 / 8 / 16: 42.4 / 129.4 / 172.5 us with
+// the decode path against 44.9 / 131.4 / 171.4 us; DSv4-shaped M = 1 / 4 /
+// 16: 106.7 / 295.1 / 813.4 against 110.8 / 298.7 / 809.2 us).
+constexpr int kDecodeMaxP = 128;
+constexpr int kDecodeAutoMaxP = 64;
+// the aux region holds the barriers (at most 16 stages), the tile prefix and
+// expert offsets for E <= 1024, and the decode routing arrays
+static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 3 * kDecodeMaxP + 8) <= kAuxBytes,
+              "aux shared memory");
 
 struct TileInfo {
   int e, wb, tok0, ntok;
@@ -145,6 +166,79 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix
   return t;
 }
 
+// Routing of a decode-sized batch, computed by every CTA from the expert ids
+// with the permutation kernels' result: the valid (token, slot) pairs grouped
+// by expert, in token order inside an expert (a token holds an expert at most
+// once); a slot whose id is outside [0,E) or repeats an earlier slot of its
+// row is skipped.  Called by all threads of the CTA (one pair per thread,
+// P <= kDecodeMaxP <= blockDim.x).  Writes offs[0..E], perm_s[pos] = pair id,
+// tok_s[m] = mask of token m's valid slots.
+__device__ __forceinline__ void decode_routing(const int32_t *ids, int M, int top_k, int E, int *offs,
+                                               int *perm_s, int *vexp_s, uint32_t *tok_s, int *scan_s,
+                                               int *err, bool report) {
+  const int P = M * top_k, tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  if (tid < P) vexp_s[tid] = __ldg(ids + tid);
+  for (int e = tid; e <= E; e += nt) offs[e] = 0;
+  for (int m = tid; m < M; m += nt) tok_s[m] = 0u;
+  __syncthreads();
+  int e = -1;
+  if (tid < P) {
+    const int m = tid / top_k, t = tid - m * top_k;
+    e = vexp_s[tid];
+    bool ok = e >= 0 && e < E;
+    if (!ok && report) report_error(err, BI_DEVERR_BAD_EXPERT_ID);
+    for (int u = 0; u < t && ok; ++u)
+      if (vexp_s[m * top_k + u] == e) {
+        ok = false;
+        if (report) report_error(err, BI_DEVERR_REPEATED_EXPERT);
+      }
+    if (!ok) e = -1;
+  }
+  __syncthreads();
+  if (tid < P) {
+    vexp_s[tid] = e;
+    if (e >= 0) {
+      atomicAdd(&offs[e], 1);  // counts: order-free
+      atomicOr(&tok_s[tid / top_k], 1u << (tid % top_k));
+    }
+  }
+  __syncthreads();
+  // exclusive scan of the counts over experts (thread t owns a chunk)
+  const int c = (E + nt - 1) / nt;
+  const int e0 = min(E, tid * c), e1 = min(E, e0 + c);
+  int local = 0;
+  for (int x = e0; x < e1; ++x) local += offs[x];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) scan_s[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int v = scan_s[w];
+    if (w < warp) base += v;
+    total += v;
+  }
+  int run = base + incl - local;
+  for (int x = e0; x < e1; ++x) {
+    const int cnt = offs[x];
+    offs[x] = run;
+    run += cnt;
+  }
+  if (tid == 0) offs[E] = total;
+  __syncthreads();
+  if (e >= 0) {
+    int rank = 0;  // valid pairs of this expert in lower (token, slot) order
+    for (int j = 0; j < tid; ++j) rank += vexp_s[j] == e;
+    perm_s[offs[e] + rank] = tid;
+  }
+  __syncthreads();
+}
+
 // act = silu(g) * u * p: a fixed fp32 sequence, one bf16 rounding.
 __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
   const float sg = __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
@@ -157,11 +251,23 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
 // group of 4 rows per lane, instead of a tiled load from the gathered copy
 // x_perm.  The bytes that land in shared memory are the same rows in the same
 // swizzled layout, so the MMAs -- and the bits -- are unchanged.
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false>
+// DECODE (decode-sized batches, one CTA per tile, narrow tiles): offsets and
+// perm are not read from memory; every CTA derives them from the expert ids
+// (decode_routing).  gate/up (with GATHER) also zeroes the arrival counters
+// and the output rows of tokens with no valid slot; down fuses the top-k
+// combine: after storing its fp32 contributions, each epilogue warp counts
+// one arrival per token of the tile on that token's counter for the warp's 32
+// features, and the warp whose arrival completes the count (all the token's
+// valid slots stored) sums the k contributions in slot order and writes the
+// bf16 output -- the same sequence of adds as the combine kernel.  No warp
+// waits for another.
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false, bool DECODE = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams prm) {
   static_assert(!GATHER || GATE_UP, "the token gather feeds the gate/up GEMM");
+  static_assert(!DECODE || (NARROW && !PAIR), "the decode path runs narrow tiles, one CTA per tile");
+  static_assert(!DECODE || !GATE_UP || GATHER, "decode gate/up gathers its token rows");
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   constexpr int kBN = C::kBN;
   constexpr int kStages = C::kStages;
@@ -181,6 +287,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *tile_prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [E+1]
   int *offs = tile_prefix + prm.E + 1;                        // [E+1] copy of prm.offsets
+  // DECODE: the routing derived in the prologue
+  int *perm_s = offs + prm.E + 1;                               // [kDecodeMaxP]
+  int *vexp_s = perm_s + kDecodeMaxP;                           // [kDecodeMaxP]
+  uint32_t *tok_s = reinterpret_cast<uint32_t *>(vexp_s + kDecodeMaxP);  // [kDecodeMaxP]
+  int *scan_s = reinterpret_cast<int *>(tok_s + kDecodeMaxP);   // [8]
+  // pair id at permuted position p
+  auto perm_at = [&](int p) {
+    if constexpr (DECODE) return perm_s[p];
+    else return __ldg(prm.perm + p);
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -229,9 +345,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // predecessor on the same SM: only these GEMM kernels allocate it and their
   // CTAs need most of an SM's shared memory.)
   griddep_wait();
-  // the expert offsets in shared memory: one global round trip for all
-  // threads instead of a chain of dependent loads in the tile scan below
-  for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
+  if constexpr (DECODE) {
+    decode_routing(prm.ids, prm.M, prm.top_k, prm.E, offs, perm_s, vexp_s, tok_s, scan_s, prm.err,
+                   GATE_UP && blockIdx.x == 0);
+    if constexpr (GATE_UP) {
+      // for the down GEMM that follows: its arrival counters start at zero,
+      // and tokens with no valid slot (no tile stores them) get zero rows
+      const int nc = prm.M * prm.n_fb32;
+      for (int i = blockIdx.x * kGemmThreads + threadIdx.x; i < nc; i += gridDim.x * kGemmThreads)
+        prm.counters[i] = 0;
+      if (blockIdx.x == 0)
+        for (int m = 0; m < prm.M; ++m)
+          if (tok_s[m] == 0u)
+            for (int h = threadIdx.x; h < prm.n_fb32 * 32; h += kGemmThreads)
+              prm.lout[static_cast<size_t>(m) * prm.n_fb32 * 32 + h] = __float2bfloat16_rn(0.0f);
+    }
+  } else {
+    // the expert offsets in shared memory: one global round trip for all
+    // threads instead of a chain of dependent loads in the tile scan below
+    for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
+  }
   __syncthreads();
   if (warp == 2) {
     // tile_prefix[e] = tiles of experts < e; each lane scans a contiguous chunk
@@ -297,6 +430,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // token 0, whose columns the epilogue never stores
       constexpr int kGroups = C::kBNc / 4;
       constexpr int kGPL = GATHER ? (kGroups + 31) / 32 : 1;
+      // GATHER: only the rows the MMAs read (the tile's tokens rounded up to
+      // 16, this CTA's share of them) are fetched, and the stage expects
+      // exactly those bytes
+      const int b_rows = PAIR ? ((ti.ntok + 15) & ~15) / 2 : ((ti.ntok + 15) & ~15);
+      const int ngroups = GATHER ? min(kGroups, (b_rows + 3) / 4) : kGroups;
+      const uint32_t stage_bytes = GATHER ? static_cast<uint32_t>(kABytes + ngroups * 4 * kBK * 2)
+                                          : static_cast<uint32_t>(kStageBytes);
       int grow[kGPL][4];
       if (GATHER) {
 #pragma unroll
@@ -306,7 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int pos = b_row + 4 * (lane + 32 * j) + i;
             int tok = 0;
             if (lane + 32 * j < kGroups && pos < ti.tok0 + ti.ntok) {
-              const int q = __ldg(prm.perm + pos);
+              const int q = perm_at(pos);
               if (static_cast<unsigned>(q) < static_cast<unsigned>(prm.P)) tok = q / prm.top_k;
             }
             grow[j][i] = tok;
@@ -324,7 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // even CTA arms with the bytes of both
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
           if (elect_one()) {
-            if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * kStageBytes);
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), GATHER ? 2u * kABytes + 2u * (stage_bytes - kABytes) : 2u * kStageBytes);
             if (INTER) {
               // 16 gate rows, the 16 up rows of the same features, and so on
 #pragma unroll
@@ -345,7 +485,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < kGPL; ++j) {
               const int g = lane + 32 * j;
-              if (g < kGroups)
+              if (g < ngroups)
                 tma_gather4_pair(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0],
                                  grow[j][1], grow[j][2], grow[j][3]);
             }
@@ -353,7 +493,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else {
           const uint32_t fb = smem_u32(&full[stage]);
           if (elect_one()) {
-            mbar_arrive_expect_tx(fb, kStageBytes);
+            mbar_arrive_expect_tx(fb, stage_bytes);
             if (INTER) {
 #pragma unroll
               for (int g = 0; g < 4; ++g) {
@@ -373,7 +513,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < kGPL; ++j) {
               const int g = lane + 32 * j;
-              if (g < kGroups)
+              if (g < ngroups)
                 tma_gather4(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0], grow[j][1],
                             grow[j][2], grow[j][3]);
             }
@@ -513,7 +653,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         const int c = 32 * i + lane;
-        nx_pair[i] = c < t.ntok ? __ldg(prm.perm + t.tok0 + c) : 0;
+        nx_pair[i] = c < t.ntok ? perm_at(t.tok0 + c) : 0;
         nx_p[i] = 0.0f;
       }
       if (GATE_UP) {
@@ -614,6 +754,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         mbar_arrive_relaxed(smem_u32(&tempty[acc]));
       }
+      if constexpr (DECODE && !GATE_UP) {
+        // fused combine for this warp's 32 features (see DECODE above): the
+        // contribution stores are made visible, one arrival per token, and
+        // each (token, 32-feature block) completed here is summed by this warp
+        const int fb32 = (ti.wb * prm.wb_rows + q * 32) / 32;
+        float *contrib = static_cast<float *>(prm.out);
+        __threadfence();
+        __syncwarp();
+        int tok = 0;
+        bool last = false;
+        if (lane < ti.ntok) {  // NARROW: at most 32 tokens per tile
+          tok = perm_s[ti.tok0 + lane] / prm.top_k;
+          const int need = __popc(tok_s[tok]);
+          last = atomicAdd(prm.counters + tok * prm.n_fb32 + fb32, 1) == need - 1;
+        }
+        unsigned todo = __ballot_sync(0xffffffffu, last);
+        while (todo) {
+          const int src = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const int m = __shfl_sync(0xffffffffu, tok, src);
+          __threadfence();  // the other slots' stores, seen through their arrivals
+          const uint32_t valid = tok_s[m];
+          const size_t f = static_cast<size_t>(fb32) * 32 + lane;
+          float sum = 0.0f;
+          bool any = false;
+          for (int t = 0; t < prm.top_k; ++t) {
+            if (!((valid >> t) & 1u)) continue;
+            const float v = __ldcg(contrib + static_cast<size_t>(m * prm.top_k + t) * prm.out_ld + f);
+            sum = any ? __fadd_rn(sum, v) : v;
+            any = true;
+          }
+          prm.lout[static_cast<size_t>(m) * prm.out_ld + f] = __float2bfloat16_rn(sum);
+        }
+      }
       if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
@@ -643,7 +817,7 @@ static std::atomic<int> g_gemm_variant{0};
 
 int set_gemm_variant(int v) { return g_gemm_variant.exchange(v); }
 
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER, bool DECODE = false>
 static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                              int64_t P, cudaStream_t stream) {
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
@@ -672,7 +846,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   {
     std::lock_guard<std::mutex> lk(mu);
     if (max_units[dev] == 0 || setup.pending(dev)) {
-      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>,
+      cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER, DECODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) {
         cudaGetLastError();  // do not leave the error for an unrelated later check
@@ -683,7 +857,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
       if (PAIR) {
         cfg.gridDim = dim3(2 * (num_sms() / 2));
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER, DECODE>, &cfg);
         if (e != cudaSuccess || clusters <= 0) {
           cudaGetLastError();
           set_error("cudaOccupancyMaxActiveClusters: %s (%d clusters)", cudaGetErrorString(e), clusters);
@@ -708,7 +882,7 @@ static bi_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, con
   if (PAIR) attr2[nattr++] = attr[0];
   cfg.attrs = attr2;
   cfg.numAttrs = nattr;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER>, tmA, tmB, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<GATE_UP, PAIR, INTER, NARROW, GATHER, DECODE>, tmA, tmB, p);
   if (e != cudaSuccess) {
     set_error("moe_gemm launch: %s", cudaGetErrorString(e));
     return BI_ERR_CUDA;
@@ -759,7 +933,7 @@ static bool use_narrow(int64_t P, int64_t E) { return P <= 16 * E; }
 // tok: the gathered copy [P, K] (GATHER = false: tiled loads of kBNc rows),
 // or the token matrix [tok_rows = M, K] itself (GATHER: one-row box for
 // tile::gather4).
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false, bool DECODE = false>
 static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const void *tok, int64_t P,
                           int64_t K, const GemmParams &p, cudaStream_t stream, int64_t tok_rows = 0) {
   CUtensorMap tmA, tmB;
@@ -767,7 +941,7 @@ static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const 
       !make_tma_2d_bf16(&tmB, tok, static_cast<uint64_t>(GATHER ? tok_rows : P), static_cast<uint64_t>(K),
                         GATHER ? 1u : static_cast<uint32_t>(GemmCfg<GATE_UP, PAIR, INTER, NARROW>::kBNc)))
     return BI_ERR_CUDA;
-  return launch_gemm<GATE_UP, PAIR, INTER, NARROW, GATHER>(tmA, tmB, p, P, stream);
+  return launch_gemm<GATE_UP, PAIR, INTER, NARROW, GATHER, DECODE>(tmA, tmB, p, P, stream);
 }
 
 // Gate/up GEMM.  tok is the gathered copy x_perm [P, H] (GATHER = false) or
@@ -784,7 +958,7 @@ static bi_status gate_up_any(const void *tok, int64_t M, const int32_t *offsets,
   const int wb_rows = inter ? (pair ? kBM : kBM / 2) : (pair ? 2 * kBM : kBM);
   const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
-               (int)(2 * I), (int)I, device_error_word(), (int)P, (int)top_k};
+               (int)(2 * I), (int)I, device_error_word(), (int)P, (int)top_k, nullptr, 0, nullptr, nullptr, 0};
   const int64_t wr = E * 2 * I;
   if (inter && pair)
     return narrow ? run_gemm<true, true, true, true, GATHER>(w13, wr, box_a, tok, P, H, p, stream, M)
@@ -819,12 +993,45 @@ bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *pe
   const bool pair = v >= 2, narrow = use_narrow(P, E);
   const int wb_rows = pair ? 2 * kBM : kBM;
   GemmParams p{offsets, perm, nullptr, contrib, (int)E, (int)I, (int)(H / wb_rows), wb_rows, (int)H,
-               (int)H, 0, device_error_word(), (int)P, (int)top_k};
+               (int)H, 0, device_error_word(), (int)P, (int)top_k, nullptr, 0, nullptr, nullptr, 0};
   if (pair)
     return narrow ? run_gemm<false, true, false, true>(w2, E * H, kBM, act, P, I, p, stream)
                   : run_gemm<false, true, false, false>(w2, E * H, kBM, act, P, I, p, stream);
   return narrow ? run_gemm<false, false, false, true>(w2, E * H, kBM, act, P, I, p, stream)
                 : run_gemm<false, false, false, false>(w2, E * H, kBM, act, P, I, p, stream);
+}
+
+// ------------------------------------------------------------- decode --
+// The expert path of a decode-sized batch in two launches: gate/up (routing
+// derived in every CTA, token rows gathered from x, counters zeroed) and down
+// (routing derived again, the top-k combine fused).  Taken by bi_moe_forward
+// for M * top_k <= kDecodeAutoMaxP under the automatic variant choice, where
+// the narrow one-CTA tiles apply anyway; same bits as the permutation,
+// gather, GEMM and combine kernels (tested).
+bool decode_path_ok(int64_t M, int64_t E, int32_t top_k) {
+  const int64_t P = M * top_k;
+  return P >= 1 && P <= kDecodeAutoMaxP && P <= kGemmThreads && use_narrow(P, E) && g_gemm_variant.load() == 0;
+}
+
+size_t decode_counter_count(int64_t M, int64_t H) { return static_cast<size_t>(M) * (H / 32); }
+
+bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts, const void *w13, const void *w2,
+                            void *act, float *contrib, int *counters, void *out, int64_t M, int64_t H,
+                            int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
+  const int64_t P = M * top_k;
+  __nv_bfloat16 *lout = static_cast<__nv_bfloat16 *>(out);
+  const int v = pick_variant(I, true, H, P, E);  // narrow: 4 (interleaved 64-feature tiles) or 1
+  const bool inter = v == 4;
+  const int wb_rows = inter ? kBM / 2 : kBM;
+  const uint32_t box_a = inter ? kInterBox / 128 : kBM;
+  GemmParams g{nullptr, nullptr, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I, (int)(2 * I),
+               (int)I, device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32)};
+  bi_status st = inter ? run_gemm<true, false, true, true, true, true>(w13, E * 2 * I, box_a, x, P, H, g, stream, M)
+                       : run_gemm<true, false, false, true, true, true>(w13, E * 2 * I, box_a, x, P, H, g, stream, M);
+  if (st != BI_OK) return st;
+  GemmParams d{nullptr, nullptr, nullptr, contrib, (int)E, (int)I, (int)(H / kBM), kBM, (int)H, (int)H, 0,
+               device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32)};
+  return run_gemm<false, false, false, true, false, true>(w2, E * H, kBM, act, P, I, d, stream);
 }
 
 }  // namespace bimoe

@@ -23,8 +23,8 @@
 
 namespace bimoe {
 
-// 64 MiB: the workspace of decode-sized batches, e.g. up to 606 tokens of a
-// Qwen3-30B-A3B-shaped layer (H=2048, E=128, top-8, I=768) or 292 tokens of
+// 64 MiB: the workspace of decode-sized batches, e.g. up to 605 tokens of a
+// Qwen3-30B-A3B-shaped layer (H=2048, E=128, top-8, I=768) or 291 tokens of
 // an H=4096, E=256, top-8, I=2048 layer.  Must match BI_NOALLOC_SCRATCH_BYTES
 // in bimoe.h.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;

@@ -430,13 +430,53 @@ def test_forward_skewed_and_small_shapes(oracle_mod, cuda):
         check_layer(out.float().cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("M", [40, 1500])
+def stage_chain(bm, x, ids, wts, w13, w2, E, k):
+    """The layer through the separate stage kernels: permutation, gather,
+    gate/up, down, combine (the path bi_moe_forward takes above decode
+    sizes)."""
+    M = x.shape[0]
+    off, perm = bm.bi_moe_permute(ids, E)
+    xp = bm.bi_moe_gather(x, off, perm, k)
+    act = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
+    con = bm.bi_moe_down(act, off, perm, w2, M, k)
+    return bm.bi_moe_combine(con, M, k)
+
+
+@pytest.mark.parametrize("shape,M,k,kind", [("qwen", 1, 8, "rand"), ("qwen", 8, 8, "rand"), ("qwen", 5, 8, "skew"),
+                                            ("dsv4", 1, 8, "rand"), ("dsv4", 5, 8, "rand"),
+                                            ("small", 64, 1, "rand"), ("small", 16, 4, "skew"),
+                                            ("e1024", 4, 16, "rand")])
+def test_decode_path_same_bits_as_stages(cuda, shape, M, k, kind):
+    """Decode-sized batches (M * top_k <= 64) run bi_moe_forward as two
+    kernels: gate/up and down each derive the routing from the ids in every
+    CTA, gate/up gathers its token rows from x, and down sums each token's
+    contributions in slot order as its last slot lands.  Same bits as the
+    permutation, gather, GEMM and combine kernels, repeated calls included
+    (the arrival counters start from zero every call)."""
+    import invariant_moe_gb300 as bm
+    H, E, I = {"qwen": (2048, 128, 768), "dsv4": (4096, 256, 2048), "small": (384, 8, 256),
+               "e1024": (256, 1024, 128)}[shape]
+    w = syn.moe_weights(H, E, I, seed=M + 101, unit=True, device="cuda")
+    x = syn.moe_tokens(M, H, seed=M + 102, unit=True).to(cuda)
+    f = syn.random_routing if kind == "rand" else syn.skewed_routing
+    ids, wts = f(M, E, k, seed=M + 103)
+    ids, wts = ids.to(cuda), wts.to(cuda)
+    ref = stage_chain(bm, x, ids, wts, w.w13, w.w2, E, k)
+    for _ in range(2):
+        out = bm.bi_moe_forward(x, ids, wts, w.w13, w.w2)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert bm.device_error() == 0
+
+
+@pytest.mark.parametrize("M", [16, 40, 1500])
 def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
     """A slot whose expert id is out of range, or repeats an earlier slot of
     its row, is skipped (the device error word records it) and adds nothing:
     the token's output is the sum over its valid slots, and a token with no
-    valid slot gets zeros.  M=40 takes the one-CTA permutation, M=1500 the
-    three-launch one; both write the mask of valid slots."""
+    valid slot gets zeros.  M=16 takes the decode path (routing derived in the
+    GEMMs, combine fused), M=40 the one-CTA permutation, M=1500 the
+    three-launch one; the last two write the mask of valid slots."""
     import invariant_moe_gb300 as bm
     H, E, I, k = 256, 8, 128, 4
     w = syn.moe_weights(H, E, I, seed=M + 7, unit=True)
@@ -467,11 +507,14 @@ def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
     assert torch.equal(out[keep], clean[keep])
 
 
-def test_forward_repeat_and_poisoned_workspace(cuda, qwen_w):
-    """Same inputs twice -> same bits; a NaN-filled workspace changes nothing."""
+@pytest.mark.parametrize("M", [300, 8])
+def test_forward_repeat_and_poisoned_workspace(cuda, qwen_w, M):
+    """Same inputs twice -> same bits; a NaN-filled workspace changes nothing
+    (M=8 takes the decode path, whose arrival counters live in the
+    workspace and must be zeroed by the call itself)."""
     import invariant_moe_gb300 as bm
     _, _, w13, w2 = qwen_w
-    M, k = 300, 8
+    k = 8
     x = syn.moe_tokens(M, QWEN["H"], seed=15).to(cuda)
     ids, wts = syn.random_routing(M, QWEN["E"], k, seed=16)
     ids, wts = ids.to(cuda), wts.to(cuda)
