@@ -241,7 +241,7 @@ BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E,
  * BI_DEVERR_REPEATED_EXPERT in the device error word) and adds nothing: that
  * token's output is the slot-order sum over its valid slots (+0 if none).
  * Launches: the permutation, gather, gate/up, down and combine kernels; for
- * decode-sized batches (M * top_k <= 64) two kernels, gate/up and down, each
+ * decode-sized batches (M * top_k <= 32) two kernels, gate/up and down, each
  * deriving the same routing from ids in every CTA, gate/up gathering its
  * token rows itself and down summing each token's contributions in slot
  * order as the last of them lands.  Same bits either way.
@@ -252,6 +252,31 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids,
                                 int64_t H, int64_t E, int32_t top_k, int64_t I,
                                 void *workspace, size_t workspace_bytes,
                                 bi_stream_t stream);
+
+/*
+ * bi_moe_layer -- the whole hot path of one MoE layer in one call: the fp32
+ * router on the bf16 tokens (read as their exact fp32 values), sigmoid top-k,
+ * and the expert path; the bits of bi_router_topk_bf16 followed by
+ * bi_moe_forward, whose contracts it combines.  The pages' router and
+ * fused-MoE are separate ops; this library adds the combination so that a
+ * decode-sized batch (M * top_k <= 32) runs in three launches: the router,
+ * then a gate/up GEMM whose every CTA selects the rows' experts from the
+ * scores itself (bi_topk's selection) and writes ids / wts once, then the
+ * down GEMM with the combine fused.  Larger batches: router, selection grid,
+ * bi_moe_forward's kernels.
+ *   x        [M,H] bf16 (device, 16-byte aligned)
+ *   w_router [E,H] fp32 (device, 16-byte aligned); bias [E] fp32 or NULL
+ *   w13, w2, out, workspace: as bi_moe_forward (workspace >=
+ *            bi_moe_workspace_bytes(M, H, E, top_k, I))
+ *   scores   [M,E] fp32, ids [M,top_k] int32, wts [M,top_k] fp32 (device,
+ *            written): as bi_router_topk's y, ids, wts
+ * Requirements: those of bi_moe_forward and bi_router_gemm, and E <= 512.
+ */
+BI_API bi_status bi_moe_layer(const bi_bf16 *x, const float *w_router, const float *bias,
+                              const bi_bf16 *w13, const bi_bf16 *w2, bi_bf16 *out,
+                              float *scores, int32_t *ids, float *wts, int64_t M,
+                              int64_t H, int64_t E, int32_t top_k, int64_t I,
+                              void *workspace, size_t workspace_bytes, bi_stream_t stream);
 
 /* ---- the stages of bi_moe_forward, callable one by one (same contracts) --
  *

@@ -37,7 +37,7 @@ EXPORTS = [
     "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
     "bi_moe_gather_routing", "bi_moe_scatter_contrib", "bi_router_topk_bf16_schedule",
-    "bi_moe_gate_up_tokens", "bi_moe_gate_up_feed",
+    "bi_moe_gate_up_tokens", "bi_moe_gate_up_feed", "bi_moe_layer",
 ]
 
 
@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_combine_consume": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_gemm_variant": ([I32, P], ST),
             "bi_moe_gate_up_feed": ([I32, P], ST),
+            "bi_moe_layer": ([P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
             "bi_moe_gate_up_tokens": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
             "bi_router_topk_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
@@ -458,9 +459,37 @@ def bi_wait_timeout_probe(stream=None):
     _call("bi_wait_timeout_probe", _stream(stream))
 
 
-def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
-    """Whole hot path of one MoE layer: router (on the bf16 tokens, read as
-    their exact fp32 values) -> top-k -> experts.  Returns (out, scores, ids, wts)."""
-    scores, ids, wts, _ = bi_router_topk(x_bf16, w_router, top_k, bias=bias, stream=stream)
-    out = bi_moe_forward(x_bf16, ids, wts, w13, w2, stream=stream)
+def bi_moe_layer(x, w_router, w13, w2, top_k, bias=None, out=None, scores=None, ids=None, wts=None,
+                 workspace=None, stream=None):
+    """Whole hot path of one MoE layer in one library call: router (on the
+    bf16 tokens, read as their exact fp32 values) -> top-k -> experts.
+    Returns (out, scores, ids, wts)."""
+    M, H = x.shape
+    E, H2 = w_router.shape
+    if H2 != H:
+        raise ValueError("w_router must be [E, H]")
+    dev = x.device
+    ids = ids if ids is not None else torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    wts = wts if wts is not None else torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    _, _, _, I, _ = _check_moe_shapes(x, ids, wts, w13, w2, out)
+    if w13.shape[0] != E:
+        raise ValueError("w_router, w13 and w2 must have the same number of experts")
+    out = out if out is not None else torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    scores = scores if scores is not None else torch.empty(M, E, dtype=torch.float32, device=dev)
+    if tuple(scores.shape) != (M, E):
+        raise ValueError("scores must be [M, E]")
+    if workspace is None:
+        workspace = moe_workspace(M, H, E, top_k, I, dev)
+    _call("bi_moe_layer", _ptr(x, torch.bfloat16, "x"), _ptr(w_router, torch.float32, "w_router", dev),
+          _ptr(bias, torch.float32, "bias", dev), _ptr(w13, torch.bfloat16, "w13", dev),
+          _ptr(w2, torch.bfloat16, "w2", dev), _ptr(out, torch.bfloat16, "out", dev),
+          _ptr(scores, torch.float32, "scores", dev), _ptr(ids, torch.int32, "ids", dev),
+          _ptr(wts, torch.float32, "wts", dev), M, H, E, top_k, I,
+          _ptr(workspace, torch.uint8, "workspace", dev), workspace.numel(), _stream(stream))
     return out, scores, ids, wts
+
+
+def moe_layer(x_bf16, w_router, w13, w2, top_k, bias=None, stream=None):
+    """Whole hot path of one MoE layer (bi_moe_layer).  Returns (out, scores,
+    ids, wts)."""
+    return bi_moe_layer(x_bf16, w_router, w13, w2, top_k, bias=bias, stream=stream)

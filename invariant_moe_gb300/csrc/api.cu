@@ -38,7 +38,8 @@ bi_status launch_gate_up_tokens(const void *, int64_t, const int32_t *, const in
 bool decode_path_ok(int64_t M, int64_t E, int32_t top_k);
 size_t decode_counter_count(int64_t M, int64_t H);
 bi_status launch_moe_decode(const void *, const int32_t *, const float *, const void *, const void *, void *,
-                            float *, int *, void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t);
+                            float *, int *, void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t,
+                            const float *scores, int32_t *ids_out, float *wts_out);
 // How bi_moe_forward feeds the gate/up GEMM its token rows: 0 automatic (the
 // copy), 1 the gather kernel's contiguous copy, 2 gathered by the GEMM itself
 // (tile::gather4).  Measured on GB300 at M=4096 the GEMM gathering its own
@@ -633,7 +634,7 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
     // decode-sized batch: two launches, the routing derived inside the GEMMs
     // and the combine fused into the down GEMM
     return launch_moe_decode(x, ids, wts, w13, w2, act, contrib, reinterpret_cast<int *>(ws + L.counters), out,
-                             M, H, E, top_k, I, s);
+                             M, H, E, top_k, I, s, nullptr, nullptr, nullptr);
   }
   if ((st = launch_permute(ids, offsets, perm, M, E, top_k, ws + L.scratch, s, slot_mask)) != BI_OK)
     return st;
@@ -650,6 +651,33 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids, const floa
   // a pair skipped for a bad id (recorded in the device error word) adds
   // nothing: the combine sums the slots the permutation marked valid
   return launch_combine(contrib, out, M, H, top_k, true, s, slot_mask);
+}
+
+BI_API bi_status bi_moe_layer(const bi_bf16 *x, const float *w_router, const float *bias,
+                              const bi_bf16 *w13, const bi_bf16 *w2, bi_bf16 *out, float *scores,
+                              int32_t *ids, float *wts, int64_t M, int64_t H, int64_t E, int32_t top_k,
+                              int64_t I, void *workspace, size_t workspace_bytes, bi_stream_t stream) {
+  bi_status st = check_moe_dims(M, H, E, top_k, I);
+  if (st != BI_OK) return st;
+  BI_REQUIRE(E <= 512, BI_ERR_UNSUPPORTED, "the layer's selection needs E <= 512 (E=%lld)", (long long)E);
+  if ((st = router_checks(x, w_router, scores, M, H, E)) != BI_OK) return st;
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(x && w_router && w13 && w2 && out && scores && ids && wts && workspace, BI_ERR_INVALID_ARG,
+             "null pointer");
+  BI_REQUIRE(aligned(x, 16) && aligned(w13, 16) && aligned(w2, 16) && aligned(out, 8) && aligned(workspace, 256),
+             BI_ERR_INVALID_ARG, "misaligned pointer (x/w13/w2 16 B, out 8 B, workspace 256 B)");
+  const MoeWorkspace L = moe_layout(M, H, E, top_k, I);
+  BI_REQUIRE(workspace_bytes >= L.total, BI_ERR_WORKSPACE, "workspace %zu < %zu bytes", workspace_bytes, L.total);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_router_bf16(x, w_router, bias, scores, M, H, E, 0, s)) != BI_OK) return st;
+  if (g_gate_up_feed.load() == 0 && decode_path_ok(M, E, top_k)) {
+    // decode-sized batch: the gate/up GEMM selects the experts itself
+    char *ws = static_cast<char *>(workspace);
+    return launch_moe_decode(x, nullptr, nullptr, w13, w2, ws + L.act, reinterpret_cast<float *>(ws + L.contrib),
+                             reinterpret_cast<int *>(ws + L.counters), out, M, H, E, top_k, I, s, scores, ids, wts);
+  }
+  if ((st = launch_topk(scores, ids, wts, nullptr, M, E, top_k, s)) != BI_OK) return st;
+  return bi_moe_forward(x, ids, wts, w13, w2, out, M, H, E, top_k, I, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

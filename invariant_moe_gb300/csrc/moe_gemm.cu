@@ -53,6 +53,7 @@
 #include <mutex>
 
 #include "bimoe_internal.cuh"
+#include "topk_warp.cuh"
 
 namespace bimoe {
 
@@ -123,21 +124,29 @@ struct GemmParams {
   int *counters;           // [M, n_fb32] contributions summed per (token, 32-feature block)
   __nv_bfloat16 *lout;     // [M, out_ld] layer output (down: the fused combine writes it)
   int n_fb32;              // out_ld / 32
+  // DECODE gate/up of the whole layer (bi_moe_layer): the router scores
+  // [M, E]; every CTA selects the top_k experts of each row itself (the
+  // selection of bi_topk) and CTA 0 writes ids / wts for the caller and the
+  // down GEMM.  Null otherwise.
+  const float *scores;
+  int32_t *ids_out;
+  float *wts_out;
 };
 
 // Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeAutoMaxP):
 // every CTA of the two expert GEMMs derives the routing from the expert ids
 // itself, so no permutation, gather or combine kernel runs (see DECODE).
 // The routing arrays hold kDecodeMaxP pairs; the automatic choice stops at
-// 64, where the two paths cross on GB300 (layer time, CUDA-graph replay,
-// cold L2: Qwen3-30B-A3B-shaped M = 1 / 8 / 16: 42.4 / 129.4 / 172.5 us with
-// the decode path against 44.9 / 131.4 / 171.4 us; DSv4-shaped M = 1 / 4 /
-// 16: 106.7 / 295.1 / 813.4 against 110.8 / 298.7 / 809.2 us).
+// 32 pairs, below which the decode path won on every GB300 measured (layer
+// time, CUDA-graph replay, cold L2, two boxes: Qwen3-30B-A3B-shaped M = 1 / 4:
+// 42.4-44.1 / 87.3-87.9 us against 44.9-46.9 / 89.5-89.6 us; DSv4-shaped
+// M = 1 / 4: 104.4-106.7 / 293.6-295.1 against 110.6-110.8 / 295.4-298.7 us);
+// at 64 pairs (M = 8) it was within +-2.5 us either way, beyond it slower.
 constexpr int kDecodeMaxP = 128;
-constexpr int kDecodeAutoMaxP = 64;
+constexpr int kDecodeAutoMaxP = 32;
 // the aux region holds the barriers (at most 16 stages), the tile prefix and
 // expert offsets for E <= 1024, and the decode routing arrays
-static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 3 * kDecodeMaxP + 8) <= kAuxBytes,
+static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 4 * kDecodeMaxP + 8) <= kAuxBytes,
               "aux shared memory");
 
 struct TileInfo {
@@ -178,7 +187,7 @@ __device__ __forceinline__ void decode_routing(const int32_t *ids, int M, int to
                                                int *err, bool report) {
   const int P = M * top_k, tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  if (tid < P) vexp_s[tid] = __ldg(ids + tid);
+  if (ids && tid < P) vexp_s[tid] = __ldg(ids + tid);  // (null: vexp_s holds them already)
   for (int e = tid; e <= E; e += nt) offs[e] = 0;
   for (int m = tid; m < M; m += nt) tok_s[m] = 0u;
   __syncthreads();
@@ -291,7 +300,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int *perm_s = offs + prm.E + 1;                               // [kDecodeMaxP]
   int *vexp_s = perm_s + kDecodeMaxP;                           // [kDecodeMaxP]
   uint32_t *tok_s = reinterpret_cast<uint32_t *>(vexp_s + kDecodeMaxP);  // [kDecodeMaxP]
-  int *scan_s = reinterpret_cast<int *>(tok_s + kDecodeMaxP);   // [8]
+  float *wts_s = reinterpret_cast<float *>(tok_s + kDecodeMaxP);          // [kDecodeMaxP]
+  int *scan_s = reinterpret_cast<int *>(wts_s + kDecodeMaxP);   // [8]
+  // routing probability of pair id q (selected in this CTA for the layer)
+  const bool own_select = DECODE && GATE_UP && prm.scores != nullptr;
+  auto wts_at = [&](int q) { return own_select ? wts_s[q] : __ldg(prm.wts + q); };
   // pair id at permuted position p
   auto perm_at = [&](int p) {
     if constexpr (DECODE) return perm_s[p];
@@ -346,8 +359,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // CTAs need most of an SM's shared memory.)
   griddep_wait();
   if constexpr (DECODE) {
-    decode_routing(prm.ids, prm.M, prm.top_k, prm.E, offs, perm_s, vexp_s, tok_s, scan_s, prm.err,
-                   GATE_UP && blockIdx.x == 0);
+    if (own_select) {
+      // the layer's top-k selection, row m by warp m % 6 (rows < M <= 64),
+      // into shared memory; CTA 0 also writes it out
+      for (int m = warp; m < prm.M; m += kGemmThreads / 32) {
+        const float *row = prm.scores + static_cast<size_t>(m) * prm.E;
+        auto load = [&](int j) { return __ldcg(row + j); };
+        int32_t *irow = vexp_s + m * prm.top_k;
+        float *wrow = wts_s + m * prm.top_k;
+        if (prm.E <= 32) topk_select_warp<1>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
+        else if (prm.E <= 64) topk_select_warp<2>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
+        else if (prm.E <= 128) topk_select_warp<4>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
+        else if (prm.E <= 256) topk_select_warp<8>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
+        else topk_select_warp<16>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
+      }
+      __syncthreads();
+      if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < prm.M * prm.top_k; i += kGemmThreads) {
+          prm.ids_out[i] = vexp_s[i];
+          prm.wts_out[i] = wts_s[i];
+        }
+    }
+    decode_routing(own_select ? nullptr : prm.ids, prm.M, prm.top_k, prm.E, offs, perm_s, vexp_s, tok_s, scan_s,
+                   prm.err, GATE_UP && blockIdx.x == 0);
     if constexpr (GATE_UP) {
       // for the down GEMM that follows: its arrival counters start at zero,
       // and tokens with no valid slot (no tile stores them) get zero rows
@@ -663,7 +697,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = 0; i < kBN / 32; ++i) {
           const int c = 32 * i + lane;
           const bool ok = static_cast<unsigned>(nx_pair[i]) < static_cast<unsigned>(prm.P);
-          nx_p[i] = c < t.ntok && ok ? __ldg(prm.wts + nx_pair[i]) : 0.0f;
+          nx_p[i] = c < t.ntok && ok ? wts_at(nx_pair[i]) : 0.0f;
         }
       }
     };
@@ -1015,9 +1049,12 @@ bool decode_path_ok(int64_t M, int64_t E, int32_t top_k) {
 
 size_t decode_counter_count(int64_t M, int64_t H) { return static_cast<size_t>(M) * (H / 32); }
 
+// scores non-null (bi_moe_layer): ids / wts are outputs, selected from the
+// router scores inside the gate/up GEMM (E <= 512).
 bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts, const void *w13, const void *w2,
                             void *act, float *contrib, int *counters, void *out, int64_t M, int64_t H,
-                            int64_t E, int32_t top_k, int64_t I, cudaStream_t stream) {
+                            int64_t E, int32_t top_k, int64_t I, cudaStream_t stream, const float *scores = nullptr,
+                            int32_t *ids_out = nullptr, float *wts_out = nullptr) {
   const int64_t P = M * top_k;
   __nv_bfloat16 *lout = static_cast<__nv_bfloat16 *>(out);
   const int v = pick_variant(I, true, H, P, E);  // narrow: 4 (interleaved 64-feature tiles) or 1
@@ -1025,12 +1062,15 @@ bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts,
   const int wb_rows = inter ? kBM / 2 : kBM;
   const uint32_t box_a = inter ? kInterBox / 128 : kBM;
   GemmParams g{nullptr, nullptr, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I, (int)(2 * I),
-               (int)I, device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32)};
+               (int)I, device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32),
+               scores, ids_out, wts_out};
   bi_status st = inter ? run_gemm<true, false, true, true, true, true>(w13, E * 2 * I, box_a, x, P, H, g, stream, M)
                        : run_gemm<true, false, false, true, true, true>(w13, E * 2 * I, box_a, x, P, H, g, stream, M);
   if (st != BI_OK) return st;
+  // down reads the ids the gate/up GEMM selected (complete before it starts)
   GemmParams d{nullptr, nullptr, nullptr, contrib, (int)E, (int)I, (int)(H / kBM), kBM, (int)H, (int)H, 0,
-               device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32)};
+               device_error_word(), (int)P, (int)top_k, scores ? ids_out : ids, (int)M, counters, lout,
+               (int)(H / 32)};
   return run_gemm<false, false, false, true, false, true>(w2, E * H, kBM, act, P, I, d, stream);
 }
 

@@ -442,12 +442,12 @@ def stage_chain(bm, x, ids, wts, w13, w2, E, k):
     return bm.bi_moe_combine(con, M, k)
 
 
-@pytest.mark.parametrize("shape,M,k,kind", [("qwen", 1, 8, "rand"), ("qwen", 8, 8, "rand"), ("qwen", 5, 8, "skew"),
-                                            ("dsv4", 1, 8, "rand"), ("dsv4", 5, 8, "rand"),
-                                            ("small", 64, 1, "rand"), ("small", 16, 4, "skew"),
-                                            ("e1024", 4, 16, "rand")])
+@pytest.mark.parametrize("shape,M,k,kind", [("qwen", 1, 8, "rand"), ("qwen", 4, 8, "rand"), ("qwen", 3, 8, "skew"),
+                                            ("dsv4", 1, 8, "rand"), ("dsv4", 4, 8, "rand"),
+                                            ("small", 32, 1, "rand"), ("small", 8, 4, "skew"),
+                                            ("e1024", 2, 16, "rand")])
 def test_decode_path_same_bits_as_stages(cuda, shape, M, k, kind):
-    """Decode-sized batches (M * top_k <= 64) run bi_moe_forward as two
+    """Decode-sized batches (M * top_k <= 32) run bi_moe_forward as two
     kernels: gate/up and down each derive the routing from the ids in every
     CTA, gate/up gathers its token rows from x, and down sums each token's
     contributions in slot order as its last slot lands.  Same bits as the
@@ -469,12 +469,12 @@ def test_decode_path_same_bits_as_stages(cuda, shape, M, k, kind):
     assert bm.device_error() == 0
 
 
-@pytest.mark.parametrize("M", [16, 40, 1500])
+@pytest.mark.parametrize("M", [8, 40, 1500])
 def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
     """A slot whose expert id is out of range, or repeats an earlier slot of
     its row, is skipped (the device error word records it) and adds nothing:
     the token's output is the sum over its valid slots, and a token with no
-    valid slot gets zeros.  M=16 takes the decode path (routing derived in the
+    valid slot gets zeros.  M=8 takes the decode path (routing derived in the
     GEMMs, combine fused), M=40 the one-CTA permutation, M=1500 the
     three-launch one; the last two write the mask of valid slots."""
     import invariant_moe_gb300 as bm
@@ -483,11 +483,11 @@ def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
     x = syn.moe_tokens(M, H, seed=M + 8, unit=True)
     ids, wts = syn.random_routing(M, E, k, seed=M + 9)
     bad = ids.clone()
-    bad[3, 1] = E + 2                 # out of range
-    bad[5, 2] = bad[5, 0]             # repeats slot 0
-    bad[7, :] = -1                    # no valid slot
+    bad[1, 1] = E + 2                 # out of range
+    bad[2, 2] = bad[2, 0]             # repeats slot 0
+    bad[4, :] = -1                    # no valid slot
     bad[M - 1, 3] = 1 << 20           # out of range, last token
-    dropped = [(3, 1), (5, 2), (7, 0), (7, 1), (7, 2), (7, 3), (M - 1, 3)]
+    dropped = [(1, 1), (2, 2), (4, 0), (4, 1), (4, 2), (4, 3), (M - 1, 3)]
     out = bm.bi_moe_forward(x.to(cuda), bad.to(cuda), wts.to(cuda), w.w13.to(cuda), w.w2.to(cuda))
     torch.cuda.synchronize()
     assert bm.device_error() in (1, 2)
@@ -499,18 +499,18 @@ def test_forward_bad_ids_add_nothing(oracle_mod, cuda, M):
     ref = oracle_mod.moe(bits(x), ids_o, wts_o, bits(w.w13), bits(w.w2), E, I)
     got = out.float().cpu().numpy()
     check_layer(got, ref)
-    assert not got[7].any(), "a token with no valid slot must get zeros"
+    assert not got[4].any(), "a token with no valid slot must get zeros"
     # tokens with every slot valid keep the bits of a call with clean ids
     clean = bm.bi_moe_forward(x.to(cuda), ids.to(cuda), wts.to(cuda), w.w13.to(cuda), w.w2.to(cuda))
     torch.cuda.synchronize()
-    keep = [m for m in range(M) if m not in (3, 5, 7, M - 1)]
+    keep = [m for m in range(M) if m not in (1, 2, 4, M - 1)]
     assert torch.equal(out[keep], clean[keep])
 
 
-@pytest.mark.parametrize("M", [300, 8])
+@pytest.mark.parametrize("M", [300, 4])
 def test_forward_repeat_and_poisoned_workspace(cuda, qwen_w, M):
     """Same inputs twice -> same bits; a NaN-filled workspace changes nothing
-    (M=8 takes the decode path, whose arrival counters live in the
+    (M=4 takes the decode path, whose arrival counters live in the
     workspace and must be zeroed by the call itself)."""
     import invariant_moe_gb300 as bm
     _, _, w13, w2 = qwen_w
@@ -524,6 +524,40 @@ def test_forward_repeat_and_poisoned_workspace(cuda, qwen_w, M):
     b = bm.bi_moe_forward(x, ids, wts, w13, w2, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("shape,M,bias,ties", [("qwen", 1, False, False), ("qwen", 4, True, False),
+                                               ("qwen", 3, False, True), ("qwen", 64, True, False),
+                                               ("dsv4", 1, True, False), ("dsv4", 4, False, True),
+                                               ("dsv4", 300, False, False), ("small", 16, True, False)])
+def test_layer_call_same_bits_as_router_topk_and_forward(cuda, shape, M, bias, ties):
+    """bi_moe_layer (router, selection and experts in one call) gives the bits
+    of bi_router_topk followed by bi_moe_forward in scores, ids, wts and out.
+    At decode sizes (M * top_k <= 32) the gate/up GEMM selects the experts
+    itself in every CTA; `ties` duplicates router rows and puts the tokens on
+    multiples of 1/8 so that exact score plateaus straddle the top-k cut."""
+    import invariant_moe_gb300 as bm
+    H, E, I, k = {"qwen": (2048, 128, 768, 8), "dsv4": (4096, 256, 2048, 8), "small": (384, 8, 256, 2)}[shape]
+    w = syn.moe_weights(H, E, I, seed=M + 121, unit=True, device="cuda")
+    wr = w.w_router.clone()
+    x = syn.moe_tokens(M, H, seed=M + 122, unit=True)
+    if ties:
+        g = syn.gen(M + 123)
+        perm = torch.randperm(E, generator=g)
+        for i in range(8):  # eight experts, each copied into three others
+            wr[perm[8 + 3 * i:8 + 3 * i + 3].to(cuda)] = wr[int(perm[i])].clone()
+        x = (torch.round(x.float() * 8.0) / 8.0).clamp(-4, 4).to(torch.bfloat16)
+    x = x.to(cuda)
+    b = syn.normal((E,), 0.01, M + 124).to(cuda) if bias else None
+    y1, i1, w1, _ = bm.bi_router_topk(x, wr, k, bias=b)
+    o1 = bm.bi_moe_forward(x, i1, w1, w.w13, w.w2)
+    o2, y2, i2, w2 = bm.bi_moe_layer(x, wr, w.w13, w.w2, k, bias=b)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "scores"
+    assert torch.equal(i1, i2), "ids"
+    assert torch.equal(w1, w2), "wts"
+    assert torch.equal(o1, o2), "out"
+    assert bm.device_error() == 0
 
 
 def full_layer(x, wr, w13, w2, k):
