@@ -255,10 +255,11 @@ def gemm_variant():
 
 @pytest.mark.parametrize("M,kind", [(1, "rand"), (17, "rand"), (100, "skew"), (300, "skew"), (4096, "rand")])
 def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
-    """One CTA per tile (M=128 MMAs), CTA pairs (M=256 MMAs over two SMs) and
-    CTA pairs with interleaved gate/up rows (one M=256 x N=256 MMA per K step)
-    evaluate the same K order, so act, the fp32 contributions and the layer
-    output agree bit for bit, ragged token blocks included."""
+    """One CTA per tile (M=128 MMAs), CTA pairs (M=256 MMAs over two SMs),
+    CTA pairs with interleaved gate/up rows (one M=256 x N=256 MMA per K
+    step) and one CTA with interleaved rows evaluate the same K order, so
+    act, the fp32 contributions and the layer output agree bit for bit with
+    each other and with the automatic choice, ragged token blocks included."""
     import invariant_moe_gb300 as bm
     _, _, w13, w2 = qwen_w
     H, E, I, k = QWEN["H"], QWEN["E"], QWEN["I"], QWEN["top_k"]
@@ -269,7 +270,7 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
     off, perm = bm.bi_moe_permute(ids, E)
     xp = bm.bi_moe_gather(x, off, perm, k)
     res = {}
-    for v in (1, 2, 3, 4):
+    for v in (0, 1, 2, 3, 4):
         gemm_variant(v)
         act = bm.bi_moe_gate_up(xp, off, perm, wts, w13, k)
         contrib = bm.bi_moe_down(act, off, perm, w2, M, k)
@@ -277,7 +278,7 @@ def test_gemm_variants_same_bits(cuda, qwen_w, gemm_variant, M, kind):
         torch.cuda.synchronize()
         res[v] = (act, contrib, out)
     assert bm.device_error() == 0
-    for v in (2, 3, 4):
+    for v in (0, 2, 3, 4):  # 0: the automatic choice
         for a, b in zip(res[1], res[v]):
             assert torch.equal(a, b), f"variant {v}"
 
