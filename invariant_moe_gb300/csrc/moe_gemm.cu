@@ -133,20 +133,19 @@ struct GemmParams {
   float *wts_out;
 };
 
-// Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeAutoMaxP):
+// Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeMaxP):
 // every CTA of the two expert GEMMs derives the routing from the expert ids
 // itself, so no permutation, gather or combine kernel runs (see DECODE).
-// The routing arrays hold kDecodeMaxP pairs; the automatic choice stops at
-// 32 pairs, below which the decode path won on every GB300 measured (layer
+// One warp routes the pairs (a lane per pair), so the path stops at 32
+// pairs; below that the decode path won on every GB300 measured (layer
 // time, CUDA-graph replay, cold L2, two boxes: Qwen3-30B-A3B-shaped M = 1 / 4:
 // 42.4-44.1 / 87.3-87.9 us against 44.9-46.9 / 89.5-89.6 us; DSv4-shaped
 // M = 1 / 4: 104.4-106.7 / 293.6-295.1 against 110.6-110.8 / 295.4-298.7 us);
 // at 64 pairs (M = 8) it was within +-2.5 us either way, beyond it slower.
-constexpr int kDecodeMaxP = 128;
-constexpr int kDecodeAutoMaxP = 32;
+constexpr int kDecodeMaxP = 32;
 // the aux region holds the barriers (at most 16 stages), the tile prefix and
-// expert offsets for E <= 1024, and the decode routing arrays
-static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 4 * kDecodeMaxP + 8) <= kAuxBytes,
+// expert offsets for E <= 1024, and the decode routing tables
+static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 8 * kDecodeMaxP + 1) <= kAuxBytes,
               "aux shared memory");
 
 struct TileInfo {
@@ -175,77 +174,60 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *tile_prefix
   return t;
 }
 
-// Routing of a decode-sized batch, computed by every CTA from the expert ids
-// with the permutation kernels' result: the valid (token, slot) pairs grouped
-// by expert, in token order inside an expert (a token holds an expert at most
-// once); a slot whose id is outside [0,E) or repeats an earlier slot of its
-// row is skipped.  Called by all threads of the CTA (one pair per thread,
-// P <= kDecodeMaxP <= blockDim.x).  Writes offs[0..E], perm_s[pos] = pair id,
-// tok_s[m] = mask of token m's valid slots.
-__device__ __forceinline__ void decode_routing(const int32_t *ids, int M, int top_k, int E, int *offs,
-                                               int *perm_s, int *vexp_s, uint32_t *tok_s, int *scan_s,
-                                               int *err, bool report) {
-  const int P = M * top_k, tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  if (ids && tid < P) vexp_s[tid] = __ldg(ids + tid);  // (null: vexp_s holds them already)
-  for (int e = tid; e <= E; e += nt) offs[e] = 0;
-  for (int m = tid; m < M; m += nt) tok_s[m] = 0u;
-  __syncthreads();
+// Routing of a decode-sized batch (at most 32 pairs), computed by one warp of
+// every CTA from the expert ids, lane i holding pair i = token * top_k +
+// slot; the result equals the permutation kernels': the valid pairs grouped
+// by expert in increasing expert order, in token order inside an expert (a
+// token holds an expert at most once).  A slot whose id is outside [0,E) or
+// repeats an earlier slot of its row is skipped.  Writes, for the nv valid
+// pairs at positions p < nv: perm_s[p] = pair id, tokp_s[p] = its token; for
+// the nd distinct experts d (increasing): dexp_s[d] = expert, dbeg_s[d] =
+// its first position, dcnt_s[d] = its pairs; tok_s[m] = mask of token m's
+// valid slots.  Returns nd on every lane.
+__device__ __forceinline__ int decode_routing_warp(const int32_t *ids, const int32_t *ids_s, int M, int top_k,
+                                                   int E, int *perm_s, int *tokp_s, int *dexp_s, int *dbeg_s,
+                                                   int *dcnt_s, uint32_t *tok_s, int *err, bool report,
+                                                   int lane) {
+  const int P = M * top_k;
+  const int m = lane / top_k;
   int e = -1;
-  if (tid < P) {
-    const int m = tid / top_k, t = tid - m * top_k;
-    e = vexp_s[tid];
-    bool ok = e >= 0 && e < E;
-    if (!ok && report) report_error(err, BI_DEVERR_BAD_EXPERT_ID);
-    for (int u = 0; u < t && ok; ++u)
-      if (vexp_s[m * top_k + u] == e) {
-        ok = false;
-        if (report) report_error(err, BI_DEVERR_REPEATED_EXPERT);
-      }
-    if (!ok) e = -1;
+  if (lane < P) e = ids ? __ldg(ids + lane) : ids_s[lane];
+  bool ok = lane < P && e >= 0 && e < E;
+  if (lane < P && !ok && report) report_error(err, BI_DEVERR_BAD_EXPERT_ID);
+  const uint32_t lower = (1u << lane) - 1u;
+  // an earlier slot of the same token holding the same expert
+  const uint32_t dup = __match_any_sync(0xffffffffu, ok ? static_cast<uint32_t>(m * E + e) : 0x80000000u | lane);
+  if (ok && (dup & lower)) {
+    ok = false;
+    if (report) report_error(err, BI_DEVERR_REPEATED_EXPERT);
   }
-  __syncthreads();
-  if (tid < P) {
-    vexp_s[tid] = e;
-    if (e >= 0) {
-      atomicAdd(&offs[e], 1);  // counts: order-free
-      atomicOr(&tok_s[tid / top_k], 1u << (tid % top_k));
+  const uint32_t valid = __ballot_sync(0xffffffffu, ok);
+  const uint32_t same = __match_any_sync(0xffffffffu, ok ? e : E + lane);  // lanes of this expert
+  const bool head = ok && !(same & lower);                                 // first lane of its expert
+  const uint32_t heads = __ballot_sync(0xffffffffu, head);
+  // valid pairs (and distinct experts) of smaller experts
+  int less = 0, dless = 0;
+  for (int j = 0; j < P; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    const bool lt = ((valid >> j) & 1u) && ej < e;
+    less += lt;
+    dless += lt && ((heads >> j) & 1u);
+  }
+  if (ok) {
+    const int pos = less + __popc(same & lower);
+    perm_s[pos] = lane;
+    tokp_s[pos] = m;
+    if (head) {
+      dexp_s[dless] = e;
+      dbeg_s[dless] = less;
+      dcnt_s[dless] = __popc(same);
     }
   }
-  __syncthreads();
-  // exclusive scan of the counts over experts (thread t owns a chunk)
-  const int c = (E + nt - 1) / nt;
-  const int e0 = min(E, tid * c), e1 = min(E, e0 + c);
-  int local = 0;
-  for (int x = e0; x < e1; ++x) local += offs[x];
-  int incl = local;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
+  if (lane < M) {
+    const uint32_t slots = top_k >= 32 ? 0xffffffffu : (1u << top_k) - 1u;
+    tok_s[lane] = (valid >> (lane * top_k)) & slots;  // lane * top_k <= 32 - top_k
   }
-  if (lane == 31) scan_s[warp] = incl;
-  __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < nw; ++w) {
-    const int v = scan_s[w];
-    if (w < warp) base += v;
-    total += v;
-  }
-  int run = base + incl - local;
-  for (int x = e0; x < e1; ++x) {
-    const int cnt = offs[x];
-    offs[x] = run;
-    run += cnt;
-  }
-  if (tid == 0) offs[E] = total;
-  __syncthreads();
-  if (e >= 0) {
-    int rank = 0;  // valid pairs of this expert in lower (token, slot) order
-    for (int j = 0; j < tid; ++j) rank += vexp_s[j] == e;
-    perm_s[offs[e] + rank] = tid;
-  }
-  __syncthreads();
+  return __popc(heads);
 }
 
 // act = silu(g) * u * p: a fixed fp32 sequence, one bf16 rounding.
@@ -262,7 +244,7 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
 // swizzled layout, so the MMAs -- and the bits -- are unchanged.
 // DECODE (decode-sized batches, one CTA per tile, narrow tiles): offsets and
 // perm are not read from memory; every CTA derives them from the expert ids
-// (decode_routing).  gate/up (with GATHER) also zeroes the arrival counters
+// (decode_routing_warp).  gate/up (with GATHER) also zeroes the arrival counters
 // and the output rows of tokens with no valid slot; down fuses the top-k
 // combine: after storing its fp32 contributions, each epilogue warp counts
 // one arrival per token of the tile on that token's counter for the warp's 32
@@ -296,12 +278,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *tile_prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [E+1]
   int *offs = tile_prefix + prm.E + 1;                        // [E+1] copy of prm.offsets
-  // DECODE: the routing derived in the prologue
-  int *perm_s = offs + prm.E + 1;                               // [kDecodeMaxP]
-  int *vexp_s = perm_s + kDecodeMaxP;                           // [kDecodeMaxP]
-  uint32_t *tok_s = reinterpret_cast<uint32_t *>(vexp_s + kDecodeMaxP);  // [kDecodeMaxP]
-  float *wts_s = reinterpret_cast<float *>(tok_s + kDecodeMaxP);          // [kDecodeMaxP]
-  int *scan_s = reinterpret_cast<int *>(wts_s + kDecodeMaxP);   // [8]
+  // DECODE: the routing derived in the prologue (decode_routing_warp)
+  int *perm_s = offs + prm.E + 1;                                        // pair id at position p
+  int *tokp_s = perm_s + kDecodeMaxP;                                    // its token
+  int *vexp_s = tokp_s + kDecodeMaxP;                                    // selected ids (own_select)
+  float *wts_s = reinterpret_cast<float *>(vexp_s + kDecodeMaxP);        // selected weights
+  uint32_t *tok_s = reinterpret_cast<uint32_t *>(wts_s + kDecodeMaxP);  // valid slots of token m
+  int *dexp_s = reinterpret_cast<int *>(tok_s + kDecodeMaxP);           // distinct experts ...
+  int *dbeg_s = dexp_s + kDecodeMaxP;                                    // ... their first position
+  int *dcnt_s = dbeg_s + kDecodeMaxP;                                    // ... and pair count
+  int *nd_s = dcnt_s + kDecodeMaxP;                                      // number of distinct experts
   // routing probability of pair id q (selected in this CTA for the layer)
   const bool own_select = DECODE && GATE_UP && prm.scores != nullptr;
   auto wts_at = [&](int q) { return own_select ? wts_s[q] : __ldg(prm.wts + q); };
@@ -374,33 +360,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else topk_select_warp<16>(load, prm.E, prm.top_k, irow, wrow, nullptr, lane);
       }
       __syncthreads();
-      if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < prm.M * prm.top_k; i += kGemmThreads) {
+      if (blockIdx.x == 0 && warp >= 2)
+        for (int i = threadIdx.x - 64; i < prm.M * prm.top_k; i += kGemmThreads - 64) {
           prm.ids_out[i] = vexp_s[i];
           prm.wts_out[i] = wts_s[i];
         }
     }
-    decode_routing(own_select ? nullptr : prm.ids, prm.M, prm.top_k, prm.E, offs, perm_s, vexp_s, tok_s, scan_s,
-                   prm.err, GATE_UP && blockIdx.x == 0);
-    if constexpr (GATE_UP) {
-      // for the down GEMM that follows: its arrival counters start at zero,
-      // and tokens with no valid slot (no tile stores them) get zero rows
+    if (warp == 0) {
+      const int nd = decode_routing_warp(own_select ? nullptr : prm.ids, vexp_s, prm.M, prm.top_k, prm.E, perm_s,
+                                         tokp_s, dexp_s, dbeg_s, dcnt_s, tok_s, prm.err,
+                                         GATE_UP && blockIdx.x == 0, lane);
+      if (lane == 0) *nd_s = nd;
+    } else if (GATE_UP) {
+      // for the down GEMM that follows: its arrival counters start at zero
       const int nc = prm.M * prm.n_fb32;
-      for (int i = blockIdx.x * kGemmThreads + threadIdx.x; i < nc; i += gridDim.x * kGemmThreads)
+      for (int i = blockIdx.x * (kGemmThreads - 32) + threadIdx.x - 32; i < nc; i += gridDim.x * (kGemmThreads - 32))
         prm.counters[i] = 0;
-      if (blockIdx.x == 0)
-        for (int m = 0; m < prm.M; ++m)
-          if (tok_s[m] == 0u)
-            for (int h = threadIdx.x; h < prm.n_fb32 * 32; h += kGemmThreads)
-              prm.lout[static_cast<size_t>(m) * prm.n_fb32 * 32 + h] = __float2bfloat16_rn(0.0f);
     }
   } else {
     // the expert offsets in shared memory: one global round trip for all
     // threads instead of a chain of dependent loads in the tile scan below
     for (int i = threadIdx.x; i <= prm.E; i += kGemmThreads) offs[i] = __ldg(prm.offsets + i);
+    __syncthreads();
   }
-  __syncthreads();
-  if (warp == 2) {
+  if (!DECODE && warp == 2) {
     // tile_prefix[e] = tiles of experts < e; each lane scans a contiguous chunk
     const int per = (prm.E + 31) / 32;
     const int e0 = min(lane * per, prm.E), e1 = min(e0 + per, prm.E);
@@ -435,7 +418,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = tile_prefix[prm.E];
+  const int total_tiles = DECODE ? *nd_s * prm.n_wb : tile_prefix[prm.E];
+  if (DECODE && GATE_UP && blockIdx.x == 0 && warp >= 2) {
+    // tokens with no valid slot (no tile stores them) get zero output rows
+    for (int m = 0; m < prm.M; ++m)
+      if (tok_s[m] == 0u)
+        for (int h = threadIdx.x - 64; h < prm.n_fb32 * 32; h += kGemmThreads - 64)
+          prm.lout[static_cast<size_t>(m) * prm.n_fb32 * 32 + h] = __float2bfloat16_rn(0.0f);
+  }
+  // the tile's expert, weight block and token range
+  auto tile_at = [&](int tile) {
+    if constexpr (DECODE) {
+      // one token tile per distinct expert (at most 32 pairs), its weight
+      // blocks in order
+      TileInfo t;
+      const int d = tile / prm.n_wb;
+      t.e = dexp_s[d];
+      t.wb = tile - d * prm.n_wb;
+      t.tok0 = dbeg_s[d];
+      t.ntok = dcnt_s[d];
+      return t;
+    } else {
+      return decode_tile<kBN>(tile, tile_prefix, offs, prm);
+    }
+  };
 
   // The producer and MMA warps run their loops on all 32 lanes (warp-uniform
   // control flow and operand math); lane 0 performs the waits and the result
@@ -453,7 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
-      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
+      const TileInfo ti = tile_at(tile);
       const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
                         static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
       // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
@@ -464,13 +470,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // token 0, whose columns the epilogue never stores
       constexpr int kGroups = C::kBNc / 4;
       constexpr int kGPL = GATHER ? (kGroups + 31) / 32 : 1;
-      // GATHER: only the rows the MMAs read (the tile's tokens rounded up to
-      // 16, this CTA's share of them) are fetched, and the stage expects
-      // exactly those bytes
-      const int b_rows = PAIR ? ((ti.ntok + 15) & ~15) / 2 : ((ti.ntok + 15) & ~15);
-      const int ngroups = GATHER ? min(kGroups, (b_rows + 3) / 4) : kGroups;
+      // GATHER: only this CTA's real token rows are fetched, four per
+      // gather, and the stage expects exactly those bytes.  The MMA N is the
+      // tile's tokens rounded up to 16; the columns past the real tokens read
+      // whatever rows the stage held before and are never stored (an
+      // accumulator column depends on its own B row only).  A gathered row
+      // costs the copy engine far more than a row of a tiled box, so at
+      // decode sizes (one token: 4 rows instead of 16) this sets the stage
+      // rate.
+      const int half = ((ti.ntok + 15) & ~15) / 2;  // PAIR: token rows staged per CTA
+      auto real_groups = [&](int r) {
+        const int rows = PAIR ? max(0, min(ti.ntok - r * half, half)) : ti.ntok;
+        return min(kGroups, (rows + 3) / 4);
+      };
+      const int ngroups = GATHER ? real_groups(static_cast<int>(rank)) : kGroups;
       const uint32_t stage_bytes = GATHER ? static_cast<uint32_t>(kABytes + ngroups * 4 * kBK * 2)
                                           : static_cast<uint32_t>(kStageBytes);
+      const uint32_t pair_bytes =
+          GATHER ? static_cast<uint32_t>(2 * kABytes + (real_groups(0) + real_groups(1)) * 4 * kBK * 2)
+                 : 2u * static_cast<uint32_t>(kStageBytes);
       int grow[kGPL][4];
       if (GATHER) {
 #pragma unroll
@@ -480,8 +498,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int pos = b_row + 4 * (lane + 32 * j) + i;
             int tok = 0;
             if (lane + 32 * j < kGroups && pos < ti.tok0 + ti.ntok) {
-              const int q = perm_at(pos);
-              if (static_cast<unsigned>(q) < static_cast<unsigned>(prm.P)) tok = q / prm.top_k;
+              if constexpr (DECODE) {
+                tok = tokp_s[pos];
+              } else {
+                const int q = perm_at(pos);
+                if (static_cast<unsigned>(q) < static_cast<unsigned>(prm.P)) tok = q / prm.top_k;
+              }
             }
             grow[j][i] = tok;
           }
@@ -498,7 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // even CTA arms with the bytes of both
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
           if (elect_one()) {
-            if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), GATHER ? 2u * kABytes + 2u * (stage_bytes - kABytes) : 2u * kStageBytes);
+            if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), pair_bytes);
             if (INTER) {
               // 16 gate rows, the 16 up rows of the same features, and so on
 #pragma unroll
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
         // the MMA N covers the tile's real tokens (a multiple of 16), so a
         // ragged last tile of an expert does not pay for padding columns
-        const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
+        const TileInfo ti = tile_at(tile);
         const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, (ti.ntok + 15) & ~15);
         if (!wait_u(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
@@ -683,7 +705,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int nx_pair[kBN / 32];
     float nx_p[kBN / 32];
     auto prefetch = [&](int tile) {
-      const TileInfo t = decode_tile<kBN>(tile, tile_prefix, offs, prm);
+      const TileInfo t = tile_at(tile);
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         const int c = 32 * i + lane;
@@ -703,7 +725,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     if (unit0 < total_tiles) prefetch(unit0);
     for (int tile = unit0; tile < total_tiles; tile += nunits) {
-      const TileInfo ti = decode_tile<kBN>(tile, tile_prefix, offs, prm);
+      const TileInfo ti = tile_at(tile);
       int my_pair[kBN / 32];
       float my_p[kBN / 32];
 #pragma unroll
@@ -799,7 +821,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int tok = 0;
         bool last = false;
         if (lane < ti.ntok) {  // NARROW: at most 32 tokens per tile
-          tok = perm_s[ti.tok0 + lane] / prm.top_k;
+          tok = tokp_s[ti.tok0 + lane];
           const int need = __popc(tok_s[tok]);
           last = atomicAdd(prm.counters + tok * prm.n_fb32 + fb32, 1) == need - 1;
         }
@@ -1039,12 +1061,12 @@ bi_status launch_down(const void *act, const int32_t *offsets, const int32_t *pe
 // The expert path of a decode-sized batch in two launches: gate/up (routing
 // derived in every CTA, token rows gathered from x, counters zeroed) and down
 // (routing derived again, the top-k combine fused).  Taken by bi_moe_forward
-// for M * top_k <= kDecodeAutoMaxP under the automatic variant choice, where
+// for M * top_k <= kDecodeMaxP under the automatic variant choice, where
 // the narrow one-CTA tiles apply anyway; same bits as the permutation,
 // gather, GEMM and combine kernels (tested).
 bool decode_path_ok(int64_t M, int64_t E, int32_t top_k) {
   const int64_t P = M * top_k;
-  return P >= 1 && P <= kDecodeAutoMaxP && P <= kGemmThreads && use_narrow(P, E) && g_gemm_variant.load() == 0;
+  return P >= 1 && P <= kDecodeMaxP && use_narrow(P, E) && g_gemm_variant.load() == 0;
 }
 
 size_t decode_counter_count(int64_t M, int64_t H) { return static_cast<size_t>(M) * (H / 32); }

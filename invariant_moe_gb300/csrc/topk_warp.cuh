@@ -55,8 +55,9 @@ __device__ __forceinline__ void topk_select_warp(Load load, int E, int top_k, in
       key[i] = 0;
     }
   }
-  int32_t my_id = 0;
-  float my_w = 0.0f;
+  // lane t keeps the winner of round t; its sigmoid is taken after the
+  // rounds, off the rounds' dependent chain
+  int32_t my_id = 0, my_key = 0;
   for (int t = 0; t < top_k; ++t) {
     // best candidate of this lane: ascending index, strictly greater key wins
     int have = 0;
@@ -84,12 +85,12 @@ __device__ __forceinline__ void topk_select_warp(Load load, int E, int top_k, in
     if ((wi & 31) == lane) avail &= ~(1u << (wi >> 5));
     if (lane == t) {
       my_id = wi;
-      my_w = sigmoid_f32(key_value(wk));
+      my_key = wk;
     }
   }
   if (lane < top_k) {
     ids_row[lane] = my_id;
-    wts_row[lane] = my_w;
+    wts_row[lane] = sigmoid_f32(key_value(my_key));
   }
 }
 
