@@ -619,8 +619,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         bool ok = true;
         // `ready` is lane 0's non-blocking test of the next stage's barrier,
-        // taken while the current stage's MMAs are being accepted, so a
-        // stage that has already landed costs no blocking wait
+        // taken as soon as the current stage's MMAs are issued, so a stage
+        // that has already landed costs no blocking wait
         bool ready = lane == 0 && mbar_test<PAIR>(smem_u32(&full[stage]), phase);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0) &&
@@ -631,17 +631,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(tiles + stage * kStageBytes);
           const uint32_t b0 = a0 + kABytes;
-          const int nstage = stage + 1 == kStages ? 0 : stage + 1;
-          const uint32_t nphase = stage + 1 == kStages ? phase ^ 1u : phase;
+          // One elected thread issues the stage's MMAs back to back, then the
+          // commit that frees the stage (in both CTAs of a pair) once they
+          // are done.  Measured on GB300: an elect and a warp sync around
+          // every MMA cost ~250 cycles an MMA whatever its shape; issued this
+          // way an M=128 MMA costs ~60 cycles at N=16 and runs at the tensor
+          // rate (~128 cycles) at N=256.
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k) {
-            if (k == kBK / kUK / 2)
-              ready = lane == 0 && kb + 1 < nkb && mbar_test<PAIR>(smem_u32(&full[nstage]), nphase);
-            const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
-            const uint64_t bdesc = sdesc_sw128(b0 + k * kUK * 2);
-            const uint64_t adesc = sdesc_sw128(a0 + k * kUK * 2);
-            const uint64_t udesc = sdesc_sw128(a0 + kTileBytes + k * kUK * 2);
-            if (elect_one()) {
+            for (int k = 0; k < kBK / kUK; ++k) {
+              const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
+              const uint64_t bdesc = sdesc_sw128(b0 + k * kUK * 2);
+              const uint64_t adesc = sdesc_sw128(a0 + k * kUK * 2);
+              const uint64_t udesc = sdesc_sw128(a0 + kTileBytes + k * kUK * 2);
               if (PAIR) {
                 umma_f16_pair(d0, adesc, bdesc, idesc, acc_in);
                 if (GATE_UP && !INTER) umma_f16_pair(d0 + kBN, udesc, bdesc, idesc, acc_in);
@@ -650,20 +652,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (GATE_UP && !INTER) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
               }
             }
-            __syncwarp();
-          }
-          issued_any = true;
-          // frees the stage (in both CTAs of a pair) once these MMAs are done;
-          // elect.sync picks the same lane as for the MMAs
-          if (elect_one()) {
             if (PAIR) umma_commit_pair(smem_u32(&empty[stage]), 0x3);
             else umma_commit(smem_u32(&empty[stage]));
           }
           __syncwarp();
+          issued_any = true;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
+          ready = lane == 0 && kb + 1 < nkb && mbar_test<PAIR>(smem_u32(&full[stage]), phase);
         }
         if (!ok) break;
         if (elect_one()) {
