@@ -144,8 +144,9 @@ struct GemmParams {
 // at 64 pairs (M = 8) it was within +-2.5 us either way, beyond it slower.
 constexpr int kDecodeMaxP = 32;
 // the aux region holds the barriers (at most 16 stages), the tile prefix and
-// expert offsets for E <= 1024, and the decode routing tables
-static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 8 * kDecodeMaxP + 1) <= kAuxBytes,
+// expert offsets for E <= 1024, the decode routing tables and the gathered
+// rows' tokens (at most 256)
+static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 8 * kDecodeMaxP + 1 + 256) <= kAuxBytes,
               "aux shared memory");
 
 struct TileInfo {
@@ -288,6 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int *dbeg_s = dexp_s + kDecodeMaxP;                                    // ... their first position
   int *dcnt_s = dbeg_s + kDecodeMaxP;                                    // ... and pair count
   int *nd_s = dcnt_s + kDecodeMaxP;                                      // number of distinct experts
+  int *grow_s = nd_s + 1;  // GATHER: token of each gathered row of the current tile [kBNc]
   // routing probability of pair id q (selected in this CTA for the layer)
   const bool own_select = DECODE && GATE_UP && prm.scores != nullptr;
   auto wts_at = [&](int q) { return own_select ? wts_s[q] : __ldg(prm.wts + q); };
@@ -443,33 +445,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   };
 
-  // The producer and MMA warps run their loops on all 32 lanes (warp-uniform
-  // control flow and operand math); lane 0 performs the waits and the result
-  // is broadcast, and one elected lane issues each TMA / tcgen05 instruction.
-  auto wait_u = [&](uint32_t bar, uint32_t parity, volatile int *ab) {
-    bool okw = true;
-    if (lane == 0) okw = wait(bar, parity, ab);
-    return __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
-  };
-  auto aborted_u = [&]() { return __shfl_sync(0xffffffffu, *abort_flag, 0) != 0; };
-
+  // The producer and MMA loops run on one elected lane of their warp alone
+  // (waits, copies, MMAs, commits).  Measured on GB300 (a tcgen05.mma
+  // probe): an elect and a warp sync around every MMA cost ~250 cycles an
+  // MMA; a loop inside one `if (elect_one())` block ~60 cycles at N=16 (the
+  // tensor rate at N=256); the same loop under `if (lane == 0)` ~150, as
+  // the operands leave uniform registers.
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
-    for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
+    for (int tile = unit0; tile < total_tiles; tile += nunits) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) break;
       const TileInfo ti = tile_at(tile);
       const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
                         static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
       // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
       const int b_row = ti.tok0 + (rank ? ((ti.ntok + 15) & ~15) / 2 : 0);
-      // GATHER: lane l fetches rows 4g .. 4g+3 of this CTA's token rows for
-      // g = l, l + 32, ...; rows past the tile's tokens (and any position
-      // whose perm entry is not a pair id, reported by the epilogue) fetch
-      // token 0, whose columns the epilogue never stores
       constexpr int kGroups = C::kBNc / 4;
-      constexpr int kGPL = GATHER ? (kGroups + 31) / 32 : 1;
       // GATHER: only this CTA's real token rows are fetched, four per
       // gather, and the stage expects exactly those bytes.  The MMA N is the
       // tile's tokens rounded up to 16; the columns past the real tokens read
@@ -489,37 +483,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t pair_bytes =
           GATHER ? static_cast<uint32_t>(2 * kABytes + (real_groups(0) + real_groups(1)) * 4 * kBK * 2)
                  : 2u * static_cast<uint32_t>(kStageBytes);
-      int grow[kGPL][4];
       if (GATHER) {
-#pragma unroll
-        for (int j = 0; j < kGPL; ++j)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int pos = b_row + 4 * (lane + 32 * j) + i;
-            int tok = 0;
-            if (lane + 32 * j < kGroups && pos < ti.tok0 + ti.ntok) {
-              if constexpr (DECODE) {
-                tok = tokp_s[pos];
-              } else {
-                const int q = perm_at(pos);
-                if (static_cast<unsigned>(q) < static_cast<unsigned>(prm.P)) tok = q / prm.top_k;
-              }
+        // the token of each gathered row (the warp fills the table, lane 0
+        // issues); rows past the tile's tokens (and any position whose perm
+        // entry is not a pair id, reported by the epilogue) fetch token 0,
+        // whose columns the epilogue never stores
+        for (int q = lane; q < ngroups * 4; q += 32) {
+          const int pos = b_row + q;
+          int tok = 0;
+          if (pos < ti.tok0 + ti.ntok) {
+            if constexpr (DECODE) {
+              tok = tokp_s[pos];
+            } else {
+              const int pq = perm_at(pos);
+              if (static_cast<unsigned>(pq) < static_cast<unsigned>(prm.P)) tok = pq / prm.top_k;
             }
-            grow[j][i] = tok;
           }
+          grow_s[q] = tok;
+        }
+        __syncwarp();
       }
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!wait_u(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t *st = tiles + stage * kStageBytes;
-        if (PAIR) {
-          // both CTAs' copies complete on the even CTA's barrier, which the
-          // even CTA arms with the bytes of both
-          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          if (elect_one()) {
+      const bool el = elect_one();
+      if (el) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = tiles + stage * kStageBytes;
+          if (PAIR) {
+            // both CTAs' copies complete on the even CTA's barrier, which the
+            // even CTA arms with the bytes of both
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
             if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), pair_bytes);
             if (INTER) {
               // 16 gate rows, the 16 up rows of the same features, and so on
@@ -535,20 +531,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tma_load_2d_pair(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
             }
             if (!GATHER) tma_load_2d_pair(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
-          }
-          if (GATHER) {
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < kGPL; ++j) {
-              const int g = lane + 32 * j;
-              if (g < ngroups)
-                tma_gather4_pair(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0],
-                                 grow[j][1], grow[j][2], grow[j][3]);
-            }
-          }
-        } else {
-          const uint32_t fb = smem_u32(&full[stage]);
-          if (elect_one()) {
+            else
+              for (int g = 0; g < ngroups; ++g)
+                tma_gather4_pair(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow_s[4 * g],
+                                 grow_s[4 * g + 1], grow_s[4 * g + 2], grow_s[4 * g + 3]);
+          } else {
+            const uint32_t fb = smem_u32(&full[stage]);
             mbar_arrive_expect_tx(fb, stage_bytes);
             if (INTER) {
 #pragma unroll
@@ -563,27 +551,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (GATE_UP && !INTER)
               tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
             if (!GATHER) tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
+            else
+              for (int g = 0; g < ngroups; ++g)
+                tma_gather4(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow_s[4 * g],
+                            grow_s[4 * g + 1], grow_s[4 * g + 2], grow_s[4 * g + 3]);
           }
-          if (GATHER) {
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < kGPL; ++j) {
-              const int g = lane + 32 * j;
-              if (g < ngroups)
-                tma_gather4(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow[j][0], grow[j][1],
-                            grow[j][2], grow[j][3]);
-            }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
           }
-        }
-        __syncwarp();
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
         }
       }
-      if (!ok) break;
+      // the ring state back on every lane (this also keeps grow_s until every
+      // gather of the tile is issued)
+      const int src = __ffs(__ballot_sync(0xffffffffu, el)) - 1;
+      stage = __shfl_sync(0xffffffffu, stage, src);
+      phase = __shfl_sync(0xffffffffu, phase, src);
+      issued_mask = __shfl_sync(0xffffffffu, issued_mask, src);
+      issued_parity = __shfl_sync(0xffffffffu, issued_parity, src);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, src) == 0) break;
     }
     if (lane == 0 && *abort_flag) {
       // let every copy this warp started land before the CTA can exit
@@ -603,91 +591,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
-    if (leader) {
+    if (!leader) {
+      // odd CTA of a pair: the even CTA's final commit arrives here
+      if (lane == 0) wait(smem_u32(drain), 0, nullptr);
+    } else if (elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool issued_any = false;
-      for (int tile = unit0; tile < total_tiles && !aborted_u(); tile += nunits) {
+      for (int tile = unit0; tile < total_tiles && !*abort_flag; tile += nunits) {
         // the MMA N covers the tile's real tokens (a multiple of 16), so a
         // ragged last tile of an expert does not pay for padding columns
         const TileInfo ti = tile_at(tile);
         const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, (ti.ntok + 15) & ~15);
-        if (!wait_u(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
+        if (!wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         bool ok = true;
-        // `ready` is lane 0's non-blocking test of the next stage's barrier,
-        // taken as soon as the current stage's MMAs are issued, so a stage
-        // that has already landed costs no blocking wait
-        bool ready = lane == 0 && mbar_test<PAIR>(smem_u32(&full[stage]), phase);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!__shfl_sync(0xffffffffu, ready ? 1 : 0, 0) &&
-              !wait_u(smem_u32(&full[stage]), phase, abort_flag)) {
+          if (!wait(smem_u32(&full[stage]), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(tiles + stage * kStageBytes);
           const uint32_t b0 = a0 + kABytes;
-          // One elected thread issues the stage's MMAs back to back, then the
-          // commit that frees the stage (in both CTAs of a pair) once they
-          // are done.  Measured on GB300: an elect and a warp sync around
-          // every MMA cost ~250 cycles an MMA whatever its shape; issued this
-          // way an M=128 MMA costs ~60 cycles at N=16 and runs at the tensor
-          // rate (~128 cycles) at N=256.
-          if (elect_one()) {
+          // the stage's MMAs back to back, then the commit that frees the
+          // stage (in both CTAs of a pair) once they are done
 #pragma unroll
-            for (int k = 0; k < kBK / kUK; ++k) {
-              const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
-              const uint64_t bdesc = sdesc_sw128(b0 + k * kUK * 2);
-              const uint64_t adesc = sdesc_sw128(a0 + k * kUK * 2);
-              const uint64_t udesc = sdesc_sw128(a0 + kTileBytes + k * kUK * 2);
-              if (PAIR) {
-                umma_f16_pair(d0, adesc, bdesc, idesc, acc_in);
-                if (GATE_UP && !INTER) umma_f16_pair(d0 + kBN, udesc, bdesc, idesc, acc_in);
-              } else {
-                umma_f16(d0, adesc, bdesc, idesc, acc_in);
-                if (GATE_UP && !INTER) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
-              }
+          for (int k = 0; k < kBK / kUK; ++k) {
+            const uint32_t acc_in = (kb | k) != 0 ? 1u : 0u;
+            const uint64_t bdesc = sdesc_sw128(b0 + k * kUK * 2);
+            const uint64_t adesc = sdesc_sw128(a0 + k * kUK * 2);
+            const uint64_t udesc = sdesc_sw128(a0 + kTileBytes + k * kUK * 2);
+            if (PAIR) {
+              umma_f16_pair(d0, adesc, bdesc, idesc, acc_in);
+              if (GATE_UP && !INTER) umma_f16_pair(d0 + kBN, udesc, bdesc, idesc, acc_in);
+            } else {
+              umma_f16(d0, adesc, bdesc, idesc, acc_in);
+              if (GATE_UP && !INTER) umma_f16(d0 + kBN, udesc, bdesc, idesc, acc_in);
             }
-            if (PAIR) umma_commit_pair(smem_u32(&empty[stage]), 0x3);
-            else umma_commit(smem_u32(&empty[stage]));
           }
-          __syncwarp();
+          if (PAIR) umma_commit_pair(smem_u32(&empty[stage]), 0x3);
+          else umma_commit(smem_u32(&empty[stage]));
           issued_any = true;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
-          ready = lane == 0 && kb + 1 < nkb && mbar_test<PAIR>(smem_u32(&full[stage]), phase);
         }
         if (!ok) break;
-        if (elect_one()) {
-          if (PAIR) umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
-          else umma_commit(smem_u32(&tfull[acc]));
-        }
-        __syncwarp();
+        if (PAIR) umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+        else umma_commit(smem_u32(&tfull[acc]));
         if (++acc == kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      if (PAIR || (aborted_u() && issued_any)) {
+      if (PAIR || (*abort_flag && issued_any)) {
         // pair: always, telling both CTAs that every MMA into their tensor
         // memory (and every read of their shared memory) has completed;
         // single CTA: after an abort, before tensor memory is released
-        if (elect_one()) {
-          if (PAIR) umma_commit_pair(smem_u32(drain), 0x3);
-          else umma_commit(smem_u32(drain));
-        }
-        __syncwarp();
-        if (lane == 0) wait(smem_u32(drain), 0, nullptr);
+        if (PAIR) umma_commit_pair(smem_u32(drain), 0x3);
+        else umma_commit(smem_u32(drain));
+        wait(smem_u32(drain), 0, nullptr);
       }
-    } else if (lane == 0) {
-      // odd CTA of a pair: the even CTA's final commit arrives here
-      wait(smem_u32(drain), 0, nullptr);
     }
     __syncwarp();
   } else {
