@@ -213,6 +213,31 @@ bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_
   return true;
 }
 
+bool make_tma_inter_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t I, uint64_t K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return false;
+  }
+  if (rows % 16 != 0 || I % 16 != 0) {
+    set_error("interleaved weight map needs rows and I multiples of 16");
+    return false;
+  }
+  const cuuint64_t dims[4] = {K, 16, 2, rows / 16};
+  const cuuint64_t strides[3] = {K * 2, I * K * 2, 16 * K * 2};
+  const cuuint32_t box[4] = {64, 16, 2, 4};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for the interleaved map [%llu x %llu], I=%llu", (int)r,
+              (unsigned long long)rows, (unsigned long long)K, (unsigned long long)I);
+    return false;
+  }
+  return true;
+}
+
 // ------------------------------------------------------- MoE workspace --
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 

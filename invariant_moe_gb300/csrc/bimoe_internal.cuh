@@ -47,6 +47,11 @@ struct ContextSetup {
 bool make_tma_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 // Same for a row-major fp32 tensor with a [box_rows, 32]-element box.
+// The gate/up weights W13 [E, 2I, K] bf16 viewed as {K, 16, 2, E*2I/16}:
+// a box {64, 16, 2, 4} at group g lands 16 gate rows, the 16 up rows of the
+// same features (I rows further), and so on for four groups: 64 features'
+// interleaved rows in one copy, 128-byte swizzled like the 2-D map's.
+bool make_tma_inter_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t I, uint64_t K);
 bool make_tma_2d_f32(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
 void set_error(const char *fmt, ...);
@@ -325,6 +330,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// 4-D tiled load (the interleaved gate/up weight map: coordinates {k, row
+// in group, gate/up half, 16-row group}).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 

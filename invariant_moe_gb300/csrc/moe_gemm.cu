@@ -84,7 +84,6 @@ constexpr int kAuxBytes = 12288;            // barriers, tile prefix, expert off
 // with few tokens per expert a CTA's time is the weight stream, and the
 // bytes it keeps in flight set its rate.
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kInterBox = 16 * kBK * 2;  // INTER: bytes of one 16-row A box
 
 template <bool GATE_UP, bool PAIR, bool INTER = false, bool NARROW = false>
 struct GemmCfg {
@@ -519,12 +518,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), pair_bytes);
             if (INTER) {
               // 16 gate rows, the 16 up rows of the same features, and so on
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                tma_load_2d_pair(smem_u32(st + (2 * g) * kInterBox), &tmA, fb, kb * kBK, a_row + 16 * g);
-                tma_load_2d_pair(smem_u32(st + (2 * g + 1) * kInterBox), &tmA, fb, kb * kBK,
-                                 a_row + prm.up_offset + 16 * g);
-              }
+              // for four groups: one copy through the 4-D interleaved map
+              tma_load_4d_pair(smem_u32(st), &tmA, fb, kb * kBK, 0, 0, a_row / 16);
             } else {
               tma_load_2d_pair(smem_u32(st), &tmA, fb, kb * kBK, a_row);
               if (GATE_UP)
@@ -539,12 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t fb = smem_u32(&full[stage]);
             mbar_arrive_expect_tx(fb, stage_bytes);
             if (INTER) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                tma_load_2d(smem_u32(st + (2 * g) * kInterBox), &tmA, fb, kb * kBK, a_row + 16 * g);
-                tma_load_2d(smem_u32(st + (2 * g + 1) * kInterBox), &tmA, fb, kb * kBK,
-                            a_row + prm.up_offset + 16 * g);
-              }
+              tma_load_4d(smem_u32(st), &tmA, fb, kb * kBK, 0, 0, a_row / 16);
             } else {
               tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
             }
@@ -960,7 +950,10 @@ template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false,
 static bi_status run_gemm(const void *wt, int64_t w_rows, uint32_t box_a, const void *tok, int64_t P,
                           int64_t K, const GemmParams &p, cudaStream_t stream, int64_t tok_rows = 0) {
   CUtensorMap tmA, tmB;
-  if (!make_tma_2d_bf16(&tmA, wt, static_cast<uint64_t>(w_rows), static_cast<uint64_t>(K), box_a) ||
+  const bool amap = INTER ? make_tma_inter_bf16(&tmA, wt, static_cast<uint64_t>(w_rows),
+                                                static_cast<uint64_t>(p.up_offset), static_cast<uint64_t>(K))
+                          : make_tma_2d_bf16(&tmA, wt, static_cast<uint64_t>(w_rows), static_cast<uint64_t>(K), box_a);
+  if (!amap ||
       !make_tma_2d_bf16(&tmB, tok, static_cast<uint64_t>(GATHER ? tok_rows : P), static_cast<uint64_t>(K),
                         GATHER ? 1u : static_cast<uint32_t>(GemmCfg<GATE_UP, PAIR, INTER, NARROW>::kBNc)))
     return BI_ERR_CUDA;
@@ -979,7 +972,7 @@ static bi_status gate_up_any(const void *tok, int64_t M, const int32_t *offsets,
   // features per tile: 128 (one CTA), 256 (pair), 128 (pair, interleaved:
   // 64 per CTA), 64 (one CTA, interleaved)
   const int wb_rows = inter ? (pair ? kBM : kBM / 2) : (pair ? 2 * kBM : kBM);
-  const uint32_t box_a = inter ? kInterBox / 128 : kBM;
+  const uint32_t box_a = kBM;  // (interleaved tiles use the 4-D map)
   GemmParams p{offsets, perm, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I,
                (int)(2 * I), (int)I, device_error_word(), (int)P, (int)top_k, nullptr, 0, nullptr, nullptr, 0};
   const int64_t wr = E * 2 * I;
@@ -1049,7 +1042,7 @@ bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts,
   const int v = pick_variant(I, true, H, P, E);  // narrow: 4 (interleaved 64-feature tiles) or 1
   const bool inter = v == 4;
   const int wb_rows = inter ? kBM / 2 : kBM;
-  const uint32_t box_a = inter ? kInterBox / 128 : kBM;
+  const uint32_t box_a = kBM;  // (interleaved tiles use the 4-D map)
   GemmParams g{nullptr, nullptr, wts, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I, (int)(2 * I),
                (int)I, device_error_word(), (int)P, (int)top_k, ids, (int)M, counters, lout, (int)(H / 32),
                scores, ids_out, wts_out};
