@@ -33,7 +33,8 @@
 //         H >= 4096 once the experts average 64 or more rows) or one CTA
 //         per tile (automatic for the smallest decode batches): each CTA
 //         holds 64 gate rows and the matching 64 up rows against up to 256
-//         tokens; a lane and its partner lane swap half of each chunk.
+//         tokens (one 4-D TMA copy lands the 16-row gate and up groups
+//         interleaved); a lane and its partner lane swap half of each chunk.
 //     and two token-tile widths: up to 128/256 tokens, or NARROW tiles of up
 //     to 32 tokens with the deepest ring shared memory allows, for batches of
 //     at most 16 rows per expert on average (decode), where the weight
@@ -44,8 +45,9 @@
 //     accumulators are double buffered (2 x 256 tensor-memory columns) so the
 //     epilogue of one tile overlaps the MMAs of the next.
 //   * warp roles: warp 0 issues TMA, warp 1 owns tensor memory and issues the
-//     MMAs (both warp-uniform, one elected lane issuing), warps 2-5 drain the
-//     accumulator (tcgen05.ld).  Every mbarrier wait is bounded.
+//     MMAs (each loop inside one elect_one() block: a single thread issues a
+//     stage's copies or MMAs back to back with uniform operands), warps 2-5
+//     drain the accumulator (tcgen05.ld).  Every mbarrier wait is bounded.
 //   * persistent grid (one CTA, or CTA pair, per SM or SM pair); tiles are
 //     ordered expert, weight block, token block, so the token blocks of a
 //     weight block run back to back and share it through L2.
