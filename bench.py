@@ -158,17 +158,41 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def code_digest(text):
+    """sha256 of C/CUDA source with its comments and all whitespace removed:
+    the same for two revisions that differ only in comments or layout."""
+    import hashlib
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # a string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return hashlib.sha256("".join("".join(out).split()).encode()).hexdigest()
+
+
 def captured_traffic(workload, M, kernel):
     """DRAM bytes per full-size launch of an expert GEMM from the committed
-    ncu capture of this workload, or None when there is none or the kernel
-    source changed since it was taken."""
-    import hashlib
+    ncu capture of this workload, or None when there is none or the kernel's
+    code (comments aside) changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"moe_gemm_{workload}_{M}_traffic.json")
     src = os.path.join(ROOT, "invariant_moe_gb300", "csrc", "moe_gemm.cu")
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
     d = json.load(open(path))
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("kernel_source_sha256"):
+    if code_digest(open(src).read()) != d.get("kernel_code_sha256"):
         return None
     k = d.get(kernel, {})
     return k.get("dram_bytes_per_full_launch") or None

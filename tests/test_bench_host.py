@@ -71,3 +71,12 @@ def test_summary_digest_keys():
     assert s["router_dsv4_warm_us_fp32frac"] == {"1": [3.7, 0.007]}
     assert s["cublas_fp32_rows_changed_vs_M4096"] == {"1": 1}
     assert s["layer_cold_us_hbmfrac"]["1"] == [100.0, 0.5]
+
+
+def test_code_digest_ignores_comments_not_code():
+    src = 'int f(int a) {  // add one\n  /* block\n comment */ return a + 1;\n}\nconst char *s = "// kept";\n'
+    same = 'int f(int a) {\n return a + 1; }   // other words\nconst char *s = "// kept";'
+    assert bench.code_digest(src) == bench.code_digest(same)
+    assert bench.code_digest(src) != bench.code_digest(src.replace("a + 1", "a + 2"))
+    assert bench.code_digest(src) != bench.code_digest(src.replace('"// kept"', '"// gone"'))
+
