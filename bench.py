@@ -981,6 +981,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--router-sweep", action="store_true",
                     help="only print the router device-time sweep (DSv4 router shape)")
+    ap.add_argument("--router-ms", default=None,
+                    help="comma-separated batch sizes for --router-sweep (default: 1 ... 4096)")
     ap.add_argument("--topk-window-sweep", action="store_true",
                     help="only print the windowed top-k device-time sweep")
     ap.add_argument("--moe-sweep", action="store_true",
@@ -997,7 +999,8 @@ def main(argv=None):
     if args.router_sweep:
         import torch
         torch.cuda.set_device(local)
-        print(json.dumps({"router_us_vs_M": router_sweep(torch.device("cuda", local))}), flush=True)
+        kw = {"Ms": tuple(int(m) for m in args.router_ms.split(","))} if args.router_ms else {}
+        print(json.dumps({"router_us_vs_M": router_sweep(torch.device("cuda", local), **kw)}), flush=True)
         return
     if args.topk_window_sweep:
         import torch
