@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT, TW>::GT
                                   TiledCfg<TMR, TN, RB, CB, G, NSTG, XT, TW>::kMinBlocks)
     router_tiled_kernel(const __grid_constant__ CUtensorMap tmW, const XT *__restrict__ x,
                         const float *__restrict__ w, const float *__restrict__ bias, float *__restrict__ y,
-                        int M, int K, int N) {
+                        int M, int K, int N, int *err) {
   using Cf = TiledCfg<TMR, TN, RB, CB, G, NSTG, XT, TW>;
   constexpr int GT = Cf::GT, BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd, WLd = Cf::WLd;
   constexpr int XS = Cf::XS, WS = Cf::WS, GS = Cf::GS;
@@ -419,9 +419,9 @@ __global__ void __launch_bounds__(TiledCfg<TMR, TN, RB, CB, G, NSTG, XT, TW>::GT
     cp_async_commit();
     const float *xb = xs + (ch % NSTG) * (BM * XLd);
     const float *wb = ws + (ch % NSTG) * WS;
-    // TW: the chunk's W copy (a timeout is recorded nowhere here: the
-    // kernel goes on and its outputs are undefined, but it ends)
-    if (TW) mbar_wait(smem_u32(&wbar[grp * NSTG + ch % NSTG]), static_cast<uint32_t>((ch / NSTG) & 1), nullptr, nullptr);
+    // TW: the chunk's W copy (a wait that times out records
+    // BI_DEVERR_WAIT_TIMEOUT; the kernel goes on, its outputs undefined)
+    if (TW) mbar_wait(smem_u32(&wbar[grp * NSTG + ch % NSTG]), static_cast<uint32_t>((ch / NSTG) & 1), nullptr, err);
 #pragma unroll
     for (int kk = 0; kk < kTBK; kk += 4) {
       float4 xv[TMR], wv[TN];
@@ -518,7 +518,7 @@ static bi_status launch_tiled_t(const XT *x, const float *w, const float *b, flo
   if (TW && !make_tma_2d_f32(&tmW, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), Cf::BN))
     return BI_ERR_CUDA;
   return launch_chained(router_tiled_kernel<TMR, TN, RB, CB, G, NSTG, XT, TW>, grid, dim3(Cf::GT * G), Cf::kSmem,
-                        stream, 1, tmW, x, w, b, y, (int)M, (int)K, (int)N);
+                        stream, 1, tmW, x, w, b, y, (int)M, (int)K, (int)N, device_error_word());
 }
 
 // The classic shapes: 8 warps per group, 4 columns per thread, 3 stages.
