@@ -69,6 +69,34 @@ def test_forced_schedules_agree(dev_inputs, M):
         assert torch.equal(ys[0], y), f"M={M}: schedule {s} differs from schedule 1"
 
 
+@pytest.mark.parametrize("N,K,xdt", [(160, 2048, torch.float32), (160, 2048, torch.bfloat16),
+                                     (96, 1024, torch.float32)])
+def test_tiled_weight_rows_past_n(oracle_mod, cuda, N, K, xdt):
+    """The 7x8 tiled schedule stages 256 (or 128) weight rows per chunk --
+    by TMA for the 256-row tiles, whose rows past N arrive as the copy's
+    zero fill -- while N is smaller: the outputs are still those of the rows
+    and split schedules, bit for bit, and within the oracle's tolerance, at
+    a batch that takes the tiled schedule automatically (M >= 3072, a ragged
+    last tile of 28 rows)."""
+    M = 3100
+    g = syn.gen(N + K)
+    x = torch.randn(M, K, generator=g).to(xdt).to(cuda)
+    w = (torch.randn(N, K, generator=g) / 64).to(cuda)
+    b = (torch.randn(N, generator=g) * 0.01).to(cuda)
+    import invariant_moe_gb300 as bm
+    y9 = bm.bi_router_gemm(x, w, b, schedule=9)
+    y0 = bm.bi_router_gemm(x, w, b)
+    y4 = bm.bi_router_gemm(x, w, b, schedule=4)
+    y1 = bm.bi_router_gemm(x[:5].contiguous(), w, b, schedule=1)
+    torch.cuda.synchronize()
+    assert torch.equal(y9, y0)
+    assert torch.equal(y9, y4)
+    assert torch.equal(y9[:5], y1)
+    rows = [0, 1, 27, 28, 3071, M - 1]
+    r = oracle_mod.router(x[rows].float().cpu().numpy(), w.cpu().numpy(), b.cpu().numpy())
+    check_parity(y9[rows].cpu().numpy(), r)
+
+
 def test_same_row_at_any_position(dev_inputs):
     """A row's bits do not depend on its position or its neighbours."""
     x, w, b = dev_inputs
