@@ -648,7 +648,7 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   return v;
 }
 
-template <int TM, int TN, int NST, int L, typename XT, int CK>
+template <int TM, int TN, int NST, int L, typename XT, int CK, bool ROLL = false>
 __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restrict__ x,
                                                               const float *__restrict__ w,
                                                               const float *__restrict__ bias,
@@ -703,7 +703,12 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
     cp_async_commit();
   }
   const int a = lane / kSpLN, b = lane % kSpLN;
-#pragma unroll
+  // ROLL: a runtime loop over the slice's chunks.  Unrolled, the slice is
+  // several thousand instructions of straight-line code that each warp runs
+  // once, and instruction fetch becomes the main stall once the warps' FMA
+  // work is long enough (measured on GB300, K=4096/N=256: 8-20 % faster for
+  // bf16 x at M >= 128, for fp32 x at M >= 1024; 1-7 % slower below)
+#pragma unroll(ROLL ? 1 : kChunks)
   for (int q = 0; q < kChunks; ++q) {
     cp_async_wait<NST - 2>();
     __syncwarp();  // every lane's pieces of chunk q landed; stage of q-1 free
@@ -772,7 +777,7 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
   cluster_sync_all();  // no CTA leaves while a peer still reads its partials
 }
 
-template <int TM, int TN, int NST, int CK, int L, typename XT>
+template <int TM, int TN, int NST, int CK, int L, typename XT, bool ROLL>
 static bi_status launch_split_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, cudaStream_t stream) {
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
@@ -782,7 +787,7 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_done.pending(dev)) {
-    if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT, CK>,
+    if (cudaFuncSetAttribute(router_split_kernel<TM, TN, NST, L, XT, CK, ROLL>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -793,7 +798,7 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   }
   dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
             static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
-  return launch_chained(router_split_kernel<TM, TN, NST, L, XT, CK>, grid, dim3(32 * L), smem, stream, C,
+  return launch_chained(router_split_kernel<TM, TN, NST, L, XT, CK, ROLL>, grid, dim3(32 * L), smem, stream, C,
                         x, w, b, y, (int)M, (int)K, (int)N);
 }
 
@@ -827,15 +832,24 @@ static int split_pick(int64_t M, int64_t N, int C) {
   return 0;
 }
 
+template <int L, typename XT, bool ROLL>
+static bi_status launch_split_r(const XT *x, const float *w, const float *b, float *y, int64_t M,
+                                int64_t K, int64_t N, int tile, cudaStream_t stream) {
+  switch (tile) {
+    case 0: return launch_split_t<2, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
+    case 1: return launch_split_t<4, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
+    case 2: return launch_split_t<4, 4, 3, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
+    default: return launch_split_t<8, 4, 2, 16, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
+  }
+}
+
+// The chunk loop rolled where that measured faster (see router_split_kernel).
 template <int L, typename XT>
 static bi_status launch_split_l(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                 int64_t K, int64_t N, int tile, cudaStream_t stream) {
-  switch (tile) {
-    case 0: return launch_split_t<2, 2, 4, 32, L, XT>(x, w, b, y, M, K, N, stream);
-    case 1: return launch_split_t<4, 2, 4, 32, L, XT>(x, w, b, y, M, K, N, stream);
-    case 2: return launch_split_t<4, 4, 3, 32, L, XT>(x, w, b, y, M, K, N, stream);
-    default: return launch_split_t<8, 4, 2, 16, L, XT>(x, w, b, y, M, K, N, stream);
-  }
+  const bool roll = M >= (sizeof(XT) == 2 ? 128 : 1024);
+  return roll ? launch_split_r<L, XT, true>(x, w, b, y, M, K, N, tile, stream)
+              : launch_split_r<L, XT, false>(x, w, b, y, M, K, N, tile, stream);
 }
 
 // tile < 0: chosen from M.  Needs split_warps(K) != 0.
