@@ -259,11 +259,13 @@ BI_API bi_status bi_moe_forward(const bi_bf16 *x, const int32_t *ids,
  * and the expert path; the bits of bi_router_topk_bf16 followed by
  * bi_moe_forward, whose contracts it combines.  The pages' router and
  * fused-MoE are separate ops; this library adds the combination so that a
- * decode-sized batch (M * top_k <= 32) runs in three launches: the router,
- * then a gate/up GEMM whose every CTA selects the rows' experts from the
- * scores itself (bi_topk's selection) and writes ids / wts once, then the
- * down GEMM with the combine fused.  Larger batches: router, selection grid,
- * bi_moe_forward's kernels.
+ * decode-sized batch (M * top_k <= 32) runs in two or three launches: the
+ * router, then the expert GEMMs, whose every CTA selects the rows' experts
+ * from the scores itself (bi_topk's selection; one CTA writes ids / wts),
+ * with the combine fused into the down GEMM: one launch for both GEMMs
+ * where the gate/up tiles fit one wave on the SMs (bi_moe_decode_fused),
+ * else a gate/up launch and a down launch.  Larger batches: router,
+ * selection grid, bi_moe_forward's kernels.
  *   x        [M,H] bf16 (device, 16-byte aligned)
  *   w_router [E,H] fp32 (device, 16-byte aligned); bias [E] fp32 or NULL
  *   w13, w2, out, workspace: as bi_moe_forward (workspace >=
@@ -567,6 +569,21 @@ BI_API bi_status bi_moe_gemm_variant(int32_t variant, int32_t *previous);
 BI_API bi_status bi_moe_gate_up_feed(int32_t mode, int32_t *previous);
 
 /*
+ * bi_moe_decode_fused -- how bi_moe_layer runs the expert GEMMs of a
+ * decode-sized batch (M * top_k <= 32 under the automatic variant, with
+ * 64-feature interleaved gate/up tiles, i.e. min(E, M * top_k) * I / 64 at
+ * most the SM count), for the whole process from the next call on:
+ *   0  automatic (the default): one launch (its gate/up tiles, a wait of
+ *      every CTA for all of them, then the down tiles with the fused
+ *      combine);
+ *   1  two launches (the gate/up GEMM, then the down GEMM with the fused
+ *      combine), as bi_moe_forward's decode path.
+ * Same bits either way (tests compare them).  *previous (may be NULL)
+ * receives the old setting; other values BI_ERR_INVALID_ARG.
+ */
+BI_API bi_status bi_moe_decode_fused(int32_t mode, int32_t *previous);
+
+/*
  * bi_fp32_fma_probe -- MEASUREMENT ONLY, not part of the MoE path: blocks x
  * 256 threads, each running 16 independent fp32 FMA chains for `iters`
  * steps (2 * 16 * iters flop per thread, no memory traffic in the loop).
@@ -580,13 +597,16 @@ BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters,
 /*
  * bi_wait_timeout_probe -- TEST USE ONLY, not part of the MoE path and not on
  * the pages (it exercises this library's bounded-wait discipline): one CTA
- * waits, through the same bounded mbarrier wait the GEMM kernels use, on a
- * barrier phase that nothing completes.  The wait gives up after its limit
- * (one second of the GPU's global timer), records BI_DEVERR_WAIT_TIMEOUT in
- * the device error word and the kernel returns; nothing faults or traps and
- * the context stays usable.  Read the outcome with bi_device_error.
+ * waits on something that never happens, through one of the bounded waits
+ * the GEMM kernels use: which = 0, the mbarrier wait of the stage rings, on
+ * a barrier phase that nothing completes; which = 1, the arrival-count wait
+ * of the one-launch decode layer, on a count that nothing raises.  The wait
+ * gives up after its limit (one second of the GPU's global timer), records
+ * BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel returns;
+ * nothing faults or traps and the context stays usable.  Read the outcome
+ * with bi_device_error.  Other values of which: BI_ERR_INVALID_ARG.
  */
-BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream);
+BI_API bi_status bi_wait_timeout_probe(int32_t which, bi_stream_t stream);
 
 
 #ifdef __cplusplus

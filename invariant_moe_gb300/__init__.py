@@ -37,7 +37,7 @@ EXPORTS = [
     "bi_fp32_fma_probe", "bi_wait_timeout_probe", "bi_moe_gemm_variant", "bi_router_topk", "bi_router_topk_schedule",
     "bi_topk_window", "bi_router_gemm_bf16", "bi_router_gemm_bf16_schedule", "bi_router_topk_bf16",
     "bi_moe_gather_routing", "bi_moe_scatter_contrib", "bi_router_topk_bf16_schedule",
-    "bi_moe_gate_up_tokens", "bi_moe_gate_up_feed", "bi_moe_layer",
+    "bi_moe_gate_up_tokens", "bi_moe_gate_up_feed", "bi_moe_layer", "bi_moe_decode_fused",
 ]
 
 
@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_moe_combine_consume": ([P, P, I64, I64, I32, P], ST),
             "bi_moe_gemm_variant": ([I32, P], ST),
             "bi_moe_gate_up_feed": ([I32, P], ST),
+            "bi_moe_decode_fused": ([I32, P], ST),
             "bi_moe_layer": ([P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, I64, P, SZ, P], ST),
             "bi_moe_gate_up_tokens": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_router_topk": ([P, P, P, P, P, P, P, I64, I64, I64, I32, P], ST),
@@ -96,7 +97,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "bi_router_topk_bf16_schedule": ([P, P, P, P, P, P, P, I64, I64, I64, I32, I32, P], ST),
             "bi_moe_forward_noalloc": ([P, P, P, P, P, P, I64, I64, I64, I32, I64, P], ST),
             "bi_fp32_fma_probe": ([P, I64, I32, P], ST),
-            "bi_wait_timeout_probe": ([P], ST),
+            "bi_wait_timeout_probe": ([I32, P], ST),
             "bi_moe_gather_routing": ([P, P, P, P, P, P, I64, I64, I32, I64, P], ST),
             "bi_moe_scatter_contrib": ([P, P, P, P, I64, I64, I64, I32, P], ST),
         }
@@ -328,6 +329,15 @@ def bi_moe_gate_up_feed(mode):
     return prev.value
 
 
+def bi_moe_decode_fused(mode):
+    """How bi_moe_layer runs a decode-sized batch's expert GEMMs (0 automatic
+    = one launch where it applies, 1 = a gate/up and a down launch); returns
+    the previous setting."""
+    prev = ctypes.c_int32(0)
+    _call("bi_moe_decode_fused", int(mode), ctypes.byref(prev))
+    return prev.value
+
+
 def bi_moe_down(act, offsets, perm, w2, M, top_k, contrib=None, stream=None):
     E, H, I = w2.shape
     dev = act.device
@@ -453,10 +463,11 @@ def bi_fp32_fma_probe(blocks, iters, stream=None, out=None):
     return out
 
 
-def bi_wait_timeout_probe(stream=None):
-    """Test use only: a kernel whose bounded mbarrier wait runs out (about one
-    second); read the recorded BI_DEVERR_WAIT_TIMEOUT with device_error()."""
-    _call("bi_wait_timeout_probe", _stream(stream))
+def bi_wait_timeout_probe(which=0, stream=None):
+    """Test use only: a kernel whose bounded wait runs out (about one second):
+    which = 0 the mbarrier wait, 1 the arrival-count wait; read the recorded
+    BI_DEVERR_WAIT_TIMEOUT with device_error()."""
+    _call("bi_wait_timeout_probe", int(which), _stream(stream))
 
 
 def bi_moe_layer(x, w_router, w13, w2, top_k, bias=None, out=None, scores=None, ids=None, wts=None,

@@ -14,7 +14,7 @@ namespace bimoe {
 bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
                         int64_t, int, cudaStream_t);
 bi_status launch_router_bf16(const void *, const float *, const float *, float *, int64_t, int64_t,
-                             int64_t, int, cudaStream_t);
+                             int64_t, int, cudaStream_t, unsigned *zero_word);
 bi_status launch_topk_window(const float *, int64_t, const int64_t *, const int64_t *, int64_t,
                              int64_t, int32_t, int32_t *, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
@@ -40,6 +40,11 @@ size_t decode_counter_count(int64_t M, int64_t H);
 bi_status launch_moe_decode(const void *, const int32_t *, const float *, const void *, const void *, void *,
                             float *, int *, void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t,
                             const float *scores, int32_t *ids_out, float *wts_out);
+int set_decode_fused(int mode);
+bool decode_fused_ok(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I);
+bi_status launch_moe_decode_fused(const void *, const void *, const void *, void *, float *, int *, unsigned *,
+                                  void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t,
+                                  const float *scores, int32_t *ids_out, float *wts_out);
 // How bi_moe_forward feeds the gate/up GEMM its token rows: 0 automatic (the
 // copy), 1 the gather kernel's contiguous copy, 2 gathered by the GEMM itself
 // (tile::gather4).  Measured on GB300 at M=4096 the GEMM gathering its own
@@ -68,7 +73,7 @@ bi_status launch_gather_routing(const int32_t *, const float *, const int32_t *,
                                 int64_t, int64_t, int32_t *, float *, cudaStream_t);
 bi_status launch_scatter_contrib(const float *, const int32_t *, const int32_t *, int64_t, int64_t, int64_t,
                                  float *, cudaStream_t);
-bi_status launch_wait_timeout_probe(cudaStream_t);
+bi_status launch_wait_timeout_probe(int, cudaStream_t);
 
 // ------------------------------------------------------------ error state --
 static thread_local char g_msg[512] = "";
@@ -242,7 +247,7 @@ bool make_tma_inter_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct MoeWorkspace {
-  size_t offsets, perm, slot_mask, scratch, xperm, act, contrib, counters, total;
+  size_t offsets, perm, slot_mask, scratch, xperm, act, contrib, counters, gridbar, total;
 };
 
 static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
@@ -257,6 +262,7 @@ static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, i
   w.act = off;     off += align256(P * I * 2);
   w.contrib = off; off += align256(P * H * sizeof(float));
   w.counters = off; off += align256(decode_counter_count(M, H) * sizeof(int));
+  w.gridbar = off; off += 256;  // the one-launch decode layer's arrival count
   w.total = off;
   return w;
 }
@@ -374,7 +380,7 @@ BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w, 
   if (st != BI_OK) return st;
   BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   if (M == 0) return BI_OK;
-  return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream));
+  return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 BI_API bi_status bi_router_gemm_bf16(const bi_bf16 *x, const float *w, const float *bias, float *y,
@@ -411,7 +417,7 @@ static bi_status launch_router_any(const float *x, const float *w, const float *
 }
 static bi_status launch_router_any(const __nv_bfloat16 *x, const float *w, const float *b, float *y,
                                    int64_t M, int64_t K, int64_t N, int schedule, cudaStream_t s) {
-  return launch_router_bf16(x, w, b, y, M, K, N, schedule, s);
+  return launch_router_bf16(x, w, b, y, M, K, N, schedule, s, nullptr);
 }
 
 // Router + selection: schedule 0 picks by M (the one-kernel path for small
@@ -491,8 +497,9 @@ BI_API bi_status bi_fp32_fma_probe(float *out, int64_t blocks, int32_t iters, bi
   return launch_fp32_fma_probe(out, blocks, iters, reinterpret_cast<cudaStream_t>(stream));
 }
 
-BI_API bi_status bi_wait_timeout_probe(bi_stream_t stream) {
-  return launch_wait_timeout_probe(reinterpret_cast<cudaStream_t>(stream));
+BI_API bi_status bi_wait_timeout_probe(int32_t which, bi_stream_t stream) {
+  BI_REQUIRE(which == 0 || which == 1, BI_ERR_INVALID_ARG, "wait probe %d not in {0, 1}", which);
+  return launch_wait_timeout_probe(which, reinterpret_cast<cudaStream_t>(stream));
 }
 
 BI_API size_t bi_moe_workspace_bytes(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
@@ -694,10 +701,19 @@ BI_API bi_status bi_moe_layer(const bi_bf16 *x, const float *w_router, const flo
   const MoeWorkspace L = moe_layout(M, H, E, top_k, I);
   BI_REQUIRE(workspace_bytes >= L.total, BI_ERR_WORKSPACE, "workspace %zu < %zu bytes", workspace_bytes, L.total);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_router_bf16(x, w_router, bias, scores, M, H, E, 0, s)) != BI_OK) return st;
-  if (g_gate_up_feed.load() == 0 && decode_path_ok(M, E, top_k)) {
+  char *ws = static_cast<char *>(workspace);
+  const bool decode = g_gate_up_feed.load() == 0 && decode_path_ok(M, E, top_k);
+  // decode-sized batch with the one-launch expert path: the router zeroes
+  // its arrival count
+  unsigned *gridbar = decode && decode_fused_ok(M, H, E, top_k, I) ? reinterpret_cast<unsigned *>(ws + L.gridbar)
+                                                                   : nullptr;
+  if ((st = launch_router_bf16(x, w_router, bias, scores, M, H, E, 0, s, gridbar)) != BI_OK) return st;
+  if (gridbar)
+    return launch_moe_decode_fused(x, w13, w2, ws + L.act, reinterpret_cast<float *>(ws + L.contrib),
+                                   reinterpret_cast<int *>(ws + L.counters), gridbar, out, M, H, E, top_k, I, s,
+                                   scores, ids, wts);
+  if (decode) {
     // decode-sized batch: the gate/up GEMM selects the experts itself
-    char *ws = static_cast<char *>(workspace);
     return launch_moe_decode(x, nullptr, nullptr, w13, w2, ws + L.act, reinterpret_cast<float *>(ws + L.contrib),
                              reinterpret_cast<int *>(ws + L.counters), out, M, H, E, top_k, I, s, scores, ids, wts);
   }
@@ -710,6 +726,13 @@ BI_API bi_status bi_moe_layer(const bi_bf16 *x, const float *w_router, const flo
 BI_API bi_status bi_moe_gate_up_feed(int32_t mode, int32_t *previous) {
   BI_REQUIRE(mode >= 0 && mode <= 2, BI_ERR_INVALID_ARG, "feed mode %d not in {0, 1, 2}", mode);
   const int old = g_gate_up_feed.exchange(mode);
+  if (previous) *previous = old;
+  return BI_OK;
+}
+
+BI_API bi_status bi_moe_decode_fused(int32_t mode, int32_t *previous) {
+  BI_REQUIRE(mode == 0 || mode == 1, BI_ERR_INVALID_ARG, "decode layer mode %d not in {0, 1}", mode);
+  const int old = bimoe::set_decode_fused(mode);
   if (previous) *previous = old;
   return BI_OK;
 }

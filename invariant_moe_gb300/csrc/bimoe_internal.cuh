@@ -262,6 +262,39 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, vola
   }
 }
 
+// ---- grid-wide arrival count (one launch whose CTAs are all resident)
+// Release-add / acquire-load of a global counter at GPU scope, and the proxy
+// fence that orders generic-proxy global accesses with the thread's later
+// TMA (async-proxy) accesses.
+__device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait for *p >= target (acquire).  Returns false (after flagging, as
+// mbar_wait) when the limit passes or *abort is set.
+__device__ __forceinline__ bool wait_count_geq(const unsigned *p, unsigned target, volatile int *abort,
+                                               int *err) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (abort) *abort = 1;
+      report_error(err, BI_DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---- thread-block clusters (CTA pairs)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -51,6 +51,10 @@
 //   * persistent grid (one CTA, or CTA pair, per SM or SM pair); tiles are
 //     ordered expert, weight block, token block, so the token blocks of a
 //     weight block run back to back and share it through L2.
+//   * decode-sized batches: every CTA derives the routing itself (DECODE);
+//     in the layer call the gate/up and down GEMMs can run as one launch
+//     (moe_decode_layer_kernel: the gate/up tiles, a bounded wait of every
+//     CTA for all of them, then the down tiles with the combine fused).
 #include <atomic>
 #include <mutex>
 
@@ -134,6 +138,18 @@ struct GemmParams {
   float *wts_out;
 };
 
+// The down phase of the one-launch decode layer (moe_decode_layer_kernel):
+// its shape, and the word the gate/up phase's epilogue warps arrive on.
+struct DownPhase {
+  void *out;              // contributions fp32 [M*top_k, H]
+  int K;                  // I
+  int n_wb;               // weight blocks per expert (H / 128)
+  int wb_rows;            // 128
+  int out_ld;             // H
+  int a_rows_per_expert;  // H
+  unsigned *grid_bar;     // arrivals: 4 per CTA (its epilogue warps); zero before the launch
+};
+
 // Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeMaxP):
 // every CTA of the two expert GEMMs derives the routing from the expert ids
 // itself, so no permutation, gather or combine kernel runs (see DECODE).
@@ -152,6 +168,13 @@ static_assert(8 * (2 * 16 + 2 * kNumAcc + 1) + 16 + 4 * (2 * 1025 + 8 * kDecodeM
 
 struct TileInfo {
   int e, wb, tok0, ntok;
+};
+
+// A compile-time phase for the per-tile code of the producer and epilogue
+// (gate/up or down), so that each phase's loops are compiled on their own.
+template <bool GU>
+struct PhaseTag {
+  static constexpr bool value = GU;
 };
 
 template <int kBN>
@@ -254,10 +277,23 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
 // valid slots stored) sums the k contributions in slot order and writes the
 // bf16 output -- the same sequence of adds as the combine kernel.  No warp
 // waits for another.
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false, bool DECODE = false>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmParams prm) {
+// FUSED (moe_decode_layer_kernel): the DECODE gate/up GEMM (interleaved rows,
+// GATHER) and the DECODE down GEMM in one launch of at most one CTA per SM.
+// The tile list is the gate/up tiles, then the down tiles (tmA2 / tmB2 / dn:
+// W2 and the activations); both phases use the same 20 KB stages.  Each
+// epilogue warp arrives on dn.grid_bar once the CTA's gate/up tiles are
+// stored; the producer may load a down tile's W2 rows before that, but loads
+// its activation rows only once every warp of every CTA has arrived (a
+// bounded wait), so the down phase reads complete activations.
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER, bool DECODE, bool FUSED>
+__device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &prm,
+                                              const CUtensorMap &tmA2, const CUtensorMap &tmB2,
+                                              const DownPhase &dn) {
+  static_assert(!FUSED || (GATE_UP && INTER && NARROW && GATHER && DECODE && !PAIR), "fused decode layer");
+  static_assert(!FUSED || (GemmCfg<true, false, true, true>::kStageBytes == GemmCfg<false, false, false, true>::kStageBytes &&
+                           GemmCfg<true, false, true, true>::kABytes == GemmCfg<false, false, false, true>::kABytes &&
+                           GemmCfg<true, false, true, true>::kBN == GemmCfg<false, false, false, true>::kBN),
+                "both phases of the fused decode layer share one stage layout");
   static_assert(!GATHER || GATE_UP, "the token gather feeds the gate/up GEMM");
   static_assert(!DECODE || (NARROW && !PAIR), "the decode path runs narrow tiles, one CTA per tile");
   static_assert(!DECODE || !GATE_UP || GATHER, "decode gate/up gathers its token rows");
@@ -302,7 +338,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nkb = prm.K / kBK;
+  // K blocks of a tile (the down tiles of FUSED reduce over dn.K)
+  auto nkb_of = [&](bool gu) { return ((FUSED && !gu) ? dn.K : prm.K) / kBK; };
   // A CTA pair walks the tile list as one unit: both CTAs see the same tiles.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
@@ -329,6 +366,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (FUSED) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
   }
   if (warp == 1) {
     if (PAIR) {
@@ -421,7 +462,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = DECODE ? *nd_s * prm.n_wb : tile_prefix[prm.E];
+  // FUSED: the gate/up tiles (n_gu of them), then the down tiles
+  const int n_gu = DECODE ? *nd_s * prm.n_wb : 0;
+  const int total_tiles = DECODE ? (FUSED ? n_gu + *nd_s * dn.n_wb : n_gu) : tile_prefix[prm.E];
+  auto gu_tile = [&](int tile) { return FUSED ? tile < n_gu : GATE_UP; };
+  const unsigned grid_arrivals = 4u * gridDim.x;  // FUSED: every epilogue warp of every CTA
   if (DECODE && GATE_UP && blockIdx.x == 0 && warp >= 2) {
     // tokens with no valid slot (no tile stores them) get zero output rows
     for (int m = 0; m < prm.M; ++m)
@@ -433,11 +478,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto tile_at = [&](int tile) {
     if constexpr (DECODE) {
       // one token tile per distinct expert (at most 32 pairs), its weight
-      // blocks in order
+      // blocks in order (FUSED: the gate/up list, then the down list)
       TileInfo t;
-      const int d = tile / prm.n_wb;
+      int local = tile, nwb = prm.n_wb;
+      if (FUSED && tile >= n_gu) {
+        local = tile - n_gu;
+        nwb = dn.n_wb;
+      }
+      const int d = local / nwb;
       t.e = dexp_s[d];
-      t.wb = tile - d * prm.n_wb;
+      t.wb = local - d * nwb;
       t.tok0 = dbeg_s[d];
       t.ntok = dcnt_s[d];
       return t;
@@ -457,11 +507,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
-    for (int tile = unit0; tile < total_tiles; tile += nunits) {
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) break;
+    bool gate = !FUSED;  // FUSED: the activations may be loaded (every gate/up tile stored)
+    // one tile's copies; returns false when the tile loop must stop
+    auto produce = [&](auto phase_tag, int tile) -> bool {
+      constexpr bool gu = decltype(phase_tag)::value;
+      constexpr bool gather_t = GATHER && gu;
       const TileInfo ti = tile_at(tile);
-      const int a_row = ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
-                        static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
+      const int nkb_t = nkb_of(gu);
+      const int a_row = (FUSED && !gu) ? ti.e * dn.a_rows_per_expert + ti.wb * dn.wb_rows
+                                       : ti.e * prm.a_rows_per_expert + ti.wb * prm.wb_rows +
+                                             static_cast<int>(rank) * (INTER ? kBM / 2 : kBM);
       // pair: the odd CTA stages tokens N/2.. of the tile's MMA N
       const int b_row = ti.tok0 + (rank ? ((ti.ntok + 15) & ~15) / 2 : 0);
       constexpr int kGroups = C::kBNc / 4;
@@ -478,13 +533,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int rows = PAIR ? max(0, min(ti.ntok - r * half, half)) : ti.ntok;
         return min(kGroups, (rows + 3) / 4);
       };
-      const int ngroups = GATHER ? real_groups(static_cast<int>(rank)) : kGroups;
-      const uint32_t stage_bytes = GATHER ? static_cast<uint32_t>(kABytes + ngroups * 4 * kBK * 2)
-                                          : static_cast<uint32_t>(kStageBytes);
+      const int ngroups = gather_t ? real_groups(static_cast<int>(rank)) : kGroups;
+      const uint32_t stage_bytes = gather_t ? static_cast<uint32_t>(kABytes + ngroups * 4 * kBK * 2)
+                                            : static_cast<uint32_t>(kStageBytes);
       const uint32_t pair_bytes =
           GATHER ? static_cast<uint32_t>(2 * kABytes + (real_groups(0) + real_groups(1)) * 4 * kBK * 2)
                  : 2u * static_cast<uint32_t>(kStageBytes);
-      if (GATHER) {
+      if (gather_t) {
         // the token of each gathered row (the warp fills the table, lane 0
         // issues); rows past the tile's tokens (and any position whose perm
         // entry is not a pair id, reported by the epilogue) fetch token 0,
@@ -507,7 +562,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       const bool el = elect_one();
       if (el) {
-        for (int kb = 0; kb < nkb; ++kb) {
+        // FUSED, before the gate opens: the stages (consecutive in the ring,
+        // from dq_stage, K blocks from dq_kb) whose weight rows are loading
+        // and whose activation rows wait for the gate/up phase
+        int dq_n = 0, dq_stage = 0, dq_kb = 0;
+        auto flush = [&]() {
+          fence_proxy_async_global();  // the activations were stored through the generic proxy
+          for (int i = 0; i < dq_n; ++i) {
+            const int s = dq_stage + i < kStages ? dq_stage + i : dq_stage + i - kStages;
+            tma_load_2d(smem_u32(tiles + s * kStageBytes + kABytes), &tmB2, smem_u32(&full[s]),
+                        (dq_kb + i) * kBK, b_row);
+          }
+          dq_n = 0;
+        };
+        for (int kb = 0; kb < nkb_t; ++kb) {
           if (!wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -535,15 +603,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             const uint32_t fb = smem_u32(&full[stage]);
             mbar_arrive_expect_tx(fb, stage_bytes);
-            if (INTER) {
+            if (INTER && gu) {
               tma_load_4d(smem_u32(st), &tmA, fb, kb * kBK, 0, 0, a_row / 16);
             } else {
-              tma_load_2d(smem_u32(st), &tmA, fb, kb * kBK, a_row);
+              tma_load_2d(smem_u32(st), (FUSED && !gu) ? &tmA2 : &tmA, fb, kb * kBK, a_row);
             }
             if (GATE_UP && !INTER)
               tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
-            if (!GATHER) tma_load_2d(smem_u32(st + kABytes), &tmB, fb, kb * kBK, b_row);
-            else
+            if (FUSED && !gu && !gate) {
+              // the stage's activation rows wait for the gate (the barrier
+              // already expects their bytes)
+              if (dq_n++ == 0) {
+                dq_stage = stage;
+                dq_kb = kb;
+              }
+              gate = ld_acquire_gpu(dn.grid_bar) >= grid_arrivals;
+              if (!gate && (dq_n == kStages || kb == nkb_t - 1)) {
+                // the ring (or the tile) is all waiting: wait for the gate/up
+                // phase.  After a timeout the loads are issued all the same,
+                // so every armed stage completes; the abort flag then stops
+                // the MMAs and the epilogue.
+                wait_count_geq(dn.grid_bar, grid_arrivals, abort_flag, prm.err);
+                gate = true;
+              }
+              if (gate) flush();
+            } else if (!gather_t) {
+              tma_load_2d(smem_u32(st + kABytes), (FUSED && !gu) ? &tmB2 : &tmB, fb, kb * kBK, b_row);
+            } else
               for (int g = 0; g < ngroups; ++g)
                 tma_gather4(smem_u32(st + kABytes + g * 4 * kBK * 2), &tmB, fb, kb * kBK, grow_s[4 * g],
                             grow_s[4 * g + 1], grow_s[4 * g + 2], grow_s[4 * g + 3]);
@@ -555,15 +641,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             phase ^= 1u;
           }
         }
+        if (FUSED && dq_n > 0) {
+          // only after a failed wait: complete the armed stages
+          flush();
+          gate = true;
+        }
       }
       // the ring state back on every lane (this also keeps grow_s until every
       // gather of the tile is issued)
       const int src = __ffs(__ballot_sync(0xffffffffu, el)) - 1;
+      if (FUSED) gate = __shfl_sync(0xffffffffu, gate ? 1 : 0, src) != 0;
       stage = __shfl_sync(0xffffffffu, stage, src);
       phase = __shfl_sync(0xffffffffu, phase, src);
       issued_mask = __shfl_sync(0xffffffffu, issued_mask, src);
       issued_parity = __shfl_sync(0xffffffffu, issued_parity, src);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, src) == 0) break;
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, src) != 0;
+    };
+    for (int tile = unit0; tile < total_tiles; tile += nunits) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0) != 0) break;
+      bool cont;
+      if constexpr (FUSED) {
+        cont = tile < n_gu ? produce(PhaseTag<true>{}, tile) : produce(PhaseTag<false>{}, tile);
+      } else {
+        cont = produce(PhaseTag<GATE_UP>{}, tile);
+      }
+      if (!cont) break;
     }
     if (lane == 0 && *abort_flag) {
       // let every copy this warp started land before the CTA can exit
@@ -596,12 +698,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the MMA N covers the tile's real tokens (a multiple of 16), so a
         // ragged last tile of an expert does not pay for padding columns
         const TileInfo ti = tile_at(tile);
+        const int nkb_t = FUSED && tile >= n_gu ? dn.K / kBK : prm.K / kBK;
         const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, (ti.ntok + 15) & ~15);
         if (!wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb_t; ++kb) {
           if (!wait(smem_u32(&full[stage]), phase, abort_flag)) {
             ok = false;
             break;
@@ -671,7 +774,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         nx_pair[i] = c < t.ntok ? perm_at(t.tok0 + c) : 0;
         nx_p[i] = 0.0f;
       }
-      if (GATE_UP) {
+      if (gu_tile(tile)) {
         // a perm entry that is not a pair id reads no probability (checked
         // again, and reported, when the tile is stored)
 #pragma unroll
@@ -682,9 +785,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     };
-    if (unit0 < total_tiles) prefetch(unit0);
-    for (int tile = unit0; tile < total_tiles; tile += nunits) {
+    // FUSED: one arrival on the gate once this warp's activation stores are
+    // done: the warp barrier orders every lane's stores before lane 0's
+    // release (cumulative, GPU scope); the proxy fence orders them before
+    // async-proxy (TMA) reads.  A fence in every lane before the warp barrier
+    // instead measured ~0.9 us slower per decode layer.
+    bool arrived = !FUSED, acquired = !FUSED;
+    auto arrive = [&]() {
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_global();
+        red_release_gpu_add(dn.grid_bar, 1u);
+      }
+      arrived = true;
+    };
+    // one tile's epilogue; returns false when the tile loop must stop
+    auto consume = [&](auto phase_tag, int tile) -> bool {
+      constexpr bool gu = decltype(phase_tag)::value;
       const TileInfo ti = tile_at(tile);
+      if (!arrived && !gu) arrive();  // this CTA's gate/up tiles are stored
+      // per-phase output (the down tiles of FUSED write dn.out)
+      const int out_ld_t = (FUSED && !gu) ? dn.out_ld : prm.out_ld;
+      void *out_t = (FUSED && !gu) ? dn.out : prm.out;
       int my_pair[kBN / 32];
       float my_p[kBN / 32];
 #pragma unroll
@@ -695,7 +817,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (tile + nunits < total_tiles) prefetch(tile + nunits);
       // one decision per warp (lanes can disagree at the instant a wait gives up)
       const bool okw = __all_sync(0xffffffffu, wait(smem_u32(&tfull[acc]), acc_phase, abort_flag) ? 1 : 0) != 0;
-      if (!okw) break;
+      if (!okw) return false;
+      if (!acquired && !gu) {
+        // the counters the combine below counts on were zeroed by every CTA
+        // before its arrival (this tile's MMAs ran after the gate opened, so
+        // the wait ends at once)
+        if (lane == 0) wait_count_geq(dn.grid_bar, grid_arrivals, abort_flag, prm.err);
+        __syncwarp();
+        acquired = true;
+      }
       {
         // perm entries of this tile that are not pair ids (the loads landed
         // long ago): reported once; nothing is stored through them below
@@ -709,15 +839,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
-      const int col = INTER ? ti.wb * prm.wb_rows + static_cast<int>(rank) * (kBM / 2) + 16 * q + (lane & 15)
-                            : ti.wb * prm.wb_rows + static_cast<int>(rank) * kBM + row;
+      const int col = (INTER && gu) ? ti.wb * prm.wb_rows + static_cast<int>(rank) * (kBM / 2) + 16 * q + (lane & 15)
+                                    : ti.wb * ((FUSED && !gu) ? dn.wb_rows : prm.wb_rows) +
+                                          static_cast<int>(rank) * kBM + row;
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         const int c0 = 32 * i;
         if (c0 >= ti.ntok) break;  // warp-uniform (and the same for both warps of a pair)
         uint32_t d[32];
         tmem_ld32(tbase + c0, d);
-        if (INTER) {
+        if (INTER && gu) {
           // lanes 0-15 hold the gate rows of 16 features, lanes 16-31 the up
           // rows of the same features: the gate lane keeps tokens 0-15 of the
           // chunk and hands 16-31 to its partner (lane ^ 16), which hands
@@ -736,7 +867,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (c0 + c < ti.ntok)
               act[static_cast<size_t>(ti.tok0 + c0 + c) * prm.out_ld + col] = swiglu_p(g, u, pc);
           }
-        } else if (GATE_UP) {
+        } else if (GATE_UP && !INTER) {
           uint32_t u[32];
           tmem_ld32(tbase + kBN + c0, u);
           tmem_ld_wait();
@@ -750,12 +881,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         } else {
           tmem_ld_wait();
-          float *contrib = static_cast<float *>(prm.out);
+          float *contrib = static_cast<float *>(out_t);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int pair = __shfl_sync(0xffffffffu, my_pair[i], c);
             if (c0 + c < ti.ntok && static_cast<unsigned>(pair) < static_cast<unsigned>(prm.P))
-              contrib[static_cast<size_t>(pair) * prm.out_ld + col] = __uint_as_float(d[c]);
+              contrib[static_cast<size_t>(pair) * out_ld_t + col] = __uint_as_float(d[c]);
           }
         }
       }
@@ -769,12 +900,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         mbar_arrive_relaxed(smem_u32(&tempty[acc]));
       }
-      if constexpr (DECODE && !GATE_UP) {
+      if (DECODE && !gu) {
         // fused combine for this warp's 32 features (see DECODE above): the
         // contribution stores are made visible, one arrival per token, and
         // each (token, 32-feature block) completed here is summed by this warp
-        const int fb32 = (ti.wb * prm.wb_rows + q * 32) / 32;
-        float *contrib = static_cast<float *>(prm.out);
+        const int fb32 = (ti.wb * ((FUSED && !gu) ? dn.wb_rows : prm.wb_rows) + q * 32) / 32;
+        float *contrib = static_cast<float *>(out_t);
         __threadfence();
         __syncwarp();
         int tok = 0;
@@ -796,18 +927,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           bool any = false;
           for (int t = 0; t < prm.top_k; ++t) {
             if (!((valid >> t) & 1u)) continue;
-            const float v = __ldcg(contrib + static_cast<size_t>(m * prm.top_k + t) * prm.out_ld + f);
+            const float v = __ldcg(contrib + static_cast<size_t>(m * prm.top_k + t) * out_ld_t + f);
             sum = any ? __fadd_rn(sum, v) : v;
             any = true;
           }
-          prm.lout[static_cast<size_t>(m) * prm.out_ld + f] = __float2bfloat16_rn(sum);
+          prm.lout[static_cast<size_t>(m) * out_ld_t + f] = __float2bfloat16_rn(sum);
         }
       }
       if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
       }
+      return true;
+    };
+    if (unit0 < total_tiles) prefetch(unit0);
+    for (int tile = unit0; tile < total_tiles; tile += nunits) {
+      bool cont;
+      if constexpr (FUSED) {
+        cont = tile < n_gu ? consume(PhaseTag<true>{}, tile) : consume(PhaseTag<false>{}, tile);
+      } else {
+        cont = consume(PhaseTag<GATE_UP>{}, tile);
+      }
+      if (!cont) break;
     }
+    if (!arrived) arrive();  // only gate/up tiles here, none, or a wait gave up
   }
 
   tc_fence_before();
@@ -820,6 +963,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
     else tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER = false, bool DECODE = false>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ GemmParams prm) {
+  moe_gemm_body<GATE_UP, PAIR, INTER, NARROW, GATHER, DECODE, false>(tmA, tmB, prm, tmA, tmB, DownPhase{});
+}
+
+// The expert path of a decode-sized layer in one launch (FUSED above): at
+// most one CTA per SM, all resident at once.
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_decode_layer_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ GemmParams prm, const __grid_constant__ CUtensorMap tmA2,
+                            const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ DownPhase dn) {
+  moe_gemm_body<true, false, true, true, true, true, true>(tmA, tmB, prm, tmA2, tmB2, dn);
 }
 
 // ------------------------------------------------------------------- host --
@@ -1056,6 +1215,85 @@ bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts,
                device_error_word(), (int)P, (int)top_k, scores ? ids_out : ids, (int)M, counters, lout,
                (int)(H / 32)};
   return run_gemm<false, false, false, true, false, true>(w2, E * H, kBM, act, P, I, d, stream);
+}
+
+// The decode-sized layer's expert path in one launch (moe_decode_layer_kernel),
+// for bi_moe_layer: where the decode gate/up GEMM runs 64-feature
+// interleaved tiles (their count fits one wave on the SMs), so that both
+// phases share the stage layout.  The caller zeroes *grid_bar in a kernel
+// earlier on the stream (the router's).  0 = automatic, 1 = never (the two
+// GEMM launches of launch_moe_decode instead).
+static std::atomic<int> g_decode_fused{0};
+
+int set_decode_fused(int mode) { return g_decode_fused.exchange(mode); }
+
+bool decode_fused_ok(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
+  const int64_t P = M * top_k;
+  return g_decode_fused.load() == 0 && decode_path_ok(M, E, top_k) && pick_variant(I, true, H, P, E) == 4;
+}
+
+bi_status launch_moe_decode_fused(const void *x, const void *w13, const void *w2, void *act, float *contrib,
+                                  int *counters, unsigned *grid_bar, void *out, int64_t M, int64_t H, int64_t E,
+                                  int32_t top_k, int64_t I, cudaStream_t stream, const float *scores,
+                                  int32_t *ids_out, float *wts_out) {
+  using C = GemmCfg<true, false, true, true>;
+  const int64_t P = M * top_k;
+  constexpr int wb_rows = kBM / 2;  // 64 interleaved gate/up features per tile
+  GemmParams g{nullptr, nullptr, nullptr, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I, (int)(2 * I),
+               (int)I, device_error_word(), (int)P, (int)top_k, nullptr, (int)M, counters,
+               static_cast<__nv_bfloat16 *>(out), (int)(H / 32), scores, ids_out, wts_out};
+  const DownPhase dn{contrib, (int)I, (int)(H / kBM), kBM, (int)H, (int)H, grid_bar};
+  CUtensorMap tmA, tmB, tmA2, tmB2;
+  if (!make_tma_inter_bf16(&tmA, w13, static_cast<uint64_t>(E * 2 * I), static_cast<uint64_t>(I),
+                           static_cast<uint64_t>(H)) ||
+      !make_tma_2d_bf16(&tmB, x, static_cast<uint64_t>(M), static_cast<uint64_t>(H), 1u) ||
+      !make_tma_2d_bf16(&tmA2, w2, static_cast<uint64_t>(E * H), static_cast<uint64_t>(I), kBM) ||
+      !make_tma_2d_bf16(&tmB2, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I), C::kBNc))
+    return BI_ERR_CUDA;
+  static std::mutex mu;
+  static ContextSetup setup;  // the shared-memory attribute is per context
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (setup.pending(dev)) {
+      cudaError_t e = cudaFuncSetAttribute(moe_decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           C::kSmemBytes);
+      int per_sm = 0;
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_layer_kernel, kGemmThreads,
+                                                          C::kSmemBytes);
+      if (e != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        set_error("decode layer kernel: cannot be resident (%s, %d per SM)", cudaGetErrorString(e), per_sm);
+        return BI_ERR_CUDA;
+      }
+      setup.done(dev);
+    }
+  }
+  // CTAs wait on one another, so all must be resident: at most one per SM
+  // (its shared memory allows no second), a cooperative launch
+  const int64_t tiles_ub = std::min<int64_t>(P, E) * (I / wb_rows + H / kBM);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), tiles_ub)));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_layer_kernel, tmA, tmB, g, tmA2, tmB2, dn);
+  if (e != cudaSuccess) {
+    set_error("decode layer launch: %s", cudaGetErrorString(e));
+    return BI_ERR_CUDA;
+  }
+  BI_CHECK_LAUNCH();
+  return BI_OK;
 }
 
 }  // namespace bimoe

@@ -27,20 +27,28 @@ __global__ void __launch_bounds__(256) fp32_fma_probe_kernel(float *__restrict__
   out[static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x] = s;
 }
 
-// One thread waits, through the library's bounded mbarrier wait, for a phase
-// of a barrier that nothing arrives on: the wait gives up after its limit,
-// records BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel
-// returns normally.
-__global__ void wait_timeout_probe_kernel(int *err) {
+// One thread waits, through one of the library's bounded waits, for
+// something that never happens: which = 0, a phase of an mbarrier that
+// nothing arrives on; which = 1, an arrival count (a word of this probe that
+// nothing raises) to reach 1.  The wait gives up after its limit, records
+// BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel returns
+// normally.
+__device__ unsigned g_probe_count;  // zero, never written
+
+__global__ void wait_timeout_probe_kernel(int which, int *err) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x != 0) return;
-  mbar_init(smem_u32(&bar), 1);
-  fence_barrier_init();
-  (void)mbar_wait(smem_u32(&bar), 0, nullptr, err);
+  if (which == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    (void)mbar_wait(smem_u32(&bar), 0, nullptr, err);
+  } else {
+    (void)wait_count_geq(&g_probe_count, 1u, nullptr, err);
+  }
 }
 
-bi_status launch_wait_timeout_probe(cudaStream_t stream) {
-  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(device_error_word());
+bi_status launch_wait_timeout_probe(int which, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(which, device_error_word());
   BI_CHECK_LAUNCH();
   return BI_OK;
 }

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ 
                                                          const float *__restrict__ w,
                                                          const float *__restrict__ bias,
                                                          float *__restrict__ y, int M, int K,
-                                                         int N, int *err) {
+                                                         int N, int *err, unsigned *zero_word) {
   constexpr int XP = XPitch<XT>::slice;
   extern __shared__ __align__(16) float sm[];
   float *ws = sm;                                              // [32][kSlicePad]
@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ 
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   griddep_wait();
+  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && lane == 0) *zero_word = 0u;
   const int S = K / kSlice;
   const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict
                                                             const float *__restrict__ w,
                                                             const float *__restrict__ bias,
                                                             float *__restrict__ y, int M, int K,
-                                                            int N, int *err) {
+                                                            int N, int *err, unsigned *zero_word) {
   constexpr int XP = XPitch<XT>::round;
   constexpr int kStageB = sl_stage_bytes<XT>();
   extern __shared__ __align__(16) float sm[];
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict
   __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
   griddep_wait();
+  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *zero_word = 0u;
   const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
   const int rounds = (S + kSlG - 1) / kSlG;
@@ -653,13 +655,14 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
                                                               const float *__restrict__ w,
                                                               const float *__restrict__ bias,
                                                               float *__restrict__ y, int M, int K,
-                                                              int N) {
+                                                              int N, unsigned *zero_word) {
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   constexpr int BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd, WLd = Cf::WLd;
   constexpr int kChunks = kSlice / CK;
   extern __shared__ __align__(16) uint8_t sp_smem[];
 
   griddep_wait();
+  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *zero_word = 0u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = K / kSlice / L;  // CTAs per cluster (the launch's cluster size)
   const int rank = static_cast<int>(cluster_ctarank());
@@ -779,7 +782,7 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
 
 template <int TM, int TN, int NST, int CK, int L, typename XT, bool ROLL>
 static bi_status launch_split_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, cudaStream_t stream) {
+                                int64_t K, int64_t N, cudaStream_t stream, unsigned *zero_word) {
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   const int C = static_cast<int>(K / kSlice) / L;
   const size_t smem = static_cast<size_t>(L) * Cf::WARP_BYTES;
@@ -799,7 +802,7 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
             static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
   return launch_chained(router_split_kernel<TM, TN, NST, L, XT, CK, ROLL>, grid, dim3(32 * L), smem, stream, C,
-                        x, w, b, y, (int)M, (int)K, (int)N);
+                        x, w, b, y, (int)M, (int)K, (int)N, zero_word);
 }
 
 // Lane tiles of the split schedule (outputs per thread TM x TN, ring depth,
@@ -834,33 +837,33 @@ static int split_pick(int64_t M, int64_t N, int C) {
 
 template <int L, typename XT, bool ROLL>
 static bi_status launch_split_r(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, int tile, cudaStream_t stream) {
+                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
   switch (tile) {
-    case 0: return launch_split_t<2, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
-    case 1: return launch_split_t<4, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
-    case 2: return launch_split_t<4, 4, 3, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
-    default: return launch_split_t<8, 4, 2, 16, L, XT, ROLL>(x, w, b, y, M, K, N, stream);
+    case 0: return launch_split_t<2, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
+    case 1: return launch_split_t<4, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
+    case 2: return launch_split_t<4, 4, 3, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
+    default: return launch_split_t<8, 4, 2, 16, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
   }
 }
 
 // The chunk loop rolled where that measured faster (see router_split_kernel).
 template <int L, typename XT>
 static bi_status launch_split_l(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, int tile, cudaStream_t stream) {
+                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
   const bool roll = M >= (sizeof(XT) == 2 ? 128 : 1024);
-  return roll ? launch_split_r<L, XT, true>(x, w, b, y, M, K, N, tile, stream)
-              : launch_split_r<L, XT, false>(x, w, b, y, M, K, N, tile, stream);
+  return roll ? launch_split_r<L, XT, true>(x, w, b, y, M, K, N, tile, stream, zw)
+              : launch_split_r<L, XT, false>(x, w, b, y, M, K, N, tile, stream, zw);
 }
 
 // tile < 0: chosen from M.  Needs split_warps(K) != 0.
 template <typename XT>
 static bi_status launch_split(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                              int64_t K, int64_t N, int tile, cudaStream_t stream) {
+                              int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
   const int L = split_warps(K);
   const int C = static_cast<int>(K / kSlice) / L;
   if (tile < 0) tile = split_pick(M, N, C);
-  return L == 4 ? launch_split_l<4, XT>(x, w, b, y, M, K, N, tile, stream)
-                : launch_split_l<8, XT>(x, w, b, y, M, K, N, tile, stream);
+  return L == 4 ? launch_split_l<4, XT>(x, w, b, y, M, K, N, tile, stream, zw)
+                : launch_split_l<8, XT>(x, w, b, y, M, K, N, tile, stream, zw);
 }
 
 // ------------------------------------------------------- negative control --
@@ -906,9 +909,13 @@ __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float 
 }
 
 // ------------------------------------------------------------------- host --
+// zero_word (optional): one word that the launched kernel sets to 0 after its
+// predecessors on the stream have finished (the rows, split and sliced
+// schedules; the decode layer's one-launch expert path counts arrivals on it).
 template <typename XT>
 static bi_status launch_router_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                 int64_t K, int64_t N, int schedule, cudaStream_t stream) {
+                                 int64_t K, int64_t N, int schedule, cudaStream_t stream,
+                                 unsigned *zero_word) {
   const int S = static_cast<int>(K / kSlice);
   // automatic: rows for one or two tokens, the cluster split up to ~3K rows,
   // the tiled kernel beyond (measured crossover on GB300: the split is 27 %
@@ -930,7 +937,7 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       set_error("router split schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    const bi_status st = launch_split(x, w, b, y, M, K, N, schedule - 5, stream);
+    const bi_status st = launch_split(x, w, b, y, M, K, N, schedule - 5, stream, zero_word);
     if (st != BI_OK) return st;
   } else if (schedule == 1) {
     const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
@@ -952,7 +959,7 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       attr.done(dv);                                                                                   \
     }                                                                                                  \
     const bi_status st_ = launch_chained(router_rows_kernel<R, XT>, grid, dim3(32), smem, stream, 1, x, w, \
-                                         b, y, (int)M, (int)K, (int)N, device_error_word());          \
+                                         b, y, (int)M, (int)K, (int)N, device_error_word(), zero_word); \
     if (st_ != BI_OK) return st_;                                                                    \
   }
     if (mr == 1) BI_ROWS(1) else if (mr == 2) BI_ROWS(2) else BI_ROWS(4)
@@ -972,8 +979,11 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       attr.done(dv);
     }
     const bi_status st = launch_chained(router_sliced_kernel<XT>, grid, dim3(256), smem, stream, 1, x, w, b,
-                                        y, (int)M, (int)K, (int)N, device_error_word());
+                                        y, (int)M, (int)K, (int)N, device_error_word(), zero_word);
     if (st != BI_OK) return st;
+  } else if (zero_word) {
+    set_error("router schedule %d cannot zero a word", schedule);
+    return BI_ERR_UNSUPPORTED;
   } else if (schedule == 9) {
     if ((M + 27) / 28 > 2147483647LL) {
       set_error("router wide schedule: M=%lld too large for it", (long long)M);
@@ -998,14 +1008,14 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
 
 bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
                         int64_t K, int64_t N, int schedule, cudaStream_t stream) {
-  return launch_router_t<float>(x, w, b, y, M, K, N, schedule, stream);
+  return launch_router_t<float>(x, w, b, y, M, K, N, schedule, stream, nullptr);
 }
 
 // The same router on bf16 x (converted exactly to fp32 as it is read).
 bi_status launch_router_bf16(const void *x, const float *w, const float *b, float *y, int64_t M,
-                             int64_t K, int64_t N, int schedule, cudaStream_t stream) {
+                             int64_t K, int64_t N, int schedule, cudaStream_t stream, unsigned *zero_word) {
   return launch_router_t<__nv_bfloat16>(static_cast<const __nv_bfloat16 *>(x), w, b, y, M, K, N,
-                                        schedule, stream);
+                                        schedule, stream, zero_word);
 }
 
 bi_status launch_router_negctl(const float *x, const float *w, const float *b, float *y,

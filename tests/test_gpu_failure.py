@@ -1,9 +1,11 @@
 """Failure detection on the GPU without a fault.  Every pipeline wait of the
-expert GEMMs is a bounded mbarrier wait: past its limit it records
-BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel unwinds.  Here
-a probe kernel waits on a barrier phase that nothing completes; the wait must
-give up after about a second, the host must read the status, and the context
-must keep running the path afterwards."""
+expert GEMMs is bounded (the stage rings' mbarrier waits, and the one-launch
+decode layer's wait for its gate/up phase, an arrival count): past its limit
+it records BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel
+unwinds.  Here a probe kernel waits on a barrier phase that nothing
+completes, or a count that nothing raises; the wait must give up after about
+a second, the host must read the status, and the context must keep running
+the path afterwards."""
 import time
 
 import pytest
@@ -16,11 +18,12 @@ pytestmark = pytest.mark.gpu
 WAIT_TIMEOUT = 3  # BI_DEVERR_WAIT_TIMEOUT
 
 
-def test_bounded_wait_gives_up_and_context_survives(cuda):
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_wait_gives_up_and_context_survives(cuda, which):
     import invariant_moe_gb300 as bm
     assert bm.device_error() == 0
     t0 = time.perf_counter()
-    bm.bi_wait_timeout_probe()
+    bm.bi_wait_timeout_probe(which)
     code = bm.device_error()  # synchronises the device
     elapsed = time.perf_counter() - t0
     assert code == WAIT_TIMEOUT

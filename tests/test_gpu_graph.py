@@ -10,10 +10,13 @@ from tests import synthetic as syn
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = {"qwen": (2048, 128, 768, 8), "dsv4": (4096, 256, 2048, 8), "small": (384, 8, 256, 2)}
+SHAPES = {"qwen": (2048, 128, 768, 8), "dsv4": (4096, 256, 2048, 8), "small": (384, 8, 256, 2),
+          "mid": (1024, 16, 512, 4)}
 
 
-@pytest.mark.parametrize("shape,M", [("qwen", 1), ("qwen", 3), ("dsv4", 1), ("dsv4", 4),
+# qwen 1 and mid 4: the decode layer's one-launch expert path, whose arrival
+# count each replay's router kernel zeroes again
+@pytest.mark.parametrize("shape,M", [("qwen", 1), ("qwen", 3), ("dsv4", 1), ("dsv4", 4), ("mid", 4),
                                      ("qwen", 300), ("small", 1000)])
 def test_layer_graph_replays_same_bits_as_eager(cuda, shape, M):
     import invariant_moe_gb300 as bm

@@ -561,6 +561,87 @@ def test_layer_call_same_bits_as_router_topk_and_forward(cuda, shape, M, bias, t
     assert bm.device_error() == 0
 
 
+@pytest.fixture
+def decode_fused_mode():
+    import invariant_moe_gb300 as bm
+    prev = bm.bi_moe_decode_fused(0)
+    yield bm
+    bm.bi_moe_decode_fused(prev)
+
+
+@pytest.mark.parametrize("shape,M,ties", [("qwen", 1, False), ("qwen", 1, True), ("small", 1, False),
+                                          ("small", 7, True), ("small", 16, False), ("mid", 2, True),
+                                          ("mid", 4, False)])
+def test_layer_decode_one_launch_same_bits(cuda, decode_fused_mode, shape, M, ties):
+    """bi_moe_layer's decode-sized expert path in one launch (every CTA's
+    gate/up tiles, a wait of every CTA for all of them, the down tiles with
+    the fused combine) gives the bits of the two-launch path and of
+    bi_router_topk + bi_moe_forward.  The workspace is NaN-filled before each
+    call, so the arrival count the one-launch path waits on must be zeroed by
+    the call itself (by its router kernel: rows for M <= 2, the cluster split
+    for "mid" M=4, the sliced schedule for "small" M > 4).  "mid" (8 + 8
+    tiles per selected expert: at M=4 up to 256 over 152 CTAs, at M=2 up to
+    128 over 128) and "small" (4 + 3 per expert, 14 CTAs at M=1) cover CTAs
+    with gate/up tiles only, down tiles only, both, and none."""
+    bm = decode_fused_mode
+    H, E, I, k = {"qwen": (2048, 128, 768, 8), "small": (384, 8, 256, 2), "mid": (1024, 16, 512, 4)}[shape]
+    w = syn.moe_weights(H, E, I, seed=M + 141, unit=True, device="cuda")
+    wr = w.w_router.clone()
+    x = syn.moe_tokens(M, H, seed=M + 142, unit=True)
+    if ties:
+        g = syn.gen(M + 143)
+        perm = torch.randperm(E, generator=g)
+        n = min(4, E // 4)
+        for i in range(n):  # each of n experts copied into two others
+            wr[perm[n + 2 * i:n + 2 * i + 2].to(cuda)] = wr[int(perm[i])].clone()
+        x = (torch.round(x.float() * 8.0) / 8.0).clamp(-4, 4).to(torch.bfloat16)
+    x = x.to(cuda)
+    b = syn.normal((E,), 0.01, M + 144).to(cuda)
+    ws = bm.moe_workspace(M, H, E, k, I, cuda)
+    res = []
+    for mode in (0, 1, 0):
+        bm.bi_moe_decode_fused(mode)
+        ws.view(torch.float32)[: ws.numel() // 4].fill_(float("nan"))
+        res.append([t.clone() for t in bm.bi_moe_layer(x, wr, w.w13, w.w2, k, bias=b, workspace=ws)])
+    bm.bi_moe_decode_fused(0)
+    y1, i1, w1, _ = bm.bi_router_topk(x, wr, k, bias=b)
+    o1 = bm.bi_moe_forward(x, i1, w1, w.w13, w.w2)
+    torch.cuda.synchronize()
+    for r in res:
+        for got, ref, name in zip(r, (o1, y1, i1, w1), ("out", "scores", "ids", "wts")):
+            assert torch.equal(got, ref), name
+    assert bm.device_error() == 0
+
+
+@pytest.mark.parametrize("shape,M", [("qwen", 1), ("qwen", 3), ("dsv4", 1), ("dsv4", 4)])
+def test_layer_selection_special_scores(cuda, shape, M):
+    """The selection bi_moe_layer makes inside its decode gate/up GEMM (qwen
+    1: the one-launch expert path; the others: the gate/up launch) gives the
+    ids and weights of bi_router_topk bit for bit on scores of +inf, -inf and
+    NaN (router rows with an infinite or NaN weight on a positive token
+    element) and on exact ties (duplicated router rows)."""
+    import invariant_moe_gb300 as bm
+    H, E, I, k = {"qwen": (2048, 128, 768, 8), "dsv4": (4096, 256, 2048, 8)}[shape]
+    w = syn.moe_weights(H, E, I, seed=M + 161, unit=True, device="cuda")
+    wr = w.w_router.clone()
+    g = syn.gen(M + 162)
+    perm = torch.randperm(E, generator=g).tolist()
+    x = syn.moe_tokens(M, H, seed=M + 163, unit=True)
+    x[:, 0] = 1.0
+    x = x.to(cuda)
+    for i, v in enumerate((float("inf"), float("inf"), float("-inf"), float("nan"), float("nan"))):
+        wr[perm[i], 0] = v
+    for i in range(6):  # six more experts, each copied into one other
+        wr[perm[5 + 2 * i + 1]] = wr[perm[5 + 2 * i]].clone()
+    y1, i1, w1, _ = bm.bi_router_topk(x, wr, k)
+    _, y2, i2, w2 = bm.bi_moe_layer(x, wr, w.w13, w.w2, k)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32)), "scores"
+    assert torch.equal(i1, i2), "ids"
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32)), "wts"
+    assert y1.isnan().any() and y1.isinf().any()
+
+
 def full_layer(x, wr, w13, w2, k):
     import invariant_moe_gb300 as bm
     out, scores, ids, wts = bm.moe_layer(x, wr, w13, w2, k)
