@@ -901,26 +901,30 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
         mbar_arrive_relaxed(smem_u32(&tempty[acc]));
       }
       if (DECODE && !gu) {
-        // fused combine for this warp's 32 features (see DECODE above): the
-        // contribution stores are made visible, one arrival per token, and
-        // each (token, 32-feature block) completed here is summed by this warp
+        // fused combine for this warp's 32 features (see DECODE above): one
+        // arrival per token, an acquire-release add by the token's lane after
+        // the warp barrier (which orders every lane's contribution stores
+        // before it; measured 0.3-0.9 us per decode layer faster than a fence
+        // in every lane before the add and another before the sum), and each
+        // (token, 32-feature block) completed here is summed by this warp
+        // once a second warp barrier orders the acquire before every lane's
+        // loads
         const int fb32 = (ti.wb * ((FUSED && !gu) ? dn.wb_rows : prm.wb_rows) + q * 32) / 32;
         float *contrib = static_cast<float *>(out_t);
-        __threadfence();
         __syncwarp();
         int tok = 0;
         bool last = false;
         if (lane < ti.ntok) {  // NARROW: at most 32 tokens per tile
           tok = tokp_s[ti.tok0 + lane];
           const int need = __popc(tok_s[tok]);
-          last = atomicAdd(prm.counters + tok * prm.n_fb32 + fb32, 1) == need - 1;
+          last = atom_add_acq_rel_gpu(prm.counters + tok * prm.n_fb32 + fb32, 1) == need - 1;
         }
         unsigned todo = __ballot_sync(0xffffffffu, last);
+        if (todo) __syncwarp();
         while (todo) {
           const int src = __ffs(todo) - 1;
           todo &= todo - 1;
           const int m = __shfl_sync(0xffffffffu, tok, src);
-          __threadfence();  // the other slots' stores, seen through their arrivals
           const uint32_t valid = tok_s[m];
           const size_t f = static_cast<size_t>(fb32) * 32 + lane;
           float sum = 0.0f;
