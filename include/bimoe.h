@@ -573,9 +573,9 @@ BI_API bi_status bi_moe_gate_up_feed(int32_t mode, int32_t *previous);
  * decode-sized batch (M * top_k <= 32 under the automatic variant, with
  * 64-feature interleaved gate/up tiles, i.e. min(E, M * top_k) * I / 64 at
  * most the SM count), for the whole process from the next call on:
- *   0  automatic (the default): one launch (its gate/up tiles, a wait of
- *      every CTA for all of them, then the down tiles with the fused
- *      combine);
+ *   0  automatic (the default): one launch (its gate/up tiles, then the
+ *      down tiles with the fused combine, each K block of a down tile
+ *      waiting for the gate/up tile that stores its activations);
  *   1  two launches (the gate/up GEMM, then the down GEMM with the fused
  *      combine), as bi_moe_forward's decode path.
  * Same bits either way (tests compare them).  *previous (may be NULL)

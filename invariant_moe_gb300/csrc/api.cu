@@ -14,7 +14,7 @@ namespace bimoe {
 bi_status launch_router(const float *, const float *, const float *, float *, int64_t, int64_t,
                         int64_t, int, cudaStream_t);
 bi_status launch_router_bf16(const void *, const float *, const float *, float *, int64_t, int64_t,
-                             int64_t, int, cudaStream_t, unsigned *zero_word);
+                             int64_t, int, cudaStream_t, unsigned *zero_words, int n_zero);
 bi_status launch_topk_window(const float *, int64_t, const int64_t *, const int64_t *, int64_t,
                              int64_t, int32_t, int32_t *, cudaStream_t);
 bi_status launch_router_negctl(const float *, const float *, const float *, float *, int64_t,
@@ -42,6 +42,7 @@ bi_status launch_moe_decode(const void *, const int32_t *, const float *, const 
                             const float *scores, int32_t *ids_out, float *wts_out);
 int set_decode_fused(int mode);
 bool decode_fused_ok(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I);
+int64_t decode_fused_ready_count(int64_t M, int64_t E, int32_t top_k, int64_t I);
 bi_status launch_moe_decode_fused(const void *, const void *, const void *, void *, float *, int *, unsigned *,
                                   void *, int64_t, int64_t, int64_t, int32_t, int64_t, cudaStream_t,
                                   const float *scores, int32_t *ids_out, float *wts_out);
@@ -262,7 +263,7 @@ static MoeWorkspace moe_layout(int64_t M, int64_t H, int64_t E, int32_t top_k, i
   w.act = off;     off += align256(P * I * 2);
   w.contrib = off; off += align256(P * H * sizeof(float));
   w.counters = off; off += align256(decode_counter_count(M, H) * sizeof(int));
-  w.gridbar = off; off += 256;  // the one-launch decode layer's arrival count
+  w.gridbar = off; off += 4096;  // the one-launch decode layer's ready counts (at most 1024)
   w.total = off;
   return w;
 }
@@ -380,7 +381,7 @@ BI_API bi_status bi_router_gemm_bf16_schedule(const bi_bf16 *x, const float *w, 
   if (st != BI_OK) return st;
   BI_REQUIRE(schedule >= 0 && schedule <= 9, BI_ERR_INVALID_ARG, "schedule %d", schedule);
   if (M == 0) return BI_OK;
-  return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream), nullptr);
+  return launch_router_bf16(x, w, bias, y, M, K, N, schedule, reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
 }
 
 BI_API bi_status bi_router_gemm_bf16(const bi_bf16 *x, const float *w, const float *bias, float *y,
@@ -417,7 +418,7 @@ static bi_status launch_router_any(const float *x, const float *w, const float *
 }
 static bi_status launch_router_any(const __nv_bfloat16 *x, const float *w, const float *b, float *y,
                                    int64_t M, int64_t K, int64_t N, int schedule, cudaStream_t s) {
-  return launch_router_bf16(x, w, b, y, M, K, N, schedule, s, nullptr);
+  return launch_router_bf16(x, w, b, y, M, K, N, schedule, s, nullptr, 0);
 }
 
 // Router + selection: schedule 0 picks by M (the one-kernel path for small
@@ -704,14 +705,17 @@ BI_API bi_status bi_moe_layer(const bi_bf16 *x, const float *w_router, const flo
   char *ws = static_cast<char *>(workspace);
   const bool decode = g_gate_up_feed.load() == 0 && decode_path_ok(M, E, top_k);
   // decode-sized batch with the one-launch expert path: the router zeroes
-  // its arrival count
-  unsigned *gridbar = decode && decode_fused_ok(M, H, E, top_k, I) ? reinterpret_cast<unsigned *>(ws + L.gridbar)
-                                                                   : nullptr;
-  if ((st = launch_router_bf16(x, w_router, bias, scores, M, H, E, 0, s, gridbar)) != BI_OK) return st;
-  if (gridbar)
+  // its combine counters and ready counts (one range: the counters, the
+  // padding after them, the ready counts)
+  const bool fused = decode && decode_fused_ok(M, H, E, top_k, I);
+  unsigned *zero_from = fused ? reinterpret_cast<unsigned *>(ws + L.counters) : nullptr;
+  const int n_zero = fused ? static_cast<int>((L.gridbar - L.counters) / 4 + decode_fused_ready_count(M, E, top_k, I))
+                           : 0;
+  if ((st = launch_router_bf16(x, w_router, bias, scores, M, H, E, 0, s, zero_from, n_zero)) != BI_OK) return st;
+  if (fused)
     return launch_moe_decode_fused(x, w13, w2, ws + L.act, reinterpret_cast<float *>(ws + L.contrib),
-                                   reinterpret_cast<int *>(ws + L.counters), gridbar, out, M, H, E, top_k, I, s,
-                                   scores, ids, wts);
+                                   reinterpret_cast<int *>(ws + L.counters), reinterpret_cast<unsigned *>(ws + L.gridbar),
+                                   out, M, H, E, top_k, I, s, scores, ids, wts);
   if (decode) {
     // decode-sized batch: the gate/up GEMM selects the experts itself
     return launch_moe_decode(x, nullptr, nullptr, w13, w2, ws + L.act, reinterpret_cast<float *>(ws + L.contrib),

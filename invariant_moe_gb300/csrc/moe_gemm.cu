@@ -53,8 +53,9 @@
 //     weight block run back to back and share it through L2.
 //   * decode-sized batches: every CTA derives the routing itself (DECODE);
 //     in the layer call the gate/up and down GEMMs can run as one launch
-//     (moe_decode_layer_kernel: the gate/up tiles, a bounded wait of every
-//     CTA for all of them, then the down tiles with the combine fused).
+//     (moe_decode_layer_kernel: the gate/up tiles, then the down tiles with
+//     the combine fused, each down K block loaded once the gate/up tile that
+//     stores it has finished: a bounded wait).
 #include <atomic>
 #include <mutex>
 
@@ -139,7 +140,7 @@ struct GemmParams {
 };
 
 // The down phase of the one-launch decode layer (moe_decode_layer_kernel):
-// its shape, and the word the gate/up phase's epilogue warps arrive on.
+// its shape, and the counts the gate/up tiles' epilogue warps arrive on.
 struct DownPhase {
   void *out;              // contributions fp32 [M*top_k, H]
   int K;                  // I
@@ -147,7 +148,7 @@ struct DownPhase {
   int wb_rows;            // 128
   int out_ld;             // H
   int a_rows_per_expert;  // H
-  unsigned *grid_bar;     // arrivals: 4 per CTA (its epilogue warps); zero before the launch
+  unsigned *ready;        // [gate/up tiles] arrivals (4 per tile: its epilogue warps); zero before the launch
 };
 
 // Decode-sized batches (bi_moe_forward with M * top_k <= kDecodeMaxP):
@@ -160,6 +161,9 @@ struct DownPhase {
 // M = 1 / 4: 104.4-106.7 / 293.6-295.1 against 110.6-110.8 / 295.4-298.7 us);
 // at 64 pairs (M = 8) it was within +-2.5 us either way, beyond it slower.
 constexpr int kDecodeMaxP = 32;
+// the one-launch decode layer's ready counts (one per gate/up tile) fit in a
+// workspace region of this many words
+constexpr int kDecodeReadyMax = 1024;
 // the aux region holds the barriers (at most 16 stages), the tile prefix and
 // expert offsets for E <= 1024, the decode routing tables and the gathered
 // rows' tokens (at most 256)
@@ -280,11 +284,16 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
 // FUSED (moe_decode_layer_kernel): the DECODE gate/up GEMM (interleaved rows,
 // GATHER) and the DECODE down GEMM in one launch of at most one CTA per SM.
 // The tile list is the gate/up tiles, then the down tiles (tmA2 / tmB2 / dn:
-// W2 and the activations); both phases use the same 20 KB stages.  Each
-// epilogue warp arrives on dn.grid_bar once the CTA's gate/up tiles are
-// stored; the producer may load a down tile's W2 rows before that, but loads
-// its activation rows only once every warp of every CTA has arrived (a
-// bounded wait), so the down phase reads complete activations.
+// W2 and the activations); both phases use the same 20 KB stages.  K block
+// kb of a down tile (64 activation features of its expert's tokens) is what
+// gate/up tile (expert, kb) stores, so each epilogue warp arrives on
+// dn.ready[gate/up tile] once that tile's activations are stored, and the
+// producer loads a down stage's W2 rows at once but its activation rows only
+// when the count of that K block's gate/up tile is complete (a bounded
+// wait): the down MMAs run as the gate/up tiles they need finish.  The
+// combine counters and dn.ready are zeroed before the launch (by the
+// router kernel of the same layer call), not here: CTAs start at different
+// moments and no point of this launch orders them all.
 template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER, bool DECODE, bool FUSED>
 __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &prm,
                                               const CUtensorMap &tmA2, const CUtensorMap &tmB2,
@@ -415,7 +424,7 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
                                          tokp_s, dexp_s, dbeg_s, dcnt_s, tok_s, prm.err,
                                          GATE_UP && blockIdx.x == 0, lane);
       if (lane == 0) *nd_s = nd;
-    } else if (GATE_UP) {
+    } else if (GATE_UP && !FUSED) {
       // for the down GEMM that follows: its arrival counters start at zero
       const int nc = prm.M * prm.n_fb32;
       for (int i = blockIdx.x * (kGemmThreads - 32) + threadIdx.x - 32; i < nc; i += gridDim.x * (kGemmThreads - 32))
@@ -466,7 +475,6 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
   const int n_gu = DECODE ? *nd_s * prm.n_wb : 0;
   const int total_tiles = DECODE ? (FUSED ? n_gu + *nd_s * dn.n_wb : n_gu) : tile_prefix[prm.E];
   auto gu_tile = [&](int tile) { return FUSED ? tile < n_gu : GATE_UP; };
-  const unsigned grid_arrivals = 4u * gridDim.x;  // FUSED: every epilogue warp of every CTA
   if (DECODE && GATE_UP && blockIdx.x == 0 && warp >= 2) {
     // tokens with no valid slot (no tile stores them) get zero output rows
     for (int m = 0; m < prm.M; ++m)
@@ -507,7 +515,6 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
-    bool gate = !FUSED;  // FUSED: the activations may be loaded (every gate/up tile stored)
     // one tile's copies; returns false when the tile loop must stop
     auto produce = [&](auto phase_tag, int tile) -> bool {
       constexpr bool gu = decltype(phase_tag)::value;
@@ -562,18 +569,37 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
       bool ok = true;
       const bool el = elect_one();
       if (el) {
-        // FUSED, before the gate opens: the stages (consecutive in the ring,
-        // from dq_stage, K blocks from dq_kb) whose weight rows are loading
-        // and whose activation rows wait for the gate/up phase
+        // FUSED down tile: the stages (consecutive in the ring, from
+        // dq_stage, K blocks from dq_kb) whose weight rows are loading and
+        // whose activation rows wait for their gate/up tile; K block kb's is
+        // gate/up tile d * n_wb + kb, d the tile's distinct expert
         int dq_n = 0, dq_stage = 0, dq_kb = 0;
-        auto flush = [&]() {
-          fence_proxy_async_global();  // the activations were stored through the generic proxy
-          for (int i = 0; i < dq_n; ++i) {
-            const int s = dq_stage + i < kStages ? dq_stage + i : dq_stage + i - kStages;
-            tma_load_2d(smem_u32(tiles + s * kStageBytes + kABytes), &tmB2, smem_u32(&full[s]),
-                        (dq_kb + i) * kBK, b_row);
+        const unsigned *rdy = nullptr;
+        if constexpr (FUSED && !gu) rdy = dn.ready + ((tile - n_gu) / dn.n_wb) * prm.n_wb;
+        // issue the waiting stages' activation loads in K order while their
+        // gate/up tiles are stored; `block` waits (bounded) for the first
+        // one, `all` for every one (after a timeout a load is issued all the
+        // same, so every armed stage completes; the abort flag then stops
+        // the MMAs and the epilogue)
+        auto flush = [&](bool block, bool all) {
+          bool fenced = false;
+          while (dq_n > 0) {
+            const unsigned *f = rdy + dq_kb;
+            if (ld_acquire_gpu(f) < 4u) {
+              if (!block) break;
+              wait_count_geq(f, 4u, abort_flag, prm.err);
+              block = all;
+            }
+            if (!fenced) {
+              fence_proxy_async_global();  // the activations were stored through the generic proxy
+              fenced = true;
+            }
+            tma_load_2d(smem_u32(tiles + dq_stage * kStageBytes + kABytes), &tmB2, smem_u32(&full[dq_stage]),
+                        dq_kb * kBK, b_row);
+            dq_stage = dq_stage + 1 == kStages ? 0 : dq_stage + 1;
+            ++dq_kb;
+            --dq_n;
           }
-          dq_n = 0;
         };
         for (int kb = 0; kb < nkb_t; ++kb) {
           if (!wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
@@ -610,23 +636,16 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
             }
             if (GATE_UP && !INTER)
               tma_load_2d(smem_u32(st + kTileBytes), &tmA, fb, kb * kBK, a_row + prm.up_offset);
-            if (FUSED && !gu && !gate) {
-              // the stage's activation rows wait for the gate (the barrier
-              // already expects their bytes)
+            if (FUSED && !gu) {
+              // the stage's activation rows wait for their gate/up tile (the
+              // barrier already expects their bytes); with the ring all
+              // waiting, wait for the first; at the tile's last K block, for
+              // all
               if (dq_n++ == 0) {
                 dq_stage = stage;
                 dq_kb = kb;
               }
-              gate = ld_acquire_gpu(dn.grid_bar) >= grid_arrivals;
-              if (!gate && (dq_n == kStages || kb == nkb_t - 1)) {
-                // the ring (or the tile) is all waiting: wait for the gate/up
-                // phase.  After a timeout the loads are issued all the same,
-                // so every armed stage completes; the abort flag then stops
-                // the MMAs and the epilogue.
-                wait_count_geq(dn.grid_bar, grid_arrivals, abort_flag, prm.err);
-                gate = true;
-              }
-              if (gate) flush();
+              flush(dq_n == kStages || kb == nkb_t - 1, kb == nkb_t - 1);
             } else if (!gather_t) {
               tma_load_2d(smem_u32(st + kABytes), (FUSED && !gu) ? &tmB2 : &tmB, fb, kb * kBK, b_row);
             } else
@@ -641,16 +660,11 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
             phase ^= 1u;
           }
         }
-        if (FUSED && dq_n > 0) {
-          // only after a failed wait: complete the armed stages
-          flush();
-          gate = true;
-        }
+        if (FUSED && dq_n > 0) flush(true, true);  // only after a failed wait: complete the armed stages
       }
       // the ring state back on every lane (this also keeps grow_s until every
       // gather of the tile is issued)
       const int src = __ffs(__ballot_sync(0xffffffffu, el)) - 1;
-      if (FUSED) gate = __shfl_sync(0xffffffffu, gate ? 1 : 0, src) != 0;
       stage = __shfl_sync(0xffffffffu, stage, src);
       phase = __shfl_sync(0xffffffffu, phase, src);
       issued_mask = __shfl_sync(0xffffffffu, issued_mask, src);
@@ -785,25 +799,10 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
         }
       }
     };
-    // FUSED: one arrival on the gate once this warp's activation stores are
-    // done: the warp barrier orders every lane's stores before lane 0's
-    // release (cumulative, GPU scope); the proxy fence orders them before
-    // async-proxy (TMA) reads.  A fence in every lane before the warp barrier
-    // instead measured ~0.9 us slower per decode layer.
-    bool arrived = !FUSED, acquired = !FUSED;
-    auto arrive = [&]() {
-      __syncwarp();
-      if (lane == 0) {
-        fence_proxy_async_global();
-        red_release_gpu_add(dn.grid_bar, 1u);
-      }
-      arrived = true;
-    };
     // one tile's epilogue; returns false when the tile loop must stop
     auto consume = [&](auto phase_tag, int tile) -> bool {
       constexpr bool gu = decltype(phase_tag)::value;
       const TileInfo ti = tile_at(tile);
-      if (!arrived && !gu) arrive();  // this CTA's gate/up tiles are stored
       // per-phase output (the down tiles of FUSED write dn.out)
       const int out_ld_t = (FUSED && !gu) ? dn.out_ld : prm.out_ld;
       void *out_t = (FUSED && !gu) ? dn.out : prm.out;
@@ -818,14 +817,6 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
       // one decision per warp (lanes can disagree at the instant a wait gives up)
       const bool okw = __all_sync(0xffffffffu, wait(smem_u32(&tfull[acc]), acc_phase, abort_flag) ? 1 : 0) != 0;
       if (!okw) return false;
-      if (!acquired && !gu) {
-        // the counters the combine below counts on were zeroed by every CTA
-        // before its arrival (this tile's MMAs ran after the gate opened, so
-        // the wait ends at once)
-        if (lane == 0) wait_count_geq(dn.grid_bar, grid_arrivals, abort_flag, prm.err);
-        __syncwarp();
-        acquired = true;
-      }
       {
         // perm entries of this tile that are not pair ids (the loads landed
         // long ago): reported once; nothing is stored through them below
@@ -888,6 +879,19 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
             if (c0 + c < ti.ntok && static_cast<unsigned>(pair) < static_cast<unsigned>(prm.P))
               contrib[static_cast<size_t>(pair) * out_ld_t + col] = __uint_as_float(d[c]);
           }
+        }
+      }
+      if (FUSED && gu) {
+        // this warp's activation stores of the tile are done: one arrival on
+        // the tile's count, which the down stages of its K block wait on.
+        // The warp barrier orders every lane's stores before lane 0's
+        // release (cumulative, GPU scope); the proxy fence orders them
+        // before async-proxy (TMA) reads.  (A fence in every lane before the
+        // warp barrier measured ~0.9 us slower per decode layer.)
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async_global();
+          red_release_gpu_add(dn.ready + tile, 1u);
         }
       }
       // the accumulator is free once its tensor-memory loads have completed
@@ -954,7 +958,6 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
       }
       if (!cont) break;
     }
-    if (!arrived) arrive();  // only gate/up tiles here, none, or a wait gave up
   }
 
   tc_fence_before();
@@ -1224,20 +1227,27 @@ bi_status launch_moe_decode(const void *x, const int32_t *ids, const float *wts,
 // The decode-sized layer's expert path in one launch (moe_decode_layer_kernel),
 // for bi_moe_layer: where the decode gate/up GEMM runs 64-feature
 // interleaved tiles (their count fits one wave on the SMs), so that both
-// phases share the stage layout.  The caller zeroes *grid_bar in a kernel
-// earlier on the stream (the router's).  0 = automatic, 1 = never (the two
+// phases share the stage layout.  The caller zeroes the combine counters
+// (M * H / 32) and ready[0 .. min(E, M * top_k) * I / 64) in a kernel earlier
+// on the stream (the router's).  0 = automatic, 1 = never (the two
 // GEMM launches of launch_moe_decode instead).
 static std::atomic<int> g_decode_fused{0};
 
 int set_decode_fused(int mode) { return g_decode_fused.exchange(mode); }
 
+// Gate/up tiles of the one-launch decode layer (at most): the ready counts.
+int64_t decode_fused_ready_count(int64_t M, int64_t E, int32_t top_k, int64_t I) {
+  return std::min<int64_t>(E, M * top_k) * (I / (kBM / 2));
+}
+
 bool decode_fused_ok(int64_t M, int64_t H, int64_t E, int32_t top_k, int64_t I) {
   const int64_t P = M * top_k;
-  return g_decode_fused.load() == 0 && decode_path_ok(M, E, top_k) && pick_variant(I, true, H, P, E) == 4;
+  return g_decode_fused.load() == 0 && decode_path_ok(M, E, top_k) && pick_variant(I, true, H, P, E) == 4 &&
+         decode_fused_ready_count(M, E, top_k, I) <= kDecodeReadyMax;
 }
 
 bi_status launch_moe_decode_fused(const void *x, const void *w13, const void *w2, void *act, float *contrib,
-                                  int *counters, unsigned *grid_bar, void *out, int64_t M, int64_t H, int64_t E,
+                                  int *counters, unsigned *ready, void *out, int64_t M, int64_t H, int64_t E,
                                   int32_t top_k, int64_t I, cudaStream_t stream, const float *scores,
                                   int32_t *ids_out, float *wts_out) {
   using C = GemmCfg<true, false, true, true>;
@@ -1246,7 +1256,7 @@ bi_status launch_moe_decode_fused(const void *x, const void *w13, const void *w2
   GemmParams g{nullptr, nullptr, nullptr, act, (int)E, (int)H, (int)(I / wb_rows), wb_rows, (int)I, (int)(2 * I),
                (int)I, device_error_word(), (int)P, (int)top_k, nullptr, (int)M, counters,
                static_cast<__nv_bfloat16 *>(out), (int)(H / 32), scores, ids_out, wts_out};
-  const DownPhase dn{contrib, (int)I, (int)(H / kBM), kBM, (int)H, (int)H, grid_bar};
+  const DownPhase dn{contrib, (int)I, (int)(H / kBM), kBM, (int)H, (int)H, ready};
   CUtensorMap tmA, tmB, tmA2, tmB2;
   if (!make_tma_inter_bf16(&tmA, w13, static_cast<uint64_t>(E * 2 * I), static_cast<uint64_t>(I),
                            static_cast<uint64_t>(H)) ||

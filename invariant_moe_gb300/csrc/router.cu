@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ 
                                                          const float *__restrict__ w,
                                                          const float *__restrict__ bias,
                                                          float *__restrict__ y, int M, int K,
-                                                         int N, int *err, unsigned *zero_word) {
+                                                         int N, int *err, unsigned *zero_words, int n_zero) {
   constexpr int XP = XPitch<XT>::slice;
   extern __shared__ __align__(16) float sm[];
   float *ws = sm;                                              // [32][kSlicePad]
@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ 
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   griddep_wait();
-  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && lane == 0) *zero_word = 0u;
+  if (zero_words && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = lane; i < n_zero; i += 32) zero_words[i] = 0u;
   const int S = K / kSlice;
   const int n = blockIdx.x;
   const int m0 = blockIdx.y * MR;
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict
                                                             const float *__restrict__ w,
                                                             const float *__restrict__ bias,
                                                             float *__restrict__ y, int M, int K,
-                                                            int N, int *err, unsigned *zero_word) {
+                                                            int N, int *err, unsigned *zero_words, int n_zero) {
   constexpr int XP = XPitch<XT>::round;
   constexpr int kStageB = sl_stage_bytes<XT>();
   extern __shared__ __align__(16) float sm[];
@@ -156,7 +157,8 @@ __global__ void __launch_bounds__(256) router_sliced_kernel(const XT *__restrict
   __shared__ __align__(8) uint64_t bars[2];
   const int tid = threadIdx.x;
   griddep_wait();
-  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *zero_word = 0u;
+  if (zero_words && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = tid; i < n_zero; i += 256) zero_words[i] = 0u;
   const int g = tid >> 5, lane = tid & 31;
   const int S = K / kSlice;
   const int rounds = (S + kSlG - 1) / kSlG;
@@ -655,14 +657,15 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
                                                               const float *__restrict__ w,
                                                               const float *__restrict__ bias,
                                                               float *__restrict__ y, int M, int K,
-                                                              int N, unsigned *zero_word) {
+                                                              int N, unsigned *zero_words, int n_zero) {
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   constexpr int BM = Cf::BM, BN = Cf::BN, XLd = Cf::XLd, WLd = Cf::WLd;
   constexpr int kChunks = kSlice / CK;
   extern __shared__ __align__(16) uint8_t sp_smem[];
 
   griddep_wait();
-  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *zero_word = 0u;
+  if (zero_words && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < n_zero; i += 32 * L) zero_words[i] = 0u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = K / kSlice / L;  // CTAs per cluster (the launch's cluster size)
   const int rank = static_cast<int>(cluster_ctarank());
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(32 * L) router_split_kernel(const XT *__restri
 
 template <int TM, int TN, int NST, int CK, int L, typename XT, bool ROLL>
 static bi_status launch_split_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, cudaStream_t stream, unsigned *zero_word) {
+                                int64_t K, int64_t N, cudaStream_t stream, unsigned *zw, int nz) {
   using Cf = SplitCfg<TM, TN, NST, XT, CK>;
   const int C = static_cast<int>(K / kSlice) / L;
   const size_t smem = static_cast<size_t>(L) * Cf::WARP_BYTES;
@@ -802,7 +805,7 @@ static bi_status launch_split_t(const XT *x, const float *w, const float *b, flo
   dim3 grid(static_cast<unsigned>(C * ((N + Cf::BN - 1) / Cf::BN)),
             static_cast<unsigned>((M + Cf::BM - 1) / Cf::BM));
   return launch_chained(router_split_kernel<TM, TN, NST, L, XT, CK, ROLL>, grid, dim3(32 * L), smem, stream, C,
-                        x, w, b, y, (int)M, (int)K, (int)N, zero_word);
+                        x, w, b, y, (int)M, (int)K, (int)N, zw, nz);
 }
 
 // Lane tiles of the split schedule (outputs per thread TM x TN, ring depth,
@@ -837,33 +840,33 @@ static int split_pick(int64_t M, int64_t N, int C) {
 
 template <int L, typename XT, bool ROLL>
 static bi_status launch_split_r(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
+                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw, int nz) {
   switch (tile) {
-    case 0: return launch_split_t<2, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
-    case 1: return launch_split_t<4, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
-    case 2: return launch_split_t<4, 4, 3, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
-    default: return launch_split_t<8, 4, 2, 16, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw);
+    case 0: return launch_split_t<2, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw, nz);
+    case 1: return launch_split_t<4, 2, 4, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw, nz);
+    case 2: return launch_split_t<4, 4, 3, 32, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw, nz);
+    default: return launch_split_t<8, 4, 2, 16, L, XT, ROLL>(x, w, b, y, M, K, N, stream, zw, nz);
   }
 }
 
 // The chunk loop rolled where that measured faster (see router_split_kernel).
 template <int L, typename XT>
 static bi_status launch_split_l(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
+                                int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw, int nz) {
   const bool roll = M >= (sizeof(XT) == 2 ? 128 : 1024);
-  return roll ? launch_split_r<L, XT, true>(x, w, b, y, M, K, N, tile, stream, zw)
-              : launch_split_r<L, XT, false>(x, w, b, y, M, K, N, tile, stream, zw);
+  return roll ? launch_split_r<L, XT, true>(x, w, b, y, M, K, N, tile, stream, zw, nz)
+              : launch_split_r<L, XT, false>(x, w, b, y, M, K, N, tile, stream, zw, nz);
 }
 
 // tile < 0: chosen from M.  Needs split_warps(K) != 0.
 template <typename XT>
 static bi_status launch_split(const XT *x, const float *w, const float *b, float *y, int64_t M,
-                              int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw) {
+                              int64_t K, int64_t N, int tile, cudaStream_t stream, unsigned *zw, int nz) {
   const int L = split_warps(K);
   const int C = static_cast<int>(K / kSlice) / L;
   if (tile < 0) tile = split_pick(M, N, C);
-  return L == 4 ? launch_split_l<4, XT>(x, w, b, y, M, K, N, tile, stream, zw)
-                : launch_split_l<8, XT>(x, w, b, y, M, K, N, tile, stream, zw);
+  return L == 4 ? launch_split_l<4, XT>(x, w, b, y, M, K, N, tile, stream, zw, nz)
+                : launch_split_l<8, XT>(x, w, b, y, M, K, N, tile, stream, zw, nz);
 }
 
 // ------------------------------------------------------- negative control --
@@ -909,13 +912,14 @@ __global__ void cast_bf16_f32_kernel(const __nv_bfloat16 *__restrict__ x, float 
 }
 
 // ------------------------------------------------------------------- host --
-// zero_word (optional): one word that the launched kernel sets to 0 after its
-// predecessors on the stream have finished (the rows, split and sliced
-// schedules; the decode layer's one-launch expert path counts arrivals on it).
+// zero_words (optional): n_zero words that the launched kernel sets to 0
+// after its predecessors on the stream have finished (the rows, split and
+// sliced schedules; the decode layer's one-launch expert path counts arrivals
+// on them).
 template <typename XT>
 static bi_status launch_router_t(const XT *x, const float *w, const float *b, float *y, int64_t M,
                                  int64_t K, int64_t N, int schedule, cudaStream_t stream,
-                                 unsigned *zero_word) {
+                                 unsigned *zero_words, int n_zero) {
   const int S = static_cast<int>(K / kSlice);
   // automatic: rows for one or two tokens, the cluster split up to ~3K rows,
   // the tiled kernel beyond (measured crossover on GB300: the split is 27 %
@@ -937,7 +941,7 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       set_error("router split schedule: M=%lld too large for it", (long long)M);
       return BI_ERR_UNSUPPORTED;
     }
-    const bi_status st = launch_split(x, w, b, y, M, K, N, schedule - 5, stream, zero_word);
+    const bi_status st = launch_split(x, w, b, y, M, K, N, schedule - 5, stream, zero_words, n_zero);
     if (st != BI_OK) return st;
   } else if (schedule == 1) {
     const int mr = M <= 1 ? 1 : (M <= 2 ? 2 : 4);
@@ -959,7 +963,7 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       attr.done(dv);                                                                                   \
     }                                                                                                  \
     const bi_status st_ = launch_chained(router_rows_kernel<R, XT>, grid, dim3(32), smem, stream, 1, x, w, \
-                                         b, y, (int)M, (int)K, (int)N, device_error_word(), zero_word); \
+                                         b, y, (int)M, (int)K, (int)N, device_error_word(), zero_words, n_zero); \
     if (st_ != BI_OK) return st_;                                                                    \
   }
     if (mr == 1) BI_ROWS(1) else if (mr == 2) BI_ROWS(2) else BI_ROWS(4)
@@ -979,10 +983,10 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
       attr.done(dv);
     }
     const bi_status st = launch_chained(router_sliced_kernel<XT>, grid, dim3(256), smem, stream, 1, x, w, b,
-                                        y, (int)M, (int)K, (int)N, device_error_word(), zero_word);
+                                        y, (int)M, (int)K, (int)N, device_error_word(), zero_words, n_zero);
     if (st != BI_OK) return st;
-  } else if (zero_word) {
-    set_error("router schedule %d cannot zero a word", schedule);
+  } else if (zero_words) {
+    set_error("router schedule %d cannot zero words", schedule);
     return BI_ERR_UNSUPPORTED;
   } else if (schedule == 9) {
     if ((M + 27) / 28 > 2147483647LL) {
@@ -1008,14 +1012,15 @@ static bi_status launch_router_t(const XT *x, const float *w, const float *b, fl
 
 bi_status launch_router(const float *x, const float *w, const float *b, float *y, int64_t M,
                         int64_t K, int64_t N, int schedule, cudaStream_t stream) {
-  return launch_router_t<float>(x, w, b, y, M, K, N, schedule, stream, nullptr);
+  return launch_router_t<float>(x, w, b, y, M, K, N, schedule, stream, nullptr, 0);
 }
 
 // The same router on bf16 x (converted exactly to fp32 as it is read).
 bi_status launch_router_bf16(const void *x, const float *w, const float *b, float *y, int64_t M,
-                             int64_t K, int64_t N, int schedule, cudaStream_t stream, unsigned *zero_word) {
+                             int64_t K, int64_t N, int schedule, cudaStream_t stream, unsigned *zero_words,
+                             int n_zero) {
   return launch_router_t<__nv_bfloat16>(static_cast<const __nv_bfloat16 *>(x), w, b, y, M, K, N,
-                                        schedule, stream, zero_word);
+                                        schedule, stream, zero_words, n_zero);
 }
 
 bi_status launch_router_negctl(const float *x, const float *w, const float *b, float *y,

@@ -1,6 +1,6 @@
 """Failure detection on the GPU without a fault.  Every pipeline wait of the
 expert GEMMs is bounded (the stage rings' mbarrier waits, and the one-launch
-decode layer's wait for its gate/up phase, an arrival count): past its limit
+decode layer's wait of a down stage for its gate/up tile, a count): past its limit
 it records BI_DEVERR_WAIT_TIMEOUT in the device error word and the kernel
 unwinds.  Here a probe kernel waits on a barrier phase that nothing
 completes, or a count that nothing raises; the wait must give up after about

@@ -574,12 +574,13 @@ def decode_fused_mode():
                                           ("mid", 4, False)])
 def test_layer_decode_one_launch_same_bits(cuda, decode_fused_mode, shape, M, ties):
     """bi_moe_layer's decode-sized expert path in one launch (every CTA's
-    gate/up tiles, a wait of every CTA for all of them, the down tiles with
-    the fused combine) gives the bits of the two-launch path and of
-    bi_router_topk + bi_moe_forward.  The workspace is NaN-filled before each
-    call, so the arrival count the one-launch path waits on must be zeroed by
-    the call itself (by its router kernel: rows for M <= 2, the cluster split
-    for "mid" M=4, the sliced schedule for "small" M > 4).  "mid" (8 + 8
+    gate/up tiles, then its down tiles with the fused combine, each down K
+    block waiting for the gate/up tile that stores it) gives the bits of the
+    two-launch path and of bi_router_topk + bi_moe_forward.  The workspace
+    is NaN-filled before each call, so the ready counts and combine counters
+    the one-launch path counts on must be zeroed by the call itself (by its
+    router kernel: rows for M <= 2, the cluster split for "mid" M=4, the
+    sliced schedule for "small" M > 4).  "mid" (8 + 8
     tiles per selected expert: at M=4 up to 256 over 152 CTAs, at M=2 up to
     128 over 128) and "small" (4 + 3 per expert, 14 CTAs at M=1) cover CTAs
     with gate/up tiles only, down tiles only, both, and none."""
