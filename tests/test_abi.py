@@ -107,6 +107,18 @@ def test_gemm_variant_setting(lib):
     assert lib.bi_moe_gemm_variant(0, ctypes.byref(prev)) == 0 and prev.value == 1
 
 
+def test_decode_fused_setting_and_probe_arguments(lib):
+    """The decode layer's one- or two-launch setting is host-side, and the
+    bounded-wait probe rejects an unknown wait kind before any launch."""
+    prev = ctypes.c_int32(-1)
+    assert lib.bi_moe_decode_fused(2, None) == 1
+    assert lib.bi_moe_decode_fused(-1, None) == 1
+    assert lib.bi_moe_decode_fused(1, ctypes.byref(prev)) == 0 and prev.value == 0
+    assert lib.bi_moe_decode_fused(0, ctypes.byref(prev)) == 0 and prev.value == 1
+    assert lib.bi_wait_timeout_probe(2, ctypes.c_void_p(None)) == 1
+    assert lib.bi_wait_timeout_probe(-1, ctypes.c_void_p(None)) == 1
+
+
 def test_host_side_rejections(lib):
     """Argument checks run on the host and never touch the GPU."""
     nul = ctypes.c_void_p(None)
