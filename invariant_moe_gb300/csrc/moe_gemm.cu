@@ -294,7 +294,8 @@ __device__ __forceinline__ __nv_bfloat16 swiglu_p(float g, float u, float p) {
 // combine counters and dn.ready are zeroed before the launch (by the
 // router kernel of the same layer call), not here: CTAs start at different
 // moments and no point of this launch orders them all.
-template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER, bool DECODE, bool FUSED>
+template <bool GATE_UP, bool PAIR, bool INTER, bool NARROW, bool GATHER, bool DECODE, bool FUSED,
+          int RING_DROP = 0>
 __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &prm,
                                               const CUtensorMap &tmA2, const CUtensorMap &tmB2,
                                               const DownPhase &dn) {
@@ -308,7 +309,7 @@ __device__ __forceinline__ void moe_gemm_body(const CUtensorMap &tmA, const CUte
   static_assert(!DECODE || !GATE_UP || GATHER, "decode gate/up gathers its token rows");
   using C = GemmCfg<GATE_UP, PAIR, INTER, NARROW>;
   constexpr int kBN = C::kBN;
-  constexpr int kStages = C::kStages;
+  constexpr int kStages = C::kStages - RING_DROP;  // FUSED beside the router: one stage fewer
   constexpr int kStageBytes = C::kStageBytes;
   constexpr int kABytes = C::kABytes;
   extern __shared__ uint8_t smem_raw[];
@@ -980,12 +981,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // The expert path of a decode-sized layer in one launch (FUSED above): at
-// most one CTA per SM, all resident at once.
+// most one CTA per SM, all resident at once.  RING_DROP = 1: a ring one
+// stage shorter, so that a CTA fits on an SM beside a CTA of the one-warp
+// router kernel, which lets its dependents start at once.
+template <int RING_DROP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_decode_layer_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ GemmParams prm, const __grid_constant__ CUtensorMap tmA2,
                             const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ DownPhase dn) {
-  moe_gemm_body<true, false, true, true, true, true, true>(tmA, tmB, prm, tmA2, tmB2, dn);
+  moe_gemm_body<true, false, true, true, true, true, true, RING_DROP>(tmA, tmB, prm, tmA2, tmB2, dn);
 }
 
 // ------------------------------------------------------------------- host --
@@ -1264,25 +1268,33 @@ bi_status launch_moe_decode_fused(const void *x, const void *w13, const void *w2
       !make_tma_2d_bf16(&tmA2, w2, static_cast<uint64_t>(E * H), static_cast<uint64_t>(I), kBM) ||
       !make_tma_2d_bf16(&tmB2, act, static_cast<uint64_t>(P), static_cast<uint64_t>(I), C::kBNc))
     return BI_ERR_CUDA;
+  // At M <= 2 the router before this launch is the one-warp rows kernel,
+  // which lets its dependents start at once: a ring one stage shorter (9 x
+  // 20 KB) fits beside one of its CTAs, so the CTAs of this launch are
+  // resident and set up before the router ends (measured on GB300: the
+  // Qwen3-30B-A3B-shaped layer at M=1 0.2 us faster cold, an H=1024 / E=16
+  // one at M=2 0.7 us; where the router is the cluster split schedule, the
+  // shorter ring alone cost 0.3-0.5 us, so it keeps 10 stages)
+  const bool beside_router = M <= 2;
+  void (*kern)(CUtensorMap, CUtensorMap, GemmParams, CUtensorMap, CUtensorMap, DownPhase) =
+      beside_router ? moe_decode_layer_kernel<1> : moe_decode_layer_kernel<0>;
+  const int smem = C::kSmemBytes - (beside_router ? C::kStageBytes : 0);
   static std::mutex mu;
-  static ContextSetup setup;  // the shared-memory attribute is per context
+  static ContextSetup setup[2];  // the shared-memory attribute is per context
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (setup.pending(dev)) {
-      cudaError_t e = cudaFuncSetAttribute(moe_decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::kSmemBytes);
+    if (setup[beside_router].pending(dev)) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       int per_sm = 0;
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_layer_kernel, kGemmThreads,
-                                                          C::kSmemBytes);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemmThreads, smem);
       if (e != cudaSuccess || per_sm < 1) {
         cudaGetLastError();
         set_error("decode layer kernel: cannot be resident (%s, %d per SM)", cudaGetErrorString(e), per_sm);
         return BI_ERR_CUDA;
       }
-      setup.done(dev);
+      setup[beside_router].done(dev);
     }
   }
   // CTAs wait on one another, so all must be resident: at most one per SM
@@ -1297,11 +1309,11 @@ bi_status launch_moe_decode_fused(const void *x, const void *w13, const void *w2
   attr[1].val.cooperative = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_layer_kernel, tmA, tmB, g, tmA2, tmB2, dn);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, g, tmA2, tmB2, dn);
   if (e != cudaSuccess) {
     set_error("decode layer launch: %s", cudaGetErrorString(e));
     return BI_ERR_CUDA;

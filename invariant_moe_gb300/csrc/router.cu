@@ -56,6 +56,10 @@ __global__ void __launch_bounds__(32) router_rows_kernel(const XT *__restrict__ 
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   griddep_wait();
+  // a single wave of one-warp CTAs: the next grid on the stream (which waits
+  // for this one before reading anything) may start beside it (the decode
+  // layer's expert launch sets up its CTAs meanwhile)
+  griddep_launch_dependents();
   if (zero_words && blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = lane; i < n_zero; i += 32) zero_words[i] = 0u;
   const int S = K / kSlice;
